@@ -1,0 +1,101 @@
+"""Seeded synthetic workloads: shapes and input generators, nothing else.
+
+Shared by the tests (GPU path and oracle alike) and the benchmark.  It holds none
+of the attention arithmetic: it only draws seeded random bf16 tensors with the
+shapes, value distributions and mask settings of the five backward workloads.
+The pages measure on no public dataset; these shapes are the whole workload
+definition.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Sq: int
+    Sk: int
+    H: int
+    Hk: int
+    D: int
+    causal: bool = False
+    window_left: int = -1
+    window_right: int = -1
+    softcap: float = 0.0
+    do_std: float = 1.0
+    seed: int = 0
+    deterministic_modes: tuple = field(default=(False,))
+
+    @property
+    def scale(self) -> float:
+        # default softmax scale 1/sqrt(D) (Triton page, `flash_attn_func`)
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def nominal_flops(self) -> float:
+        """Backward FLOPs by the stated convention: 10*B*H*Sq*Sk*D, halved when causal."""
+        f = 10.0 * self.B * self.H * self.Sq * self.Sk * self.D
+        return f / 2 if self.causal else f
+
+    def visible_pairs_per_head(self) -> int:
+        """Number of (query, key) pairs the mask keeps (closed form per row)."""
+        wr = 0 if self.causal else self.window_right
+        wl = self.window_left
+        delta = self.Sk - self.Sq
+        total = 0
+        for i in range(self.Sq):
+            hi = self.Sk - 1 if wr < 0 else min(self.Sk - 1, i + delta + wr)
+            lo = 0 if wl < 0 else max(0, i + delta - wl)
+            if hi >= lo:
+                total += hi - lo + 1
+        return total
+
+    @property
+    def algorithmic_flops(self) -> float:
+        """10*D flops (five multiply-adds over D) per visible pair, logical D."""
+        return 10.0 * self.D * self.B * self.H * self.visible_pairs_per_head()
+
+    def describe(self) -> dict:
+        return dict(workload=self.name, B=self.B, Sq=self.Sq, Sk=self.Sk, H=self.H, Hk=self.Hk,
+                    D=self.D, causal=self.causal, window_left=self.window_left,
+                    window_right=self.window_right, softcap=self.softcap)
+
+
+WORKLOADS = {
+    "tiny_mha": Workload("tiny_mha", 1, 128, 128, 2, 2, 64, seed=0),
+    "mha_causal": Workload("mha_causal", 2, 1024, 1024, 16, 16, 128, causal=True, seed=1,
+                           deterministic_modes=(False, True)),
+    "gqa_causal": Workload("gqa_causal", 4, 2048, 2048, 32, 8, 128, causal=True, do_std=0.1,
+                           seed=2),
+    "swa_softcap": Workload("swa_softcap", 1, 8192, 8192, 16, 2, 128, window_left=1024,
+                            window_right=0, softcap=30.0, seed=3),
+    "ragged_d72": Workload("ragged_d72", 8, 512, 4096, 12, 12, 72, causal=True, seed=4),
+}
+
+HEADLINE = "gqa_causal"
+
+
+def make_inputs(w: Workload, device="cpu", seed: int | None = None):
+    """q, k, v, do as bf16 tensors in the (B, S, H, D) layout, drawn from N(0, 1)
+    (dO from N(0, do_std^2)) with a CPU generator so that every device sees the
+    same values."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    q = torch.randn(w.B, w.Sq, w.H, w.D, generator=g, dtype=torch.float32)
+    k = torch.randn(w.B, w.Sk, w.Hk, w.D, generator=g, dtype=torch.float32)
+    v = torch.randn(w.B, w.Sk, w.Hk, w.D, generator=g, dtype=torch.float32)
+    do = torch.randn(w.B, w.Sq, w.H, w.D, generator=g, dtype=torch.float32) * w.do_std
+    out = [t.to(torch.bfloat16) for t in (q, k, v, do)]
+    if device != "cpu":
+        out = [t.to(device) for t in out]
+    return out
+
+
+def custom(name, B, Sq, Sk, H, Hk, D, **kw) -> Workload:
+    return Workload(name, B, Sq, Sk, H, Hk, D, **kw)
