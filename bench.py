@@ -1,0 +1,353 @@
+#!/usr/bin/env python
+"""Benchmark of the FlashAttention backward (fa_bwd: preprocess + main + convert).
+
+One step = one fa_bwd call over one batch of the workload (default: the GQA causal
+workload B=4, Sq=Sk=2048, H=32, Hk=8, D=128), inputs resident in HBM, L2 flushed
+(256 MiB write) between steps outside the timed events.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
+same workload (one batch x one kv-head group per step).  Under torchrun (N > 1) every
+rank runs an independent replica (the path shards over (batch, kv-head) units with no
+exchange); value = work of all ranks / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention-backward TFLOP/s (bf16) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "flashattention_backward_pass_gb300", "csrc")
+    for f in ("fa_bwd_main.cu", "fa_ptx.cuh", "fa_kernels.h", "fa_tiles.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload):
+    """DRAM bytes per main-kernel launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", f"fa_bwd_main.{workload}.traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") == _kernel_source_hash():
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        # samples taken while the GPU was busy: those at the highest power draw half
+        pw = [num(r[3]) or 0.0 for r in rows]
+        thr = sorted(pw)[len(pw) // 2] if pw else 0.0
+        busy = [num(r[1]) for r, p in zip(rows, pw) if p >= thr and num(r[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(busy or sm) if (busy or sm) else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def run_ours(args, ws_, rank, local):
+    import torch
+    import flashattention_backward_pass_gb300 as fa
+    from flashattention_backward_pass_gb300 import _abi
+    from flashattention_backward_pass_gb300.workloads import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load()
+    q, k, v, do = make_inputs(w, dev)
+    out, lse = fa.attention_forward(q, k, v, w.scale, w.causal, w.window_left, w.window_right,
+                                    w.softcap)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsp = fa.alloc_bwd_workspace(q, k, args.deterministic)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    _abi.profile_enable(True)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_bwd(do, q, k, v, out, lse, dq, dk, dv, w.scale, w.causal, w.window_left,
+                  w.window_right, w.softcap, args.deterministic, wsp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert fa.fa_bwd_status(wsp) == 0
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    if ws_ > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    main_ms, pre_ms, conv_ms = [], [], []
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        a, b_, c = _abi.profile_read()
+        pre_ms.append(a)
+        main_ms.append(b_)
+        conv_ms.append(c)
+    torch.cuda.synchronize()
+    if ws_ > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    status = fa.fa_bwd_status(wsp)
+    if ws_ > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end-to-end through the public API with host buffers (pinned), copies in the region
+    e2e = None
+    if not args.no_e2e:
+        host_in = [x.cpu().pin_memory() for x in (do, q, k, v, out, lse)]
+        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (dq, dk, dv)]
+        dev_in = [torch.empty_like(x) for x in (do, q, k, v, out, lse)]
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        n_e2e = max(3, min(args.steps, 20))
+        for it in range(2 + n_e2e):
+            if it == 2:
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            for dsrc, hsrc in zip(dev_in, host_in):
+                dsrc.copy_(hsrc, non_blocking=True)
+            fa.fa_bwd(*dev_in, dq, dk, dv, w.scale, w.causal, w.window_left, w.window_right,
+                      w.softcap, args.deterministic, wsp)
+            for hdst, dsrc in zip(host_out, (dq, dk, dv)):
+                hdst.copy_(dsrc, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": round(w.nominal_flops / (e2e_ms * 1e-3) / 1e12 * ws_, 3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4)}
+
+    peaks, peak_src = _peaks()
+    ms_per_step = total_ms / args.steps
+    value = w.nominal_flops * args.steps * ws_ / (total_ms * 1e-3) / 1e12
+    main_avg = statistics.mean(main_ms)
+    achieved = w.algorithmic_flops / (main_avg * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
+        "config": dict(w.describe(), deterministic=bool(args.deterministic),
+                       l2="flushed between steps (256 MiB write, outside the timed events)",
+                       parallelism=f"replicas x{ws_}" if ws_ > 1 else "single GPU",
+                       flop_convention="10*B*H*Sq*Sk*D, halved for causal"),
+        "pct_of_bf16_peak": round(100 * value / ws_ / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": _traffic(args.workload), "kernel": "fa::bwd_main_kernel",
+                     "flops_per_launch": w.algorithmic_flops,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4)},
+        "kernel_ms": {"preprocess": round(statistics.mean(pre_ms), 4), "main": round(main_avg, 4),
+                      "convert": round(statistics.mean(conv_ms), 4)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "device_status": status,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return res
+
+
+def _oracle_sample(w, b, hk, q, k, v, do):
+    import numpy as np
+    from oracle import attention_backward
+    G = w.H // w.Hk
+    hs = slice(hk * G, hk * G + G)
+    f = lambda t: np.asarray(t, dtype=np.float64)
+    attention_backward(f(do[b:b + 1, :, hs]), f(q[b:b + 1, :, hs]), f(k[b:b + 1, :, hk:hk + 1]),
+                       f(v[b:b + 1, :, hk:hk + 1]), w.scale, causal=w.causal,
+                       window_left=w.window_left, window_right=w.window_right, softcap=w.softcap)
+    return w.nominal_flops / (w.B * w.Hk)
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """The fp64 oracle, as it stands, on this host's cores: (batch, kv-head group) slices
+    of the workload until about `budget_s` seconds of work."""
+    from flashattention_backward_pass_gb300.workloads import make_inputs
+    q, k, v, do = (t.float().numpy() for t in make_inputs(w, "cpu"))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    flops, n = 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        b, hk = divmod(n % (w.B * w.Hk), w.Hk)
+        flops += _oracle_sample(w, b, hk, q, k, v, do)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} slice(s) of 1 batch x 1 kv-head group ({w.H // w.Hk} q-heads) of "
+                      f"{w.name}, fp64 NumPy, {dt:.1f} s", "seconds": round(dt, 2)}
+
+
+def run_reference(args, ws_, rank):
+    from flashattention_backward_pass_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    q, k, v, do = (t.float().numpy() for t in make_inputs(w, "cpu"))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    for i in range(args.warmup):
+        b, hk = divmod(i % (w.B * w.Hk), w.Hk)
+        _oracle_sample(w, b, hk, q, k, v, do)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        b, hk = divmod(i % (w.B * w.Hk), w.Hk)
+        flops += _oracle_sample(w, b, hk, q, k, v, do)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"each step: the fp64 oracle backward on 1 batch x 1 kv-head group "
+              f"({w.H // w.Hk} q-heads) of {w.name}")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(w.describe()),
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gqa_causal")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws_, rank, local = _dist()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, ws_, rank)), flush=True)
+        return
+
+    if ws_ > 1:
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, ws_, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws_ > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

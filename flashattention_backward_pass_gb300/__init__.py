@@ -1,0 +1,48 @@
+"""GB300-native (sm_103a) FlashAttention forward/backward behind a C ABI.
+
+Public Python surface (thin wrappers over include/fa.h):
+
+    fa_fwd(q, k, v, out, lse, softmax_scale, causal, window_left, window_right, softcap)
+    fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal, window_left,
+           window_right, softcap, deterministic, workspace=None)
+    attention_forward(q, k, v, ...)  -> (out, lse)            allocates outputs with torch
+    attention_backward(dout, q, k, v, out, lse, ...) -> (dq, dk, dv)
+
+Layouts: q/out/dout/dq (B, Sq, H, D) bf16; k/v/dk/dv (B, Sk, Hk, D) bf16; lse (B, H, Sq)
+fp32 natural log.  All compute runs in libfa_gb300.so.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from ._abi import (FaError, alloc_bwd_workspace, bwd_workspace_size, fa_bwd, fa_bwd_status,
+                   fa_fwd, load)
+
+__all__ = ["FaError", "alloc_bwd_workspace", "attention_backward", "attention_forward",
+           "bwd_workspace_size", "fa_bwd", "fa_bwd_status", "fa_fwd", "load"]
+
+
+def _scale(q, softmax_scale):
+    return softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(q.shape[-1])
+
+
+def attention_forward(q, k, v, softmax_scale=None, causal=False, window_left=-1, window_right=-1,
+                      softcap=0.0):
+    B, Sq, H, D = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, out, lse, _scale(q, softmax_scale), causal, window_left, window_right, softcap)
+    return out, lse
+
+
+def attention_backward(dout, q, k, v, out, lse, softmax_scale=None, causal=False, window_left=-1,
+                       window_right=-1, softcap=0.0, deterministic=False, workspace=None):
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, _scale(q, softmax_scale), causal, window_left,
+           window_right, softcap, deterministic, workspace)
+    return dq, dk, dv

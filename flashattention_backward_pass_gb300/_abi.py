@@ -1,0 +1,183 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+Every step of the forward and backward runs in the CUDA kernels of libfa_gb300.so;
+this module only turns torch tensors into `fa_tensor` views, allocates the caller-side
+workspace with torch, and passes the current CUDA stream.  It raises when the library
+is missing: there is no fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_DTYPE_BF16 = 0
+FA_DTYPE_FP32 = 1
+
+STATUS = {
+    0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_SHAPE", -3: "FA_ERR_DTYPE", -4: "FA_ERR_HEADDIM",
+    -5: "FA_ERR_LAYOUT", -6: "FA_ERR_ALIGNMENT", -7: "FA_ERR_WORKSPACE", -8: "FA_ERR_UNSUPPORTED",
+    -9: "FA_ERR_ARG", -10: "FA_ERR_CUDA", -11: "FA_ERR_DEVICE_TIMEOUT",
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status})")
+
+
+class FaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("shape", ctypes.c_int64 * 4),
+                ("stride", ctypes.c_int64 * 4), ("ndim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libfa_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(FaTensor)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.fa_abi_version.restype = ctypes.c_int
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    lib.fa_fwd_workspace_size.restype = sz
+    lib.fa_fwd_workspace_size.argtypes = [ctypes.c_int] * 6
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 7
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_fwd.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_float, vp, sz, vp]
+    lib.fa_bwd.restype = ctypes.c_int
+    lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_int, ctypes.c_float, ctypes.c_int, vp, sz, vp]
+    lib.fa_bwd_status.restype = ctypes.c_int
+    lib.fa_bwd_status.argtypes = [vp, sz, vp, ctypes.POINTER(ctypes.c_int)]
+    lib.fa_debug_set_wait_limit.restype = ctypes.c_int
+    lib.fa_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
+    lib.fa_debug_poison_ordering.restype = ctypes.c_int
+    lib.fa_debug_poison_ordering.argtypes = [ctypes.c_int]
+    lib.fa_profile_enable.restype = ctypes.c_int
+    lib.fa_profile_enable.argtypes = [ctypes.c_int]
+    lib.fa_profile_read.restype = ctypes.c_int
+    lib.fa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float)]
+    _lib = lib
+    return lib
+
+
+def declared_functions(header: str = HEADER_PATH):
+    """Names of the functions include/fa.h declares."""
+    with open(header) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(fa_[a-z0-9_]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def tensor_view(t: torch.Tensor) -> FaTensor:
+    if t.dtype == torch.bfloat16:
+        dt = FA_DTYPE_BF16
+    elif t.dtype == torch.float32:
+        dt = FA_DTYPE_FP32
+    else:
+        dt = 99
+    v = FaTensor()
+    v.data = t.data_ptr() if t.numel() > 0 else None
+    for i in range(4):
+        v.shape[i] = t.shape[i] if i < t.dim() else 0
+        v.stride[i] = t.stride(i) if i < t.dim() else 0
+    v.ndim = t.dim()
+    v.dtype = dt
+    return v
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise FaError(st, where)
+
+
+def bwd_workspace_size(B, H, Hk, Sq, Sk, D, deterministic=False) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, Hk, Sq, Sk, D, int(bool(deterministic))))
+
+
+def alloc_bwd_workspace(q: torch.Tensor, k: torch.Tensor, deterministic=False) -> torch.Tensor:
+    B, Sq, H, D = q.shape
+    Sk, Hk = k.shape[1], k.shape[2]
+    n = bwd_workspace_size(B, H, Hk, Sq, Sk, D, deterministic)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def fa_fwd(q, k, v, out, lse, softmax_scale, causal=False, window_left=-1, window_right=-1,
+           softcap=0.0, stream=None):
+    """Writes O into `out` and natural-log LSE into `lse` (C call `fa_fwd`)."""
+    lib = load()
+    tv = [tensor_view(x) for x in (q, k, v, out, lse)]
+    st = lib.fa_fwd(*[ctypes.byref(x) for x in tv], float(softmax_scale), int(bool(causal)),
+                    int(window_left), int(window_right), float(softcap), None, 0,
+                    _stream_ptr(stream))
+    _check(st, "fa_fwd")
+
+
+def fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal=False, window_left=-1,
+           window_right=-1, softcap=0.0, deterministic=False, workspace=None, stream=None):
+    """Writes dQ, dK, dV in place (C call `fa_bwd`).  Returns the workspace used."""
+    lib = load()
+    if workspace is None:
+        workspace = alloc_bwd_workspace(q, k, deterministic)
+    tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    st = lib.fa_bwd(*[ctypes.byref(x) for x in tv], float(softmax_scale), int(bool(causal)),
+                    int(window_left), int(window_right), float(softcap), int(bool(deterministic)),
+                    ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    _check(st, "fa_bwd")
+    return workspace
+
+
+def fa_bwd_status(workspace, stream=None) -> int:
+    """Device status word of the last fa_bwd on `workspace` (0 = every wait completed)."""
+    lib = load()
+    out = ctypes.c_int(0)
+    st = lib.fa_bwd_status(ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                           _stream_ptr(stream), ctypes.byref(out))
+    _check(st, "fa_bwd_status")
+    return int(out.value)
+
+
+def set_wait_limit(cycles: int):
+    _check(load().fa_debug_set_wait_limit(int(cycles)), "fa_debug_set_wait_limit")
+
+
+def poison_ordering(enable: bool):
+    _check(load().fa_debug_poison_ordering(int(bool(enable))), "fa_debug_poison_ordering")
+
+
+def profile_enable(enable: bool = True):
+    """Record CUDA events around the three backward kernels of every later fa_bwd."""
+    _check(load().fa_profile_enable(int(bool(enable))), "fa_profile_enable")
+
+
+def profile_read():
+    """(preprocess_ms, main_ms, convert_ms) of the most recent fa_bwd (waits for it)."""
+    ms = (ctypes.c_float * 3)()
+    _check(load().fa_profile_read(ms), "fa_profile_read")
+    return float(ms[0]), float(ms[1]), float(ms[2])

@@ -1,0 +1,415 @@
+// fa_api.cu — host side of the C ABI declared in include/fa.h: argument validation,
+// workspace carving, TMA tensor-map encoding and the kernel launches.
+//
+// Validation rules follow the pages: non-null inputs, matching dims, K/V shape match,
+// equal dtypes, head dim bounds and H % Hk == 0 (Triton page, `validate_inputs`); fp32
+// LSE (`flash_bwd_sm90.py` page, `_check_type`); head dim a multiple of 8
+// (`can_implement`); 16-byte-divisible strides for the TMA copies (the sm90 page's
+// `__call__` assumes 128-bit-divisible strides); Sq == 0 launches nothing (call-trace
+// page, `mha_bwd` launches only when seqlen_q > 0).
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+#include "fa_tiles.h"
+
+using namespace fa;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Test hooks (process-wide): a shorter bounded-wait limit and, for the deterministic
+// path, an ordering counter that no contributor will ever match (so the ordered wait
+// must run out and report FA_ERR_DEVICE_TIMEOUT).
+long long g_wait_limit = 2000000000ll;
+int g_poison_first_counter = 0;
+
+// Optional timing of the three backward kernels: events recorded on the caller's stream
+// before the preprocess, before and after the main kernel and after the convert.
+bool g_profile = false;
+cudaEvent_t g_ev[4] = {nullptr, nullptr, nullptr, nullptr};
+
+void prof_record(int i, cudaStream_t s) {
+  if (g_profile) cudaEventRecord(g_ev[i], s);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int padded_dim(int D) {
+  if (D <= 64) return 64;
+  if (D <= 80) return 80;
+  if (D <= 96) return 96;
+  return 128;
+}
+
+struct BwdLayout {
+  int Mb, Sq_r, Dp;
+  size_t off_lse2, off_dsum, off_accum, off_sems, total, zero_bytes;
+};
+
+bool bwd_layout(int B, int H, int Sq, int D, BwdLayout* L) {
+  if (B < 0 || H <= 0 || Sq < 0 || D <= 0) return false;
+  L->Dp = padded_dim(D);
+  L->Mb = (Sq + kTileQ - 1) / kTileQ;
+  L->Sq_r = L->Mb * kTileQ;
+  const size_t rows = (size_t)B * H * L->Sq_r;
+  size_t off = WS_HEADER_BYTES;
+  L->off_lse2 = off;
+  off = align_up(off + rows * 4, 256);
+  L->off_dsum = off;
+  off = align_up(off + rows * 4, 256);
+  L->off_accum = off;
+  const size_t accum = (size_t)B * H * L->Mb * kTileQ * L->Dp * 4;
+  off += accum;
+  L->off_sems = off;
+  const size_t sems = align_up((size_t)B * H * L->Mb * 4, 16);
+  off += sems;
+  L->zero_bytes = accum + sems;
+  L->total = align_up(off, 256);
+  return true;
+}
+
+bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_bf16_4d(const fa_tensor* t, int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
+  if (!t) return FA_ERR_NULL;
+  if (t->ndim != 4) return FA_ERR_SHAPE;
+  if (t->dtype != FA_DTYPE_BF16) return FA_ERR_DTYPE;
+  if (t->shape[0] != d0 || t->shape[1] != d1 || t->shape[2] != d2 || t->shape[3] != d3)
+    return FA_ERR_SHAPE;
+  if (t->stride[3] != 1) return FA_ERR_LAYOUT;
+  const int64_t numel = d0 * d1 * d2 * d3;
+  if (numel > 0 && !t->data) return FA_ERR_NULL;
+  if (numel > 0) {
+    if (!is_aligned16(t->data)) return FA_ERR_ALIGNMENT;
+    for (int i = 0; i < 3; ++i)
+      if (t->shape[i] > 1 && (t->stride[i] % 8 != 0 || t->stride[i] <= 0)) return FA_ERR_ALIGNMENT;
+  }
+  return FA_OK;
+}
+
+int check_lse(const fa_tensor* t, int64_t B, int64_t H, int64_t Sq) {
+  if (!t) return FA_ERR_NULL;
+  if (t->ndim != 3) return FA_ERR_SHAPE;
+  if (t->dtype != FA_DTYPE_FP32) return FA_ERR_DTYPE;
+  if (t->shape[0] != B || t->shape[1] != H || t->shape[2] != Sq) return FA_ERR_SHAPE;
+  if (B * H * Sq > 0 && !t->data) return FA_ERR_NULL;
+  return FA_OK;
+}
+
+// Shapes shared by fa_fwd and fa_bwd.  Returns a status; fills the problem sizes.
+int check_qkv(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, int* B, int* Sq,
+              int* Sk, int* H, int* Hk, int* D) {
+  if (!q || !k || !v) return FA_ERR_NULL;
+  if (q->ndim != 4 || k->ndim != 4 || v->ndim != 4) return FA_ERR_SHAPE;
+  if (q->dtype != FA_DTYPE_BF16 || k->dtype != FA_DTYPE_BF16 || v->dtype != FA_DTYPE_BF16)
+    return FA_ERR_DTYPE;
+  const int64_t b = q->shape[0], sq = q->shape[1], h = q->shape[2], d = q->shape[3];
+  const int64_t sk = k->shape[1], hk = k->shape[2];
+  if (b < 0 || sq < 0 || sk < 0 || h <= 0 || hk <= 0 || d <= 0) return FA_ERR_SHAPE;
+  if (k->shape[0] != b || k->shape[3] != d) return FA_ERR_SHAPE;
+  for (int i = 0; i < 4; ++i)
+    if (v->shape[i] != k->shape[i]) return FA_ERR_SHAPE;
+  if (h % hk != 0) return FA_ERR_SHAPE;
+  if (d % 8 != 0 || d > 128) return FA_ERR_HEADDIM;
+  if (b > (1 << 20) || sq > (1 << 30) || sk > (1 << 30) || h > 65535) return FA_ERR_UNSUPPORTED;
+  int st = check_bf16_4d(q, b, sq, h, d);
+  if (st) return st;
+  st = check_bf16_4d(k, b, sk, hk, d);
+  if (st) return st;
+  st = check_bf16_4d(v, b, sk, hk, d);
+  if (st) return st;
+  *B = (int)b;
+  *Sq = (int)sq;
+  *Sk = (int)sk;
+  *H = (int)h;
+  *Hk = (int)hk;
+  *D = (int)d;
+  return FA_OK;
+}
+
+int check_scalars(float scale, float softcap) {
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_ARG;
+  if (!(softcap >= 0.f) || !isfinite(softcap)) return FA_ERR_ARG;
+  return FA_OK;
+}
+
+void mask_bounds(int Sq, int Sk, int causal, int wl, int wr, long long* lo, long long* hi) {
+  MaskGeom g = make_geom(Sq, Sk, causal, wl, wr, kTileQ, kTileK);
+  *lo = g.lo;
+  *hi = g.hi;
+}
+
+int clamp30(long long x) {
+  const long long lim = 1ll << 30;
+  return (int)(x < -lim ? -lim : (x > lim ? lim : x));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Tensor map over a bf16 (B, S, H, D) operand, box = (width, 1, 128, 1) at 128B/64B/32B
+// swizzle.  Out-of-range rows and columns (S tail, D padding) read as zero.
+bool encode_operand(CUtensorMap* map, const fa_tensor* t, int width) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
+                        (cuuint64_t)t->shape[0]};
+  cuuint64_t strides[3] = {(cuuint64_t)(t->shape[2] > 1 ? t->stride[2] : t->shape[3]) * 2,
+                           (cuuint64_t)(t->shape[1] > 1 ? t->stride[1] : t->shape[3]) * 2,
+                           (cuuint64_t)(t->shape[0] > 1 ? t->stride[0] : t->shape[3]) * 2};
+  cuuint32_t box[4] = {(cuuint32_t)width, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMapSwizzle swz = width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                       : (width == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_32B);
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_pair(OperandMaps* m, const fa_tensor* t, int Dp) {
+  memset(m, 0, sizeof(*m));
+  if (!encode_operand(&m->full, t, 64)) return false;
+  const int tail = Dp % 64;
+  if (tail) return encode_operand(&m->tail, t, tail);
+  m->tail = m->full;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_abi_version(void) { return FA_ABI_VERSION; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_NULL: return "FA_ERR_NULL: a required pointer is NULL";
+    case FA_ERR_SHAPE: return "FA_ERR_SHAPE: tensor shapes do not match";
+    case FA_ERR_DTYPE: return "FA_ERR_DTYPE: unsupported dtype";
+    case FA_ERR_HEADDIM: return "FA_ERR_HEADDIM: head dim must be a multiple of 8 and <= 128";
+    case FA_ERR_LAYOUT: return "FA_ERR_LAYOUT: last dimension must be contiguous";
+    case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT: base or stride not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: outside what this build implements";
+    case FA_ERR_ARG: return "FA_ERR_ARG: invalid scalar argument";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call or launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    default: return "unknown fa status";
+  }
+}
+
+size_t fa_fwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D) {
+  (void)B; (void)H; (void)Hk; (void)Sq; (void)Sk; (void)D;
+  return 0;
+}
+
+int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out,
+           fa_tensor* lse, float softmax_scale, int causal, int window_left, int window_right,
+           float softcap, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace; (void)workspace_bytes;
+  int B, Sq, Sk, H, Hk, D;
+  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D);
+  if (st) return st;
+  if ((st = check_bf16_4d(out, B, Sq, H, D))) return st;
+  if ((st = check_lse(lse, B, H, Sq))) return st;
+  if ((st = check_scalars(softmax_scale, softcap))) return st;
+  if (B == 0 || Sq == 0) return FA_OK;
+  long long lo, hi;
+  mask_bounds(Sq, Sk, causal, window_left, window_right, &lo, &hi);
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.q = (const __nv_bfloat16*)q->data;
+  p.k = (const __nv_bfloat16*)k->data;
+  p.v = (const __nv_bfloat16*)v->data;
+  p.o = (__nv_bfloat16*)out->data;
+  p.lse = (float*)lse->data;
+  p.q_sb = q->stride[0]; p.q_ss = q->stride[1]; p.q_sh = q->stride[2];
+  p.k_sb = k->stride[0]; p.k_ss = k->stride[1]; p.k_sh = k->stride[2];
+  p.v_sb = v->stride[0]; p.v_ss = v->stride[1]; p.v_sh = v->stride[2];
+  p.o_sb = out->stride[0]; p.o_ss = out->stride[1]; p.o_sh = out->stride[2];
+  p.lse_sb = lse->stride[0]; p.lse_sh = lse->stride[1]; p.lse_ss = lse->stride[2];
+  p.B = B; p.H = H; p.Hk = Hk; p.G = H / Hk; p.Sq = Sq; p.Sk = Sk; p.D = D;
+  p.lo = clamp30(lo);
+  p.hi = clamp30(hi);
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.softcap_on = softcap > 0.f;
+  p.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
+  p.cap_log2 = softcap * kLog2e;
+  if (launch_fwd(p, padded_dim(D), (cudaStream_t)stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int deterministic) {
+  (void)Hk; (void)Sk; (void)deterministic;
+  BwdLayout L;
+  if (!bwd_layout(B, H, Sq, D, &L)) return 0;
+  return L.total;
+}
+
+int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+           const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq, fa_tensor* dk,
+           fa_tensor* dv, float softmax_scale, int causal, int window_left, int window_right,
+           float softcap, int deterministic, void* workspace, size_t workspace_bytes,
+           void* stream) {
+  int B, Sq, Sk, H, Hk, D;
+  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D);
+  if (st) return st;
+  if ((st = check_bf16_4d(dout, B, Sq, H, D))) return st;
+  if ((st = check_bf16_4d(out, B, Sq, H, D))) return st;
+  if ((st = check_bf16_4d(dq, B, Sq, H, D))) return st;
+  if ((st = check_bf16_4d(dk, B, Sk, Hk, D))) return st;
+  if ((st = check_bf16_4d(dv, B, Sk, Hk, D))) return st;
+  if ((st = check_lse(lse, B, H, Sq))) return st;
+  if ((st = check_scalars(softmax_scale, softcap))) return st;
+  if (B == 0 || Sq == 0) return FA_OK;
+  BwdLayout L;
+  if (!bwd_layout(B, H, Sq, D, &L)) return FA_ERR_SHAPE;
+  if (!workspace || workspace_bytes < L.total) return FA_ERR_WORKSPACE;
+  if (!is_aligned16(workspace)) return FA_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+
+  long long lo, hi;
+  mask_bounds(Sq, Sk, causal, window_left, window_right, &lo, &hi);
+  const int Dp = L.Dp;
+
+  BwdPreParams pre;
+  memset(&pre, 0, sizeof(pre));
+  pre.dout = (const __nv_bfloat16*)dout->data;
+  pre.out = (const __nv_bfloat16*)out->data;
+  pre.lse = (const float*)lse->data;
+  pre.do_sb = dout->stride[0]; pre.do_ss = dout->stride[1]; pre.do_sh = dout->stride[2];
+  pre.o_sb = out->stride[0]; pre.o_ss = out->stride[1]; pre.o_sh = out->stride[2];
+  pre.lse_sb = lse->stride[0]; pre.lse_sh = lse->stride[1]; pre.lse_ss = lse->stride[2];
+  pre.B = B; pre.H = H; pre.Sq = Sq; pre.Sq_r = L.Sq_r; pre.D = D;
+  pre.lse2 = (float*)(ws + L.off_lse2);
+  pre.dsum = (float*)(ws + L.off_dsum);
+  pre.zero_ptr = (float4*)(ws + L.off_accum);
+  pre.zero_count = (int64_t)(L.zero_bytes / 16);
+  pre.header = (int*)ws;
+  prof_record(0, s);
+  if (launch_bwd_preprocess(pre, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (g_poison_first_counter && deterministic) {
+    const int poison = -1000000;
+    if (cudaMemcpyAsync(ws + L.off_sems, &poison, sizeof(int), cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+
+  const int Nb = (Sk + kTileK - 1) / kTileK;
+  const int num_ctas = Nb * B * Hk;
+  prof_record(1, s);
+  if (num_ctas > 0) {
+    OperandMaps mq, mk, mv, mdo;
+    if (!encode_pair(&mq, q, Dp) || !encode_pair(&mk, k, Dp) || !encode_pair(&mv, v, Dp) ||
+        !encode_pair(&mdo, dout, Dp))
+      return FA_ERR_CUDA;
+    BwdMainParams p;
+    memset(&p, 0, sizeof(p));
+    p.B = B; p.H = H; p.Hk = Hk; p.G = H / Hk; p.Sq = Sq; p.Sk = Sk; p.D = D;
+    p.Mb = L.Mb; p.Nb = Nb; p.Sq_r = L.Sq_r;
+    p.lo = clamp30(lo);
+    p.hi = clamp30(hi);
+    p.lo64 = lo;
+    p.hi64 = hi;
+    p.scale_log2 = softmax_scale * kLog2e;
+    p.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
+    p.cap_log2 = softcap * kLog2e;
+    p.dk_scale = softmax_scale;
+    p.deterministic = deterministic ? 1 : 0;
+    p.lse2 = (const float*)(ws + L.off_lse2);
+    p.dsum = (const float*)(ws + L.off_dsum);
+    p.dq_accum = (float*)(ws + L.off_accum);
+    p.sems = (int*)(ws + L.off_sems);
+    p.status = (int*)ws + WS_STATUS;
+    p.ticket = (int*)ws + WS_TICKET;
+    p.dk = (__nv_bfloat16*)dk->data;
+    p.dv = (__nv_bfloat16*)dv->data;
+    p.dk_sb = dk->stride[0]; p.dk_ss = dk->stride[1]; p.dk_sh = dk->stride[2];
+    p.dv_sb = dv->stride[0]; p.dv_ss = dv->stride[1]; p.dv_sh = dv->stride[2];
+    p.wait_limit = g_wait_limit;
+    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, num_ctas, s) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+
+  prof_record(2, s);
+  BwdConvParams cp;
+  memset(&cp, 0, sizeof(cp));
+  cp.dq_accum = (const float*)(ws + L.off_accum);
+  cp.dq = (__nv_bfloat16*)dq->data;
+  cp.dq_sb = dq->stride[0]; cp.dq_ss = dq->stride[1]; cp.dq_sh = dq->stride[2];
+  cp.B = B; cp.H = H; cp.Sq = Sq; cp.D = D; cp.Dp = Dp; cp.Mb = L.Mb;
+  cp.scale = softmax_scale;
+  if (launch_bwd_convert(cp, s) != cudaSuccess) return FA_ERR_CUDA;
+  prof_record(3, s);
+  return FA_OK;
+}
+
+int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* device_status) {
+  if (!workspace || !device_status) return FA_ERR_NULL;
+  if (workspace_bytes < WS_HEADER_BYTES) return FA_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  int v = 0;
+  if (cudaMemcpyAsync(&v, (int*)workspace + WS_STATUS, sizeof(int), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyAsync((int*)workspace + WS_STATUS, &zero, sizeof(int), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  *device_status = v;
+  return FA_OK;
+}
+
+int fa_debug_set_wait_limit(long long cycles) {
+  if (cycles <= 0) return FA_ERR_ARG;
+  g_wait_limit = cycles;
+  return FA_OK;
+}
+
+int fa_debug_poison_ordering(int enable) {
+  g_poison_first_counter = enable ? 1 : 0;
+  return FA_OK;
+}
+
+int fa_profile_enable(int enable) {
+  if (enable && !g_ev[0]) {
+    for (int i = 0; i < 4; ++i)
+      if (cudaEventCreate(&g_ev[i]) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  g_profile = enable != 0;
+  return FA_OK;
+}
+
+int fa_profile_read(float* ms3) {
+  if (!ms3) return FA_ERR_NULL;
+  if (!g_ev[0]) return FA_ERR_ARG;
+  if (cudaEventSynchronize(g_ev[3]) != cudaSuccess) return FA_ERR_CUDA;
+  for (int i = 0; i < 3; ++i)
+    if (cudaEventElapsedTime(&ms3[i], g_ev[i], g_ev[i + 1]) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+}  // extern "C"

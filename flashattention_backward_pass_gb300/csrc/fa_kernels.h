@@ -1,0 +1,95 @@
+// fa_kernels.h — parameter blocks and launchers shared by the host API and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+constexpr int kTileQ = 128;   // queries per tile (M of dQ, N of S^T / dP^T)
+constexpr int kTileK = 128;   // keys per CTA (M of S^T, dP^T, dK, dV)
+
+// Status-word slots at the start of the backward workspace.
+enum : int { WS_STATUS = 0, WS_TICKET = 1, WS_HEADER_BYTES = 256 };
+
+struct BwdPreParams {
+  const __nv_bfloat16* dout;
+  const __nv_bfloat16* out;
+  const float* lse;
+  int64_t do_sb, do_ss, do_sh;   // element strides of dO (B, S, H)
+  int64_t o_sb, o_ss, o_sh;      // element strides of O
+  int64_t lse_sb, lse_sh, lse_ss;
+  int B, H, Sq, Sq_r, D;
+  float* lse2;                   // (B*H, Sq_r) LSE * log2(e); +inf on padded rows
+  float* dsum;                   // (B*H, Sq_r) rowsum(dO*O); 0 on padded rows
+  float4* zero_ptr;              // dQ accumulator + counters, zeroed here
+  int64_t zero_count;            // in float4 units
+  int* header;                   // status word + tile ticket, zeroed here
+};
+
+struct BwdMainParams {
+  int B, H, Hk, G, Sq, Sk, D;
+  int Mb, Nb, Sq_r;
+  int lo, hi;                    // visible iff lo <= j - i <= hi (clamped to +-2^30)
+  long long lo64, hi64;          // the same bounds, unclamped (tile ranges)
+  float scale_log2;              // scale * log2(e)
+  float cap_scale;               // scale / softcap
+  float cap_log2;                // softcap * log2(e)
+  float dk_scale;                // scale (dK = scale * dA^T Q)
+  int deterministic;
+  const float* lse2;
+  const float* dsum;
+  float* dq_accum;               // tiles of (Dp/4, 128, 4) fp32 per (b, h, m-tile)
+  int* sems;                     // (B*H*Mb) ordering counters (deterministic mode)
+  int* status;
+  int* ticket;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int64_t dk_sb, dk_ss, dk_sh;
+  int64_t dv_sb, dv_ss, dv_sh;
+  long long wait_limit;
+};
+
+struct BwdConvParams {
+  const float* dq_accum;
+  __nv_bfloat16* dq;
+  int64_t dq_sb, dq_ss, dq_sh;
+  int B, H, Sq, D, Dp, Mb;
+  float scale;
+};
+
+struct FwdParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;
+  float* lse;
+  int64_t q_sb, q_ss, q_sh;
+  int64_t k_sb, k_ss, k_sh;
+  int64_t v_sb, v_ss, v_sh;
+  int64_t o_sb, o_ss, o_sh;
+  int64_t lse_sb, lse_sh, lse_ss;
+  int B, H, Hk, G, Sq, Sk, D;
+  int lo, hi;
+  float scale_log2, cap_scale, cap_log2;
+  int softcap_on;
+};
+
+// Tensor maps for one bf16 (B, S, H, D) operand: a 64-column 128B-swizzled box and,
+// when Dp % 64 != 0, a narrower box for the remaining 16 or 32 columns.
+struct OperandMaps {
+  CUtensorMap full;
+  CUtensorMap tail;
+};
+
+size_t bwd_main_smem_bytes(int Dp);
+cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t s);
+cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
+                            const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
+                            int num_ctas, cudaStream_t s);
+cudaError_t launch_bwd_convert(const BwdConvParams& p, cudaStream_t s);
+cudaError_t launch_fwd(const FwdParams& p, int Dp, cudaStream_t s);
+
+}  // namespace fa

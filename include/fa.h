@@ -1,0 +1,167 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) FlashAttention forward/backward library.
+ *
+ * The operation is softmax attention and its gradient as traced on the
+ * "FlashAttention backward call trace" page (`mha_bwd` signature, `softmax_d`,
+ * in-place `dq, dk, dv`, GQA `sum_out`), the "Fused Attention (Flash Attention v2)"
+ * Triton page (`_attn_fwd_inner`, `_bwd_kernel_dk/dv/dq`), the "GQA/MQA" page
+ * (kv-head map, bottom-right causal block range) and the `flash_bwd_sm90.py` page
+ * (`mma_one_m_block`: P = exp2(S*scale*log2e - LSE2), dS = P*(dP - dPsum)).
+ *
+ *   forward : O = softmax(mask(z)) V,  z = softcap>0 ? c*tanh(scale*QK^T/c) : scale*QK^T
+ *             LSE_i = ln sum_j exp(z_ij)           (natural log; +inf for a row with no key)
+ *   backward: D_i = sum_d dO_id O_id,  dZ = P*(dO V^T - D),  dA = dZ*(1 - tanh^2) (softcap),
+ *             dV = P^T dO,  dK = scale dA^T Q,  dQ = scale dA K,
+ *             dK/dV of kv-head hk summed over its H/Hk q-heads.
+ *
+ * Masking (bottom-right aligned, offset Sk - Sq): key j visible to query i iff
+ *   j <= i + (Sk-Sq) + window_right  (window_right >= 0; causal forces window_right = 0) and
+ *   j >= i + (Sk-Sq) - window_left   (window_left  >= 0).  Negative bounds are unbounded.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are described by fa_tensor (element strides; the last dimension must
+ *     have stride 1).  Q, O, dO, dQ: (B, Sq, H, D).  K, V, dK, dV: (B, Sk, Hk, D).
+ *     LSE: (B, H, Sq) fp32.  Data type: bf16 for Q/K/V/O/dO/dQ/dK/dV.
+ *   - Every pointer is device memory owned by the caller.  The library allocates
+ *     nothing and frees nothing; scratch comes from the caller's workspace buffer.
+ *   - Calls are asynchronous on `stream` (cudaStream_t passed as void*; NULL = the
+ *     legacy default stream).  A return of FA_OK means "validated and enqueued".
+ *   - All argument errors are detected on the host before any launch and leave the
+ *     outputs untouched.  A device-side wait that runs out of time records
+ *     FA_ERR_DEVICE_TIMEOUT in the workspace status word (see fa_bwd_status).
+ *   - Limits of this build: D % 8 == 0 and D <= 128 (padded inside to a multiple of
+ *     16); H % Hk == 0; base pointers 16-byte aligned; every non-unit stride a
+ *     multiple of 8 elements (16 bytes).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_ABI_VERSION 1
+
+typedef enum {
+    FA_DTYPE_BF16 = 0,
+    FA_DTYPE_FP32 = 1
+} fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,          /* a required pointer is NULL                          */
+    FA_ERR_SHAPE = -2,         /* mismatched dims, K/V mismatch, H % Hk != 0, ndim    */
+    FA_ERR_DTYPE = -3,         /* not bf16 (tensors) / not fp32 (LSE)                 */
+    FA_ERR_HEADDIM = -4,       /* D % 8 != 0 or D > 128                               */
+    FA_ERR_LAYOUT = -5,        /* last dimension not contiguous                       */
+    FA_ERR_ALIGNMENT = -6,     /* base not 16-byte aligned or stride not 16-byte mult */
+    FA_ERR_WORKSPACE = -7,     /* workspace NULL or smaller than the size query       */
+    FA_ERR_UNSUPPORTED = -8,   /* argument outside what this build implements         */
+    FA_ERR_ARG = -9,           /* invalid scalar (scale <= 0, softcap < 0, ...)       */
+    FA_ERR_CUDA = -10,         /* a CUDA runtime/driver call or launch failed         */
+    FA_ERR_DEVICE_TIMEOUT = -11 /* a bounded device-side wait gave up (status word)   */
+} fa_status;
+
+/* Strided view of a tensor.  `ndim` is 4 (B,S,H,D) or 3 (LSE: B,H,S).  shape and
+ * stride are in elements; unused trailing entries are ignored. */
+typedef struct {
+    void* data;
+    int64_t shape[4];
+    int64_t stride[4];
+    int32_t ndim;
+    int32_t dtype; /* fa_dtype */
+} fa_tensor;
+
+/* Library/ABI version (FA_ABI_VERSION). */
+int fa_abi_version(void);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * Workspace the forward needs, in bytes (0 for this build: the forward keeps its
+ * statistics in registers and writes O and LSE directly).
+ */
+size_t fa_fwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D);
+
+/*
+ * fa_fwd — O (bf16, (B,Sq,H,D)) and natural-log LSE (fp32, (B,H,Sq)) from Q, K, V.
+ * Defined by the Triton page's `_attn_fwd_inner`/`_attn_fwd_kernel` (online softmax,
+ * LSE saved per row) with the mask/softcap conventions above.  `out` and `lse` are
+ * written in place.  softmax_scale > 0 (callers normally pass 1/sqrt(D)).
+ * Returns a fa_status.
+ */
+int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+           fa_tensor* out, fa_tensor* lse,
+           float softmax_scale, int causal, int window_left, int window_right,
+           float softcap, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace the backward needs, in bytes, for the given problem.  It holds the fp32
+ * dQ accumulator, D = rowsum(dO*O), LSE in log2 units, the deterministic-mode
+ * ordering counters and a status word.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int deterministic);
+
+/*
+ * fa_bwd — dQ (B,Sq,H,D), dK and dV (B,Sk,Hk,D), bf16, written in place (the call-trace
+ * page's `_flash_attn_backward` mutates dq, dk, dv).  Inputs: dout, q, k, v, out and the
+ * forward's natural-log lse.  dropout is not supported (p = 0).
+ *
+ * Three kernels run on `stream`: a preprocess (D = rowsum(dO*O), LSE*log2e, zeroing of
+ * the dQ accumulator and counters), the main tcgen05 kernel (one CTA per 128-key tile
+ * of one kv-head; recomputes P per 128-query tile; dK/dV accumulate in tensor memory
+ * over all q-heads of the kv-head, so the GQA reduction happens in-kernel; dQ partials
+ * are added in fp32 to the accumulator) and a convert kernel (dQ = scale * accumulator
+ * -> bf16).  deterministic != 0 orders the dQ additions by key tile, which makes every
+ * output bitwise reproducible run to run.
+ *
+ * B == 0 or Sq == 0 returns FA_OK without launching (and, when Sk > 0 and Sq == 0,
+ * without touching dK/dV).  Returns a fa_status.
+ */
+int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+           const fa_tensor* out, const fa_tensor* lse,
+           fa_tensor* dq, fa_tensor* dk, fa_tensor* dv,
+           float softmax_scale, int causal, int window_left, int window_right, float softcap,
+           int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd_status — waits for `stream`, then reads the device status word that the last
+ * fa_bwd on this workspace left (0 when every bounded wait completed) into
+ * *device_status, and clears it.  Returns FA_OK, or FA_ERR_CUDA if the copy failed.
+ */
+int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* device_status);
+
+/*
+ * Test hooks for failure detection (process-wide, not thread-safe; not for production).
+ *
+ * fa_debug_set_wait_limit — cycles a bounded device-side wait (mbarrier phase, ordered
+ *   dQ counter) may spin before it gives up and records FA_ERR_DEVICE_TIMEOUT in the
+ *   workspace status word.  Default 2e9 (about one second).  cycles <= 0: FA_ERR_ARG.
+ * fa_debug_poison_ordering — when enable != 0, every later deterministic fa_bwd sets the
+ *   ordering counter of the first dQ tile to a value no contributor will match, so the
+ *   ordered wait must run out: the kernels end, the status word reads the timeout, and
+ *   the context stays usable.  No effect on non-deterministic calls.
+ */
+int fa_debug_set_wait_limit(long long cycles);
+int fa_debug_poison_ordering(int enable);
+
+/*
+ * Kernel timing (process-wide).  fa_profile_enable(1) creates four CUDA events on the
+ * current device; every later fa_bwd records them on its stream before the preprocess,
+ * before and after the main kernel, and after the convert.  fa_profile_read waits for
+ * the last event and writes the three durations of the most recent fa_bwd, in ms, to
+ * ms3[0] (preprocess), ms3[1] (main) and ms3[2] (convert).  Returns FA_ERR_ARG if
+ * profiling was never enabled.
+ */
+int fa_profile_enable(int enable);
+int fa_profile_read(float* ms3);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

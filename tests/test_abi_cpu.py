@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for sm_103a,
+loads, exports every function include/fa.h declares, and rejects bad arguments with
+the documented status codes before touching CUDA."""
+
+import ctypes
+
+import pytest
+
+from tests.helpers import ensure_built
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    from flashattention_backward_pass_gb300 import _abi
+    return _abi.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    from flashattention_backward_pass_gb300._abi import declared_functions
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_status",
+                     "fa_status_string", "fa_abi_version", "fa_fwd_workspace_size"):
+        assert required in names
+    for n in names:
+        assert hasattr(lib, n), f"libfa_gb300.so does not export {n}"
+
+
+def test_version_and_strings(lib):
+    assert lib.fa_abi_version() == 1
+    for code in range(0, -12, -1):
+        s = lib.fa_status_string(code)
+        assert s and s.startswith(b"FA_")
+    assert lib.fa_status_string(12345) == b"unknown fa status"
+
+
+def _view(shape, strides=None, dtype=0, data=4096):
+    from flashattention_backward_pass_gb300._abi import FaTensor
+    t = FaTensor()
+    t.data = data
+    nd = len(shape)
+    if strides is None:
+        strides = [0] * nd
+        acc = 1
+        for i in reversed(range(nd)):
+            strides[i] = acc
+            acc *= shape[i]
+    for i in range(4):
+        t.shape[i] = shape[i] if i < nd else 0
+        t.stride[i] = strides[i] if i < nd else 0
+    t.ndim = nd
+    t.dtype = dtype
+    return t
+
+
+def _bwd_args(B=1, Sq=128, Sk=128, H=2, Hk=2, D=64, **over):
+    a = dict(dout=_view((B, Sq, H, D)), q=_view((B, Sq, H, D)), k=_view((B, Sk, Hk, D)),
+             v=_view((B, Sk, Hk, D)), out=_view((B, Sq, H, D)), lse=_view((B, H, Sq), dtype=1),
+             dq=_view((B, Sq, H, D)), dk=_view((B, Sk, Hk, D)), dv=_view((B, Sk, Hk, D)))
+    a.update(over)
+    return a
+
+
+def _call_bwd(lib, a, scale=0.125, causal=0, wl=-1, wr=-1, softcap=0.0, det=0, ws=4096, ws_bytes=1 << 30):
+    order = ("dout", "q", "k", "v", "out", "lse", "dq", "dk", "dv")
+    ptrs = [ctypes.byref(a[n]) if a[n] is not None else None for n in order]
+    return lib.fa_bwd(*ptrs, scale, causal, wl, wr, softcap, det, ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_bwd_validation_codes(lib):
+    assert _call_bwd(lib, _bwd_args(q=None)) == -1                       # FA_ERR_NULL
+    a = _bwd_args(); a["k"] = _view((1, 128, 2, 32))
+    assert _call_bwd(lib, a) == -2                                       # K head dim mismatch
+    a = _bwd_args(); a["v"] = _view((1, 64, 2, 64))
+    assert _call_bwd(lib, a) == -2                                       # K/V mismatch
+    assert _call_bwd(lib, _bwd_args(H=3, Hk=2)) == -2                    # H % Hk
+    a = _bwd_args(); a["q"] = _view((1, 128, 2, 64), dtype=1)
+    assert _call_bwd(lib, a) == -3                                       # dtype
+    a = _bwd_args(); a["lse"] = _view((1, 2, 128), dtype=0)
+    assert _call_bwd(lib, a) == -3                                       # LSE must be fp32
+    assert _call_bwd(lib, _bwd_args(D=60)) == -4                         # D % 8
+    assert _call_bwd(lib, _bwd_args(D=136)) == -4                        # D > 128
+    a = _bwd_args(); a["q"] = _view((1, 128, 2, 64), strides=(128 * 2 * 64, 2 * 64, 64, 2))
+    assert _call_bwd(lib, a) == -5                                       # last dim not contiguous
+    a = _bwd_args(); a["q"] = _view((1, 128, 2, 64), data=4096 + 8)
+    assert _call_bwd(lib, a) == -6                                       # base misaligned
+    a = _bwd_args(); a["q"] = _view((1, 128, 2, 64), strides=(128 * 2 * 68, 2 * 68, 68, 1))
+    assert _call_bwd(lib, a) == -6                                       # stride not 16 B
+    assert _call_bwd(lib, _bwd_args(), ws_bytes=16) == -7                # workspace too small
+    assert _call_bwd(lib, _bwd_args(), ws=0) == -7                       # no workspace
+    assert _call_bwd(lib, _bwd_args(), scale=0.0) == -9                  # scale <= 0
+    assert _call_bwd(lib, _bwd_args(), scale=float("nan")) == -9
+    assert _call_bwd(lib, _bwd_args(), softcap=-1.0) == -9
+    a = _bwd_args(); a["dq"] = _view((1, 128, 2, 64), data=0)
+    assert _call_bwd(lib, a) == -1                                       # null output
+
+
+def test_empty_problems_launch_nothing(lib):
+    # Sq == 0 and B == 0 return FA_OK without any CUDA call (this machine has no GPU,
+    # so reaching a launch would fail with FA_ERR_CUDA).
+    assert _call_bwd(lib, _bwd_args(Sq=0)) == 0
+    assert _call_bwd(lib, _bwd_args(B=0)) == 0
+
+
+def test_workspace_size(lib):
+    f = lib.fa_bwd_workspace_size
+    f.restype = ctypes.c_size_t
+    # header 256 + LSE2 + D (B*H*Sq_r fp32 each) + accumulator (B*H*Mb*128*Dp fp32) + counters
+    B, H, Sq, D = 4, 32, 2048, 128
+    rows = B * H * Sq
+    want = 256 + rows * 4 + rows * 4 + B * H * 16 * 128 * 128 * 4 + B * H * 16 * 4
+    assert f(B, H, 8, Sq, Sq, D, 0) == want
+    assert f(1, 1, 1, 77, 99, 72, 1) >= 256 + 2 * 128 * 4 + 128 * 80 * 4
+
+
+def test_fwd_validation_codes(lib):
+    q = _view((1, 64, 2, 64)); k = _view((1, 64, 2, 64)); v = _view((1, 64, 2, 64))
+    o = _view((1, 64, 2, 64)); l = _view((1, 2, 64), dtype=1)
+    args = lambda **kw: [ctypes.byref(x) for x in (kw.get("q", q), kw.get("k", k), v, kw.get("o", o), l)]
+    assert lib.fa_fwd(*args(o=_view((1, 64, 2, 32))), ctypes.c_float(0.1), 0, -1, -1, ctypes.c_float(0), None, 0, None) == -2
+    assert lib.fa_fwd(*args(), ctypes.c_float(-1.0), 0, -1, -1, ctypes.c_float(0), None, 0, None) == -9
+    q0 = _view((1, 0, 2, 64))
+    o0 = _view((1, 0, 2, 64))
+    l0 = _view((1, 2, 0), dtype=1)
+    assert lib.fa_fwd(ctypes.byref(q0), ctypes.byref(k), ctypes.byref(v), ctypes.byref(o0), ctypes.byref(l0),
+                      ctypes.c_float(0.1), 0, -1, -1, ctypes.c_float(0), None, 0, None) == 0

@@ -1,0 +1,73 @@
+"""The tile-range header (which query tiles a key tile visits, and the first key tile
+of a query tile, used to order deterministic dQ additions) against brute force over
+every element of every tile.  Compiled with g++; no GPU."""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+HARNESS = r'''
+#include <cstdio>
+#include "fa_tiles.h"
+using namespace fa;
+static bool vis(const MaskGeom& g, long i, long j) {
+  return i < g.Sq && j < g.Sk && (j - i) >= g.lo && (j - i) <= g.hi;
+}
+int main() {
+  long bad = 0, cases = 0;
+  const int sizes[] = {1, 5, 64, 127, 128, 129, 200, 256, 300, 513};
+  const int wins[] = {-1, 0, 1, 100, 128, 300};
+  for (int Sq : sizes) for (int Sk : sizes) for (int causal = 0; causal < 2; ++causal)
+  for (int wl : wins) for (int wr : wins) {
+    MaskGeom g = make_geom(Sq, Sk, causal, wl, wr, 128, 128);
+    for (long n = 0; n < g.Nb; ++n) {
+      long mb, me; m_range(g, n, &mb, &me);
+      for (long m = 0; m < g.Mb; ++m) {
+        bool any = false, all = true;
+        for (long i = m * 128; i < m * 128 + 128; ++i)
+          for (long j = n * 128; j < n * 128 + 128; ++j) {
+            bool v = vis(g, i, j);
+            any = any || v;
+            // tile_full promises every (i, j) with j < Sk is visible (rows past Sq may be
+            // anything: their P is forced to zero by LSE = +inf)
+            if (i < g.Sq && !v) all = false;
+            if (i >= g.Sq && j < g.Sk && !((j - i) >= g.lo && (j - i) <= g.hi)) all = false;
+          }
+        bool act = tile_active(g, m, n);
+        bool in_range = m >= mb && m < me;
+        if (act != any || in_range != any) { ++bad; if (bad < 5) printf("range Sq=%d Sk=%d c=%d wl=%d wr=%d m=%ld n=%ld any=%d act=%d in=%d\n", Sq, Sk, causal, wl, wr, m, n, any, act, in_range); }
+        if (tile_full(g, m, n) && !all) { ++bad; if (bad < 5) printf("full Sq=%d Sk=%d m=%ld n=%ld\n", Sq, Sk, m, n); }
+        if (tile_full(g, m, n) && (n * 128 + 128 > g.Sk)) ++bad;
+        ++cases;
+      }
+    }
+    for (long m = 0; m < g.Mb; ++m) {
+      long nb, ne; n_range(g, m, &nb, &ne);
+      for (long n = 0; n < g.Nb; ++n) {
+        bool in = n >= nb && n < ne;
+        if (in != tile_active(g, m, n)) { ++bad; if (bad < 5) printf("nrange Sq=%d Sk=%d m=%ld n=%ld\n", Sq, Sk, m, n); }
+      }
+    }
+  }
+  printf("cases=%ld bad=%ld\n", cases, bad);
+  return bad != 0;
+}
+'''
+
+
+def test_tile_ranges_brute_force(tmp_path):
+    gxx = shutil.which("g++") or shutil.which("c++")
+    if gxx is None:
+        pytest.skip("no C++ compiler")
+    src = tmp_path / "tiles.cpp"
+    src.write_text(HARNESS)
+    exe = tmp_path / "tiles"
+    inc = os.path.join(ROOT, "flashattention_backward_pass_gb300", "csrc")
+    subprocess.run([gxx, "-O2", "-std=c++17", "-I", inc, str(src), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "bad=0" in r.stdout
