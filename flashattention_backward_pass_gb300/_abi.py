@@ -181,3 +181,21 @@ def profile_read():
     ms = (ctypes.c_float * 3)()
     _check(load().fa_profile_read(ms), "fa_profile_read")
     return float(ms[0]), float(ms[1]), float(ms[2])
+
+
+def fa_bwd_noalloc(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal=False,
+                   window_left=-1, window_right=-1, softcap=0.0, deterministic=False,
+                   stream=None):
+    """C call `fa_bwd_noalloc`: the backward with the library's own fixed scratch (for
+    callers that cannot allocate device memory); raises FaError on a non-zero status."""
+    lib = load()
+    fn = lib.fa_bwd_noalloc
+    P = ctypes.POINTER(FaTensor)
+    fn.restype = ctypes.c_int
+    fn.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
+    tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    st = fn(*[ctypes.byref(x) for x in tv], float(softmax_scale), int(bool(causal)),
+            int(window_left), int(window_right), float(softcap), int(bool(deterministic)),
+            _stream_ptr(stream))
+    _check(st, "fa_bwd_noalloc")

@@ -136,6 +136,30 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
 int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* device_status);
 
 /*
+ * fa_bwd_noalloc — the same backward as fa_bwd (same arguments, layouts, results and
+ * errors) for callers that cannot allocate device memory: code running where a
+ * cudaMalloc is not allowed (a serving or real-time loop that must not synchronize the
+ * device, a region recorded into a CUDA graph) or an embedding with a fixed memory
+ * budget that has no allocator to provide fa_bwd's workspace.  The source pages have no
+ * counterpart to this entry point.
+ *
+ * It allocates nothing.  Its scratch is one library-owned device array of
+ * FA_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading the library keeps until the
+ * process exits.  A problem whose fa_bwd_workspace_size exceeds that is rejected with
+ * FA_ERR_WORKSPACE before any launch.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current) and caches it; make
+ * that first call outside any stream capture.  All calls on a device share the array:
+ * each call clears what must start at zero, but calls that overlap on the GPU race, so
+ * order them on one stream.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int fa_bwd_noalloc(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
+                   const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
+                   fa_tensor* dq, fa_tensor* dk, fa_tensor* dv,
+                   float softmax_scale, int causal, int window_left, int window_right,
+                   float softcap, int deterministic, void* stream);
+
+/*
  * Test hooks for failure detection (process-wide, not thread-safe; not for production).
  *
  * fa_debug_set_wait_limit — cycles a bounded device-side wait (mbarrier phase, ordered
