@@ -45,18 +45,22 @@ def _stamp(extra_flags) -> str:
     return h.hexdigest()
 
 
-def build(verbose: bool = False, extra_flags=(), force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
-    stamp_path = os.path.join(BUILD, "libfa_gb300.stamp")
+def build(verbose: bool = False, extra_flags=(), force: bool = False, lib_path: str = LIB,
+          tag: str = "") -> str:
+    """Compile and link; `lib_path` / `tag` give variant builds (e.g. with -DFA_TRACE)
+    their own library file and object directory."""
+    build_dir = os.path.join(BUILD, tag) if tag else BUILD
+    os.makedirs(build_dir, exist_ok=True)
+    stamp_path = os.path.join(build_dir, "libfa_gb300.stamp")
     stamp = _stamp(extra_flags)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_path):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_path):
         with open(stamp_path) as fh:
             if fh.read() == stamp:
-                return LIB
+                return lib_path
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -69,15 +73,15 @@ def build(verbose: bool = False, extra_flags=(), force: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp_path, "w") as fh:
         fh.write(stamp)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

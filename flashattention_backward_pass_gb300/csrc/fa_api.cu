@@ -394,6 +394,13 @@ int fa_debug_poison_ordering(int enable) {
   return FA_OK;
 }
 
+#ifdef FA_TRACE
+// Tracing builds only: copies the per-phase timestamps of the main kernel to the host.
+int fa_trace_read(void* host, size_t bytes) {
+  return bwd_trace_copy(host, bytes) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+#endif
+
 int fa_profile_enable(int enable) {
   if (enable && !g_ev[0]) {
     for (int i = 0; i < 4; ++i)

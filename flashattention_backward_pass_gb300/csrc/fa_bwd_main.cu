@@ -21,8 +21,9 @@
 // Warp roles (16 warps, 512 threads):
 //   warp 0      TMA producer: K, V once; Q+LSE2+D and dO per step into 2-stage rings
 //   warp 1      TMEM allocator and the single MMA-issuing thread
-//   warps 4-7   dQ drain: TMEM -> registers -> red.global.add.v4.f32 (or the ordered
-//               path when deterministic)
+//   warps 4-7   dQ drain (176 registers each via setmaxnreg): TMEM -> registers, release
+//               the TMEM columns, then two 32 KB halves through a staging buffer into
+//               cp.reduce.async.bulk fp32 adds (ordered by key tile when deterministic)
 //   warps 8-15  two compute warpgroups: warpgroup w handles queries [64w, 64w+64) of
 //               the tile for every key row (thread = key = TMEM lane); epilogue dK / dV
 //
@@ -33,7 +34,8 @@
 //
 // Shared memory (1024-byte aligned tiles, 128B swizzle for 64-column panels, 32B/64B
 // swizzle for a 16/32-column tail panel when Dp % 64 != 0):
-//   K, V, Q[2], dO[2] (128 rows x Dp bf16 each), dS^T (128 keys x 128 queries bf16)
+//   K, V, Q[2], dO (128 rows x Dp bf16 each), dS^T (128 keys x 128 queries bf16),
+//   dQ staging (128 x 64 fp32)
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 #include "fa_tiles.h"
@@ -60,10 +62,12 @@ struct Geo {
   static constexpr uint32_t OFF_K = SMALL;
   static constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
   static constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;            // 2 stages
-  static constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE_BYTES;       // 2 stages
-  static constexpr uint32_t OFF_DS = OFF_DO + 2 * TILE_BYTES;
+  static constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE_BYTES;       // 1 stage
+  static constexpr uint32_t OFF_DS = OFF_DO + TILE_BYTES;
   static constexpr uint32_t DS_BYTES = 128u * 128u * 2u;
-  static constexpr uint32_t TOTAL = OFF_DS + DS_BYTES;
+  static constexpr uint32_t OFF_STG = OFF_DS + DS_BYTES;           // dQ reduction staging
+  static constexpr uint32_t STG_BYTES = 128u * 64u * 4u;           // 64 fp32 columns
+  static constexpr uint32_t TOTAL = OFF_STG + STG_BYTES;
   static_assert(TILE_BYTES % 1024 == 0, "tiles stay 1024-byte aligned");
   static_assert(TOTAL <= 232448, "fits the 227 KB opt-in shared memory");
 };
@@ -88,6 +92,22 @@ constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_S = 256, TM_DP = 384;
 // Error codes written on a timed-out wait (all map to FA_ERR_DEVICE_TIMEOUT on the host;
 // the low bits say which wait gave up).
 constexpr int kTimeoutBase = -1100;
+
+#ifdef FA_TRACE
+// Optional per-phase timestamps (clock64 relative to the CTA's start) of the first
+// FA_TRACE_CTAS CTAs, for pipeline tuning.  Off in the normal build.
+constexpr int FA_TRACE_CTAS = 4, FA_TRACE_ITERS = 64, FA_TRACE_EV = 12;
+__device__ long long g_fa_trace[FA_TRACE_CTAS][FA_TRACE_ITERS][FA_TRACE_EV];
+#define FA_TR(ev, it)                                                              \
+  do {                                                                             \
+    if (blockIdx.x < FA_TRACE_CTAS && (it) < FA_TRACE_ITERS)                       \
+      g_fa_trace[blockIdx.x][(it)][(ev)] = clock64() - t_start;                    \
+  } while (0)
+#else
+#define FA_TR(ev, it) \
+  do {                \
+  } while (0)
+#endif
 
 // K-major operand, 128 rows, K-step ks (16 columns) of a Dp-wide tile.
 template <int DP>
@@ -144,6 +164,49 @@ __device__ __forceinline__ TileCoord decode_tile(const BwdMainParams& p, int t) 
 
 }  // namespace
 
+// Phase A of one step for one thread (key row = TMEM lane): reads its 64 S^T columns,
+// forms P = exp2(S*scale*log2e - LSE2) (softcap: exp2(c*log2e*tanh(S*scale/c) - LSE2)),
+// zeroes masked entries (MASK: visible iff qmin <= column <= qmax), writes P^T as bf16
+// pairs back over the S^T columns already read (the A operand of dV += P^T dO), and keeps
+// P (times 1 - tanh^2 under softcap) as f16 pairs in `pc` for dS.
+template <bool MASK, bool SOFTCAP>
+__device__ __forceinline__ void phase_p(const BwdMainParams& p, uint32_t taddr, const float* lse,
+                                        int qmin, int qmax, uint32_t (&pc)[32]) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    uint32_t pk[16];
+#pragma unroll
+    for (int v4 = 0; v4 < 8; ++v4) {
+      const float4 l4 = reinterpret_cast<const float4*>(lse + c * 32)[v4];
+      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+      float pv[4], pcv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int ql = c * 32 + v4 * 4 + u;
+        const float sv = __uint_as_float(r[v4 * 4 + u]);
+        float pr, fac = 1.f;
+        if (SOFTCAP) {
+          const float t = tanh_exp2(sv * p.cap_scale);
+          pr = ex2_approx(fmaf(t, p.cap_log2, -lv[u]));
+          fac = fmaf(-t, t, 1.f);
+        } else {
+          pr = ex2_approx(fmaf(sv, p.scale_log2, -lv[u]));
+        }
+        if (MASK) pr = (ql >= qmin && ql <= qmax) ? pr : 0.f;
+        pv[u] = pr;
+        pcv[u] = SOFTCAP ? pr * fac : pr;
+      }
+      pk[v4 * 2] = pack_bf16(pv[0], pv[1]);
+      pk[v4 * 2 + 1] = pack_bf16(pv[2], pv[3]);
+      pc[c * 16 + v4 * 2] = pack_f16(pcv[0], pcv[1]);
+      pc[c * 16 + v4 * 2 + 1] = pack_f16(pcv[2], pcv[3]);
+    }
+    tmem_st16(taddr + c * 16, pk);
+  }
+}
+
 template <int DP, bool SOFTCAP>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ BwdMainParams p,
@@ -153,6 +216,9 @@ __global__ void __launch_bounds__(512, 1)
                     const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tdo_t) {
   using G = Geo<DP>;
+#ifdef FA_TRACE
+  const long long t_start = clock64();
+#endif
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -221,7 +287,13 @@ __global__ void __launch_bounds__(512, 1)
   const int total = (*s_abort) ? 0 : m_count * p.G;  // steps: (g, m) with m fastest
   const int n0 = tc.n * kTileK;
 
-  if (warp == 0) {
+  // Register split (launch: 512 threads x 128 = 65536): the producer / MMA warpgroup
+  // gives registers to the dQ drain warpgroup, which keeps a whole dQ row in registers.
+  // 128 * (80 + 176 + 128 + 128) = 65536; the host refuses to launch unless the kernel
+  // was compiled to exactly 128 registers per thread, so the split always fits.
+  if (warp < 4) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
@@ -268,14 +340,16 @@ __global__ void __launch_bounds__(512, 1)
         bulk_load(sbase + SM_LSE + s * 512, p.lse2 + row, 512, bar(B_QF0 + s));
         bulk_load(sbase + SM_DSUM + s * 512, p.dsum + row, 512, bar(B_QF0 + s));
         issued_q[s] = it / 2 + 1;
+        FA_TR(10, it);
 
-        if (it >= 2 && !mbar_wait(bar(B_DOE0 + s), ((it - 2) >> 1) & 1, st, kTimeoutBase - 2)) break;
-        const uint32_t ddst = sbase + G::OFF_DO + s * G::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(B_DOF0 + s), G::TILE_BYTES);
+        // dO has one buffer: dO_i+1 may land once dV_i (its last reader) is complete
+        if (it >= 1 && !mbar_wait(bar(B_DOE0), (it - 1) & 1, st, kTimeoutBase - 2)) break;
+        const uint32_t ddst = sbase + G::OFF_DO;
+        mbar_arrive_expect_tx(bar(B_DOF0), G::TILE_BYTES);
         for (int pnl = 0; pnl < G::NFULL; ++pnl)
-          tma_load_4d(ddst + pnl * G::FULL_BYTES, &tdo, pnl * 64, h, m0, tc.b, bar(B_DOF0 + s));
-        if (G::TAIL) tma_load_4d(ddst + G::TAIL_OFF, &tdo_t, G::NFULL * 64, h, m0, tc.b, bar(B_DOF0 + s));
-        issued_do[s] = it / 2 + 1;
+          tma_load_4d(ddst + pnl * G::FULL_BYTES, &tdo, pnl * 64, h, m0, tc.b, bar(B_DOF0));
+        if (G::TAIL) tma_load_4d(ddst + G::TAIL_OFF, &tdo_t, G::NFULL * 64, h, m0, tc.b, bar(B_DOF0));
+        issued_do[0] = it + 1;
       }
       // Before the CTA may exit, every copy this thread started must have landed (on an
       // abort the consumers may not have waited for them).
@@ -285,11 +359,16 @@ __global__ void __launch_bounds__(512, 1)
       if (kv_issued) mbar_wait(bar(B_KV), 0, drain, kTimeoutBase - 3);
       for (int s = 0; s < 2; ++s) {
         if (issued_q[s]) mbar_wait(bar(B_QF0 + s), (issued_q[s] - 1) & 1, drain, kTimeoutBase - 3);
-        if (issued_do[s]) mbar_wait(bar(B_DOF0 + s), (issued_do[s] - 1) & 1, drain, kTimeoutBase - 3);
+        if (s == 0 && issued_do[0]) mbar_wait(bar(B_DOF0), (issued_do[0] - 1) & 1, drain, kTimeoutBase - 3);
       }
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // Order per step i (after the prologue S_0, dP_0):
+    //   dV_i  (needs P^T_i)       -> frees dO stage, signals dv_done
+    //   S_i+1 (needs dv_done_i: P^T_i aliases the S^T columns)   -- overlaps phase B_i
+    //   dK_i, dQ_i (need dS_i)    -> dq_full
+    //   dP_i+1 (needs the dQ_i columns drained)
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_KV = idesc_bf16(128, G::NFULL * 64, false, true);
@@ -297,46 +376,56 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t ID_Q = idesc_bf16(128, G::NFULL * 64, true, true);
       constexpr uint32_t ID_Q_T = idesc_bf16(128, G::TAIL ? G::TAIL : 16, true, true);
       const uint32_t sK = sbase + G::OFF_K, sV = sbase + G::OFF_V, sDS = sbase + G::OFF_DS;
-      uint32_t acc = 0;
-      bool issued_any = false;
-      for (int it = 0; it < total; ++it) {
+      auto issue_S = [&](int it) -> bool {
         const int s = it & 1;
-        const uint32_t ph2 = (it >> 1) & 1;
-        const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
-        const uint32_t sDO = sbase + G::OFF_DO + s * G::TILE_BYTES;
-        if (it == 0 && !mbar_wait(bar(B_KV), 0, st, kTimeoutBase - 10)) break;
-        if (!mbar_wait(bar(B_QF0 + s), ph2, st, kTimeoutBase - 11)) break;
-        // P^T of the previous step (aliasing the S^T columns) must have been consumed
-        if (it > 0 && !mbar_wait(bar(B_DVDONE), (it - 1) & 1, st, kTimeoutBase - 12)) break;
+        if (!mbar_wait(bar(B_QF0 + s), (it >> 1) & 1, st, kTimeoutBase - 11)) return false;
         tc_fence_after();
+        FA_TR(0, it);
+        const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
         for (int ks = 0; ks < G::KSTEPS; ++ks)
           mma_ss(tmem + TM_S, desc_kmajor<DP>(sK, ks), desc_kmajor<DP>(sQ, ks), ID_S, ks > 0);
         mma_commit(bar(B_SFULL));
-        issued_any = true;
-
-        if (!mbar_wait(bar(B_DOF0 + s), ph2, st, kTimeoutBase - 13)) break;
-        // the previous dQ tile (aliasing the dP^T columns) must have been drained
-        if (it > 0 && !mbar_wait(bar(B_DQEMPTY), (it - 1) & 1, st, kTimeoutBase - 14)) break;
+        return true;
+      };
+      auto issue_dP = [&](int it) -> bool {
+        if (!mbar_wait(bar(B_DOF0), it & 1, st, kTimeoutBase - 13)) return false;
         tc_fence_after();
+        FA_TR(1, it);
+        const uint32_t sDO = sbase + G::OFF_DO;
         for (int ks = 0; ks < G::KSTEPS; ++ks)
           mma_ss(tmem + TM_DP, desc_kmajor<DP>(sV, ks), desc_kmajor<DP>(sDO, ks), ID_S, ks > 0);
         mma_commit(bar(B_DPFULL));
-
+        return true;
+      };
+      uint32_t acc = 0;
+      bool issued_any = false;
+      bool ok = total > 0 && mbar_wait(bar(B_KV), 0, st, kTimeoutBase - 10);
+      if (ok) ok = issue_S(0) && issue_dP(0);
+      issued_any = ok;
+      for (int it = 0; ok && it < total; ++it) {
+        const int s = it & 1;
+        const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
+        const uint32_t sDO = sbase + G::OFF_DO;
         // dV += P^T dO : A = P^T from TMEM (bf16 pairs), K = 128 queries in 8 steps
         if (!mbar_wait(bar(B_PFULL), it & 1, st, kTimeoutBase - 15)) break;
         tc_fence_after();
+        FA_TR(2, it);
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t a_t = tmem + TM_S + (ks >> 2) * 64 + (ks & 3) * 8;
           const uint32_t en = (acc | (uint32_t)ks) ? 1u : 0u;
           mma_ts(tmem + TM_DV, a_t, desc_mn_full<DP>(sDO, ks), ID_KV, en);
           if (G::TAIL) mma_ts(tmem + TM_DV + G::NFULL * 64, a_t, desc_mn_tail<DP>(sDO, ks), ID_KV_T, en);
         }
-        mma_commit(bar(B_DOE0 + s));
+        mma_commit(bar(B_DOE0));
         mma_commit(bar(B_DVDONE));
-
+        if (it + 1 < total) {
+          if (!mbar_wait(bar(B_DVDONE), it & 1, st, kTimeoutBase - 12)) break;
+          if (!issue_S(it + 1)) break;
+        }
         // dK += dS^T Q : A = dS^T (K-major in shared memory), K = 128 queries
         if (!mbar_wait(bar(B_DSFULL), it & 1, st, kTimeoutBase - 16)) break;
         tc_fence_after();
+        FA_TR(3, it);
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t a = smem_desc(sDS + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, SWZ_128B);
           const uint32_t en = (acc | (uint32_t)ks) ? 1u : 0u;
@@ -353,6 +442,10 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(bar(B_DQFULL));
         mma_commit(bar(B_DSEMPTY));
         acc = 1;
+        if (it + 1 < total) {
+          if (!mbar_wait(bar(B_DQEMPTY), it & 1, st, kTimeoutBase - 14)) break;
+          if (!issue_dP(it + 1)) break;
+        }
       }
       mma_commit(bar(B_ACC));
       if (issued_any) {
@@ -364,8 +457,15 @@ __global__ void __launch_bounds__(512, 1)
         mbar_wait(bar(B_DRAIN), 0, drain, kTimeoutBase - 17);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+   }
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
     // ------------------------------------------------------------------ dQ drain
+    // The whole dQ tile row of this thread (Dp fp32) is loaded from TMEM into registers
+    // and the TMEM columns are released at once; the partial then reaches the fp32
+    // accumulator through a dedicated staging buffer and bulk fp32 adds, at the L2's pace,
+    // without holding anything the main loop needs.  The accumulator tile layout
+    // (Dp/4, 128, 4) makes each staged half one contiguous range.
     const int qd = warp & 3;
     const int q = qd * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
@@ -375,15 +475,37 @@ __global__ void __launch_bounds__(512, 1)
       const int m = m_begin + (it - g * m_count);
       const int h = tc.hk * p.G + g;
       bool ok = warp_wait(bar(B_DQFULL), it & 1, st, kTimeoutBase - 20);
+      if (threadIdx.x == 128) FA_TR(8, it);
+      uint32_t v[DP];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DP / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_lane + TM_DP + c * 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[c * 32 + e] = r[e];
+        }
+        if (DP % 32) {
+          uint32_t r[16];
+          tmem_ld16(t_lane + TM_DP + (DP / 32) * 32, r);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[(DP / 32) * 32 + e] = r[e];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DQEMPTY));
+      }
+      if (threadIdx.x == 128) FA_TR(9, it);
       const size_t tile_id = ((size_t)tc.b * p.H + h) * p.Mb + m;
       float* dst = p.dq_accum + tile_id * (size_t)(128 * DP);
       int* sem = p.sems + tile_id;
       if (p.deterministic) {
         // Ordered mode: contributions to one dQ tile are added in ascending key-tile
-        // order.  No thread leaves this loop early, so the two named barriers per step
+        // order.  No drain thread leaves the loop early, so both named barriers of a step
         // are always reached by all 128 drain threads.
         if (threadIdx.x == 128) {
-          int stop = *s_abort;
+          int stop = (*s_abort) || !ok;
           if (!stop) {
             int64_t nb, ne;
             n_range(gm, m, &nb, &ne);
@@ -392,7 +514,10 @@ __global__ void __launch_bounds__(512, 1)
             while (true) {
               int cur;
               asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cur) : "l"(sem) : "memory");
-              if (cur == want) break;
+              if (cur == want) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                break;
+              }
               if (*s_abort) { stop = 1; break; }
               if (clock64() - t0 > p.wait_limit) {
                 raise_timeout(st, kTimeoutBase - 21);
@@ -405,35 +530,51 @@ __global__ void __launch_bounds__(512, 1)
         }
         named_bar_sync(1, 128);
         ok = ok && (*s_skip == 0);
-        ok = __all_sync(0xffffffffu, ok);
       }
-      if (ok) {
-        tc_fence_after();
+      // Two halves (column groups [0, 16) and [16, Dp/4)) go through the 32 KB staging
+      // buffer: all drain threads store a half, one thread issues the bulk fp32 add, and
+      // the buffer is reused once the bulk engine has read it.  The bulk engine, not the
+      // SM's load/store path, carries the reduction traffic to L2.
+      constexpr int CGN = DP / 4;
+      constexpr int NH = CGN > 16 ? 2 : 1;
+      const uint32_t stg = sbase + G::OFF_STG;
 #pragma unroll
-        for (int c = 0; c < DP / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld16(t_lane + TM_DP + c * 16, r);
+      for (int hf = 0; hf < NH; ++hf) {
+        const int cg0 = hf * 16;
+        const int ncg = (CGN - cg0) < 16 ? (CGN - cg0) : 16;
+        // the previous bulk add must have finished reading the buffer
+        if (threadIdx.x == 128) bulk_wait_read_all();
+        named_bar_sync(1, 128);
+        if (ok) {
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            const int cg = c * 4 + g4;
-            red_add_v4(dst + ((size_t)cg * 128 + q) * 4, __uint_as_float(r[4 * g4]),
-                       __uint_as_float(r[4 * g4 + 1]), __uint_as_float(r[4 * g4 + 2]),
-                       __uint_as_float(r[4 * g4 + 3]));
+          for (int k = 0; k < 16; ++k) {
+            if (k < ncg) {
+              const int cg = cg0 + k;
+              st_shared_v4(stg + ((uint32_t)k * 128 + q) * 16, v[4 * cg], v[4 * cg + 1],
+                           v[4 * cg + 2], v[4 * cg + 3]);
+            }
           }
+          fence_proxy_async_smem();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DQEMPTY));
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 128 && ok) {
+          bulk_reduce_add_f32(dst + (size_t)cg0 * 128 * 4, stg, (uint32_t)ncg * 128 * 16);
+          bulk_commit();
+        }
       }
       if (p.deterministic) {
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (threadIdx.x == 128 && *s_skip == 0)
-          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-      } else if (!ok) {
-        break;
+        if (threadIdx.x == 128) {
+          bulk_wait_all();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          if (*s_skip == 0)
+            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+        }
       }
+      // no early exit: every drain thread reaches every named barrier of every step (on an
+      // abort the waits return at once and the stores and bulk adds are skipped)
     }
+    if (threadIdx.x == 128) bulk_wait_all();
   } else if (warp >= 8) {
     // ------------------------------------------------------------------ compute
     const int wg = (warp - 8) >> 2;        // query half of the tile
@@ -451,66 +592,49 @@ __global__ void __launch_bounds__(512, 1)
       const int m = m_begin + (it - g * m_count);
       const int m0 = m * kTileQ;
       const bool need_mask = !tile_full(gm, m, tc.n);
-      const int base = j - m0 - col0;       // (j - i) = base - local query index
+      // visible columns: lo <= (j - i) <= hi with i = m0 + col0 + ql  <=>  ql in [qmin, qmax]
+      const int base = j - m0 - col0;
+      const int qmin = row_ok ? max(base - p.hi, -1) : 1 << 20;
+      const int qmax = row_ok ? min(base - p.lo, 1 << 20) : -1;
       const float* lse = s_lse + s * 128 + col0;
       const float* dsum = s_dsum + s * 128 + col0;
 
       if (!warp_wait(bar(B_SFULL), it & 1, st, kTimeoutBase - 30)) break;
       tc_fence_after();
+      if (threadIdx.x == 256) FA_TR(4, it);
       uint32_t pc[32];  // P (times 1 - tanh^2 with softcap) as f16 pairs, reused for dS
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_lane + TM_S + col0 + c * 32, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], pcv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int ql = c * 32 + e + u;
-            const float sv = __uint_as_float(r[e + u]);
-            float pr, fac = 1.f;
-            if (SOFTCAP) {
-              const float t = tanh_exp2(sv * p.cap_scale);
-              pr = ex2_approx(fmaf(t, p.cap_log2, -lse[ql]));
-              fac = fmaf(-t, t, 1.f);
-            } else {
-              pr = ex2_approx(fmaf(sv, p.scale_log2, -lse[ql]));
-            }
-            if (need_mask) {
-              const int d = base - ql;
-              const bool vis = row_ok && d >= p.lo && d <= p.hi;
-              pr = vis ? pr : 0.f;
-            }
-            pv[u] = pr;
-            pcv[u] = pr * fac;
-          }
-          pk[e >> 1] = pack_bf16(pv[0], pv[1]);
-          pc[c * 16 + (e >> 1)] = pack_f16(pcv[0], pcv[1]);
-        }
-        tmem_st16(t_lane + TM_S + col0 + c * 16, pk);
-      }
+      if (need_mask)
+        phase_p<true, SOFTCAP>(p, t_lane + TM_S + col0, lse, qmin, qmax, pc);
+      else
+        phase_p<false, SOFTCAP>(p, t_lane + TM_S + col0, lse, qmin, qmax, pc);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PFULL));
+      if (threadIdx.x == 256) FA_TR(5, it);
+      if (threadIdx.x == 384) FA_TR(11, it);
 
       if (!warp_wait(bar(B_DPFULL), it & 1, st, kTimeoutBase - 31)) break;
       if (it > 0 && !warp_wait(bar(B_DSEMPTY), (it - 1) & 1, st, kTimeoutBase - 32)) break;
       tc_fence_after();
+      if (threadIdx.x == 256) FA_TR(6, it);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
         tmem_ld32(t_lane + TM_DP + col0 + c * 32, r);
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 pcv = unpack_f16(pc[c * 16 + (e >> 1)]);
-          const int ql = c * 32 + e;
-          const float d0 = pcv.x * (__uint_as_float(r[e]) - dsum[ql]);
-          const float d1 = pcv.y * (__uint_as_float(r[e + 1]) - dsum[ql + 1]);
-          pk[e >> 1] = pack_bf16(d0, d1);
+        for (int v4 = 0; v4 < 8; ++v4) {
+          const float4 d4 = reinterpret_cast<const float4*>(dsum + c * 32)[v4];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int e = v4 * 4 + e2 * 2;
+            const float2 pcv = unpack_f16(pc[c * 16 + (e >> 1)]);
+            const float d0 = pcv.x * (__uint_as_float(r[e]) - dv[2 * e2]);
+            const float d1 = pcv.y * (__uint_as_float(r[e + 1]) - dv[2 * e2 + 1]);
+            pk[e >> 1] = pack_bf16(d0, d1);
+          }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -522,6 +646,7 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DSFULL));
+      if (threadIdx.x == 256) FA_TR(7, it);
     }
 
     // ------------------------------------------------------------------ dK / dV epilogue
@@ -568,6 +693,13 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
+#ifdef FA_TRACE
+cudaError_t bwd_trace_copy(void* host, size_t bytes) {
+  if (bytes > sizeof(g_fa_trace)) bytes = sizeof(g_fa_trace);
+  return cudaMemcpyFromSymbol(host, g_fa_trace, bytes);
+}
+#endif
+
 size_t bwd_main_smem_bytes(int Dp) {
   switch (Dp) {
     case 64: return Geo<64>::TOTAL;
@@ -584,6 +716,11 @@ static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, cons
                               cudaStream_t s) {
   auto kern = bwd_main_kernel<DP, SC>;
   const size_t smem = Geo<DP>::TOTAL;
+  // The in-kernel register split assumes exactly 128 registers per thread at launch.
+  cudaFuncAttributes attr;
+  cudaError_t ea = cudaFuncGetAttributes(&attr, kern);
+  if (ea != cudaSuccess) return ea;
+  if (attr.numRegs != 128) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<num_ctas, 512, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail, d.full, d.tail);

@@ -91,5 +91,8 @@ cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const 
                             int num_ctas, cudaStream_t s);
 cudaError_t launch_bwd_convert(const BwdConvParams& p, cudaStream_t s);
 cudaError_t launch_fwd(const FwdParams& p, int Dp, cudaStream_t s);
+#ifdef FA_TRACE
+cudaError_t bwd_trace_copy(void* host, size_t bytes);
+#endif
 
 }  // namespace fa
