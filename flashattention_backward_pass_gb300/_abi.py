@@ -76,6 +76,9 @@ def load(path: str = LIB_PATH):
     lib.fa_profile_enable.argtypes = [ctypes.c_int]
     lib.fa_profile_read.restype = ctypes.c_int
     lib.fa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float)]
+    lib.fa_bwd_set_algorithm.restype = ctypes.c_int
+    lib.fa_bwd_set_algorithm.argtypes = [ctypes.c_int]
+    lib.fa_bwd_get_algorithm.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -161,6 +164,20 @@ def fa_bwd_status(workspace, stream=None) -> int:
                            _stream_ptr(stream), ctypes.byref(out))
     _check(st, "fa_bwd_status")
     return int(out.value)
+
+
+ALGO_SPLIT = 0
+ALGO_FUSED = 1
+
+
+def set_algorithm(algo: int):
+    """Backward algorithm for later fa_bwd calls: ALGO_SPLIT (dK/dV kernel + dQ kernel, no
+    atomics) or ALGO_FUSED (one kernel, fp32 dQ accumulator, ordered when deterministic)."""
+    _check(load().fa_bwd_set_algorithm(int(algo)), "fa_bwd_set_algorithm")
+
+
+def get_algorithm() -> int:
+    return int(load().fa_bwd_get_algorithm())
 
 
 def set_wait_limit(cycles: int):

@@ -28,6 +28,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // must run out and report FA_ERR_DEVICE_TIMEOUT).
 long long g_wait_limit = 2000000000ll;
 int g_poison_first_counter = 0;
+int g_bwd_algorithm = FA_BWD_ALGO_FUSED;
 
 // Optional timing of the three backward kernels: events recorded on the caller's stream
 // before the preprocess, before and after the main kernel and after the convert.
@@ -292,6 +293,10 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   long long lo, hi;
   mask_bounds(Sq, Sk, causal, window_left, window_right, &lo, &hi);
   const int Dp = L.Dp;
+  // The split algorithm needs key tiles to build its tensor maps; with Sk == 0 (every dQ
+  // row is zero, dK/dV are empty) the fused path's zeroed accumulator and convert give
+  // the zero dQ.
+  const bool split = g_bwd_algorithm == FA_BWD_ALGO_SPLIT && Sk > 0;
 
   BwdPreParams pre;
   memset(&pre, 0, sizeof(pre));
@@ -305,7 +310,7 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   pre.lse2 = (float*)(ws + L.off_lse2);
   pre.dsum = (float*)(ws + L.off_dsum);
   pre.zero_ptr = (float4*)(ws + L.off_accum);
-  pre.zero_count = (int64_t)(L.zero_bytes / 16);
+  pre.zero_count = split ? 0 : (int64_t)(L.zero_bytes / 16);
   pre.header = (int*)ws;
   prof_record(0, s);
   if (launch_bwd_preprocess(pre, s) != cudaSuccess) return FA_ERR_CUDA;
@@ -347,7 +352,20 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
     p.dv = (__nv_bfloat16*)dv->data;
     p.dk_sb = dk->stride[0]; p.dk_ss = dk->stride[1]; p.dk_sh = dk->stride[2];
     p.dv_sb = dv->stride[0]; p.dv_ss = dv->stride[1]; p.dv_sh = dv->stride[2];
+    p.ticket_dq = (int*)ws + WS_TICKET_DQ;
+    p.dq = (__nv_bfloat16*)dq->data;
+    p.dq_sb = dq->stride[0]; p.dq_ss = dq->stride[1]; p.dq_sh = dq->stride[2];
     p.wait_limit = g_wait_limit;
+    if (split) {
+      if (launch_bwd_split(p, mq, mk, mv, mdo, Dp, softcap > 0.f, num_ctas, 0, s) != cudaSuccess)
+        return FA_ERR_CUDA;
+      prof_record(2, s);
+      if (launch_bwd_split(p, mq, mk, mv, mdo, Dp, softcap > 0.f, 0, B * H * L.Mb, s) !=
+          cudaSuccess)
+        return FA_ERR_CUDA;
+      prof_record(3, s);
+      return FA_OK;
+    }
     if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, num_ctas, s) != cudaSuccess)
       return FA_ERR_CUDA;
   }
@@ -383,6 +401,14 @@ int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* de
   return FA_OK;
 }
 
+int fa_bwd_set_algorithm(int algorithm) {
+  if (algorithm != FA_BWD_ALGO_SPLIT && algorithm != FA_BWD_ALGO_FUSED) return FA_ERR_ARG;
+  g_bwd_algorithm = algorithm;
+  return FA_OK;
+}
+
+int fa_bwd_get_algorithm(void) { return g_bwd_algorithm; }
+
 int fa_debug_set_wait_limit(long long cycles) {
   if (cycles <= 0) return FA_ERR_ARG;
   g_wait_limit = cycles;
@@ -398,6 +424,9 @@ int fa_debug_poison_ordering(int enable) {
 // Tracing builds only: copies the per-phase timestamps of the main kernel to the host.
 int fa_trace_read(void* host, size_t bytes) {
   return bwd_trace_copy(host, bytes) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+int fa_trace_read_split(void* host, size_t bytes) {
+  return split_trace_copy(host, bytes) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 #endif
 

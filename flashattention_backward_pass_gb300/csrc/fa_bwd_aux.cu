@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
 
-  if (blockIdx.x == 0 && threadIdx.x < 2) p.header[threadIdx.x] = 0;
+  if (blockIdx.x == 0 && threadIdx.x < 4) p.header[threadIdx.x] = 0;
 
   for (int64_t r2 = wid; 2 * r2 < nrows; r2 += warps_total) {
     const int64_t r = 2 * r2 + half;

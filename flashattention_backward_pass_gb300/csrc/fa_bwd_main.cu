@@ -36,27 +36,15 @@
 // swizzle for a 16/32-column tail panel when Dp % 64 != 0):
 //   K, V, Q[2], dO (128 rows x Dp bf16 each), dS^T (128 keys x 128 queries bf16),
 //   dQ staging (128 x 64 fp32)
-#include "fa_kernels.h"
-#include "fa_ptx.cuh"
-#include "fa_tiles.h"
+#include "fa_bwd_common.cuh"
 
 namespace fa {
 
 namespace {
 
 template <int DP>
-struct Geo {
-  static_assert(DP % 16 == 0 && DP >= 64 && DP <= 128, "Dp in [64, 128], multiple of 16");
-  static constexpr int NFULL = DP / 64;        // 64-column panels (128B swizzle)
-  static constexpr int TAIL = DP % 64;         // 0, 16 or 32 columns
-  static_assert(TAIL == 0 || TAIL == 16 || TAIL == 32, "tail panel of 16 or 32 columns");
-  static constexpr uint32_t FULL_BYTES = 128u * 128u;            // 128 rows x 128 B
-  static constexpr uint32_t TAIL_ROWB = TAIL * 2;                // bytes per row in tail
-  static constexpr uint32_t TAIL_OFF = NFULL * FULL_BYTES;
-  static constexpr uint32_t TILE_BYTES = NFULL * FULL_BYTES + 128u * TAIL_ROWB;
-  static constexpr uint32_t TAIL_SWZ = TAIL == 16 ? SWZ_32B : SWZ_64B;
-  static constexpr int KSTEPS = DP / 16;
-
+struct Geo : Panels<DP> {
+  using Panels<DP>::TILE_BYTES;
   // shared-memory layout (offsets from a 1024-aligned base)
   static constexpr uint32_t SMALL = 3072;
   static constexpr uint32_t OFF_K = SMALL;
@@ -68,7 +56,6 @@ struct Geo {
   static constexpr uint32_t OFF_STG = OFF_DS + DS_BYTES;           // dQ reduction staging
   static constexpr uint32_t STG_BYTES = 128u * 64u * 4u;           // 64 fp32 columns
   static constexpr uint32_t TOTAL = OFF_STG + STG_BYTES;
-  static_assert(TILE_BYTES % 1024 == 0, "tiles stay 1024-byte aligned");
   static_assert(TOTAL <= 232448, "fits the 227 KB opt-in shared memory");
 };
 
@@ -109,42 +96,6 @@ __device__ long long g_fa_trace[FA_TRACE_CTAS][FA_TRACE_ITERS][FA_TRACE_EV];
   } while (0)
 #endif
 
-// K-major operand, 128 rows, K-step ks (16 columns) of a Dp-wide tile.
-template <int DP>
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int ks) {
-  using G = Geo<DP>;
-  if (ks < G::NFULL * 4) {
-    uint32_t addr = tile + (ks >> 2) * G::FULL_BYTES + (ks & 3) * 32;
-    return smem_desc(addr, 16, 1024, SWZ_128B);
-  }
-  int kk = ks - G::NFULL * 4;
-  uint32_t addr = tile + G::TAIL_OFF + kk * 32;
-  return smem_desc(addr, 16, 8 * G::TAIL_ROWB, G::TAIL_SWZ);
-}
-
-// MN-major operand whose rows are the contraction index (16 rows per K-step) and whose
-// columns (Dp wide) are N: descriptor for the 64-column panels (all of them, LBO = panel
-// stride) or for the tail panel.
-template <int DP>
-__device__ __forceinline__ uint64_t desc_mn_full(uint32_t tile, int ks) {
-  return smem_desc(tile + ks * 16 * 128, Geo<DP>::FULL_BYTES, 1024, SWZ_128B);
-}
-template <int DP>
-__device__ __forceinline__ uint64_t desc_mn_tail(uint32_t tile, int ks) {
-  using G = Geo<DP>;
-  return smem_desc(tile + G::TAIL_OFF + ks * 16 * G::TAIL_ROWB, 128u * G::TAIL_ROWB,
-                   8 * G::TAIL_ROWB, G::TAIL_SWZ);
-}
-
-// Every lane waits (each needs the barrier's acquire), then the warp agrees: a lane
-// that saw the abort flag makes the whole warp stop, so .sync.aligned tcgen05 ops that
-// follow are always executed by all 32 lanes or by none.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const AbortState& st,
-                                          int code) {
-  const bool ok = mbar_wait(bar, parity, st, code);
-  return __all_sync(0xffffffffu, ok);
-}
-
 struct TileCoord {
   int n, b, hk;
 };
@@ -170,7 +121,7 @@ __device__ __forceinline__ TileCoord decode_tile(const BwdMainParams& p, int t) 
 // pairs back over the S^T columns already read (the A operand of dV += P^T dO), and keeps
 // P (times 1 - tanh^2 under softcap) as f16 pairs in `pc` for dS.
 template <bool MASK, bool SOFTCAP>
-__device__ __forceinline__ void phase_p(const BwdMainParams& p, uint32_t taddr, const float* lse,
+__device__ __forceinline__ void phase_p(const SoftmaxConsts& kc, uint32_t taddr, const float* lse,
                                         int qmin, int qmax, uint32_t (&pc)[32]) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
@@ -185,15 +136,8 @@ __device__ __forceinline__ void phase_p(const BwdMainParams& p, uint32_t taddr, 
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int ql = c * 32 + v4 * 4 + u;
-        const float sv = __uint_as_float(r[v4 * 4 + u]);
-        float pr, fac = 1.f;
-        if (SOFTCAP) {
-          const float t = tanh_exp2(sv * p.cap_scale);
-          pr = ex2_approx(fmaf(t, p.cap_log2, -lv[u]));
-          fac = fmaf(-t, t, 1.f);
-        } else {
-          pr = ex2_approx(fmaf(sv, p.scale_log2, -lv[u]));
-        }
+        float fac;
+        float pr = prob<SOFTCAP>(kc, __uint_as_float(r[v4 * 4 + u]), lv[u], &fac);
         if (MASK) pr = (ql >= qmin && ql <= qmax) ? pr : 0.f;
         pv[u] = pr;
         pcv[u] = SOFTCAP ? pr * fac : pr;
@@ -585,6 +529,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t sDS = sbase + G::OFF_DS + wg * 16384 + jl * 128;
     const int j = n0 + jl;
     const bool row_ok = j < p.Sk;
+    const SoftmaxConsts kc{p.scale_log2, p.cap_scale, p.cap_log2};
 
     for (int it = 0; it < total; ++it) {
       const int s = it & 1;
@@ -604,9 +549,9 @@ __global__ void __launch_bounds__(512, 1)
       if (threadIdx.x == 256) FA_TR(4, it);
       uint32_t pc[32];  // P (times 1 - tanh^2 with softcap) as f16 pairs, reused for dS
       if (need_mask)
-        phase_p<true, SOFTCAP>(p, t_lane + TM_S + col0, lse, qmin, qmax, pc);
+        phase_p<true, SOFTCAP>(kc, t_lane + TM_S + col0, lse, qmin, qmax, pc);
       else
-        phase_p<false, SOFTCAP>(p, t_lane + TM_S + col0, lse, qmin, qmax, pc);
+        phase_p<false, SOFTCAP>(kc, t_lane + TM_S + col0, lse, qmin, qmax, pc);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -12,7 +12,7 @@ constexpr int kTileQ = 128;   // queries per tile (M of dQ, N of S^T / dP^T)
 constexpr int kTileK = 128;   // keys per CTA (M of S^T, dP^T, dK, dV)
 
 // Status-word slots at the start of the backward workspace.
-enum : int { WS_STATUS = 0, WS_TICKET = 1, WS_HEADER_BYTES = 256 };
+enum : int { WS_STATUS = 0, WS_TICKET = 1, WS_TICKET_DQ = 2, WS_HEADER_BYTES = 256 };
 
 struct BwdPreParams {
   const __nv_bfloat16* dout;
@@ -49,6 +49,10 @@ struct BwdMainParams {
   __nv_bfloat16* dv;
   int64_t dk_sb, dk_ss, dk_sh;
   int64_t dv_sb, dv_ss, dv_sh;
+  // split algorithm: the dQ kernel's tile ticket and its bf16 output
+  int* ticket_dq;
+  __nv_bfloat16* dq;
+  int64_t dq_sb, dq_ss, dq_sh;
   long long wait_limit;
 };
 
@@ -90,9 +94,15 @@ cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const 
                             const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
                             int num_ctas, cudaStream_t s);
 cudaError_t launch_bwd_convert(const BwdConvParams& p, cudaStream_t s);
+// dK/dV kernel (num_kv_ctas = key tiles x batch x kv-heads) then dQ kernel (num_q_ctas =
+// query tiles x batch x q-heads), both on stream s.
+cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
+                             const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
+                             int num_kv_ctas, int num_q_ctas, cudaStream_t s);
 cudaError_t launch_fwd(const FwdParams& p, int Dp, cudaStream_t s);
 #ifdef FA_TRACE
 cudaError_t bwd_trace_copy(void* host, size_t bytes);
+cudaError_t split_trace_copy(void* host, size_t bytes);
 #endif
 
 }  // namespace fa

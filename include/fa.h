@@ -111,13 +111,19 @@ size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int de
  * page's `_flash_attn_backward` mutates dq, dk, dv).  Inputs: dout, q, k, v, out and the
  * forward's natural-log lse.  dropout is not supported (p = 0).
  *
- * Three kernels run on `stream`: a preprocess (D = rowsum(dO*O), LSE*log2e, zeroing of
- * the dQ accumulator and counters), the main tcgen05 kernel (one CTA per 128-key tile
- * of one kv-head; recomputes P per 128-query tile; dK/dV accumulate in tensor memory
- * over all q-heads of the kv-head, so the GQA reduction happens in-kernel; dQ partials
- * are added in fp32 to the accumulator) and a convert kernel (dQ = scale * accumulator
- * -> bf16).  deterministic != 0 orders the dQ additions by key tile, which makes every
- * output bitwise reproducible run to run.
+ * Two algorithms (see fa_bwd_set_algorithm), both hand-written tcgen05/TMEM/TMA kernels on
+ * `stream`, after a preprocess kernel (D = rowsum(dO*O), LSE*log2e):
+ *   FA_BWD_ALGO_SPLIT: a dK/dV kernel (one CTA per 128-key tile of one kv-head;
+ *     recomputes P per 128-query tile; dK/dV accumulate in tensor memory over all q-heads
+ *     of the kv-head, so the GQA reduction happens in-kernel) and a dQ kernel (one CTA per
+ *     128-query tile of one q-head; recomputes P and dS over its key tiles; dQ accumulates
+ *     in tensor memory and is written once).  No atomics: every output is summed in a
+ *     fixed order, so results are bitwise reproducible whatever `deterministic` says.
+ *   FA_BWD_ALGO_FUSED (default): one kernel computes all five products per (key tile, query tile)
+ *     and adds fp32 dQ partials into an accumulator in the workspace (bulk reductions),
+ *     then a convert kernel writes dQ = bf16(scale * accumulator).  deterministic != 0
+ *     orders the dQ additions by key tile through per-tile counters (bitwise
+ *     reproducible); deterministic == 0 lets them land in any order.
  *
  * B == 0 or Sq == 0 returns FA_OK without launching (and, when Sk > 0 and Sq == 0,
  * without touching dK/dV).  Returns a fa_status.
@@ -158,6 +164,16 @@ int fa_bwd_noalloc(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k
                    fa_tensor* dq, fa_tensor* dk, fa_tensor* dv,
                    float softmax_scale, int causal, int window_left, int window_right,
                    float softcap, int deterministic, void* stream);
+
+/*
+ * Backward algorithm for later fa_bwd calls in this process (not thread-safe).
+ * fa_bwd_set_algorithm returns FA_ERR_ARG for an unknown value; fa_bwd_get_algorithm
+ * returns the current one.
+ */
+#define FA_BWD_ALGO_SPLIT 0
+#define FA_BWD_ALGO_FUSED 1
+int fa_bwd_set_algorithm(int algorithm);
+int fa_bwd_get_algorithm(void);
 
 /*
  * Test hooks for failure detection (process-wide, not thread-safe; not for production).

@@ -42,3 +42,13 @@ def check_lse(got, want, tol=LSE_TOL):
 
 def to64(t):
     return t.detach().float().cpu().double().numpy()
+
+
+def algorithm_fixture_body(request):
+    """Runs the test under the requested backward algorithm, then restores the default."""
+    ensure_built()
+    from flashattention_backward_pass_gb300 import _abi
+    _abi.load()
+    _abi.set_algorithm(request.param)
+    yield request.param
+    _abi.set_algorithm(_abi.ALGO_FUSED)

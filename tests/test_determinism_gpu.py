@@ -5,9 +5,14 @@ import pytest
 import torch
 
 from flashattention_backward_pass_gb300.workloads import WORKLOADS, custom, make_inputs
-from tests.helpers import ensure_built
+from tests.helpers import algorithm_fixture_body, ensure_built
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[0, 1], ids=["split", "fused"], autouse=True)
+def algorithm(request):
+    yield from algorithm_fixture_body(request)
 
 
 @pytest.fixture(scope="module")

@@ -30,6 +30,7 @@ def test_ordered_wait_times_out_and_recovers(fa):
     q, k, v, do = make_inputs(w, "cuda")
     out, lse = fa.attention_forward(q, k, v, w.scale, True)
     ws = fa.alloc_bwd_workspace(q, k, True)
+    _abi.set_algorithm(_abi.ALGO_FUSED)    # the ordered dQ wait belongs to the fused path
     _abi.set_wait_limit(20_000_000)        # ~10 ms per wait
     _abi.poison_ordering(True)
     try:
@@ -39,7 +40,9 @@ def test_ordered_wait_times_out_and_recovers(fa):
     finally:
         _abi.poison_ordering(False)
         _abi.set_wait_limit(2_000_000_000)
+        _abi.set_algorithm(_abi.ALGO_FUSED)
     assert status != 0, "the poisoned ordered wait should have reported a timeout"
+    _abi.set_algorithm(_abi.ALGO_FUSED)
     # the context still works: a clean deterministic run gives the right answer
     dq1, dk1, dv1 = fa.attention_backward(do, q, k, v, out, lse, w.scale, True, deterministic=True,
                                           workspace=ws)
@@ -47,5 +50,9 @@ def test_ordered_wait_times_out_and_recovers(fa):
     assert fa.fa_bwd_status(ws) == 0
     dq2, dk2, dv2 = fa.attention_backward(do, q, k, v, out, lse, w.scale, True, deterministic=False)
     torch.cuda.synchronize()
-    for a, b in ((dq1, dq2), (dk1, dk2), (dv1, dv2)):
-        check_close("det vs non-det", to64(a), to64(b), rel=1e-2, abs_=1e-3)
+    _abi.set_algorithm(_abi.ALGO_SPLIT)
+    dq3, dk3, dv3 = fa.attention_backward(do, q, k, v, out, lse, w.scale, True)
+    torch.cuda.synchronize()
+    _abi.set_algorithm(_abi.ALGO_FUSED)
+    for a, b in ((dq1, dq2), (dk1, dk2), (dv1, dv2), (dq1, dq3), (dk1, dk3), (dv1, dv3)):
+        check_close("ordered vs unordered vs split", to64(a), to64(b), rel=1e-2, abs_=1e-3)

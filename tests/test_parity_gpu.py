@@ -17,9 +17,14 @@ import torch
 
 from oracle import attention_backward, attention_forward
 from flashattention_backward_pass_gb300.workloads import WORKLOADS, custom, make_inputs
-from tests.helpers import check_close, check_lse, ensure_built, to64
+from tests.helpers import algorithm_fixture_body, check_close, check_lse, ensure_built, to64
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[0, 1], ids=["split", "fused"], autouse=True)
+def algorithm(request):
+    yield from algorithm_fixture_body(request)
 
 
 @pytest.fixture(scope="module")
