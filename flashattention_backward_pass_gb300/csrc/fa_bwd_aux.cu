@@ -18,45 +18,64 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Two rows per warp, 16 lanes per row, 8 bf16 per lane (D <= 128).
-__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p) {
+// Blocks [0, row_blocks) compute D and LSE2: each warp takes 4 rows per pass (8 lanes per
+// row, 16 bf16 per lane as two 16-byte loads each of dO and O), so a warp keeps 8 loads per
+// lane in flight.  Blocks [row_blocks, gridDim.x) clear the accumulator with 16-byte stores.
+// The two kinds of blocks run side by side, so the latency-bound row reductions overlap
+// the bandwidth-bound clearing.
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p, int row_blocks) {
+  if (blockIdx.x == 0 && threadIdx.x < 4) p.header[threadIdx.x] = 0;
+  if ((int)blockIdx.x >= row_blocks) {
+    const int64_t nthreads = (int64_t)(gridDim.x - row_blocks) * blockDim.x;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t k = (int64_t)(blockIdx.x - row_blocks) * blockDim.x + threadIdx.x;
+         k < p.zero_count; k += nthreads)
+      p.zero_ptr[k] = z;
+    return;
+  }
   const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int l16 = lane & 15;
+  const int sub = lane >> 3;  // row within the warp's group of 4
+  const int l8 = lane & 7;    // 16-column slice of the row
   const int64_t nrows = (int64_t)p.B * p.H * p.Sq_r;
-  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t warps_total = (int64_t)row_blocks * (blockDim.x >> 5);
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
 
-  if (blockIdx.x == 0 && threadIdx.x < 4) p.header[threadIdx.x] = 0;
-
-  for (int64_t r2 = wid; 2 * r2 < nrows; r2 += warps_total) {
-    const int64_t r = 2 * r2 + half;
+  for (int64_t r4 = wid; 4 * r4 < nrows; r4 += warps_total) {
+    const int64_t r = 4 * r4 + sub;
     float acc = 0.f;
     int64_t bh = 0, i = 0;
     const bool valid_row = r < nrows;
     if (valid_row) {
       bh = r / p.Sq_r;
       i = r - bh * p.Sq_r;
-      if (i < p.Sq && l16 * 8 < p.D) {
+      if (i < p.Sq) {
         const int64_t b = bh / p.H, h = bh - (bh / p.H) * p.H;
-        const uint4 a = *reinterpret_cast<const uint4*>(p.dout + b * p.do_sb + i * p.do_ss +
-                                                         h * p.do_sh + l16 * 8);
-        const uint4 o = *reinterpret_cast<const uint4*>(p.out + b * p.o_sb + i * p.o_ss +
-                                                         h * p.o_sh + l16 * 8);
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+        const __nv_bfloat16* a = p.dout + b * p.do_sb + i * p.do_ss + h * p.do_sh;
+        const __nv_bfloat16* o = p.out + b * p.o_sb + i * p.o_ss + h * p.o_sh;
+        uint4 av[2], ov[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 af = __bfloat1622float2(a2[e]);
-          const float2 of = __bfloat1622float2(o2[e]);
-          acc = fmaf(af.x, of.x, acc);
-          acc = fmaf(af.y, of.y, acc);
+        for (int u = 0; u < 2; ++u) {
+          const int c = l8 * 16 + u * 8;
+          av[u] = c < p.D ? *reinterpret_cast<const uint4*>(a + c) : make_uint4(0, 0, 0, 0);
+          ov[u] = c < p.D ? *reinterpret_cast<const uint4*>(o + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av[u]);
+          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 af = __bfloat1622float2(a2[e]);
+            const float2 of = __bfloat1622float2(o2[e]);
+            acc = fmaf(af.x, of.x, acc);
+            acc = fmaf(af.y, of.y, acc);
+          }
         }
       }
     }
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (valid_row && l16 == 0) {
+    for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (valid_row && l8 == 0) {
       float l2 = INFINITY;
       if (i < p.Sq) {
         const int64_t b = bh / p.H, h = bh - (bh / p.H) * p.H;
@@ -67,11 +86,6 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
       p.lse2[r] = l2;
     }
   }
-
-  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < p.zero_count; k += nthreads)
-    p.zero_ptr[k] = z;
 }
 
 // Block (16, 16): threadIdx.x = 8-column group, threadIdx.y = query row.  A warp covers two
@@ -103,14 +117,15 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t s) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t row_pairs = ((int64_t)p.B * p.H * p.Sq_r + 1) / 2;
-  const int64_t need = (row_pairs + 7) / 8;            // 8 warps per block
-  const int64_t need_zero = (p.zero_count + 255) / 256;
-  int64_t blocks = need > need_zero ? need : need_zero;
-  const int64_t cap = (int64_t)sms * 16;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  bwd_preprocess_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  const int64_t row_quads = ((int64_t)p.B * p.H * p.Sq_r + 3) / 4;
+  int64_t row_blocks = (row_quads + 7) / 8;                 // 8 warps per block
+  const int64_t row_cap = (int64_t)sms * 8;
+  if (row_blocks > row_cap) row_blocks = row_cap;
+  if (row_blocks < 1) row_blocks = 1;
+  int64_t zero_blocks = (p.zero_count + 255) / 256;
+  const int64_t zero_cap = (int64_t)sms * 8;
+  if (zero_blocks > zero_cap) zero_blocks = zero_cap;
+  bwd_preprocess_kernel<<<(unsigned)(row_blocks + zero_blocks), 256, 0, s>>>(p, (int)row_blocks);
   return cudaGetLastError();
 }
 

@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t sK = sbase + G::OFF_K, sV = sbase + G::OFF_V, sDS = sbase + G::OFF_DS;
       auto issue_S = [&](int it) -> bool {
         const int s = it & 1;
-        if (!mbar_wait(bar(B_QF0 + s), (it >> 1) & 1, st, kTimeoutBase - 11)) return false;
+        if (!mbar_wait_spin(bar(B_QF0 + s), (it >> 1) & 1, st, kTimeoutBase - 11)) return false;
         tc_fence_after();
         FA_TR(0, it);
         const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(512, 1)
         return true;
       };
       auto issue_dP = [&](int it) -> bool {
-        if (!mbar_wait(bar(B_DOF0), it & 1, st, kTimeoutBase - 13)) return false;
+        if (!mbar_wait_spin(bar(B_DOF0), it & 1, st, kTimeoutBase - 13)) return false;
         tc_fence_after();
         FA_TR(1, it);
         const uint32_t sDO = sbase + G::OFF_DO;
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(512, 1)
       };
       uint32_t acc = 0;
       bool issued_any = false;
-      bool ok = total > 0 && mbar_wait(bar(B_KV), 0, st, kTimeoutBase - 10);
+      bool ok = total > 0 && mbar_wait_spin(bar(B_KV), 0, st, kTimeoutBase - 10);
       if (ok) ok = issue_S(0) && issue_dP(0);
       issued_any = ok;
       for (int it = 0; ok && it < total; ++it) {
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
         const uint32_t sDO = sbase + G::OFF_DO;
         // dV += P^T dO : A = P^T from TMEM (bf16 pairs), K = 128 queries in 8 steps
-        if (!mbar_wait(bar(B_PFULL), it & 1, st, kTimeoutBase - 15)) break;
+        if (!mbar_wait_spin(bar(B_PFULL), it & 1, st, kTimeoutBase - 15)) break;
         tc_fence_after();
         FA_TR(2, it);
         for (int ks = 0; ks < 8; ++ks) {
@@ -363,11 +363,11 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(bar(B_DOE0));
         mma_commit(bar(B_DVDONE));
         if (it + 1 < total) {
-          if (!mbar_wait(bar(B_DVDONE), it & 1, st, kTimeoutBase - 12)) break;
+          if (!mbar_wait_spin(bar(B_DVDONE), it & 1, st, kTimeoutBase - 12)) break;
           if (!issue_S(it + 1)) break;
         }
         // dK += dS^T Q : A = dS^T (K-major in shared memory), K = 128 queries
-        if (!mbar_wait(bar(B_DSFULL), it & 1, st, kTimeoutBase - 16)) break;
+        if (!mbar_wait_spin(bar(B_DSFULL), it & 1, st, kTimeoutBase - 16)) break;
         tc_fence_after();
         FA_TR(3, it);
         for (int ks = 0; ks < 8; ++ks) {
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(bar(B_DSEMPTY));
         acc = 1;
         if (it + 1 < total) {
-          if (!mbar_wait(bar(B_DQEMPTY), it & 1, st, kTimeoutBase - 14)) break;
+          if (!mbar_wait_spin(bar(B_DQEMPTY), it & 1, st, kTimeoutBase - 14)) break;
           if (!issue_dP(it + 1)) break;
         }
       }

@@ -317,8 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // prologue S_0, dP_0; then per step i:
-    //   dV_i (needs P^T_i) ; S_i+1 (needs dV_i done: P^T_i aliases the S^T columns)
-    //   dK_i (needs dS^T_i) ; dP_i+1 (needs dK_i done: dS^T_i aliases the dP^T columns)
+    //   dV_i (needs P^T_i) ; dK_i (needs dS^T_i) ;
+    //   S_i+1 (needs dV_i done: P^T_i aliases the S^T columns) ;
+    //   dP_i+1 (needs dK_i done: dS^T_i aliases the dP^T columns)
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_N = idesc_bf16(128, G::NFULL * 64, false, true);
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_v = 0, acc_k = 0;
       auto issue_S = [&](int it) -> bool {
         const int s = it & 1;
-        if (!mbar_wait(bar(KB_QF0 + s), (it >> 1) & 1, st, kTimeoutKV - 11)) return false;
+        if (!mbar_wait_spin(bar(KB_QF0 + s), (it >> 1) & 1, st, kTimeoutKV - 11)) return false;
         tc_fence_after();
         ST_TR(0, 0, it);
         const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_dP = [&](int it) -> bool {
         const int s = it & 1;
-        if (!mbar_wait(bar(KB_DOF0 + s), (it >> 1) & 1, st, kTimeoutKV - 13)) return false;
+        if (!mbar_wait_spin(bar(KB_DOF0 + s), (it >> 1) & 1, st, kTimeoutKV - 13)) return false;
         tc_fence_after();
         ST_TR(0, 1, it);
         const uint32_t sDO = sbase + G::OFF_DO + s * G::TILE_BYTES;
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(KB_DPFULL));
         return true;
       };
-      bool ok = total > 0 && mbar_wait(bar(KB_KV), 0, st, kTimeoutKV - 10);
+      bool ok = total > 0 && mbar_wait_spin(bar(KB_KV), 0, st, kTimeoutKV - 10);
       const bool issued_any = ok;
       if (ok) ok = issue_S(0) && issue_dP(0);
       for (int it = 0; ok && it < total; ++it) {
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
         const uint32_t sDO = sbase + G::OFF_DO + s * G::TILE_BYTES;
         // dV += P^T dO : A = P^T (bf16 pairs over the S^T columns), K = 128 queries
-        if (!mbar_wait(bar(KB_PFULL), it & 1, st, kTimeoutKV - 15)) break;
+        if (!mbar_wait_spin(bar(KB_PFULL), it & 1, st, kTimeoutKV - 15)) break;
         tc_fence_after();
         ST_TR(0, 2, it);
         for (int ks = 0; ks < 8; ++ks) {
@@ -367,12 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_v = 1;
         mma_commit(bar(KB_DOE0 + s));
         mma_commit(bar(KB_DVDONE));
-        if (it + 1 < total) {
-          if (!mbar_wait(bar(KB_DVDONE), it & 1, st, kTimeoutKV - 12)) break;
-          if (!issue_S(it + 1)) break;
-        }
         // dK += dS^T Q : A = dS^T (bf16 pairs over the dP^T columns), K = 128 queries
-        if (!mbar_wait(bar(KB_DSFULL), it & 1, st, kTimeoutKV - 16)) break;
+        if (!mbar_wait_spin(bar(KB_DSFULL), it & 1, st, kTimeoutKV - 16)) break;
         tc_fence_after();
         ST_TR(0, 3, it);
         for (int ks = 0; ks < 8; ++ks) {
@@ -385,7 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(KB_QE0 + s));
         mma_commit(bar(KB_DKDONE));
         if (it + 1 < total) {
-          if (!mbar_wait(bar(KB_DKDONE), it & 1, st, kTimeoutKV - 14)) break;
+          // dV_i completed while dK_i was being issued, and dK_i completes while S_i+1 is
+          // being issued, so neither TMEM reuse below waits on an idle pipe
+          if (!mbar_wait_spin(bar(KB_DVDONE), it & 1, st, kTimeoutKV - 12)) break;
+          if (!issue_S(it + 1)) break;
+          if (!mbar_wait_spin(bar(KB_DKDONE), it & 1, st, kTimeoutKV - 14)) break;
           if (!issue_dP(it + 1)) break;
         }
       }
@@ -602,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQ = sbase + G::OFF_Q, sDO = sbase + G::OFF_DO;
       auto issue_S = [&](int it) -> bool {
         const int ks = it % G::KST;
-        if (!mbar_wait(bar(QB_KF0 + ks), (it / G::KST) & 1, st, kTimeoutQ - 11)) return false;
+        if (!mbar_wait_spin(bar(QB_KF0 + ks), (it / G::KST) & 1, st, kTimeoutQ - 11)) return false;
         tc_fence_after();
         ST_TR(1, 0, it);
         const uint32_t sK = sbase + G::OFF_K + ks * G::TILE_BYTES;
@@ -614,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_dP = [&](int it) -> bool {
         const int vs = it & 1;
-        if (!mbar_wait(bar(QB_VF0 + vs), (it >> 1) & 1, st, kTimeoutQ - 13)) return false;
+        if (!mbar_wait_spin(bar(QB_VF0 + vs), (it >> 1) & 1, st, kTimeoutQ - 13)) return false;
         tc_fence_after();
         ST_TR(1, 1, it);
         const uint32_t sV = sbase + G::OFF_V + vs * G::TILE_BYTES;
@@ -624,17 +625,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(QB_VE0 + vs));
         return true;
       };
-      bool ok = total > 0 && mbar_wait(bar(QB_QDO), 0, st, kTimeoutQ - 10);
+      bool ok = total > 0 && mbar_wait_spin(bar(QB_QDO), 0, st, kTimeoutQ - 10);
       const bool issued_any = ok;
       if (ok) ok = issue_S(0) && issue_dP(0);
       if (ok && total > 1) ok = issue_S(1);
       for (int it = 0; ok && it < total; ++it) {
         if (it + 1 < total) {
-          if (!mbar_wait(bar(QB_DPFREE), it & 1, st, kTimeoutQ - 14)) break;
+          if (!mbar_wait_spin(bar(QB_DPFREE), it & 1, st, kTimeoutQ - 14)) break;
           if (!issue_dP(it + 1)) break;
         }
         // dQ += dS K : A = dS (bf16 pairs over S_it's columns), B = K_it MN-major, K = keys
-        if (!mbar_wait(bar(QB_DSFULL), it & 1, st, kTimeoutQ - 16)) break;
+        if (!mbar_wait_spin(bar(QB_DSFULL), it & 1, st, kTimeoutQ - 16)) break;
         tc_fence_after();
         ST_TR(1, 2, it);
         const int ks = it % G::KST;
@@ -649,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(QB_KE0 + ks));
         mma_commit(bar(QB_DQDONE));
         if (it + 2 < total) {
-          if (!mbar_wait(bar(QB_DQDONE), it & 1, st, kTimeoutQ - 12)) break;
+          if (!mbar_wait_spin(bar(QB_DQDONE), it & 1, st, kTimeoutQ - 12)) break;
           if (!issue_S(it + 2)) break;
         }
       }

@@ -66,6 +66,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded busy wait with the non-blocking test: no suspension, so the phase change is seen
+// within a few cycles.  For the single thread that issues the MMAs, where every cycle of
+// wake-up latency leaves the tensor pipe idle.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const AbortState& st,
+                                               int code) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (*st.cta_abort) return false;
+    if (clock64() - t0 > st.wait_limit) {
+      raise_timeout(st, code);
+      return false;
+    }
+  }
+}
+
 // Bounded wait for phase `parity` of barrier `bar`.  Returns false when the CTA is
 // aborting (this wait timed out, or another role's did).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const AbortState& st,
