@@ -333,6 +333,7 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
     memset(&p, 0, sizeof(p));
     p.B = B; p.H = H; p.Hk = Hk; p.G = H / Hk; p.Sq = Sq; p.Sk = Sk; p.D = D;
     p.Mb = L.Mb; p.Nb = Nb; p.Sq_r = L.Sq_r;
+    p.num_tiles = num_ctas;
     p.lo = clamp30(lo);
     p.hi = clamp30(hi);
     p.lo64 = lo;
@@ -366,7 +367,13 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
       prof_record(3, s);
       return FA_OK;
     }
-    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, num_ctas, s) != cudaSuccess)
+    // persistent: one CTA per SM at most, each looping over key tiles
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    const int grid = num_ctas < sms ? num_ctas : sms;
+    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, grid, s) != cudaSuccess)
       return FA_ERR_CUDA;
   }
 

@@ -32,6 +32,7 @@ struct BwdPreParams {
 struct BwdMainParams {
   int B, H, Hk, G, Sq, Sk, D;
   int Mb, Nb, Sq_r;
+  int num_tiles;                 // key tiles x batch x kv-heads (persistent CTAs loop over them)
   int lo, hi;                    // visible iff lo <= j - i <= hi (clamped to +-2^30)
   long long lo64, hi64;          // the same bounds, unclamped (tile ranges)
   float scale_log2;              // scale * log2(e)

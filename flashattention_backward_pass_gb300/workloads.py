@@ -39,9 +39,11 @@ class Workload:
 
     @property
     def nominal_flops(self) -> float:
-        """Backward FLOPs by the stated convention: 10*B*H*Sq*Sk*D, halved when causal."""
+        """Backward FLOPs by the stated convention: 10*B*H*Sq*Sk*D, halved when causal.
+        A window with window_right == 0 is causal (no key after the diagonal) and is
+        counted as such."""
         f = 10.0 * self.B * self.H * self.Sq * self.Sk * self.D
-        return f / 2 if self.causal else f
+        return f / 2 if (self.causal or self.window_right == 0) else f
 
     def visible_pairs_per_head(self) -> int:
         """Number of (query, key) pairs the mask keeps (closed form per row)."""
