@@ -18,14 +18,22 @@
 // for MHA after its m-block loop); dQ partials are unscaled and the convert kernel
 // applies the scale.
 //
+// The grid is persistent (at most one CTA per SM): CTAs take key tiles from a ticket
+// counter in key-tile-major order, so under causal masking the longest tiles go first.
+//
 // Warp roles (16 warps, 512 threads):
-//   warp 0      TMA producer: K, V once; Q+LSE2+D and dO per step into 2-stage rings
+//   warp 0      TMA producer: K, V per tile (the next tile's K/V prefetched into L2 while
+//               the current one finishes); Q+LSE2+D and dO per step (2-stage Q ring,
+//               one dO buffer)
 //   warp 1      TMEM allocator and the single MMA-issuing thread
+//   warp 2      tile scheduler: claims the next ticket when the current tile starts its
+//               last step and publishes it in a 2-slot ring
 //   warps 4-7   dQ drain (160 registers each via setmaxnreg): TMEM -> registers, release
 //               the TMEM columns, then two 32 KB halves through a staging buffer into
-//               cp.reduce.async.bulk fp32 adds (ordered by key tile when deterministic)
+//               cp.reduce.async.bulk fp32 adds (ordered by key tile when deterministic);
+//               at the end of each tile, the dK / dV epilogue
 //   warps 8-15  two compute warpgroups: warpgroup w handles queries [64w, 64w+64) of
-//               the tile for every key row (thread = key = TMEM lane); epilogue dK / dV
+//               the tile for every key row (thread = key = TMEM lane)
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0, Dp)        dK accumulator          [128, 128+Dp)  dV accumulator
@@ -69,10 +77,10 @@ constexpr uint32_t SM_LSE = 1024;       // 2 stages x 128 fp32
 constexpr uint32_t SM_DSUM = 2048;      // 2 stages x 128 fp32
 
 enum Bar : int {
-  B_KV = 0, B_QF0, B_QF1, B_QE0, B_QE1, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
+  B_K = 0, B_V, B_QF0, B_QF1, B_QE0, B_QE1, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
   B_SFULL, B_DPFULL, B_PFULL, B_DSFULL, B_DVDONE, B_DQFULL, B_DQEMPTY, B_DSEMPTY,
-  B_ACC, B_DRAIN, B_TILEF0, B_TILEF1, B_TILEE0, B_TILEE1, B_KVEMPTY, B_ACCEMPTY, B_NEXT,
-  B_COUNT
+  B_ACC, B_DRAIN, B_TILEF0, B_TILEF1, B_TILEE0, B_TILEE1, B_KEMPTY, B_VEMPTY, B_DVEMPTY,
+  B_DKEMPTY, B_NEXT, B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 mbarriers");
 
@@ -102,7 +110,23 @@ __device__ long long g_fa_trace[FA_TRACE_CTAS][FA_TRACE_ITERS][FA_TRACE_EV];
     if (blockIdx.x < FA_TRACE_CTAS && (it) < FA_TRACE_ITERS)                       \
       g_fa_trace[blockIdx.x][(it)][(ev)] = clock64() - t_start;                    \
   } while (0)
+// Whole-kernel tile timeline (global timer, ns): per CTA and per tile it ran.
+constexpr int FA_TL_CTAS = 160, FA_TL_TILES = 24, FA_TL_EV = 8;
+__device__ long long g_fa_tl[FA_TL_CTAS][FA_TL_TILES][FA_TL_EV];
+__device__ __forceinline__ long long gtimer() {
+  long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+#define FA_TL(t, ev, val)                                                          \
+  do {                                                                             \
+    if (blockIdx.x < FA_TL_CTAS && (t) < FA_TL_TILES)                              \
+      g_fa_tl[blockIdx.x][(t)][(ev)] = (val);                                      \
+  } while (0)
 #else
+#define FA_TL(t, ev, val) \
+  do {                    \
+  } while (0)
 #define FA_TR(ev, it) \
   do {                \
   } while (0)
@@ -163,6 +187,105 @@ __device__ __forceinline__ void phase_p(const SoftmaxConsts& kc, uint32_t taddr,
   }
 }
 
+// The five contractions as issued by the single MMA thread.  Each operand tile's
+// descriptors are built once; a K-step only adds a constant to the low descriptor word.
+// The K-step loops are fully unrolled, so consecutive MMAs reach the tensor pipe back to
+// back.
+
+// Descriptors of one 128-row operand tile: K-major (rows = M or N, Dp contiguous columns
+// = the contraction) and MN-major (rows = the contraction, Dp columns = N) views of the
+// 64-column panels and of the tail panel.
+struct TileDescs {
+  DescWords kfull, ktail, mfull, mtail;
+};
+
+template <int DP>
+__device__ __forceinline__ TileDescs tile_descs(uint32_t tile) {
+  using P = Panels<DP>;
+  TileDescs o;
+  o.kfull = desc_words(tile, 16, 1024, SWZ_128B);
+  o.mfull = desc_words(tile, P::FULL_BYTES, 1024, SWZ_128B);
+  o.ktail = desc_words(tile + P::TAIL_OFF, 16, 8 * P::TAIL_ROWB, P::TAIL_SWZ);
+  o.mtail = desc_words(tile + P::TAIL_OFF, 128u * P::TAIL_ROWB, 8 * P::TAIL_ROWB, P::TAIL_SWZ);
+  return o;
+}
+
+// D = A B^T with both operands K-major over Dp (S^T = K Q^T, dP^T = V dO^T).
+template <int DP>
+__device__ __forceinline__ void mma_kmajor(uint32_t d, const TileDescs& A, const TileDescs& B) {
+  using P = Panels<DP>;
+  constexpr uint32_t ID = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int ks = 0; ks < P::NFULL * 4; ++ks) {
+    const uint32_t off = (ks >> 2) * (P::FULL_BYTES >> 4) + (ks & 3) * 2;
+    if (ks == 0)
+      mma_ss_w<0>(d, A.kfull, off, B.kfull, off, ID);
+    else
+      mma_ss_w<1>(d, A.kfull, off, B.kfull, off, ID);
+  }
+#pragma unroll
+  for (int kk = 0; kk < P::TAIL / 16; ++kk) mma_ss_w<1>(d, A.ktail, kk * 2, B.ktail, kk * 2, ID);
+}
+
+// dV (+)= P^T dO: A = P^T from tensor memory (bf16 pairs written over the S^T columns),
+// B = dO (N = Dp, MN-major), K = 128 queries.
+template <int DP>
+__device__ __forceinline__ void mma_dv(uint32_t d, uint32_t a_tmem, const TileDescs& B, uint32_t acc) {
+  using P = Panels<DP>;
+  constexpr uint32_t ID = idesc_bf16(128, P::NFULL * 64, false, true);
+  constexpr uint32_t ID_T = idesc_bf16(128, P::TAIL ? P::TAIL : 16, false, true);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t a_t = a_tmem + (ks >> 2) * 64 + (ks & 3) * 8;
+    if (ks == 0) {
+      mma_ts_wp(d, a_t, B.mfull, 0, ID, acc);
+      if (P::TAIL) mma_ts_wp(d + P::NFULL * 64, a_t, B.mtail, 0, ID_T, acc);
+    } else {
+      mma_ts_w<1>(d, a_t, B.mfull, ks * 128, ID);
+      if (P::TAIL) mma_ts_w<1>(d + P::NFULL * 64, a_t, B.mtail, ks * P::TAIL_ROWB, ID_T);
+    }
+  }
+}
+
+// dK (+)= dS^T Q: A = dS^T (K-major, 128B swizzle, `ds` = its descriptor), B = Q (N = Dp,
+// MN-major), K = 128 queries.
+template <int DP>
+__device__ __forceinline__ void mma_dk(uint32_t d, DescWords ds, const TileDescs& B, uint32_t acc) {
+  using P = Panels<DP>;
+  constexpr uint32_t ID = idesc_bf16(128, P::NFULL * 64, false, true);
+  constexpr uint32_t ID_T = idesc_bf16(128, P::TAIL ? P::TAIL : 16, false, true);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t a_off = (ks >> 2) * 1024 + (ks & 3) * 2;
+    if (ks == 0) {
+      mma_ss_wp(d, ds, a_off, B.mfull, 0, ID, acc);
+      if (P::TAIL) mma_ss_wp(d + P::NFULL * 64, ds, a_off, B.mtail, 0, ID_T, acc);
+    } else {
+      mma_ss_w<1>(d, ds, a_off, B.mfull, ks * 128, ID);
+      if (P::TAIL) mma_ss_w<1>(d + P::NFULL * 64, ds, a_off, B.mtail, ks * P::TAIL_ROWB, ID_T);
+    }
+  }
+}
+
+// dQ tile = dS K: A = dS (M = queries, MN-major view of the dS^T tile, `ds` = its
+// descriptor), B = K (N = Dp, MN-major), K = 128 keys.
+template <int DP>
+__device__ __forceinline__ void mma_dq(uint32_t d, DescWords ds, const TileDescs& B) {
+  using P = Panels<DP>;
+  constexpr uint32_t ID = idesc_bf16(128, P::NFULL * 64, true, true);
+  constexpr uint32_t ID_T = idesc_bf16(128, P::TAIL ? P::TAIL : 16, true, true);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    if (ks == 0) {
+      mma_ss_w<0>(d, ds, 0, B.mfull, 0, ID);
+      if (P::TAIL) mma_ss_w<0>(d + P::NFULL * 64, ds, 0, B.mtail, 0, ID_T);
+    } else {
+      mma_ss_w<1>(d, ds, ks * 128, B.mfull, ks * 128, ID);
+      if (P::TAIL) mma_ss_w<1>(d + P::NFULL * 64, ds, ks * 128, B.mtail, ks * P::TAIL_ROWB, ID_T);
+    }
+  }
+}
+
 template <int DP, bool SOFTCAP>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ BwdMainParams p,
@@ -182,12 +305,17 @@ __global__ void __launch_bounds__(512, 1)
 
   uint8_t* small = smem_raw;
   volatile int* s_abort = reinterpret_cast<volatile int*>(small + SM_ABORT);
-  volatile int* s_tile = reinterpret_cast<volatile int*>(small + SM_TILE);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(small + SM_TMEM);
   const float* s_lse = reinterpret_cast<const float*>(small + SM_LSE);
   const float* s_dsum = reinterpret_cast<const float*>(small + SM_DSUM);
   auto bar = [&](int i) -> uint32_t { return sbase + SM_BAR + 8u * i; };
 
+#ifdef FA_TRACE
+  if (threadIdx.x == 0) {
+    FA_TL(FA_TL_TILES - 1, 0, gtimer());
+    FA_TL(FA_TL_TILES - 1, 1, clock64());
+  }
+#endif
   if (threadIdx.x == 0) {
     *s_abort = 0;
     if ((sbase & 1023u) != 0) {
@@ -195,7 +323,8 @@ __global__ void __launch_bounds__(512, 1)
       atomicExch(p.status, kTimeoutBase - 99);
       *s_abort = 1;
     }
-    mbar_init(bar(B_KV), 1);
+    mbar_init(bar(B_K), 1);
+    mbar_init(bar(B_V), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_QF0 + s), 1);
       mbar_init(bar(B_QE0 + s), 1);
@@ -214,8 +343,10 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar(B_DSEMPTY), 1);
     mbar_init(bar(B_ACC), 1);
     mbar_init(bar(B_DRAIN), 1);
-    mbar_init(bar(B_KVEMPTY), 1);
-    mbar_init(bar(B_ACCEMPTY), 8);
+    mbar_init(bar(B_KEMPTY), 1);
+    mbar_init(bar(B_VEMPTY), 1);
+    mbar_init(bar(B_DVEMPTY), 8);
+    mbar_init(bar(B_DKEMPTY), 8);
     mbar_init(bar(B_NEXT), 1);
     fence_barrier_init();
   }
@@ -251,6 +382,11 @@ __global__ void __launch_bounds__(512, 1)
     if (ok) d = ring[t & 1];
     return ok && d.valid;
   };
+  auto read_tile_ool = [&](int t, TileDesc& d) -> bool {
+    const bool ok = mbar_wait_ool(bar(B_TILEF0 + (t & 1)), (t >> 1) & 1, st, kTimeoutBase - 40);
+    if (ok) d = ring[t & 1];
+    return ok && d.valid;
+  };
 
   // Register split (launch: 512 threads x 128 = 65536): the producer / MMA warpgroup
   // gives registers to the dQ drain warpgroup, which keeps a whole dQ row in registers.
@@ -267,14 +403,16 @@ __global__ void __launch_bounds__(512, 1)
         // producer starts its last step), so that tiles stay in longest-first order across
         // CTAs instead of being claimed a whole tile ahead.
         const bool ready =
-            (t == 0 || mbar_wait(bar(B_NEXT), (t - 1) & 1, st, kTimeoutBase - 42)) &&
-            (t < 2 || mbar_wait(bar(B_TILEE0 + k), ((t - 2) >> 1) & 1, st, kTimeoutBase - 41));
+            (t == 0 || mbar_wait_ool(bar(B_NEXT), (t - 1) & 1, st, kTimeoutBase - 42)) &&
+            (t < 2 || mbar_wait_ool(bar(B_TILEE0 + k), ((t - 2) >> 1) & 1, st, kTimeoutBase - 41));
         if (!ready) {
           ring[k].valid = 0;
           mbar_arrive(bar(B_TILEF0 + k));
           break;
         }
         const int ticket = (*s_abort) ? p.num_tiles : atomicAdd(p.ticket, 1);
+        FA_TL(t, 0, ticket);
+        FA_TL(t, 1, gtimer());
         TileDesc d{};
         d.valid = ticket < p.num_tiles;
         if (d.valid) {
@@ -306,29 +444,50 @@ __global__ void __launch_bounds__(512, 1)
         tma_prefetch_desc(&tv_t);
         tma_prefetch_desc(&tdo_t);
       }
-      int git = 0, kt = 0, ndo = 0;
+      int git = 0, nk = 0, nv = 0, ndo = 0;
       bool alive = true;
       for (int t = 0; alive; ++t) {
         TileDesc d;
-        if (!read_tile(t, d)) break;
+        if (!read_tile_ool(t, d)) break;
         mbar_arrive(bar(B_TILEE0 + (t & 1)));
         if (d.total == 0) {
           mbar_arrive(bar(B_NEXT));
           continue;
         }
         const int n0 = d.n * kTileK;
-        // K and V of the previous tile are free once all of its MMAs are complete
-        if (kt > 0 && !mbar_wait(bar(B_KVEMPTY), (kt - 1) & 1, st, kTimeoutBase - 4)) break;
-        mbar_arrive_expect_tx(bar(B_KV), 2 * G::TILE_BYTES);
-        for (int pnl = 0; pnl < G::NFULL; ++pnl) {
-          tma_load_4d(sbase + G::OFF_K + pnl * G::FULL_BYTES, &tk, pnl * 64, d.hk, n0, d.b, bar(B_KV));
-          tma_load_4d(sbase + G::OFF_V + pnl * G::FULL_BYTES, &tv, pnl * 64, d.hk, n0, d.b, bar(B_KV));
+        auto load_k = [&]() {
+          ++nk;
+          mbar_arrive_expect_tx(bar(B_K), G::TILE_BYTES);
+          _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
+            tma_load_4d(sbase + G::OFF_K + pnl * G::FULL_BYTES, &tk, pnl * 64, d.hk, n0, d.b, bar(B_K));
+          if (G::TAIL) tma_load_4d(sbase + G::OFF_K + G::TAIL_OFF, &tk_t, G::NFULL * 64, d.hk, n0, d.b, bar(B_K));
+        };
+        auto load_v = [&]() {
+          ++nv;
+          mbar_arrive_expect_tx(bar(B_V), G::TILE_BYTES);
+          _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
+            tma_load_4d(sbase + G::OFF_V + pnl * G::FULL_BYTES, &tv, pnl * 64, d.hk, n0, d.b, bar(B_V));
+          if (G::TAIL) tma_load_4d(sbase + G::OFF_V + G::TAIL_OFF, &tv_t, G::NFULL * 64, d.hk, n0, d.b, bar(B_V));
+        };
+        const bool kv_busy = nk > 0;  // the previous tile may still be reading K and V
+        if (kv_busy) {
+          // warm L2 with this tile's K and V so that the loads below, which must wait for
+          // the previous tile's last MMAs, hit L2
+          _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl) {
+            tma_prefetch_4d(&tk, pnl * 64, d.hk, n0, d.b);
+            tma_prefetch_4d(&tv, pnl * 64, d.hk, n0, d.b);
+          }
+          if (G::TAIL) {
+            tma_prefetch_4d(&tk_t, G::NFULL * 64, d.hk, n0, d.b);
+            tma_prefetch_4d(&tv_t, G::NFULL * 64, d.hk, n0, d.b);
+          }
+        } else {
+          load_k();
+          load_v();
         }
-        if (G::TAIL) {
-          tma_load_4d(sbase + G::OFF_K + G::TAIL_OFF, &tk_t, G::NFULL * 64, d.hk, n0, d.b, bar(B_KV));
-          tma_load_4d(sbase + G::OFF_V + G::TAIL_OFF, &tv_t, G::NFULL * 64, d.hk, n0, d.b, bar(B_KV));
-        }
-        ++kt;
+        // After the first tile, the loads of a tile's first step go out in the order their
+        // buffers are released by the previous tile: Q (its dK two steps back), V (its last
+        // dP), dO (its last dV), K (its last dQ).
         for (int it = 0; it < d.total; ++it, ++git) {
           const int s = git & 1;
           const int g = it / d.m_count;
@@ -336,21 +495,29 @@ __global__ void __launch_bounds__(512, 1)
           const int h = d.hk * p.G + g;
           const int m0 = m * kTileQ;
           if (it == d.total - 1) mbar_arrive(bar(B_NEXT));  // time to claim the next tile
-          if (git >= 2 && !mbar_wait(bar(B_QE0 + s), ((git - 2) >> 1) & 1, st, kTimeoutBase - 1)) {
+          if (git >= 2 && !mbar_wait_ool(bar(B_QE0 + s), ((git - 2) >> 1) & 1, st, kTimeoutBase - 1)) {
             alive = false;
             break;
           }
           const uint32_t qdst = sbase + G::OFF_Q + s * G::TILE_BYTES;
           mbar_arrive_expect_tx(bar(B_QF0 + s), G::TILE_BYTES + 2 * 512);
-          for (int pnl = 0; pnl < G::NFULL; ++pnl)
+          _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
             tma_load_4d(qdst + pnl * G::FULL_BYTES, &tq, pnl * 64, h, m0, d.b, bar(B_QF0 + s));
           if (G::TAIL) tma_load_4d(qdst + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, m0, d.b, bar(B_QF0 + s));
           const size_t row = ((size_t)d.b * p.H + h) * p.Sq_r + m0;
           bulk_load(sbase + SM_LSE + s * 512, p.lse2 + row, 512, bar(B_QF0 + s));
           bulk_load(sbase + SM_DSUM + s * 512, p.dsum + row, 512, bar(B_QF0 + s));
           FA_TR(10, git);
+          if (it == 0 && kv_busy) {
+            if (!mbar_wait_ool(bar(B_VEMPTY), (nv - 1) & 1, st, kTimeoutBase - 4)) {
+              ++git;
+              alive = false;
+              break;
+            }
+            load_v();
+          }
           // dO has one buffer: dO_i+1 may land once dV_i (its last reader) is complete
-          if (git >= 1 && !mbar_wait(bar(B_DOE0), (git - 1) & 1, st, kTimeoutBase - 2)) {
+          if (git >= 1 && !mbar_wait_ool(bar(B_DOE0), (git - 1) & 1, st, kTimeoutBase - 2)) {
             ++git;
             alive = false;
             break;
@@ -358,9 +525,17 @@ __global__ void __launch_bounds__(512, 1)
           ++ndo;
           const uint32_t ddst = sbase + G::OFF_DO;
           mbar_arrive_expect_tx(bar(B_DOF0), G::TILE_BYTES);
-          for (int pnl = 0; pnl < G::NFULL; ++pnl)
+          _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
             tma_load_4d(ddst + pnl * G::FULL_BYTES, &tdo, pnl * 64, h, m0, d.b, bar(B_DOF0));
           if (G::TAIL) tma_load_4d(ddst + G::TAIL_OFF, &tdo_t, G::NFULL * 64, h, m0, d.b, bar(B_DOF0));
+          if (it == 0 && kv_busy) {
+            if (!mbar_wait_ool(bar(B_KEMPTY), (nk - 1) & 1, st, kTimeoutBase - 5)) {
+              ++git;
+              alive = false;
+              break;
+            }
+            load_k();
+          }
         }
       }
       // Before the CTA may exit, every copy this thread started must have landed (on an
@@ -368,12 +543,13 @@ __global__ void __launch_bounds__(512, 1)
       // barrier can still be pending.
       volatile int no_abort = 0;
       AbortState dr{&no_abort, p.status, p.wait_limit};
-      if (kt > 0) mbar_wait(bar(B_KV), (kt - 1) & 1, dr, kTimeoutBase - 3);
+      if (nk > 0) mbar_wait_ool(bar(B_K), (nk - 1) & 1, dr, kTimeoutBase - 3);
+      if (nv > 0) mbar_wait_ool(bar(B_V), (nv - 1) & 1, dr, kTimeoutBase - 3);
       for (int s = 0; s < 2; ++s) {
         const int nq = (git - s + 1) / 2;  // loads issued into Q stage s
-        if (nq > 0) mbar_wait(bar(B_QF0 + s), (nq - 1) & 1, dr, kTimeoutBase - 3);
+        if (nq > 0) mbar_wait_ool(bar(B_QF0 + s), (nq - 1) & 1, dr, kTimeoutBase - 3);
       }
-      if (ndo > 0) mbar_wait(bar(B_DOF0), (ndo - 1) & 1, dr, kTimeoutBase - 3);
+      if (ndo > 0) mbar_wait_ool(bar(B_DOF0), (ndo - 1) & 1, dr, kTimeoutBase - 3);
     }
    } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -384,21 +560,17 @@ __global__ void __launch_bounds__(512, 1)
     //   dK_i, dQ_i (need dS_i)                          -> dq_full
     //   dP_i+1 (needs the dQ_i columns drained)
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t ID_KV = idesc_bf16(128, G::NFULL * 64, false, true);
-      constexpr uint32_t ID_KV_T = idesc_bf16(128, G::TAIL ? G::TAIL : 16, false, true);
-      constexpr uint32_t ID_Q = idesc_bf16(128, G::NFULL * 64, true, true);
-      constexpr uint32_t ID_Q_T = idesc_bf16(128, G::TAIL ? G::TAIL : 16, true, true);
-      const uint32_t sK = sbase + G::OFF_K, sV = sbase + G::OFF_V, sDS = sbase + G::OFF_DS;
-      const uint32_t sDO = sbase + G::OFF_DO;
+      const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K), dV_ = tile_descs<DP>(sbase + G::OFF_V);
+      const TileDescs dDO = tile_descs<DP>(sbase + G::OFF_DO);
+      const TileDescs dQ0 = tile_descs<DP>(sbase + G::OFF_Q), dQ1 = tile_descs<DP>(sbase + G::OFF_Q + G::TILE_BYTES);
+      const DescWords dsK = desc_words(sbase + G::OFF_DS, 16, 1024, SWZ_128B);      // dS^T, K-major
+      const DescWords dsM = desc_words(sbase + G::OFF_DS, 16384, 1024, SWZ_128B);   // dS, MN-major
       auto issue_S = [&](int g) -> bool {
         const int s = g & 1;
         if (!mbar_wait_spin(bar(B_QF0 + s), (g >> 1) & 1, st, kTimeoutBase - 11)) return false;
         tc_fence_after();
         FA_TR(0, g);
-        const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
-        for (int ks = 0; ks < G::KSTEPS; ++ks)
-          mma_ss(tmem + TM_S, desc_kmajor<DP>(sK, ks), desc_kmajor<DP>(sQ, ks), ID_S, ks > 0);
+        mma_kmajor<DP>(tmem + TM_S, dK_, s ? dQ1 : dQ0);
         mma_commit(bar(B_SFULL));
         return true;
       };
@@ -406,8 +578,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!mbar_wait_spin(bar(B_DOF0), g & 1, st, kTimeoutBase - 13)) return false;
         tc_fence_after();
         FA_TR(1, g);
-        for (int ks = 0; ks < G::KSTEPS; ++ks)
-          mma_ss(tmem + TM_DP, desc_kmajor<DP>(sV, ks), desc_kmajor<DP>(sDO, ks), ID_S, ks > 0);
+        mma_kmajor<DP>(tmem + TM_DP, dV_, dDO);
         mma_commit(bar(B_DPFULL));
         return true;
       };
@@ -415,36 +586,35 @@ __global__ void __launch_bounds__(512, 1)
       bool ok = true;
       for (int t = 0; ok; ++t) {
         TileDesc d;
-        if (!read_tile(t, d)) break;
+        if (!read_tile_ool(t, d)) break;
         mbar_arrive(bar(B_TILEE0 + (t & 1)));
         if (d.total == 0) continue;
-        if (!mbar_wait_spin(bar(B_KV), kt & 1, st, kTimeoutBase - 10)) break;
         // the previous tile's last P^T and dQ columns must be consumed before S_0 / dP_0
         if (git > 0 && !mbar_wait_spin(bar(B_DVDONE), (git - 1) & 1, st, kTimeoutBase - 12)) break;
+        if (!mbar_wait_spin(bar(B_K), kt & 1, st, kTimeoutBase - 10)) break;
+        FA_TL(t, 2, gtimer());
+        FA_TL(t, 7, d.total);
         if (!issue_S(git)) break;
         if (git > 0 && !mbar_wait_spin(bar(B_DQEMPTY), (git - 1) & 1, st, kTimeoutBase - 14)) break;
+        if (!mbar_wait_spin(bar(B_V), kt & 1, st, kTimeoutBase - 19)) break;
         if (!issue_dP(git)) break;
+        if (d.total == 1) mma_commit(bar(B_VEMPTY));  // V's last reader is the tile's last dP
         uint32_t acc = 0;
         for (int it = 0; it < d.total; ++it, ++git) {
           const int s = git & 1;
-          const uint32_t sQ = sbase + G::OFF_Q + s * G::TILE_BYTES;
           // dV += P^T dO : A = P^T from TMEM (bf16 pairs), K = 128 queries in 8 steps
           if (!mbar_wait_spin(bar(B_PFULL), git & 1, st, kTimeoutBase - 15)) { ok = false; break; }
           // the accumulators are overwritten by this tile's first dV / dK: the previous
           // tile's epilogue must have read them
           if (it == 0 && kt > 0 &&
-              !mbar_wait_spin(bar(B_ACCEMPTY), (kt - 1) & 1, st, kTimeoutBase - 18)) {
+              !mbar_wait_spin(bar(B_DVEMPTY), (kt - 1) & 1, st, kTimeoutBase - 18)) {
             ok = false;
             break;
           }
           tc_fence_after();
           FA_TR(2, git);
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t a_t = tmem + TM_S + (ks >> 2) * 64 + (ks & 3) * 8;
-            const uint32_t en = (acc | (uint32_t)ks) ? 1u : 0u;
-            mma_ts(tmem + TM_DV, a_t, desc_mn_full<DP>(sDO, ks), ID_KV, en);
-            if (G::TAIL) mma_ts(tmem + TM_DV + G::NFULL * 64, a_t, desc_mn_tail<DP>(sDO, ks), ID_KV_T, en);
-          }
+          if (it == 0) FA_TL(t, 3, gtimer());
+          mma_dv<DP>(tmem + TM_DV, tmem + TM_S, dDO, acc);
           mma_commit(bar(B_DOE0));
           mma_commit(bar(B_DVDONE));
           if (it + 1 < d.total) {
@@ -453,32 +623,29 @@ __global__ void __launch_bounds__(512, 1)
           }
           // dK += dS^T Q : A = dS^T (K-major in shared memory), K = 128 queries
           if (!mbar_wait_spin(bar(B_DSFULL), git & 1, st, kTimeoutBase - 16)) { ok = false; break; }
+          if (it == 0 && kt > 0 &&
+              !mbar_wait_spin(bar(B_DKEMPTY), (kt - 1) & 1, st, kTimeoutBase - 18)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           FA_TR(3, git);
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = smem_desc(sDS + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, SWZ_128B);
-            const uint32_t en = (acc | (uint32_t)ks) ? 1u : 0u;
-            mma_ss(tmem + TM_DK, a, desc_mn_full<DP>(sQ, ks), ID_KV, en);
-            if (G::TAIL) mma_ss(tmem + TM_DK + G::NFULL * 64, a, desc_mn_tail<DP>(sQ, ks), ID_KV_T, en);
-          }
+          mma_dk<DP>(tmem + TM_DK, dsK, s ? dQ1 : dQ0, acc);
           mma_commit(bar(B_QE0 + s));
-          // dQ tile = dS K : A = dS (M = queries, MN-major), B = K (N = Dp, MN-major), K = keys
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = smem_desc(sDS + ks * 16 * 128, 16384, 1024, SWZ_128B);
-            mma_ss(tmem + TM_DP, a, desc_mn_full<DP>(sK, ks), ID_Q, ks > 0);
-            if (G::TAIL) mma_ss(tmem + TM_DP + G::NFULL * 64, a, desc_mn_tail<DP>(sK, ks), ID_Q_T, ks > 0);
-          }
+          mma_dq<DP>(tmem + TM_DP, dsM, dK_);  // the dQ tile goes where dP^T was
           mma_commit(bar(B_DQFULL));
           mma_commit(bar(B_DSEMPTY));
           acc = 1;
           if (it + 1 < d.total) {
             if (!mbar_wait_spin(bar(B_DQEMPTY), git & 1, st, kTimeoutBase - 14)) { ok = false; break; }
             if (!issue_dP(git + 1)) { ok = false; break; }
+            if (it + 2 == d.total) mma_commit(bar(B_VEMPTY));
           }
         }
         if (!ok) break;
-        mma_commit(bar(B_ACC));      // this tile's dK / dV are final
-        mma_commit(bar(B_KVEMPTY));  // and its K / V buffers may be refilled
+        FA_TL(t, 4, gtimer());
+        mma_commit(bar(B_ACC));     // this tile's dK / dV are final
+        mma_commit(bar(B_KEMPTY));  // and its K buffer may be refilled
         ++kt;
       }
       if (git > 0 || kt > 0) {
@@ -486,7 +653,7 @@ __global__ void __launch_bounds__(512, 1)
         mma_commit(bar(B_DRAIN));
         volatile int no_abort = 0;
         AbortState dr{&no_abort, p.status, p.wait_limit};
-        mbar_wait(bar(B_DRAIN), 0, dr, kTimeoutBase - 17);
+        mbar_wait_ool(bar(B_DRAIN), 0, dr, kTimeoutBase - 17);
       }
     }
    }
@@ -613,6 +780,7 @@ __global__ void __launch_bounds__(512, 1)
         // no early exit: every drain thread reaches every named barrier of every step (on
         // an abort the waits return at once and the stores and bulk adds are skipped)
       }
+
     }
     if (threadIdx.x == 128) bulk_wait_all();
   } else if (warp >= 8) {
@@ -703,51 +871,72 @@ __global__ void __launch_bounds__(512, 1)
       if (!alive) break;
 
       // ---------------------------------------------------------------- dK / dV epilogue
-      __nv_bfloat16* outp = wg == 0 ? p.dk : p.dv;
-      const int64_t sb = wg == 0 ? p.dk_sb : p.dv_sb;
-      const int64_t ss = wg == 0 ? p.dk_ss : p.dv_ss;
-      const int64_t sh = wg == 0 ? p.dk_sh : p.dv_sh;
-      const float sc = wg == 0 ? p.dk_scale : 1.f;
-      const uint32_t tcol = wg == 0 ? TM_DK : TM_DV;
-      __nv_bfloat16* rowp = outp + (int64_t)d.b * sb + (int64_t)j * ss + (int64_t)d.hk * sh;
+      // Each warpgroup writes half of the columns of both accumulators for its key row.
+      // dV is final as soon as the tile's last dV is complete, so it is read out while
+      // the last dK / dQ still run; dK follows once every MMA of the tile is complete.
+      // Each accumulator's columns are released to the next tile as soon as they are in
+      // registers.
       const bool have = d.total > 0;
-      if (have) {
-        if (!warp_wait(bar(B_ACC), kt & 1, st, kTimeoutBase - 33)) break;
-        tc_fence_after();
-      }
-      const bool write = __all_sync(0xffffffffu, *s_abort == 0);
-#pragma unroll
-      for (int c = 0; c < DP / 16; ++c) {
-        uint32_t r[16];
+      bool acc_ok = true;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
         if (have) {
-          tmem_ld16(t_lane + tcol + c * 16, r);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = 0u;
+          acc_ok = acc_ok && (which ? warp_wait(bar(B_ACC), kt & 1, st, kTimeoutBase - 33)
+                                    : warp_wait(bar(B_DVDONE), (git - 1) & 1, st, kTimeoutBase - 34));
+          if (acc_ok) tc_fence_after();
+          if (which && threadIdx.x == 256) FA_TL(t, 5, gtimer());
         }
-        if (have && c == DP / 16 - 1) {
-          // all accumulator columns are read: the next tile's dV / dK may overwrite them
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_ACCEMPTY));
-        }
-        uint32_t pk[8];
+        const bool store = acc_ok && *s_abort == 0 && row_ok;
+        const uint32_t tcol = which ? TM_DK : TM_DV;
+        const float sc = which ? p.dk_scale : 1.f;
+        __nv_bfloat16* row = which ? p.dk + (int64_t)d.b * p.dk_sb + (int64_t)j * p.dk_ss + (int64_t)d.hk * p.dk_sh
+                                   : p.dv + (int64_t)d.b * p.dv_sb + (int64_t)j * p.dv_ss + (int64_t)d.hk * p.dv_sh;
+        constexpr int NCH = DP / 16;          // 16-column chunks per accumulator row
+        constexpr int NCH0 = (NCH + 1) / 2;   // chunks of warpgroup 0
+        const int c0 = wg ? NCH0 : 0;
+        const int nch = wg ? NCH - NCH0 : NCH0;
+#pragma unroll 1
+        for (int cc = 0; cc < NCH0; ++cc) {
+          if (cc < nch) {
+            const int c = c0 + cc;
+            uint32_t r[16];
+            if (have && acc_ok) {
+              tmem_ld16(t_lane + tcol + c * 16, r);
+            } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
-        if (write && row_ok) {
-          if (c * 16 < p.D)
-            *reinterpret_cast<uint4*>(rowp + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          if (c * 16 + 8 < p.D)
-            *reinterpret_cast<uint4*>(rowp + c * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              for (int e = 0; e < 16; ++e) r[e] = 0u;  // no visible query: zero rows
+            }
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
+            if (store) {
+              if (c * 16 < p.D)
+                *reinterpret_cast<uint4*>(row + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              if (c * 16 + 8 < p.D)
+                *reinterpret_cast<uint4*>(row + c * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+          if (cc == NCH0 - 1 && have && acc_ok) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(which ? B_DKEMPTY : B_DVEMPTY));
+          }
         }
       }
       if (have) ++kt;
+      if (threadIdx.x == 256) FA_TL(t, 6, gtimer());
     }
   }
 
   tc_fence_before();
   __syncthreads();
+#ifdef FA_TRACE
+  if (threadIdx.x == 0) {
+    FA_TL(FA_TL_TILES - 1, 2, gtimer());
+    FA_TL(FA_TL_TILES - 1, 3, clock64());
+  }
+#endif
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -758,6 +947,14 @@ __global__ void __launch_bounds__(512, 1)
 cudaError_t bwd_trace_copy(void* host, size_t bytes) {
   if (bytes > sizeof(g_fa_trace)) bytes = sizeof(g_fa_trace);
   return cudaMemcpyFromSymbol(host, g_fa_trace, bytes);
+}
+cudaError_t bwd_timeline_copy(void* host, size_t bytes, bool clear) {
+  if (clear) {
+    static long long zero[FA_TL_CTAS][FA_TL_TILES][FA_TL_EV];
+    return cudaMemcpyToSymbol(g_fa_tl, zero, sizeof(zero));
+  }
+  if (bytes > sizeof(g_fa_tl)) bytes = sizeof(g_fa_tl);
+  return cudaMemcpyFromSymbol(host, g_fa_tl, bytes);
 }
 #endif
 

@@ -104,6 +104,7 @@ cudaError_t launch_fwd(const FwdParams& p, int Dp, cudaStream_t s);
 #ifdef FA_TRACE
 cudaError_t bwd_trace_copy(void* host, size_t bytes);
 cudaError_t split_trace_copy(void* host, size_t bytes);
+cudaError_t bwd_timeline_copy(void* host, size_t bytes, bool clear);
 #endif
 
 }  // namespace fa

@@ -81,6 +81,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // Bounded busy wait with the non-blocking test: no suspension, so the phase change is seen
 // within a few cycles.  For the single thread that issues the MMAs, where every cycle of
 // wake-up latency leaves the tensor pipe idle.
+// Bounded busy wait with the non-blocking test: no suspension, so the phase change is seen
+// within a few cycles.  For the single thread that issues the MMAs, where every cycle of
+// wake-up latency leaves the tensor pipe idle.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const AbortState& st,
                                                int code) {
   if (mbar_test_wait(bar, parity)) return true;
@@ -95,6 +98,30 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, co
       return false;
     }
   }
+}
+
+// The suspending wait with its slow path out of line: each wait site then costs one test
+// and a call, which keeps code that is not latency-critical small (it shares the
+// instruction caches with the hot loops).  Only code that runs with its launch-time
+// register count or less may call functions.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* cta_abort,
+                                            int* status, long long limit, int code) {
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*cta_abort) return false;
+    if (clock64() - t0 > limit) {
+      *cta_abort = 1;
+      atomicExch(status, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_ool(uint32_t bar, uint32_t parity, const AbortState& st,
+                                              int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, st.cta_abort, st.global_status, st.wait_limit, code);
 }
 
 // Bounded wait for phase `parity` of barrier `bar`.  Returns false when the CTA is
@@ -126,6 +153,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+// Prefetch of one 4-D tile into L2 (no shared-memory destination, no completion signal).
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 
@@ -228,6 +264,68 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same MMAs with each descriptor given as its two 32-bit words.  The low word holds
+// the start address (bits 0-13, in 16-byte units) and the leading byte offset; a tile's
+// descriptor is built once and advanced along the tile by adding (byte offset >> 4) to
+// the low word (no carry leaves the address field while the address stays below 256 KB).
+struct DescWords {
+  uint32_t lo, hi;
+};
+
+__device__ __forceinline__ DescWords desc_words(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                                uint32_t swz) {
+  const uint64_t d = smem_desc(addr, lbo_bytes, sbo_bytes, swz);
+  return DescWords{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
+template <uint32_t ACC>
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, DescWords a, uint32_t a_off16, DescWords b,
+                                         uint32_t b_off16, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo + a_off16), "r"(a.hi), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_wp(uint32_t d_tmem, DescWords a, uint32_t a_off16, DescWords b,
+                                          uint32_t b_off16, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo + a_off16), "r"(a.hi), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <uint32_t ACC>
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, DescWords b, uint32_t b_off16,
+                                         uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_wp(uint32_t d_tmem, uint32_t a_tmem, DescWords b, uint32_t b_off16,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
