@@ -25,7 +25,7 @@
 //   warp 0      TMA producer: K, V per tile (the next tile's K/V prefetched into L2 while
 //               the current one finishes); Q+LSE2+D and dO per step (2-stage Q ring,
 //               one dO buffer)
-//   warp 1      TMEM allocator and the single MMA-issuing thread
+//   warp 1      TMEM allocator and MMA issue (one elected lane issues)
 //   warp 2      tile scheduler: claims the next ticket when the current tile starts its
 //               last step and publishes it in a 2-slot ring
 //   warps 4-7   dQ drain (160 registers each via setmaxnreg): TMEM -> registers, release
@@ -559,7 +559,14 @@ __global__ void __launch_bounds__(512, 1)
     //   S_i+1 (needs dv_done_i: P^T_i aliases the S^T columns) -- overlaps phase B_i
     //   dK_i, dQ_i (need dS_i)                          -> dq_full
     //   dP_i+1 (needs the dQ_i columns drained)
-    if (lane == 0) {
+    // The whole warp runs this code (its values are warp-uniform, so the descriptor
+    // arithmetic stays on the uniform datapath); one elected lane issues the MMAs and
+    // commits, and every wait is agreed on by the warp.
+    {
+      const bool leader = elect_one();
+      auto wspin = [&](uint32_t b, uint32_t par, int code) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait_spin(b, par, st, code));
+      };
       const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K), dV_ = tile_descs<DP>(sbase + G::OFF_V);
       const TileDescs dDO = tile_descs<DP>(sbase + G::OFF_DO);
       const TileDescs dQ0 = tile_descs<DP>(sbase + G::OFF_Q), dQ1 = tile_descs<DP>(sbase + G::OFF_Q + G::TILE_BYTES);
@@ -567,90 +574,90 @@ __global__ void __launch_bounds__(512, 1)
       const DescWords dsM = desc_words(sbase + G::OFF_DS, 16384, 1024, SWZ_128B);   // dS, MN-major
       auto issue_S = [&](int g) -> bool {
         const int s = g & 1;
-        if (!mbar_wait_spin(bar(B_QF0 + s), (g >> 1) & 1, st, kTimeoutBase - 11)) return false;
+        if (!wspin(bar(B_QF0 + s), (g >> 1) & 1, kTimeoutBase - 11)) return false;
         tc_fence_after();
-        FA_TR(0, g);
-        mma_kmajor<DP>(tmem + TM_S, dK_, s ? dQ1 : dQ0);
-        mma_commit(bar(B_SFULL));
+        if (leader) FA_TR(0, g);
+        if (leader) mma_kmajor<DP>(tmem + TM_S, dK_, s ? dQ1 : dQ0);
+        if (leader) mma_commit(bar(B_SFULL));
         return true;
       };
       auto issue_dP = [&](int g) -> bool {
-        if (!mbar_wait_spin(bar(B_DOF0), g & 1, st, kTimeoutBase - 13)) return false;
+        if (!wspin(bar(B_DOF0), g & 1, kTimeoutBase - 13)) return false;
         tc_fence_after();
-        FA_TR(1, g);
-        mma_kmajor<DP>(tmem + TM_DP, dV_, dDO);
-        mma_commit(bar(B_DPFULL));
+        if (leader) FA_TR(1, g);
+        if (leader) mma_kmajor<DP>(tmem + TM_DP, dV_, dDO);
+        if (leader) mma_commit(bar(B_DPFULL));
         return true;
       };
       int git = 0, kt = 0;
       bool ok = true;
       for (int t = 0; ok; ++t) {
         TileDesc d;
-        if (!read_tile_ool(t, d)) break;
-        mbar_arrive(bar(B_TILEE0 + (t & 1)));
+        if (!__all_sync(0xffffffffu, read_tile_ool(t, d))) break;
+        if (leader) mbar_arrive(bar(B_TILEE0 + (t & 1)));
         if (d.total == 0) continue;
         // the previous tile's last P^T and dQ columns must be consumed before S_0 / dP_0
-        if (git > 0 && !mbar_wait_spin(bar(B_DVDONE), (git - 1) & 1, st, kTimeoutBase - 12)) break;
-        if (!mbar_wait_spin(bar(B_K), kt & 1, st, kTimeoutBase - 10)) break;
-        FA_TL(t, 2, gtimer());
-        FA_TL(t, 7, d.total);
+        if (git > 0 && !wspin(bar(B_DVDONE), (git - 1) & 1, kTimeoutBase - 12)) break;
+        if (!wspin(bar(B_K), kt & 1, kTimeoutBase - 10)) break;
+        if (leader) FA_TL(t, 2, gtimer());
+        if (leader) FA_TL(t, 7, d.total);
         if (!issue_S(git)) break;
-        if (git > 0 && !mbar_wait_spin(bar(B_DQEMPTY), (git - 1) & 1, st, kTimeoutBase - 14)) break;
-        if (!mbar_wait_spin(bar(B_V), kt & 1, st, kTimeoutBase - 19)) break;
+        if (git > 0 && !wspin(bar(B_DQEMPTY), (git - 1) & 1, kTimeoutBase - 14)) break;
+        if (!wspin(bar(B_V), kt & 1, kTimeoutBase - 19)) break;
         if (!issue_dP(git)) break;
-        if (d.total == 1) mma_commit(bar(B_VEMPTY));  // V's last reader is the tile's last dP
+        if (d.total == 1) if (leader) mma_commit(bar(B_VEMPTY));  // V's last reader is the tile's last dP
         uint32_t acc = 0;
         for (int it = 0; it < d.total; ++it, ++git) {
           const int s = git & 1;
           // dV += P^T dO : A = P^T from TMEM (bf16 pairs), K = 128 queries in 8 steps
-          if (!mbar_wait_spin(bar(B_PFULL), git & 1, st, kTimeoutBase - 15)) { ok = false; break; }
+          if (!wspin(bar(B_PFULL), git & 1, kTimeoutBase - 15)) { ok = false; break; }
           // the accumulators are overwritten by this tile's first dV / dK: the previous
           // tile's epilogue must have read them
           if (it == 0 && kt > 0 &&
-              !mbar_wait_spin(bar(B_DVEMPTY), (kt - 1) & 1, st, kTimeoutBase - 18)) {
+              !wspin(bar(B_DVEMPTY), (kt - 1) & 1, kTimeoutBase - 18)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          FA_TR(2, git);
-          if (it == 0) FA_TL(t, 3, gtimer());
-          mma_dv<DP>(tmem + TM_DV, tmem + TM_S, dDO, acc);
-          mma_commit(bar(B_DOE0));
-          mma_commit(bar(B_DVDONE));
+          if (leader) FA_TR(2, git);
+          if (it == 0) if (leader) FA_TL(t, 3, gtimer());
+          if (leader) mma_dv<DP>(tmem + TM_DV, tmem + TM_S, dDO, acc);
+          if (leader) mma_commit(bar(B_DOE0));
+          if (leader) mma_commit(bar(B_DVDONE));
           if (it + 1 < d.total) {
-            if (!mbar_wait_spin(bar(B_DVDONE), git & 1, st, kTimeoutBase - 12)) { ok = false; break; }
+            if (!wspin(bar(B_DVDONE), git & 1, kTimeoutBase - 12)) { ok = false; break; }
             if (!issue_S(git + 1)) { ok = false; break; }
           }
           // dK += dS^T Q : A = dS^T (K-major in shared memory), K = 128 queries
-          if (!mbar_wait_spin(bar(B_DSFULL), git & 1, st, kTimeoutBase - 16)) { ok = false; break; }
+          if (!wspin(bar(B_DSFULL), git & 1, kTimeoutBase - 16)) { ok = false; break; }
           if (it == 0 && kt > 0 &&
-              !mbar_wait_spin(bar(B_DKEMPTY), (kt - 1) & 1, st, kTimeoutBase - 18)) {
+              !wspin(bar(B_DKEMPTY), (kt - 1) & 1, kTimeoutBase - 18)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          FA_TR(3, git);
-          mma_dk<DP>(tmem + TM_DK, dsK, s ? dQ1 : dQ0, acc);
-          mma_commit(bar(B_QE0 + s));
-          mma_dq<DP>(tmem + TM_DP, dsM, dK_);  // the dQ tile goes where dP^T was
-          mma_commit(bar(B_DQFULL));
-          mma_commit(bar(B_DSEMPTY));
+          if (leader) FA_TR(3, git);
+          if (leader) mma_dk<DP>(tmem + TM_DK, dsK, s ? dQ1 : dQ0, acc);
+          if (leader) mma_commit(bar(B_QE0 + s));
+          if (leader) mma_dq<DP>(tmem + TM_DP, dsM, dK_);  // the dQ tile goes where dP^T was
+          if (leader) mma_commit(bar(B_DQFULL));
+          if (leader) mma_commit(bar(B_DSEMPTY));
           acc = 1;
           if (it + 1 < d.total) {
-            if (!mbar_wait_spin(bar(B_DQEMPTY), git & 1, st, kTimeoutBase - 14)) { ok = false; break; }
+            if (!wspin(bar(B_DQEMPTY), git & 1, kTimeoutBase - 14)) { ok = false; break; }
             if (!issue_dP(git + 1)) { ok = false; break; }
-            if (it + 2 == d.total) mma_commit(bar(B_VEMPTY));
+            if (it + 2 == d.total) if (leader) mma_commit(bar(B_VEMPTY));
           }
         }
         if (!ok) break;
-        FA_TL(t, 4, gtimer());
-        mma_commit(bar(B_ACC));     // this tile's dK / dV are final
-        mma_commit(bar(B_KEMPTY));  // and its K buffer may be refilled
+        if (leader) FA_TL(t, 4, gtimer());
+        if (leader) mma_commit(bar(B_ACC));     // this tile's dK / dV are final
+        if (leader) mma_commit(bar(B_KEMPTY));  // and its K buffer may be refilled
         ++kt;
       }
       if (git > 0 || kt > 0) {
         // every MMA must be complete before the CTA releases tensor memory
-        mma_commit(bar(B_DRAIN));
+        if (leader) mma_commit(bar(B_DRAIN));
         volatile int no_abort = 0;
         AbortState dr{&no_abort, p.status, p.wait_limit};
         mbar_wait_ool(bar(B_DRAIN), 0, dr, kTimeoutBase - 17);

@@ -140,6 +140,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
   }
 }
 
+// One lane of the (converged) warp: the one that issues single-thread tcgen05 ops.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------ TMA / bulk copies
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
