@@ -435,6 +435,9 @@ int fa_trace_read(void* host, size_t bytes) {
 int fa_trace_read_split(void* host, size_t bytes) {
   return split_trace_copy(host, bytes) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+int fa_trace_mma(void* host, size_t bytes) {
+  return bwd_trace_mma_copy(host, bytes) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 int fa_trace_timeline(void* host, size_t bytes, int clear) {
   return bwd_timeline_copy(host, bytes, clear != 0) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

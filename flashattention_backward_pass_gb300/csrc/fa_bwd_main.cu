@@ -110,6 +110,10 @@ __device__ long long g_fa_trace[FA_TRACE_CTAS][FA_TRACE_ITERS][FA_TRACE_EV];
     if (blockIdx.x < FA_TRACE_CTAS && (it) < FA_TRACE_ITERS)                       \
       g_fa_trace[blockIdx.x][(it)][(ev)] = clock64() - t_start;                    \
   } while (0)
+// Completion times (clock64 relative to the CTA's start) of the MMA groups of the first
+// FA_TRACE_ITERS steps of the first FA_TRACE_CTAS CTAs, observed by the otherwise idle
+// warp 3: S, dP, dV, dK, dQ.
+__device__ long long g_fa_mma_done[FA_TRACE_CTAS][FA_TRACE_ITERS][5];
 // Whole-kernel tile timeline (global timer, ns): per CTA and per tile it ran.
 constexpr int FA_TL_CTAS = 160, FA_TL_TILES = 24, FA_TL_EV = 8;
 __device__ long long g_fa_tl[FA_TL_CTAS][FA_TL_TILES][FA_TL_EV];
@@ -158,7 +162,7 @@ __device__ __forceinline__ TileCoord decode_tile(const BwdMainParams& p, int t) 
 // P (times 1 - tanh^2 under softcap) as f16 pairs in `pc` for dS.
 template <bool MASK, bool SOFTCAP>
 __device__ __forceinline__ void phase_p(const SoftmaxConsts& kc, uint32_t taddr, const float* lse,
-                                        int qmin, int qmax, uint32_t (&pc)[32]) {
+                                        const float (&lreg)[2], int qmin, int qmax, uint32_t (&pc)[32]) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint32_t r[32];
@@ -166,8 +170,17 @@ __device__ __forceinline__ void phase_p(const SoftmaxConsts& kc, uint32_t taddr,
     uint32_t pk[16];
 #pragma unroll
     for (int v4 = 0; v4 < 8; ++v4) {
-      const float4 l4 = reinterpret_cast<const float4*>(lse + c * 32)[v4];
-      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+      float lv[4];
+      if (SOFTCAP) {
+        const float4 l4 = reinterpret_cast<const float4*>(lse + c * 32)[v4];
+        lv[0] = l4.x;
+        lv[1] = l4.y;
+        lv[2] = l4.z;
+        lv[3] = l4.w;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) lv[u] = __shfl_sync(0xffffffffu, lreg[c], v4 * 4 + u);
+      }
       float pv[4], pcv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -394,6 +407,29 @@ __global__ void __launch_bounds__(512, 1)
   // was compiled to exactly 128 registers per thread, so the split always fits.
   if (warp < 4) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+#ifdef FA_TRACE
+   if (warp == 3 && lane == 0 && blockIdx.x < FA_TRACE_CTAS) {
+     // observer: poll the completion barriers in order of their phases
+     const int bars[5] = {B_SFULL, B_DPFULL, B_DVDONE, -1, B_DQFULL};
+     int k[5] = {0, 0, 0, 0, 0};
+     const long long t_lim = clock64() + 400000000ll;
+     while (clock64() < t_lim && !*s_abort) {
+       bool all = true;
+#pragma unroll
+       for (int e = 0; e < 5; ++e) {
+         if (k[e] >= FA_TRACE_ITERS) continue;
+         all = false;
+         const uint32_t b = e == 3 ? bar(B_QE0 + (k[e] & 1)) : bar(bars[e]);
+         const uint32_t par = e == 3 ? ((k[e] >> 1) & 1) : (k[e] & 1);
+         if (mbar_test_wait(b, par)) {
+           g_fa_mma_done[blockIdx.x][k[e]][e] = clock64() - t_start;
+           ++k[e];
+         }
+       }
+       if (all) break;
+     }
+   }
+#endif
    if (warp == 2) {
     // ------------------------------------------------------------------ tile scheduler
     if (lane == 0) {
@@ -822,15 +858,25 @@ __global__ void __launch_bounds__(512, 1)
         const int qmax = row_ok ? min(base - p.lo, 1 << 20) : -1;
         const float* lse = s_lse + s * 128 + col0;
         const float* dsum = s_dsum + s * 128 + col0;
+        // Without softcap each lane holds the LSE2 / D of columns lane and 32 + lane of its
+        // warpgroup's half, and the values reach the other lanes by shuffles: a broadcast
+        // shared-memory read costs a shared-memory wavefront per 4 bytes, and the port is
+        // what the step is bound by.  The ALU-heavier softcap step keeps the broadcast
+        // reads, which cost fewer issue slots.
 
         if (!warp_wait(bar(B_SFULL), git & 1, st, kTimeoutBase - 30)) { alive = false; break; }
         tc_fence_after();
         if (threadIdx.x == 256) FA_TR(4, git);
+        float lreg[2] = {0.f, 0.f};
+        if (!SOFTCAP) {
+          lreg[0] = lse[lane];
+          lreg[1] = lse[32 + lane];
+        }
         uint32_t pc[32];  // P (times 1 - tanh^2 with softcap) as f16 pairs, reused for dS
         if (need_mask)
-          phase_p<true, SOFTCAP>(kc, t_lane + TM_S + col0, lse, qmin, qmax, pc);
+          phase_p<true, SOFTCAP>(kc, t_lane + TM_S + col0, lse, lreg, qmin, qmax, pc);
         else
-          phase_p<false, SOFTCAP>(kc, t_lane + TM_S + col0, lse, qmin, qmax, pc);
+          phase_p<false, SOFTCAP>(kc, t_lane + TM_S + col0, lse, lreg, qmin, qmax, pc);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -845,6 +891,11 @@ __global__ void __launch_bounds__(512, 1)
         }
         tc_fence_after();
         if (threadIdx.x == 256) FA_TR(6, git);
+        float dreg[2] = {0.f, 0.f};
+        if (!SOFTCAP) {
+          dreg[0] = dsum[lane];
+          dreg[1] = dsum[32 + lane];
+        }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
@@ -852,8 +903,17 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 d4 = reinterpret_cast<const float4*>(dsum + c * 32)[v4];
-            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float dv[4];
+            if (SOFTCAP) {
+              const float4 d4 = reinterpret_cast<const float4*>(dsum + c * 32)[v4];
+              dv[0] = d4.x;
+              dv[1] = d4.y;
+              dv[2] = d4.z;
+              dv[3] = d4.w;
+            } else {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) dv[u] = __shfl_sync(0xffffffffu, dreg[c], v4 * 4 + u);
+            }
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
               const int e = v4 * 4 + e2 * 2;
@@ -953,7 +1013,12 @@ __global__ void __launch_bounds__(512, 1)
 #ifdef FA_TRACE
 cudaError_t bwd_trace_copy(void* host, size_t bytes) {
   if (bytes > sizeof(g_fa_trace)) bytes = sizeof(g_fa_trace);
-  return cudaMemcpyFromSymbol(host, g_fa_trace, bytes);
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_fa_trace, bytes);
+  return e;
+}
+cudaError_t bwd_trace_mma_copy(void* host, size_t bytes) {
+  if (bytes > sizeof(g_fa_mma_done)) bytes = sizeof(g_fa_mma_done);
+  return cudaMemcpyFromSymbol(host, g_fa_mma_done, bytes);
 }
 cudaError_t bwd_timeline_copy(void* host, size_t bytes, bool clear) {
   if (clear) {

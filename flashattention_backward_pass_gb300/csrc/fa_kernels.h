@@ -105,6 +105,7 @@ cudaError_t launch_fwd(const FwdParams& p, int Dp, cudaStream_t s);
 cudaError_t bwd_trace_copy(void* host, size_t bytes);
 cudaError_t split_trace_copy(void* host, size_t bytes);
 cudaError_t bwd_timeline_copy(void* host, size_t bytes, bool clear);
+cudaError_t bwd_trace_mma_copy(void* host, size_t bytes);
 #endif
 
 }  // namespace fa
