@@ -52,7 +52,7 @@ def _peaks():
 def _kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flashattention_backward_pass_gb300", "csrc")
-    for f in ("fa_bwd_main.cu", "fa_ptx.cuh", "fa_kernels.h", "fa_tiles.h"):
+    for f in ("fa_bwd_main.cu", "fa_bwd_common.cuh", "fa_ptx.cuh", "fa_kernels.h", "fa_tiles.h"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
