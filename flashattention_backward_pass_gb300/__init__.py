@@ -8,8 +8,8 @@ Public Python surface (thin wrappers over include/fa.h):
     attention_forward(q, k, v, ...)  -> (out, lse)            allocates outputs with torch
     attention_backward(dout, q, k, v, out, lse, ...) -> (dq, dk, dv)
 
-Layouts: q/out/dout/dq (B, Sq, H, D) bf16; k/v/dk/dv (B, Sk, Hk, D) bf16; lse (B, H, Sq)
-fp32 natural log.  All compute runs in libfa_gb300.so.
+Layouts: q/out/dout/dq (B, Sq, H, D); k/v/dk/dv (B, Sk, Hk, D); all of one 16-bit type, bf16
+or f16; lse (B, H, Sq) fp32 natural log.  All compute runs in libfa_gb300.so.
 """
 
 from __future__ import annotations

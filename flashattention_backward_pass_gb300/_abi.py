@@ -20,6 +20,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
 
 FA_DTYPE_BF16 = 0
 FA_DTYPE_FP32 = 1
+FA_DTYPE_F16 = 2
 
 STATUS = {
     0: "FA_OK", -1: "FA_ERR_NULL", -2: "FA_ERR_SHAPE", -3: "FA_ERR_DTYPE", -4: "FA_ERR_HEADDIM",
@@ -97,6 +98,8 @@ def tensor_view(t: torch.Tensor) -> FaTensor:
         dt = FA_DTYPE_BF16
     elif t.dtype == torch.float32:
         dt = FA_DTYPE_FP32
+    elif t.dtype == torch.float16:
+        dt = FA_DTYPE_F16
     else:
         dt = 99
     v = FaTensor()

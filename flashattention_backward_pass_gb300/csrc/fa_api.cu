@@ -77,10 +77,11 @@ bool bwd_layout(int B, int H, int Sq, int D, BwdLayout* L) {
 
 bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_bf16_4d(const fa_tensor* t, int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
+// A (B, S, H, D) view of 16-bit elements of type `dtype` (FA_DTYPE_BF16 or FA_DTYPE_F16).
+int check_h16_4d(const fa_tensor* t, int dtype, int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
   if (!t) return FA_ERR_NULL;
   if (t->ndim != 4) return FA_ERR_SHAPE;
-  if (t->dtype != FA_DTYPE_BF16) return FA_ERR_DTYPE;
+  if (t->dtype != dtype) return FA_ERR_DTYPE;
   if (t->shape[0] != d0 || t->shape[1] != d1 || t->shape[2] != d2 || t->shape[3] != d3)
     return FA_ERR_SHAPE;
   if (t->stride[3] != 1) return FA_ERR_LAYOUT;
@@ -104,12 +105,13 @@ int check_lse(const fa_tensor* t, int64_t B, int64_t H, int64_t Sq) {
 }
 
 // Shapes shared by fa_fwd and fa_bwd.  Returns a status; fills the problem sizes.
+// Also returns the shared 16-bit element type of q, k and v in *dtype.
 int check_qkv(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, int* B, int* Sq,
-              int* Sk, int* H, int* Hk, int* D) {
+              int* Sk, int* H, int* Hk, int* D, int* dtype) {
   if (!q || !k || !v) return FA_ERR_NULL;
   if (q->ndim != 4 || k->ndim != 4 || v->ndim != 4) return FA_ERR_SHAPE;
-  if (q->dtype != FA_DTYPE_BF16 || k->dtype != FA_DTYPE_BF16 || v->dtype != FA_DTYPE_BF16)
-    return FA_ERR_DTYPE;
+  if (q->dtype != FA_DTYPE_BF16 && q->dtype != FA_DTYPE_F16) return FA_ERR_DTYPE;
+  if (k->dtype != q->dtype || v->dtype != q->dtype) return FA_ERR_DTYPE;
   const int64_t b = q->shape[0], sq = q->shape[1], h = q->shape[2], d = q->shape[3];
   const int64_t sk = k->shape[1], hk = k->shape[2];
   if (b < 0 || sq < 0 || sk < 0 || h <= 0 || hk <= 0 || d <= 0) return FA_ERR_SHAPE;
@@ -119,12 +121,13 @@ int check_qkv(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, int* B
   if (h % hk != 0) return FA_ERR_SHAPE;
   if (d % 8 != 0 || d > 128) return FA_ERR_HEADDIM;
   if (b > (1 << 20) || sq > (1 << 30) || sk > (1 << 30) || h > 65535) return FA_ERR_UNSUPPORTED;
-  int st = check_bf16_4d(q, b, sq, h, d);
+  int st = check_h16_4d(q, q->dtype, b, sq, h, d);
   if (st) return st;
-  st = check_bf16_4d(k, b, sk, hk, d);
+  st = check_h16_4d(k, q->dtype, b, sk, hk, d);
   if (st) return st;
-  st = check_bf16_4d(v, b, sk, hk, d);
+  st = check_h16_4d(v, q->dtype, b, sk, hk, d);
   if (st) return st;
+  *dtype = q->dtype;
   *B = (int)b;
   *Sq = (int)sq;
   *Sk = (int)sk;
@@ -165,8 +168,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tensor map over a bf16 (B, S, H, D) operand, box = (width, 1, 128, 1) at 128B/64B/32B
-// swizzle.  Out-of-range rows and columns (S tail, D padding) read as zero.
+// Tensor map over a bf16 or f16 (B, S, H, D) operand, box = (width, 1, 128, 1) at
+// 128B/64B/32B swizzle.  Out-of-range rows and columns (S tail, D padding) read as zero.
 bool encode_operand(CUtensorMap* map, const fa_tensor* t, int width) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -180,7 +183,9 @@ bool encode_operand(CUtensorMap* map, const fa_tensor* t, int width) {
   CUtensorMapSwizzle swz = width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                        : (width == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                       : CU_TENSOR_MAP_SWIZZLE_32B);
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+  const CUtensorMapDataType ty =
+      t->dtype == FA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(map, ty, 4, t->data, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -228,10 +233,10 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor
            fa_tensor* lse, float softmax_scale, int causal, int window_left, int window_right,
            float softcap, void* workspace, size_t workspace_bytes, void* stream) {
   (void)workspace; (void)workspace_bytes;
-  int B, Sq, Sk, H, Hk, D;
-  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D);
+  int B, Sq, Sk, H, Hk, D, dt;
+  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &dt);
   if (st) return st;
-  if ((st = check_bf16_4d(out, B, Sq, H, D))) return st;
+  if ((st = check_h16_4d(out, dt, B, Sq, H, D))) return st;
   if ((st = check_lse(lse, B, H, Sq))) return st;
   if ((st = check_scalars(softmax_scale, softcap))) return st;
   if (B == 0 || Sq == 0) return FA_OK;
@@ -256,7 +261,8 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor
   p.softcap_on = softcap > 0.f;
   p.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
   p.cap_log2 = softcap * kLog2e;
-  if (launch_fwd(p, padded_dim(D), (cudaStream_t)stream) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_fwd(p, padded_dim(D), dt == FA_DTYPE_F16, (cudaStream_t)stream) != cudaSuccess)
+    return FA_ERR_CUDA;
   return FA_OK;
 }
 
@@ -272,14 +278,17 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
            fa_tensor* dv, float softmax_scale, int causal, int window_left, int window_right,
            float softcap, int deterministic, void* workspace, size_t workspace_bytes,
            void* stream) {
-  int B, Sq, Sk, H, Hk, D;
-  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D);
+  int B, Sq, Sk, H, Hk, D, dt;
+  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &dt);
   if (st) return st;
-  if ((st = check_bf16_4d(dout, B, Sq, H, D))) return st;
-  if ((st = check_bf16_4d(out, B, Sq, H, D))) return st;
-  if ((st = check_bf16_4d(dq, B, Sq, H, D))) return st;
-  if ((st = check_bf16_4d(dk, B, Sk, Hk, D))) return st;
-  if ((st = check_bf16_4d(dv, B, Sk, Hk, D))) return st;
+  if ((st = check_h16_4d(dout, dt, B, Sq, H, D))) return st;
+  if ((st = check_h16_4d(out, dt, B, Sq, H, D))) return st;
+  if ((st = check_h16_4d(dq, dt, B, Sq, H, D))) return st;
+  if ((st = check_h16_4d(dk, dt, B, Sk, Hk, D))) return st;
+  if ((st = check_h16_4d(dv, dt, B, Sk, Hk, D))) return st;
+  const bool f16 = dt == FA_DTYPE_F16;
+  // the split algorithm is built for bf16 only
+  if (f16 && g_bwd_algorithm == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;
   if ((st = check_lse(lse, B, H, Sq))) return st;
   if ((st = check_scalars(softmax_scale, softcap))) return st;
   if (B == 0 || Sq == 0) return FA_OK;
@@ -313,7 +322,7 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   pre.zero_count = split ? 0 : (int64_t)(L.zero_bytes / 16);
   pre.header = (int*)ws;
   prof_record(0, s);
-  if (launch_bwd_preprocess(pre, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_preprocess(pre, f16, s) != cudaSuccess) return FA_ERR_CUDA;
   if (g_poison_first_counter && deterministic) {
     const int poison = -1000000;
     if (cudaMemcpyAsync(ws + L.off_sems, &poison, sizeof(int), cudaMemcpyHostToDevice, s) !=
@@ -373,7 +382,7 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return FA_ERR_CUDA;
     const int grid = num_ctas < sms ? num_ctas : sms;
-    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, grid, s) != cudaSuccess)
+    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, f16, grid, s) != cudaSuccess)
       return FA_ERR_CUDA;
   }
 
@@ -385,7 +394,7 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   cp.dq_sb = dq->stride[0]; cp.dq_ss = dq->stride[1]; cp.dq_sh = dq->stride[2];
   cp.B = B; cp.H = H; cp.Sq = Sq; cp.D = D; cp.Dp = Dp; cp.Mb = L.Mb;
   cp.scale = softmax_scale;
-  if (launch_bwd_convert(cp, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_convert(cp, f16, s) != cudaSuccess) return FA_ERR_CUDA;
   prof_record(3, s);
   return FA_OK;
 }

@@ -9,6 +9,7 @@
 // convert (call-trace page: the "reduction kernel" after the dq_accum stores):
 //   dQ = bf16(scale * accumulator), cropped to Sq rows and D columns.
 #include "fa_kernels.h"
+#include "fa_ptx.cuh"
 
 #include <math.h>
 
@@ -23,6 +24,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // lane in flight.  Blocks [row_blocks, gridDim.x) clear the accumulator with 16-byte stores.
 // The two kinds of blocks run side by side, so the latency-bound row reductions overlap
 // the bandwidth-bound clearing.
+// F16: dO and O are f16 (else bf16).
+template <bool F16>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p, int row_blocks) {
   if (blockIdx.x == 0 && threadIdx.x < 4) p.header[threadIdx.x] = 0;
   if ((int)blockIdx.x >= row_blocks) {
@@ -61,12 +64,12 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av[u]);
-          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+          const uint32_t aw[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
+          const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 af = __bfloat1622float2(a2[e]);
-            const float2 of = __bfloat1622float2(o2[e]);
+            const float2 af = unpack_h2<F16>(aw[e]);
+            const float2 of = unpack_h2<F16>(ow[e]);
             acc = fmaf(af.x, of.x, acc);
             acc = fmaf(af.y, of.y, acc);
           }
@@ -91,6 +94,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
 // Block (16, 16): threadIdx.x = 8-column group, threadIdx.y = query row.  A warp covers two
 // rows: its reads are whole 32-byte sectors of the accumulator tile layout and its writes
 // are two contiguous 256-byte row segments of dQ.
+// F16: dQ is written as f16 (else bf16).
+template <bool F16>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p) {
   const int o = threadIdx.x;                    // 8-column group
   const int i = blockIdx.x * 16 + threadIdx.y;  // query row
@@ -102,18 +107,15 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p)
   const float4 lo = *reinterpret_cast<const float4*>(tile + ((size_t)(2 * o) * 128 + q) * 4);
   const float4 hi = *reinterpret_cast<const float4*>(tile + ((size_t)(2 * o + 1) * 128 + q) * 4);
   const float s = p.scale;
-  __nv_bfloat162 r[4];
-  r[0] = __floats2bfloat162_rn(lo.x * s, lo.y * s);
-  r[1] = __floats2bfloat162_rn(lo.z * s, lo.w * s);
-  r[2] = __floats2bfloat162_rn(hi.x * s, hi.y * s);
-  r[3] = __floats2bfloat162_rn(hi.z * s, hi.w * s);
+  const uint4 r = make_uint4(pack_h2<F16>(lo.x * s, lo.y * s), pack_h2<F16>(lo.z * s, lo.w * s),
+                             pack_h2<F16>(hi.x * s, hi.y * s), pack_h2<F16>(hi.z * s, hi.w * s));
   *reinterpret_cast<uint4*>(p.dq + (int64_t)b * p.dq_sb + (int64_t)i * p.dq_ss +
-                            (int64_t)h * p.dq_sh + o * 8) = *reinterpret_cast<uint4*>(r);
+                            (int64_t)h * p.dq_sh + o * 8) = r;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t s) {
+cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t s) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -125,14 +127,20 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t s) {
   int64_t zero_blocks = (p.zero_count + 255) / 256;
   const int64_t zero_cap = (int64_t)sms * 8;
   if (zero_blocks > zero_cap) zero_blocks = zero_cap;
-  bwd_preprocess_kernel<<<(unsigned)(row_blocks + zero_blocks), 256, 0, s>>>(p, (int)row_blocks);
+  if (f16)
+    bwd_preprocess_kernel<true><<<(unsigned)(row_blocks + zero_blocks), 256, 0, s>>>(p, (int)row_blocks);
+  else
+    bwd_preprocess_kernel<false><<<(unsigned)(row_blocks + zero_blocks), 256, 0, s>>>(p, (int)row_blocks);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_convert(const BwdConvParams& p, cudaStream_t s) {
+cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s) {
   if (p.Sq == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
   dim3 grid((p.Sq + 15) / 16, p.B * p.H);
-  bwd_convert_kernel<<<grid, dim3(16, 16), 0, s>>>(p);
+  if (f16)
+    bwd_convert_kernel<true><<<grid, dim3(16, 16), 0, s>>>(p);
+  else
+    bwd_convert_kernel<false><<<grid, dim3(16, 16), 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -160,7 +160,7 @@ __device__ __forceinline__ TileCoord decode_tile(const BwdMainParams& p, int t) 
 // zeroes masked entries (MASK: visible iff qmin <= column <= qmax), writes P^T as bf16
 // pairs back over the S^T columns already read (the A operand of dV += P^T dO), and keeps
 // P (times 1 - tanh^2 under softcap) as f16 pairs in `pc` for dS.
-template <bool MASK, bool SOFTCAP>
+template <bool MASK, bool SOFTCAP, bool F16>
 __device__ __forceinline__ void phase_p(const SoftmaxConsts& kc, uint32_t taddr, const float* lse,
                                         const float (&lreg)[2], int qmin, int qmax, uint32_t (&pc)[32]) {
 #pragma unroll
@@ -191,8 +191,8 @@ __device__ __forceinline__ void phase_p(const SoftmaxConsts& kc, uint32_t taddr,
         pv[u] = pr;
         pcv[u] = SOFTCAP ? pr * fac : pr;
       }
-      pk[v4 * 2] = pack_bf16(pv[0], pv[1]);
-      pk[v4 * 2 + 1] = pack_bf16(pv[2], pv[3]);
+      pk[v4 * 2] = pack_h2<F16>(pv[0], pv[1]);
+      pk[v4 * 2 + 1] = pack_h2<F16>(pv[2], pv[3]);
       pc[c * 16 + v4 * 2] = pack_f16(pcv[0], pcv[1]);
       pc[c * 16 + v4 * 2 + 1] = pack_f16(pcv[2], pcv[3]);
     }
@@ -224,10 +224,10 @@ __device__ __forceinline__ TileDescs tile_descs(uint32_t tile) {
 }
 
 // D = A B^T with both operands K-major over Dp (S^T = K Q^T, dP^T = V dO^T).
-template <int DP>
+template <int DP, bool F16>
 __device__ __forceinline__ void mma_kmajor(uint32_t d, const TileDescs& A, const TileDescs& B) {
   using P = Panels<DP>;
-  constexpr uint32_t ID = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t ID = idesc_h<F16>(128, 128, false, false);
 #pragma unroll
   for (int ks = 0; ks < P::NFULL * 4; ++ks) {
     const uint32_t off = (ks >> 2) * (P::FULL_BYTES >> 4) + (ks & 3) * 2;
@@ -242,11 +242,11 @@ __device__ __forceinline__ void mma_kmajor(uint32_t d, const TileDescs& A, const
 
 // dV (+)= P^T dO: A = P^T from tensor memory (bf16 pairs written over the S^T columns),
 // B = dO (N = Dp, MN-major), K = 128 queries.
-template <int DP>
+template <int DP, bool F16>
 __device__ __forceinline__ void mma_dv(uint32_t d, uint32_t a_tmem, const TileDescs& B, uint32_t acc) {
   using P = Panels<DP>;
-  constexpr uint32_t ID = idesc_bf16(128, P::NFULL * 64, false, true);
-  constexpr uint32_t ID_T = idesc_bf16(128, P::TAIL ? P::TAIL : 16, false, true);
+  constexpr uint32_t ID = idesc_h<F16>(128, P::NFULL * 64, false, true);
+  constexpr uint32_t ID_T = idesc_h<F16>(128, P::TAIL ? P::TAIL : 16, false, true);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t a_t = a_tmem + (ks >> 2) * 64 + (ks & 3) * 8;
@@ -262,11 +262,11 @@ __device__ __forceinline__ void mma_dv(uint32_t d, uint32_t a_tmem, const TileDe
 
 // dK (+)= dS^T Q: A = dS^T (K-major, 128B swizzle, `ds` = its descriptor), B = Q (N = Dp,
 // MN-major), K = 128 queries.
-template <int DP>
+template <int DP, bool F16>
 __device__ __forceinline__ void mma_dk(uint32_t d, DescWords ds, const TileDescs& B, uint32_t acc) {
   using P = Panels<DP>;
-  constexpr uint32_t ID = idesc_bf16(128, P::NFULL * 64, false, true);
-  constexpr uint32_t ID_T = idesc_bf16(128, P::TAIL ? P::TAIL : 16, false, true);
+  constexpr uint32_t ID = idesc_h<F16>(128, P::NFULL * 64, false, true);
+  constexpr uint32_t ID_T = idesc_h<F16>(128, P::TAIL ? P::TAIL : 16, false, true);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t a_off = (ks >> 2) * 1024 + (ks & 3) * 2;
@@ -282,11 +282,11 @@ __device__ __forceinline__ void mma_dk(uint32_t d, DescWords ds, const TileDescs
 
 // dQ tile = dS K: A = dS (M = queries, MN-major view of the dS^T tile, `ds` = its
 // descriptor), B = K (N = Dp, MN-major), K = 128 keys.
-template <int DP>
+template <int DP, bool F16>
 __device__ __forceinline__ void mma_dq(uint32_t d, DescWords ds, const TileDescs& B) {
   using P = Panels<DP>;
-  constexpr uint32_t ID = idesc_bf16(128, P::NFULL * 64, true, true);
-  constexpr uint32_t ID_T = idesc_bf16(128, P::TAIL ? P::TAIL : 16, true, true);
+  constexpr uint32_t ID = idesc_h<F16>(128, P::NFULL * 64, true, true);
+  constexpr uint32_t ID_T = idesc_h<F16>(128, P::TAIL ? P::TAIL : 16, true, true);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     if (ks == 0) {
@@ -299,7 +299,8 @@ __device__ __forceinline__ void mma_dq(uint32_t d, DescWords ds, const TileDescs
   }
 }
 
-template <int DP, bool SOFTCAP>
+// F16: the operands, P^T / dS and the dK / dV outputs are f16 (else bf16).
+template <int DP, bool SOFTCAP, bool F16>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ BwdMainParams p,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tq_t,
@@ -613,7 +614,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!wspin(bar(B_QF0 + s), (g >> 1) & 1, kTimeoutBase - 11)) return false;
         tc_fence_after();
         if (leader) FA_TR(0, g);
-        if (leader) mma_kmajor<DP>(tmem + TM_S, dK_, s ? dQ1 : dQ0);
+        if (leader) mma_kmajor<DP, F16>(tmem + TM_S, dK_, s ? dQ1 : dQ0);
         if (leader) mma_commit(bar(B_SFULL));
         return true;
       };
@@ -621,7 +622,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!wspin(bar(B_DOF0), g & 1, kTimeoutBase - 13)) return false;
         tc_fence_after();
         if (leader) FA_TR(1, g);
-        if (leader) mma_kmajor<DP>(tmem + TM_DP, dV_, dDO);
+        if (leader) mma_kmajor<DP, F16>(tmem + TM_DP, dV_, dDO);
         if (leader) mma_commit(bar(B_DPFULL));
         return true;
       };
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(512, 1)
           tc_fence_after();
           if (leader) FA_TR(2, git);
           if (it == 0) if (leader) FA_TL(t, 3, gtimer());
-          if (leader) mma_dv<DP>(tmem + TM_DV, tmem + TM_S, dDO, acc);
+          if (leader) mma_dv<DP, F16>(tmem + TM_DV, tmem + TM_S, dDO, acc);
           if (leader) mma_commit(bar(B_DOE0));
           if (leader) mma_commit(bar(B_DVDONE));
           if (it + 1 < d.total) {
@@ -673,9 +674,9 @@ __global__ void __launch_bounds__(512, 1)
           }
           tc_fence_after();
           if (leader) FA_TR(3, git);
-          if (leader) mma_dk<DP>(tmem + TM_DK, dsK, s ? dQ1 : dQ0, acc);
+          if (leader) mma_dk<DP, F16>(tmem + TM_DK, dsK, s ? dQ1 : dQ0, acc);
           if (leader) mma_commit(bar(B_QE0 + s));
-          if (leader) mma_dq<DP>(tmem + TM_DP, dsM, dK_);  // the dQ tile goes where dP^T was
+          if (leader) mma_dq<DP, F16>(tmem + TM_DP, dsM, dK_);  // the dQ tile goes where dP^T was
           if (leader) mma_commit(bar(B_DQFULL));
           if (leader) mma_commit(bar(B_DSEMPTY));
           acc = 1;
@@ -874,9 +875,9 @@ __global__ void __launch_bounds__(512, 1)
         }
         uint32_t pc[32];  // P (times 1 - tanh^2 with softcap) as f16 pairs, reused for dS
         if (need_mask)
-          phase_p<true, SOFTCAP>(kc, t_lane + TM_S + col0, lse, lreg, qmin, qmax, pc);
+          phase_p<true, SOFTCAP, F16>(kc, t_lane + TM_S + col0, lse, lreg, qmin, qmax, pc);
         else
-          phase_p<false, SOFTCAP>(kc, t_lane + TM_S + col0, lse, lreg, qmin, qmax, pc);
+          phase_p<false, SOFTCAP, F16>(kc, t_lane + TM_S + col0, lse, lreg, qmin, qmax, pc);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -920,7 +921,7 @@ __global__ void __launch_bounds__(512, 1)
               const float2 pcv = unpack_f16(pc[c * 16 + (e >> 1)]);
               const float d0 = pcv.x * (__uint_as_float(r[e]) - dv[2 * e2]);
               const float d1 = pcv.y * (__uint_as_float(r[e + 1]) - dv[2 * e2 + 1]);
-              pk[e >> 1] = pack_bf16(d0, d1);
+              pk[e >> 1] = pack_h2<F16>(d0, d1);
             }
           }
 #pragma unroll
@@ -976,7 +977,7 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
+              pk[e] = pack_h2<F16>(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
             if (store) {
               if (c * 16 < p.D)
                 *reinterpret_cast<uint4*>(row + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -1040,11 +1041,11 @@ size_t bwd_main_smem_bytes(int Dp) {
   }
 }
 
-template <int DP, bool SC>
+template <int DP, bool SC, bool F16>
 static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                               const OperandMaps& v, const OperandMaps& d, int num_ctas,
                               cudaStream_t s) {
-  auto kern = bwd_main_kernel<DP, SC>;
+  auto kern = bwd_main_kernel<DP, SC, F16>;
   const size_t smem = Geo<DP>::TOTAL;
   // The in-kernel register split assumes exactly 128 registers per thread at launch.
   cudaFuncAttributes attr;
@@ -1059,12 +1060,15 @@ static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, cons
 
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& d, int Dp, bool softcap,
-                            int num_ctas, cudaStream_t s) {
+                            bool f16, int num_ctas, cudaStream_t s) {
   if (num_ctas <= 0) return cudaSuccess;
-#define FA_CASE(DPV)                                                          \
-  case DPV:                                                                   \
-    return softcap ? launch_one<DPV, true>(p, q, k, v, d, num_ctas, s)        \
-                   : launch_one<DPV, false>(p, q, k, v, d, num_ctas, s);
+#define FA_CASE(DPV)                                                                    \
+  case DPV:                                                                             \
+    if (f16)                                                                            \
+      return softcap ? launch_one<DPV, true, true>(p, q, k, v, d, num_ctas, s)          \
+                     : launch_one<DPV, false, true>(p, q, k, v, d, num_ctas, s);        \
+    return softcap ? launch_one<DPV, true, false>(p, q, k, v, d, num_ctas, s)           \
+                   : launch_one<DPV, false, false>(p, q, k, v, d, num_ctas, s);
   switch (Dp) {
     FA_CASE(64)
     FA_CASE(80)

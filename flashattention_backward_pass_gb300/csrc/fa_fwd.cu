@@ -1,4 +1,5 @@
-// fa_fwd.cu — forward attention producing O (bf16) and the natural-log LSE (fp32).
+// fa_fwd.cu — forward attention producing O (bf16 or f16, the inputs' type) and the
+// natural-log LSE (fp32).
 //
 // This is the prerequisite step of the backward (its O and LSE are the backward's
 // inputs).  It follows the Triton page's `_attn_fwd_inner` online softmax: per 64-key
@@ -6,7 +7,7 @@
 // accumulator by exp2(m_old - m_new), acc += P V, and at the end O = acc / l and
 // LSE = (m + log2 l) * ln 2 (natural log; +inf for a row with no visible key).
 //
-// The contractions use warp-level mma.sync (m16n8k16, bf16 -> fp32): one CTA of 4 warps
+// The contractions use warp-level mma.sync (m16n8k16, bf16 or f16 -> fp32): one CTA of 4 warps
 // owns 64 query rows (16 per warp) of one (batch, q-head).  Masking is the same
 // bottom-right aligned band as the backward (lo <= j - i <= hi, j < Sk).
 #include "fa_kernels.h"
@@ -20,13 +21,21 @@ namespace {
 constexpr int kFwdRows = 64;
 constexpr int kFwdKeys = 64;
 
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  if (F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
@@ -53,12 +62,18 @@ __device__ __forceinline__ float tanh_exp2f(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(e + 1.f));
   return 1.f - 2.f * r;
 }
+template <bool F16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if (F16) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int DP>
+// F16: inputs and O are f16 (else bf16); the 16-bit pointers of FwdParams hold that type.
+template <int DP, bool F16>
 __global__ void __launch_bounds__(128) fwd_kernel(const FwdParams p) {
   constexpr int LDS = DP + 8;  // padded smem row (elements): conflict-free fragment loads
   constexpr int KT = DP / 16;  // k-steps of the S contraction
@@ -125,7 +140,7 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdParams p) {
         const __nv_bfloat16* kr = sK + (nt * 8 + g) * LDS + kk * 16 + 2 * t;
         const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr);
         const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 8);
-        mma_bf16_16816(s[nt], qf[kk], b0, b1);
+        mma_16816<F16>(s[nt], qf[kk], b0, b1);
       }
     }
     // scores in log2 units, masked entries -> -inf
@@ -178,11 +193,11 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdParams p) {
       }
       const int kk = nt >> 1;
       if ((nt & 1) == 0) {
-        pa[kk][0] = pack2(pv[0], pv[1]);
-        pa[kk][1] = pack2(pv[2], pv[3]);
+        pa[kk][0] = pack2<F16>(pv[0], pv[1]);
+        pa[kk][1] = pack2<F16>(pv[2], pv[3]);
       } else {
-        pa[kk][2] = pack2(pv[0], pv[1]);
-        pa[kk][3] = pack2(pv[2], pv[3]);
+        pa[kk][2] = pack2<F16>(pv[0], pv[1]);
+        pa[kk][3] = pack2<F16>(pv[2], pv[3]);
       }
     }
     // O += P V : B fragments from V [key][d] with ldmatrix.trans, two n8 tiles per call
@@ -194,8 +209,8 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdParams p) {
         const int colv = n * 8 + ((lane >> 4) << 3);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(sV_addr + (uint32_t)(rowk * LDS + colv) * 2u, b0, b1, b2, b3);
-        mma_bf16_16816(o[n], pa[kk], b0, b1);
-        mma_bf16_16816(o[n + 1], pa[kk], b2, b3);
+        mma_16816<F16>(o[n], pa[kk], b0, b1);
+        mma_16816<F16>(o[n + 1], pa[kk], b2, b3);
       }
     }
   }
@@ -216,9 +231,9 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdParams p) {
     const int col = n * 8 + 2 * t;
     if (col < p.D) {
       if (r0 < p.Sq)
-        *reinterpret_cast<uint32_t*>(ob + (int64_t)r0 * p.o_ss + col) = pack2(o[n][0] * inv[0], o[n][1] * inv[0]);
+        *reinterpret_cast<uint32_t*>(ob + (int64_t)r0 * p.o_ss + col) = pack2<F16>(o[n][0] * inv[0], o[n][1] * inv[0]);
       if (r1 < p.Sq)
-        *reinterpret_cast<uint32_t*>(ob + (int64_t)r1 * p.o_ss + col) = pack2(o[n][2] * inv[1], o[n][3] * inv[1]);
+        *reinterpret_cast<uint32_t*>(ob + (int64_t)r1 * p.o_ss + col) = pack2<F16>(o[n][2] * inv[1], o[n][3] * inv[1]);
     }
   }
   if (t == 0) {
@@ -230,15 +245,23 @@ __global__ void __launch_bounds__(128) fwd_kernel(const FwdParams p) {
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdParams& p, int Dp, cudaStream_t s) {
+cudaError_t launch_fwd(const FwdParams& p, int Dp, bool f16, cudaStream_t s) {
   dim3 grid((p.Sq + kFwdRows - 1) / kFwdRows, p.H, p.B);
+#define FA_FWD_CASE(DPV)                                   \
+  case DPV:                                                \
+    if (f16)                                               \
+      fwd_kernel<DPV, true><<<grid, 128, 0, s>>>(p);       \
+    else                                                   \
+      fwd_kernel<DPV, false><<<grid, 128, 0, s>>>(p);      \
+    break;
   switch (Dp) {
-    case 64: fwd_kernel<64><<<grid, 128, 0, s>>>(p); break;
-    case 80: fwd_kernel<80><<<grid, 128, 0, s>>>(p); break;
-    case 96: fwd_kernel<96><<<grid, 128, 0, s>>>(p); break;
-    case 128: fwd_kernel<128><<<grid, 128, 0, s>>>(p); break;
+    FA_FWD_CASE(64)
+    FA_FWD_CASE(80)
+    FA_FWD_CASE(96)
+    FA_FWD_CASE(128)
     default: return cudaErrorInvalidValue;
   }
+#undef FA_FWD_CASE
   return cudaGetLastError();
 }
 

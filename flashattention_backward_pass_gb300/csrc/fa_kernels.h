@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -90,17 +91,18 @@ struct OperandMaps {
 };
 
 size_t bwd_main_smem_bytes(int Dp);
-cudaError_t launch_bwd_preprocess(const BwdPreParams& p, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t s);
+// f16: the 16-bit operands and outputs are f16 (else bf16)
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
-                            int num_ctas, cudaStream_t s);
-cudaError_t launch_bwd_convert(const BwdConvParams& p, cudaStream_t s);
+                            bool f16, int num_ctas, cudaStream_t s);
+cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s);
 // dK/dV kernel (num_kv_ctas = key tiles x batch x kv-heads) then dQ kernel (num_q_ctas =
 // query tiles x batch x q-heads), both on stream s.
 cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                              const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
                              int num_kv_ctas, int num_q_ctas, cudaStream_t s);
-cudaError_t launch_fwd(const FwdParams& p, int Dp, cudaStream_t s);
+cudaError_t launch_fwd(const FwdParams& p, int Dp, bool f16, cudaStream_t s);
 #ifdef FA_TRACE
 cudaError_t bwd_trace_copy(void* host, size_t bytes);
 cudaError_t split_trace_copy(void* host, size_t bytes);

@@ -255,16 +255,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
+// Instruction descriptor for kind::f16 with fp32 accumulation; A and B are both bf16
+// (F16 = false) or both f16 (F16 = true): kind::f16 takes one type for both operands.
 // a_mn / b_mn select MN-major ("transposed") operands.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+template <bool F16>
+__host__ __device__ constexpr uint32_t idesc_h(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4)                                   // D format: f32
-         | (1u << 7)                                 // A format: bf16
-         | (1u << 10)                                // B format: bf16
+         | ((F16 ? 0u : 1u) << 7)                    // A format: f16 = 0, bf16 = 1
+         | ((F16 ? 0u : 1u) << 10)                   // B format: f16 = 0, bf16 = 1
          | ((a_mn ? 1u : 0u) << 15)                  // A major-ness
          | ((b_mn ? 1u : 0u) << 16)                  // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_h<false>(M, N, a_mn, b_mn);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]
@@ -435,6 +440,19 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_f16(uint32_t u) {
   __half2 v = *reinterpret_cast<__half2*>(&u);
   return __half22float2(v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(v);
+}
+// The 16-bit element type of a kernel's operands and outputs: bf16 or (F16) f16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float2 unpack_h2(uint32_t u) {
+  return F16 ? unpack_f16(u) : unpack_bf16(u);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -83,17 +83,17 @@ WORKLOADS = {
 HEADLINE = "gqa_causal"
 
 
-def make_inputs(w: Workload, device="cpu", seed: int | None = None):
-    """q, k, v, do as bf16 tensors in the (B, S, H, D) layout, drawn from N(0, 1)
-    (dO from N(0, do_std^2)) with a CPU generator so that every device sees the
-    same values."""
+def make_inputs(w: Workload, device="cpu", seed: int | None = None, dtype=torch.bfloat16):
+    """q, k, v, do as 16-bit tensors (bf16 by default, or f16) in the (B, S, H, D)
+    layout, drawn from N(0, 1) (dO from N(0, do_std^2)) with a CPU generator so that
+    every device sees the same values."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
     q = torch.randn(w.B, w.Sq, w.H, w.D, generator=g, dtype=torch.float32)
     k = torch.randn(w.B, w.Sk, w.Hk, w.D, generator=g, dtype=torch.float32)
     v = torch.randn(w.B, w.Sk, w.Hk, w.D, generator=g, dtype=torch.float32)
     do = torch.randn(w.B, w.Sq, w.H, w.D, generator=g, dtype=torch.float32) * w.do_std
-    out = [t.to(torch.bfloat16) for t in (q, k, v, do)]
+    out = [t.to(dtype) for t in (q, k, v, do)]
     if device != "cpu":
         out = [t.to(device) for t in out]
     return out

@@ -45,16 +45,20 @@ extern "C" {
 
 #define FA_ABI_VERSION 1
 
+/* Element types.  Q, K, V, O, dO, dQ, dK and dV of one call share one 16-bit type:
+ * bf16, or f16 (the call-trace page's dispatch covers both, `run_mha_bwd_constexpr`);
+ * LSE is fp32. */
 typedef enum {
     FA_DTYPE_BF16 = 0,
-    FA_DTYPE_FP32 = 1
+    FA_DTYPE_FP32 = 1,
+    FA_DTYPE_F16 = 2
 } fa_dtype;
 
 typedef enum {
     FA_OK = 0,
     FA_ERR_NULL = -1,          /* a required pointer is NULL                          */
     FA_ERR_SHAPE = -2,         /* mismatched dims, K/V mismatch, H % Hk != 0, ndim    */
-    FA_ERR_DTYPE = -3,         /* not bf16 (tensors) / not fp32 (LSE)                 */
+    FA_ERR_DTYPE = -3,         /* tensors not all bf16 or all f16 / LSE not fp32      */
     FA_ERR_HEADDIM = -4,       /* D % 8 != 0 or D > 128                               */
     FA_ERR_LAYOUT = -5,        /* last dimension not contiguous                       */
     FA_ERR_ALIGNMENT = -6,     /* base not 16-byte aligned or stride not 16-byte mult */

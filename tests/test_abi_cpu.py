@@ -95,6 +95,30 @@ def test_bwd_validation_codes(lib):
     assert _call_bwd(lib, a) == -1                                       # null output
 
 
+def _f16_args(**kw):
+    a = _bwd_args(**kw)
+    for n in ("dout", "q", "k", "v", "out", "dq", "dk", "dv"):
+        a[n].dtype = 2                                                   # FA_DTYPE_F16
+    return a
+
+
+def test_f16_validation(lib):
+    # every 16-bit tensor f16 passes validation (an empty problem then launches nothing)
+    assert _call_bwd(lib, _f16_args(Sq=0)) == 0
+    for n in ("dout", "k", "v", "out", "dq", "dk", "dv"):
+        a = _f16_args()
+        a[n].dtype = 0                                                   # one bf16 among f16
+        assert _call_bwd(lib, a) == -3, n
+    a = _bwd_args(); a["dq"].dtype = 2                                   # one f16 among bf16
+    assert _call_bwd(lib, a) == -3
+    # the split algorithm is bf16 only: refused before any launch
+    assert lib.fa_bwd_set_algorithm(0) == 0
+    try:
+        assert _call_bwd(lib, _f16_args()) == -8                         # FA_ERR_UNSUPPORTED
+    finally:
+        assert lib.fa_bwd_set_algorithm(1) == 0
+
+
 def test_empty_problems_launch_nothing(lib):
     # Sq == 0 and B == 0 return FA_OK without any CUDA call (this machine has no GPU,
     # so reaching a launch would fail with FA_ERR_CUDA).
