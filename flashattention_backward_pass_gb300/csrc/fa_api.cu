@@ -50,7 +50,7 @@ int padded_dim(int D) {
 
 struct BwdLayout {
   int Mb, Sq_r, Dp;
-  size_t off_lse2, off_dsum, off_accum, off_sems, total, zero_bytes;
+  size_t off_lse2, off_dsum, off_accum, off_sems, total, accum_bytes, sems_bytes;
 };
 
 bool bwd_layout(int B, int H, int Sq, int D, BwdLayout* L) {
@@ -70,7 +70,8 @@ bool bwd_layout(int B, int H, int Sq, int D, BwdLayout* L) {
   L->off_sems = off;
   const size_t sems = align_up((size_t)B * H * L->Mb * 4, 16);
   off += sems;
-  L->zero_bytes = accum + sems;
+  L->accum_bytes = accum;
+  L->sems_bytes = sems;
   L->total = align_up(off, 256);
   return true;
 }
@@ -120,7 +121,8 @@ int check_qkv(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, int* B
     if (v->shape[i] != k->shape[i]) return FA_ERR_SHAPE;
   if (h % hk != 0) return FA_ERR_SHAPE;
   if (d % 8 != 0 || d > 128) return FA_ERR_HEADDIM;
-  if (b > (1 << 20) || sq > (1 << 30) || sk > (1 << 30) || h > 65535) return FA_ERR_UNSUPPORTED;
+  // launch-grid limits: the forward's grid has B in z and H in y (each at most 65535)
+  if (b > 65535 || sq > (1 << 30) || sk > (1 << 30) || h > 65535) return FA_ERR_UNSUPPORTED;
   int st = check_h16_4d(q, q->dtype, b, sq, h, d);
   if (st) return st;
   st = check_h16_4d(k, q->dtype, b, sk, hk, d);
@@ -303,8 +305,7 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   mask_bounds(Sq, Sk, causal, window_left, window_right, &lo, &hi);
   const int Dp = L.Dp;
   // The split algorithm needs key tiles to build its tensor maps; with Sk == 0 (every dQ
-  // row is zero, dK/dV are empty) the fused path's zeroed accumulator and convert give
-  // the zero dQ.
+  // row is zero, dK/dV are empty) the fused path's convert writes the zero dQ.
   const bool split = g_bwd_algorithm == FA_BWD_ALGO_SPLIT && Sk > 0;
 
   BwdPreParams pre;
@@ -318,8 +319,11 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   pre.B = B; pre.H = H; pre.Sq = Sq; pre.Sq_r = L.Sq_r; pre.D = D;
   pre.lse2 = (float*)(ws + L.off_lse2);
   pre.dsum = (float*)(ws + L.off_dsum);
-  pre.zero_ptr = (float4*)(ws + L.off_accum);
-  pre.zero_count = split ? 0 : (int64_t)(L.zero_bytes / 16);
+  // The accumulator and the counters are adjacent.  The ordered mode stores the first
+  // contribution to each dQ tile, so only its counters are cleared.
+  pre.zero_ptr = (float4*)(ws + (deterministic ? L.off_sems : L.off_accum));
+  pre.zero_count =
+      split ? 0 : (int64_t)((deterministic ? L.sems_bytes : L.accum_bytes + L.sems_bytes) / 16);
   pre.header = (int*)ws;
   prof_record(0, s);
   if (launch_bwd_preprocess(pre, f16, s) != cudaSuccess) return FA_ERR_CUDA;
@@ -390,6 +394,7 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   BwdConvParams cp;
   memset(&cp, 0, sizeof(cp));
   cp.dq_accum = (const float*)(ws + L.off_accum);
+  cp.sems = deterministic ? (const int*)(ws + L.off_sems) : nullptr;
   cp.dq = (__nv_bfloat16*)dq->data;
   cp.dq_sb = dq->stride[0]; cp.dq_ss = dq->stride[1]; cp.dq_sh = dq->stride[2];
   cp.B = B; cp.H = H; cp.Sq = Sq; cp.D = D; cp.Dp = Dp; cp.Mb = L.Mb;

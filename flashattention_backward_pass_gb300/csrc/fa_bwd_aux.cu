@@ -5,9 +5,12 @@
 //   D_i   = sum_d dO_id * O_id   (fp32; 0 on the padded rows of the last query tile)
 //   LSE2  = LSE * log2(e)        (the sm90 page's P = exp2(S*scale*log2e - LSE_log2); +inf
 //                                 on padded rows, which makes P = 0 there)
-//   zero the dQ accumulator, the deterministic-mode counters and the status/ticket words.
+//   zero the fp32 dQ accumulator, the per-dQ-tile counters and the status/ticket words.
+//   In the ordered (deterministic) mode the accumulator is not cleared: the main kernel
+//   stores the first contribution to each tile and adds the later ones.
 // convert (call-trace page: the "reduction kernel" after the dq_accum stores):
-//   dQ = bf16(scale * accumulator), cropped to Sq rows and D columns.
+//   dQ = bf16(scale * accumulator), cropped to Sq rows and D columns; in the ordered mode
+//   tiles that no key tile contributed to (counter 0) give zero rows.
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 
@@ -21,9 +24,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Blocks [0, row_blocks) compute D and LSE2: each warp takes 4 rows per pass (8 lanes per
 // row, 16 bf16 per lane as two 16-byte loads each of dO and O), so a warp keeps 8 loads per
-// lane in flight.  Blocks [row_blocks, gridDim.x) clear the accumulator with 16-byte stores.
-// The two kinds of blocks run side by side, so the latency-bound row reductions overlap
-// the bandwidth-bound clearing.
+// lane in flight.  Blocks [row_blocks, gridDim.x) clear the accumulator and the counters
+// with 16-byte stores.  The two kinds of blocks run side by side, so the latency-bound row
+// reductions overlap the bandwidth-bound clearing.
 // F16: dO and O are f16 (else bf16).
 template <bool F16>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p, int row_blocks) {
@@ -91,26 +94,48 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
   }
 }
 
-// Block (16, 16): threadIdx.x = 8-column group, threadIdx.y = query row.  A warp covers two
-// rows: its reads are whole 32-byte sectors of the accumulator tile layout and its writes
-// are two contiguous 256-byte row segments of dQ.
+// Block (16, 16) covers 64 query rows of one (b, h): threadIdx.x = 8-column group,
+// threadIdx.y = row within each of 4 groups of 16 rows.  A thread issues its 8 loads (two
+// per row) before any store, so a warp keeps 8 x 32 bytes per lane in flight.  Per row
+// group a warp covers two rows: its reads are whole 32-byte sectors of the accumulator
+// tile layout and its writes two contiguous 256-byte row segments of dQ.
 // F16: dQ is written as f16 (else bf16).
+constexpr int kConvRows = 4;
 template <bool F16>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p) {
-  const int o = threadIdx.x;                    // 8-column group
-  const int i = blockIdx.x * 16 + threadIdx.y;  // query row
-  const int bh = blockIdx.y;
-  if (i >= p.Sq || o * 8 >= p.D) return;
+  const int o = threadIdx.x;  // 8-column group
+  const int nrb = (p.Sq + 16 * kConvRows - 1) / (16 * kConvRows);   // row blocks per (b, h)
+  const int bh = (int)(blockIdx.x / (unsigned)nrb);
+  const int rb = (int)(blockIdx.x - (unsigned)bh * (unsigned)nrb);
+  if (o * 8 >= p.D) return;
   const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
-  const int m = i >> 7, q = i & 127;
-  const float* tile = p.dq_accum + ((size_t)bh * p.Mb + m) * (size_t)(128 * p.Dp);
-  const float4 lo = *reinterpret_cast<const float4*>(tile + ((size_t)(2 * o) * 128 + q) * 4);
-  const float4 hi = *reinterpret_cast<const float4*>(tile + ((size_t)(2 * o + 1) * 128 + q) * 4);
+  const int row0 = rb * (16 * kConvRows);   // inside one 128-row tile
+  const size_t tile_id = (size_t)bh * p.Mb + (row0 >> 7);
+  const float* tile = p.dq_accum + tile_id * (size_t)(128 * p.Dp);
+  // Ordered mode: a tile that no key tile contributed to was never written (its rows are
+  // zero); otherwise the accumulator was cleared.
+  const bool written = p.sems == nullptr || p.sems[tile_id] != 0;
+  float4 lo[kConvRows], hi[kConvRows];
+#pragma unroll
+  for (int r = 0; r < kConvRows; ++r) {
+    const int i = row0 + r * 16 + threadIdx.y;
+    const int q = i & 127;
+    lo[r] = hi[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (written && i < p.Sq) {
+      lo[r] = __ldcs(reinterpret_cast<const float4*>(tile + ((size_t)(2 * o) * 128 + q) * 4));
+      hi[r] = __ldcs(reinterpret_cast<const float4*>(tile + ((size_t)(2 * o + 1) * 128 + q) * 4));
+    }
+  }
   const float s = p.scale;
-  const uint4 r = make_uint4(pack_h2<F16>(lo.x * s, lo.y * s), pack_h2<F16>(lo.z * s, lo.w * s),
-                             pack_h2<F16>(hi.x * s, hi.y * s), pack_h2<F16>(hi.z * s, hi.w * s));
-  *reinterpret_cast<uint4*>(p.dq + (int64_t)b * p.dq_sb + (int64_t)i * p.dq_ss +
-                            (int64_t)h * p.dq_sh + o * 8) = r;
+#pragma unroll
+  for (int r = 0; r < kConvRows; ++r) {
+    const int i = row0 + r * 16 + threadIdx.y;
+    if (i >= p.Sq) break;
+    const uint4 v = make_uint4(pack_h2<F16>(lo[r].x * s, lo[r].y * s), pack_h2<F16>(lo[r].z * s, lo[r].w * s),
+                               pack_h2<F16>(hi[r].x * s, hi[r].y * s), pack_h2<F16>(hi[r].z * s, hi[r].w * s));
+    *reinterpret_cast<uint4*>(p.dq + (int64_t)b * p.dq_sb + (int64_t)i * p.dq_ss +
+                              (int64_t)h * p.dq_sh + o * 8) = v;
+  }
 }
 
 }  // namespace
@@ -136,7 +161,9 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t 
 
 cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s) {
   if (p.Sq == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
-  dim3 grid((p.Sq + 15) / 16, p.B * p.H);
+  const int64_t blocks = (int64_t)((p.Sq + 16 * kConvRows - 1) / (16 * kConvRows)) * p.B * p.H;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)blocks);
   if (f16)
     bwd_convert_kernel<true><<<grid, dim3(16, 16), 0, s>>>(p);
   else

@@ -25,7 +25,8 @@ struct BwdPreParams {
   int B, H, Sq, Sq_r, D;
   float* lse2;                   // (B*H, Sq_r) LSE * log2(e); +inf on padded rows
   float* dsum;                   // (B*H, Sq_r) rowsum(dO*O); 0 on padded rows
-  float4* zero_ptr;              // dQ accumulator + counters, zeroed here
+  float4* zero_ptr;              // region zeroed here: the dQ accumulator (unless ordered)
+                                 // and the per-dQ-tile counters
   int64_t zero_count;            // in float4 units
   int* header;                   // status word + tile ticket, zeroed here
 };
@@ -43,8 +44,11 @@ struct BwdMainParams {
   int deterministic;
   const float* lse2;
   const float* dsum;
-  float* dq_accum;               // tiles of (Dp/4, 128, 4) fp32 per (b, h, m-tile)
-  int* sems;                     // (B*H*Mb) ordering counters (deterministic mode)
+  float* dq_accum;               // tiles of (Dp/4, 128, 4) fp32 per (b, h, m-tile); cleared
+                                 // by the preprocess, except in the ordered mode, where the
+                                 // first contribution to a tile is a store
+  int* sems;                     // (B*H*Mb) per dQ tile: completed contributions (ordered
+                                 // mode)
   int* status;
   int* ticket;
   __nv_bfloat16* dk;
@@ -60,6 +64,8 @@ struct BwdMainParams {
 
 struct BwdConvParams {
   const float* dq_accum;
+  const int* sems;               // ordered mode: per dQ tile, 0 = no contribution (the
+                                 // tile was never written and its rows are zero); else null
   __nv_bfloat16* dq;
   int64_t dq_sb, dq_ss, dq_sh;
   int B, H, Sq, D, Dp, Mb;

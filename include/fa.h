@@ -63,7 +63,8 @@ typedef enum {
     FA_ERR_LAYOUT = -5,        /* last dimension not contiguous                       */
     FA_ERR_ALIGNMENT = -6,     /* base not 16-byte aligned or stride not 16-byte mult */
     FA_ERR_WORKSPACE = -7,     /* workspace NULL or smaller than the size query       */
-    FA_ERR_UNSUPPORTED = -8,   /* argument outside what this build implements         */
+    FA_ERR_UNSUPPORTED = -8,   /* outside what this build implements (B or H > 65535, */
+                               /* S > 2^30, the split algorithm with f16)             */
     FA_ERR_ARG = -9,           /* invalid scalar (scale <= 0, softcap < 0, ...)       */
     FA_ERR_CUDA = -10,         /* a CUDA runtime/driver call or launch failed         */
     FA_ERR_DEVICE_TIMEOUT = -11 /* a bounded device-side wait gave up (status word)   */

@@ -80,6 +80,7 @@ def test_bwd_validation_codes(lib):
     assert _call_bwd(lib, a) == -3                                       # LSE must be fp32
     assert _call_bwd(lib, _bwd_args(D=60)) == -4                         # D % 8
     assert _call_bwd(lib, _bwd_args(D=136)) == -4                        # D > 128
+    assert _call_bwd(lib, _bwd_args(B=65536)) == -8                      # B above the grid limit
     a = _bwd_args(); a["q"] = _view((1, 128, 2, 64), strides=(128 * 2 * 64, 2 * 64, 64, 2))
     assert _call_bwd(lib, a) == -5                                       # last dim not contiguous
     a = _bwd_args(); a["q"] = _view((1, 128, 2, 64), data=4096 + 8)
