@@ -319,11 +319,9 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   pre.B = B; pre.H = H; pre.Sq = Sq; pre.Sq_r = L.Sq_r; pre.D = D;
   pre.lse2 = (float*)(ws + L.off_lse2);
   pre.dsum = (float*)(ws + L.off_dsum);
-  // The accumulator and the counters are adjacent.  The ordered mode stores the first
-  // contribution to each dQ tile, so only its counters are cleared.
-  pre.zero_ptr = (float4*)(ws + (deterministic ? L.off_sems : L.off_accum));
-  pre.zero_count =
-      split ? 0 : (int64_t)((deterministic ? L.sems_bytes : L.accum_bytes + L.sems_bytes) / 16);
+  // the accumulator and the counters are adjacent and cleared together
+  pre.zero_ptr = (float4*)(ws + L.off_accum);
+  pre.zero_count = split ? 0 : (int64_t)((L.accum_bytes + L.sems_bytes) / 16);
   pre.header = (int*)ws;
   prof_record(0, s);
   if (launch_bwd_preprocess(pre, f16, s) != cudaSuccess) return FA_ERR_CUDA;
@@ -394,7 +392,6 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   BwdConvParams cp;
   memset(&cp, 0, sizeof(cp));
   cp.dq_accum = (const float*)(ws + L.off_accum);
-  cp.sems = deterministic ? (const int*)(ws + L.off_sems) : nullptr;
   cp.dq = (__nv_bfloat16*)dq->data;
   cp.dq_sb = dq->stride[0]; cp.dq_ss = dq->stride[1]; cp.dq_sh = dq->stride[2];
   cp.B = B; cp.H = H; cp.Sq = Sq; cp.D = D; cp.Dp = Dp; cp.Mb = L.Mb;

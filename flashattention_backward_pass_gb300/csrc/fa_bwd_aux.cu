@@ -5,12 +5,10 @@
 //   D_i   = sum_d dO_id * O_id   (fp32; 0 on the padded rows of the last query tile)
 //   LSE2  = LSE * log2(e)        (the sm90 page's P = exp2(S*scale*log2e - LSE_log2); +inf
 //                                 on padded rows, which makes P = 0 there)
-//   zero the fp32 dQ accumulator, the per-dQ-tile counters and the status/ticket words.
-//   In the ordered (deterministic) mode the accumulator is not cleared: the main kernel
-//   stores the first contribution to each tile and adds the later ones.
+//   zero the fp32 dQ accumulator, the deterministic-mode counters and the status/ticket
+//   words.
 // convert (call-trace page: the "reduction kernel" after the dq_accum stores):
-//   dQ = bf16(scale * accumulator), cropped to Sq rows and D columns; in the ordered mode
-//   tiles that no key tile contributed to (counter 0) give zero rows.
+//   dQ = bf16(scale * accumulator), cropped to Sq rows and D columns.
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 
@@ -107,21 +105,18 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p)
   const int nrb = (p.Sq + 16 * kConvRows - 1) / (16 * kConvRows);   // row blocks per (b, h)
   const int bh = (int)(blockIdx.x / (unsigned)nrb);
   const int rb = (int)(blockIdx.x - (unsigned)bh * (unsigned)nrb);
-  if (o * 8 >= p.D) return;
+  const bool active = o * 8 < p.D;
   const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
   const int row0 = rb * (16 * kConvRows);   // inside one 128-row tile
   const size_t tile_id = (size_t)bh * p.Mb + (row0 >> 7);
   const float* tile = p.dq_accum + tile_id * (size_t)(128 * p.Dp);
-  // Ordered mode: a tile that no key tile contributed to was never written (its rows are
-  // zero); otherwise the accumulator was cleared.
-  const bool written = p.sems == nullptr || p.sems[tile_id] != 0;
   float4 lo[kConvRows], hi[kConvRows];
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
     const int i = row0 + r * 16 + threadIdx.y;
     const int q = i & 127;
     lo[r] = hi[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (written && i < p.Sq) {
+    if (active && i < p.Sq) {
       lo[r] = __ldcs(reinterpret_cast<const float4*>(tile + ((size_t)(2 * o) * 128 + q) * 4));
       hi[r] = __ldcs(reinterpret_cast<const float4*>(tile + ((size_t)(2 * o + 1) * 128 + q) * 4));
     }
@@ -130,11 +125,22 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p)
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
     const int i = row0 + r * 16 + threadIdx.y;
-    if (i >= p.Sq) break;
+    if (!active || i >= p.Sq) break;
     const uint4 v = make_uint4(pack_h2<F16>(lo[r].x * s, lo[r].y * s), pack_h2<F16>(lo[r].z * s, lo[r].w * s),
                                pack_h2<F16>(hi[r].x * s, hi[r].y * s), pack_h2<F16>(hi[r].z * s, hi[r].w * s));
     *reinterpret_cast<uint4*>(p.dq + (int64_t)b * p.dq_sb + (int64_t)i * p.dq_ss +
                               (int64_t)h * p.dq_sh + o * 8) = v;
+  }
+  // The block's 64 accumulator rows are dead now (every load above has been consumed by
+  // a store).  Their L2 lines are still dirty from the main kernel's adds: drop them
+  // without a write-back to DRAM.  A 128-byte line holds 8 rows of one 4-column group.
+  __syncthreads();
+  const int nlines = (p.Dp / 4) * (16 * kConvRows / 8);
+  const int tid = threadIdx.y * 16 + threadIdx.x;
+  for (int l = tid; l < nlines; l += 256) {
+    const int cg = l >> 3, ro = l & 7;
+    const float* line = tile + ((size_t)cg * 128 + (row0 & 127) + ro * 8) * 4;
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
   }
 }
 

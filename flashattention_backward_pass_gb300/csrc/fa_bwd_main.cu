@@ -750,10 +750,6 @@ __global__ void __launch_bounds__(512, 1)
         const size_t tile_id = ((size_t)d.b * p.H + h) * p.Mb + m;
         float* dst = p.dq_accum + tile_id * (size_t)(128 * DP);
         int* sem = p.sems + tile_id;
-        // In the ordered mode the accumulator is not cleared beforehand: the contribution
-        // of rank 0 (the lowest key tile that sees this query tile) is stored and the later
-        // ones are added.  Otherwise every contribution is added to the cleared tile.
-        bool first = false;
         if (p.deterministic) {
           // Ordered mode: contributions to one dQ tile are added in ascending key-tile
           // order.  No drain thread leaves a step early, so the named barriers of a step
@@ -764,7 +760,6 @@ __global__ void __launch_bounds__(512, 1)
               int64_t nb, ne;
               n_range(gm, m, &nb, &ne);
               const int want = d.n - (int)nb;
-              first = want == 0;
               long long t0 = clock64();
               while (true) {
                 int cur;
@@ -813,10 +808,7 @@ __global__ void __launch_bounds__(512, 1)
           }
           named_bar_sync(1, 128);
           if (threadIdx.x == 128 && ok) {
-            if (first)
-              bulk_store(dst + (size_t)cg0 * 128 * 4, stg, (uint32_t)ncg * 128 * 16);
-            else
-              bulk_reduce_add_f32(dst + (size_t)cg0 * 128 * 4, stg, (uint32_t)ncg * 128 * 16);
+            bulk_reduce_add_f32(dst + (size_t)cg0 * 128 * 4, stg, (uint32_t)ncg * 128 * 16);
             bulk_commit();
           }
         }

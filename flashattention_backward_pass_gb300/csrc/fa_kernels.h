@@ -25,8 +25,7 @@ struct BwdPreParams {
   int B, H, Sq, Sq_r, D;
   float* lse2;                   // (B*H, Sq_r) LSE * log2(e); +inf on padded rows
   float* dsum;                   // (B*H, Sq_r) rowsum(dO*O); 0 on padded rows
-  float4* zero_ptr;              // region zeroed here: the dQ accumulator (unless ordered)
-                                 // and the per-dQ-tile counters
+  float4* zero_ptr;              // dQ accumulator + counters, zeroed here
   int64_t zero_count;            // in float4 units
   int* header;                   // status word + tile ticket, zeroed here
 };
@@ -44,11 +43,8 @@ struct BwdMainParams {
   int deterministic;
   const float* lse2;
   const float* dsum;
-  float* dq_accum;               // tiles of (Dp/4, 128, 4) fp32 per (b, h, m-tile); cleared
-                                 // by the preprocess, except in the ordered mode, where the
-                                 // first contribution to a tile is a store
-  int* sems;                     // (B*H*Mb) per dQ tile: completed contributions (ordered
-                                 // mode)
+  float* dq_accum;               // tiles of (Dp/4, 128, 4) fp32 per (b, h, m-tile)
+  int* sems;                     // (B*H*Mb) ordering counters (deterministic mode)
   int* status;
   int* ticket;
   __nv_bfloat16* dk;
@@ -64,8 +60,6 @@ struct BwdMainParams {
 
 struct BwdConvParams {
   const float* dq_accum;
-  const int* sems;               // ordered mode: per dQ tile, 0 = no contribution (the
-                                 // tile was never written and its rows are zero); else null
   __nv_bfloat16* dq;
   int64_t dq_sb, dq_ss, dq_sh;
   int B, H, Sq, D, Dp, Mb;

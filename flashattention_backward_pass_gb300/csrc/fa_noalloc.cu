@@ -22,10 +22,8 @@
 //
 // Every call on a device shares the one array and leaves its contents behind.  The parts
 // that must start at zero (dQ accumulator, ordering counters, status word, tile ticket)
-// are cleared by the preprocess kernel at the start of every call (in the deterministic
-// mode the accumulator is instead overwritten by each tile's first contribution, and
-// tiles without one are never read), and the other parts are fully rewritten, so a call
-// never reads a previous call's values.  Two calls whose
+// are cleared by the preprocess kernel at the start of every call, and the other parts
+// are fully rewritten, so a call never reads a previous call's values.  Two calls whose
 // kernels overlap on the GPU (different streams without ordering between them) race on
 // the array: order them on one stream, or use fa_bwd with separate workspaces.
 #include <cuda_runtime.h>
