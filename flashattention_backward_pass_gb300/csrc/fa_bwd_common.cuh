@@ -83,4 +83,67 @@ __device__ __forceinline__ float prob(const SoftmaxConsts& k, float s, float lse
   return ex2_approx(fmaf(s, k.scale_log2, -lse2));
 }
 
+// Contractions issued by a single MMA thread.  Each operand tile's descriptors are built
+// once; a K-step only adds a constant to the low descriptor word.  The K-step loops are
+// fully unrolled, so consecutive MMAs reach the tensor pipe back to back.
+
+// Descriptors of one 128-row operand tile: K-major (rows = M or N, Dp contiguous columns
+// = the contraction) and MN-major (rows = the contraction, Dp columns = N) views of the
+// 64-column panels and of the tail panel.
+struct TileDescs {
+  DescWords kfull, ktail, mfull, mtail;
+};
+
+template <int DP>
+__device__ __forceinline__ TileDescs tile_descs(uint32_t tile) {
+  using P = Panels<DP>;
+  TileDescs o;
+  o.kfull = desc_words(tile, 16, 1024, SWZ_128B);
+  o.mfull = desc_words(tile, P::FULL_BYTES, 1024, SWZ_128B);
+  o.ktail = desc_words(tile + P::TAIL_OFF, 16, 8 * P::TAIL_ROWB, P::TAIL_SWZ);
+  o.mtail = desc_words(tile + P::TAIL_OFF, 128u * P::TAIL_ROWB, 8 * P::TAIL_ROWB, P::TAIL_SWZ);
+  return o;
+}
+
+// D = A B^T with both operands K-major over Dp (backward: S^T = K Q^T, dP^T = V dO^T;
+// forward: S = Q K^T).
+template <int DP, bool F16>
+__device__ __forceinline__ void mma_kmajor(uint32_t d, const TileDescs& A, const TileDescs& B) {
+  using P = Panels<DP>;
+  constexpr uint32_t ID = idesc_h<F16>(128, 128, false, false);
+#pragma unroll
+  for (int ks = 0; ks < P::NFULL * 4; ++ks) {
+    const uint32_t off = (ks >> 2) * (P::FULL_BYTES >> 4) + (ks & 3) * 2;
+    if (ks == 0)
+      mma_ss_w<0>(d, A.kfull, off, B.kfull, off, ID);
+    else
+      mma_ss_w<1>(d, A.kfull, off, B.kfull, off, ID);
+  }
+#pragma unroll
+  for (int kk = 0; kk < P::TAIL / 16; ++kk) mma_ss_w<1>(d, A.ktail, kk * 2, B.ktail, kk * 2, ID);
+}
+
+// D (+)= A B with A (128 x 128, 16-bit pairs) in tensor memory and B a 128-row tile read
+// MN-major (N = Dp): backward dV += P^T dO (P^T written over the S^T columns), forward
+// O += P V (P written over the S columns).  K-steps 0-3 read A's columns [0, 32), K-steps
+// 4-7 its columns [64, 96): each half of the 128-column score tile holds its 64 values as
+// pairs at the start of its own 64 columns.
+template <int DP, bool F16>
+__device__ __forceinline__ void mma_dv(uint32_t d, uint32_t a_tmem, const TileDescs& B, uint32_t acc) {
+  using P = Panels<DP>;
+  constexpr uint32_t ID = idesc_h<F16>(128, P::NFULL * 64, false, true);
+  constexpr uint32_t ID_T = idesc_h<F16>(128, P::TAIL ? P::TAIL : 16, false, true);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t a_t = a_tmem + (ks >> 2) * 64 + (ks & 3) * 8;
+    if (ks == 0) {
+      mma_ts_wp(d, a_t, B.mfull, 0, ID, acc);
+      if (P::TAIL) mma_ts_wp(d + P::NFULL * 64, a_t, B.mtail, 0, ID_T, acc);
+    } else {
+      mma_ts_w<1>(d, a_t, B.mfull, ks * 128, ID);
+      if (P::TAIL) mma_ts_w<1>(d + P::NFULL * 64, a_t, B.mtail, ks * P::TAIL_ROWB, ID_T);
+    }
+  }
+}
+
 }  // namespace fa

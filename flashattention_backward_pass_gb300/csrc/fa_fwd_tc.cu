@@ -1,0 +1,404 @@
+// fa_fwd_tc.cu — the forward (O and the natural-log LSE) on tcgen05 / TMEM / TMA for sm_103a.
+//
+// It computes what the Triton page's `_attn_fwd_inner` computes — per key block, scores,
+// running row maximum, rescaled running sum and accumulator, and at the end O = acc / l,
+// LSE = (m + log2 l) * ln 2 — with the same mask (bottom-right aligned band lo <= j - i
+// <= hi, j < Sk) and softcap (z = c * tanh(scale * s / c)) as the backward.
+//
+// One CTA owns one 128-query tile of one (batch, q-head) and walks the key tiles with a
+// visible entry (GQA/MQA page: the kv-head is h / (H / Hk)):
+//   S = Q K^T        (M = 128 queries, N = 128 keys, K = Dp; both operands K-major)
+//   P = exp2(z * log2e - m)  written as 16-bit pairs over the S columns already read
+//   O (+)= P V       (A = P from tensor memory, B = V read MN-major, N = Dp)
+// Each softmax thread owns one query row (= TMEM lane) and all 128 columns of the score
+// tile, so the row maximum and row sum need no exchange between threads.
+//
+// The running maximum m is only moved (and O, l rescaled by exp2(m_old - m_new)) when
+// a new score exceeds it by more than 8 in log2 units; otherwise the stale m is kept and
+// P may reach 2^8, well inside bf16 / f16 and the fp32 sums.  O = acc / l and the LSE use
+// the same m, so the result is exact up to rounding either way.  After the first key
+// tiles a rescale is rare.
+//
+// Warp roles (8 warps): warp 0 TMA producer (Q once, K and V per key tile into 3- and
+// 2-stage rings); warp 1 TMEM allocator and single MMA-issuing thread; warps 4-7 softmax
+// and epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31).  Warps 2-3 only join the CTA
+// barriers.
+//
+// Tensor memory: S double buffer [0, 128) and [128, 256) (P written over its first 32
+// columns of each 64-column half), O accumulator [256, 256 + Dp).
+#include "fa_bwd_common.cuh"
+
+#include <math.h>
+
+namespace fa {
+
+namespace {
+
+constexpr int kFwdThreads = 256;
+constexpr int kFwdTimeout = -1400;
+
+constexpr uint32_t FSM_BAR = 0;     // mbarriers
+constexpr uint32_t FSM_TMEM = 256;  // TMEM base address slot
+constexpr uint32_t FSM_ABORT = 260;
+constexpr uint32_t FSMALL = 1024;
+
+template <int DP>
+struct GeoF : Panels<DP> {
+  using Panels<DP>::TILE_BYTES;
+  static constexpr int KST = 3;  // K ring stages
+  static constexpr int VST = 2;  // V ring stages
+  static constexpr uint32_t OFF_Q = FSMALL;
+  static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES;
+  static constexpr uint32_t TOTAL = OFF_V + VST * TILE_BYTES;
+  static_assert(TOTAL <= 232448, "fits the 227 KB opt-in shared memory");
+};
+
+enum FBar : int {
+  F_Q = 0, F_KF0, F_KF1, F_KF2, F_KE0, F_KE1, F_KE2, F_VF0, F_VF1, F_VE0, F_VE1,
+  F_SF0, F_SF1, F_PF0, F_PF1, F_OD, F_ACC, F_DRAIN, F_COUNT
+};
+static_assert(F_COUNT <= 32, "barrier area holds 32 mbarriers");
+
+constexpr uint32_t FT_S0 = 0, FT_S1 = 128, FT_O = 256;
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Scores of one row of the tile in log2 units (scale * s * log2e, or with softcap
+// c * log2e * tanh(scale * s / c)); masked columns (MASK: visible iff cmin <= column <=
+// cmax) are -inf.  Returns the row maximum.
+template <bool MASK, bool SOFTCAP>
+__device__ __forceinline__ float fwd_scores(const SoftmaxConsts& kc, uint32_t sbuf, int cmin,
+                                            int cmax, float (&x)[128]) {
+  float mx = kNegInf;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld32(sbuf + c * 32, r);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int col = c * 32 + e;
+      const float s = __uint_as_float(r[e]);
+      float v = SOFTCAP ? kc.cap_log2 * tanh_exp2(s * kc.cap_scale) : s * kc.scale_log2;
+      if (MASK) v = (col >= cmin && col <= cmax) ? v : kNegInf;
+      x[col] = v;
+      mx = fmaxf(mx, v);
+    }
+  }
+  return mx;
+}
+
+// P = exp2(x - m) as 16-bit pairs over the S columns: columns [0, 64) of the row go to
+// TMEM columns [0, 32), columns [64, 128) to [64, 96) (the A layout the P V product
+// reads).  Returns the row sum of P (fp32, before rounding).
+template <bool F16>
+__device__ __forceinline__ float fwd_probs(uint32_t sbuf, float m, const float (&x)[128]) {
+  float sum = 0.f;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int col = hh * 64 + q * 32 + 2 * e;
+        const float p0 = ex2_approx(x[col] - m);
+        const float p1 = ex2_approx(x[col + 1] - m);
+        sum += p0 + p1;
+        pk[e] = pack_h2<F16>(p0, p1);
+      }
+      tmem_st16(sbuf + hh * 64 + q * 16, pk);
+    }
+  }
+  return sum;
+}
+
+}  // namespace
+
+template <int DP, bool SOFTCAP, bool F16>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ FwdTcParams p,
+                  const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tq_t,
+                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tk_t,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tv_t) {
+  using G = GeoF<DP>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem_raw + FSM_ABORT);
+  auto bar = [&](int i) -> uint32_t { return sbase + FSM_BAR + 8u * i; };
+
+  if (threadIdx.x == 0) {
+    *s_abort = 0;
+    if ((sbase & 1023u) != 0) {
+      // the tile layout assumes a 1024-byte aligned dynamic shared-memory base
+      if (p.status) atomicExch(p.status, kFwdTimeout - 99);
+      *s_abort = 1;
+    }
+    for (int i = 0; i < F_COUNT; ++i) mbar_init(bar(i), (i == F_PF0 || i == F_PF1) ? 4 : 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + FSM_TMEM, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem_raw + FSM_TMEM);
+  AbortState st{s_abort, p.status, p.wait_limit};
+
+  // query tiles with the most key tiles first (under causal masking: the last ones)
+  const int per_m = p.B * p.H;
+  const int m = p.Mb - 1 - (int)(blockIdx.x / (unsigned)per_m);
+  const int bh = (int)blockIdx.x - (p.Mb - 1 - m) * per_m;
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
+  const int hk = h / p.G;
+  MaskGeom gm;
+  gm.Sq = p.Sq;
+  gm.Sk = p.Sk;
+  gm.lo = p.lo64;
+  gm.hi = p.hi64;
+  gm.tm = kTileQ;
+  gm.tn = kTileK;
+  gm.Mb = p.Mb;
+  gm.Nb = p.Nb;
+  int64_t nb64, ne64;
+  n_range(gm, m, &nb64, &ne64);
+  const int n_begin = (int)nb64;
+  const int total = (*s_abort) ? 0 : (int)(ne64 - nb64);
+  const int m0 = m * kTileQ;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      int issued_k[G::KST] = {}, issued_v[G::VST] = {};
+      if (total > 0) {
+        mbar_arrive_expect_tx(bar(F_Q), G::TILE_BYTES);
+        for (int pn = 0; pn < G::NFULL; ++pn)
+          tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, h, m0, b, bar(F_Q));
+        if (G::TAIL) tma_load_4d(sbase + G::OFF_Q + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, m0, b, bar(F_Q));
+      }
+      for (int it = 0; it < total; ++it) {
+        const int n0 = (n_begin + it) * kTileK;
+        const int ks = it % G::KST;
+        if (it >= G::KST &&
+            !mbar_wait(bar(F_KE0 + ks), ((it - G::KST) / G::KST) & 1, st, kFwdTimeout - 1))
+          break;
+        const uint32_t kdst = sbase + G::OFF_K + ks * G::TILE_BYTES;
+        mbar_arrive_expect_tx(bar(F_KF0 + ks), G::TILE_BYTES);
+        for (int pn = 0; pn < G::NFULL; ++pn)
+          tma_load_4d(kdst + pn * G::FULL_BYTES, &tk, pn * 64, hk, n0, b, bar(F_KF0 + ks));
+        if (G::TAIL) tma_load_4d(kdst + G::TAIL_OFF, &tk_t, G::NFULL * 64, hk, n0, b, bar(F_KF0 + ks));
+        issued_k[ks] = it / G::KST + 1;
+        const int vs = it % G::VST;
+        if (it >= G::VST &&
+            !mbar_wait(bar(F_VE0 + vs), ((it - G::VST) / G::VST) & 1, st, kFwdTimeout - 2))
+          break;
+        const uint32_t vdst = sbase + G::OFF_V + vs * G::TILE_BYTES;
+        mbar_arrive_expect_tx(bar(F_VF0 + vs), G::TILE_BYTES);
+        for (int pn = 0; pn < G::NFULL; ++pn)
+          tma_load_4d(vdst + pn * G::FULL_BYTES, &tv, pn * 64, hk, n0, b, bar(F_VF0 + vs));
+        if (G::TAIL) tma_load_4d(vdst + G::TAIL_OFF, &tv_t, G::NFULL * 64, hk, n0, b, bar(F_VF0 + vs));
+        issued_v[vs] = it / G::VST + 1;
+      }
+      // every copy this thread started must land before the CTA may exit
+      volatile int no_abort = 0;
+      AbortState dr{&no_abort, p.status, p.wait_limit};
+      if (total > 0) mbar_wait(bar(F_Q), 0, dr, kFwdTimeout - 3);
+      for (int s = 0; s < G::KST; ++s)
+        if (issued_k[s]) mbar_wait(bar(F_KF0 + s), (issued_k[s] - 1) & 1, dr, kFwdTimeout - 3);
+      for (int s = 0; s < G::VST; ++s)
+        if (issued_v[s]) mbar_wait(bar(F_VF0 + s), (issued_v[s] - 1) & 1, dr, kFwdTimeout - 3);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    // S_0, S_1; then per key tile j: O (+)= P_j V_j once P_j is written (and O rescaled),
+    // then S_j+2 once that product is done (P_j lives in S_j's columns, which S_j+2 reuses).
+    if (lane == 0) {
+      const TileDescs dQ_ = tile_descs<DP>(sbase + G::OFF_Q);
+      auto issue_S = [&](int it) -> bool {
+        const int ks = it % G::KST;
+        if (!mbar_wait_spin(bar(F_KF0 + ks), (it / G::KST) & 1, st, kFwdTimeout - 11)) return false;
+        tc_fence_after();
+        const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K + ks * G::TILE_BYTES);
+        mma_kmajor<DP, F16>(tmem + ((it & 1) ? FT_S1 : FT_S0), dQ_, dK_);
+        mma_commit(bar(F_SF0 + (it & 1)));
+        mma_commit(bar(F_KE0 + ks));
+        return true;
+      };
+      bool ok = total > 0 && mbar_wait_spin(bar(F_Q), 0, st, kFwdTimeout - 10);
+      const bool issued_any = ok;
+      if (ok) ok = issue_S(0);
+      if (ok && total > 1) ok = issue_S(1);
+      for (int it = 0; ok && it < total; ++it) {
+        const int sb = it & 1;
+        if (!mbar_wait_spin(bar(F_PF0 + sb), (it >> 1) & 1, st, kFwdTimeout - 12)) break;
+        const int vs = it % G::VST;
+        if (!mbar_wait_spin(bar(F_VF0 + vs), (it / G::VST) & 1, st, kFwdTimeout - 13)) break;
+        tc_fence_after();
+        const TileDescs dV_ = tile_descs<DP>(sbase + G::OFF_V + vs * G::TILE_BYTES);
+        mma_dv<DP, F16>(tmem + FT_O, tmem + (sb ? FT_S1 : FT_S0), dV_, it > 0 ? 1u : 0u);
+        mma_commit(bar(F_VE0 + vs));
+        mma_commit(bar(F_OD));
+        if (it + 2 < total) {
+          if (!mbar_wait_spin(bar(F_OD), it & 1, st, kFwdTimeout - 14)) break;
+          if (!issue_S(it + 2)) break;
+        }
+      }
+      if (issued_any) {
+        mma_commit(bar(F_ACC));
+        mma_commit(bar(F_DRAIN));
+        volatile int no_abort = 0;
+        AbortState dr{&no_abort, p.status, p.wait_limit};
+        mbar_wait(bar(F_DRAIN), 0, dr, kFwdTimeout - 15);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int qd = warp & 3;               // TMEM lane quadrant
+    const int r = qd * 32 + lane;          // query row inside the tile = TMEM lane
+    const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
+    const int i = m0 + r;
+    const SoftmaxConsts kc{p.scale_log2, p.cap_scale, p.cap_log2};
+    float mrow = kNegInf;  // running maximum (log2 units); moved only by more than 8
+    float lrow = 0.f;      // running sum of P relative to mrow
+    bool alive = true;
+    for (int it = 0; it < total; ++it) {
+      const int n = n_begin + it;
+      const int kb = n * kTileK;  // key index of column 0
+      const bool need_mask = !tile_full(gm, m, n);
+      // visible columns: lo <= key - i <= hi and key < Sk  <=>  c in [cmin, cmax]
+      const int cmin = max(i + p.lo - kb, -1);
+      const int cmax = min(min(i + p.hi - kb, p.Sk - 1 - kb), 1 << 20);
+      const uint32_t sbuf = t_lane + ((it & 1) ? FT_S1 : FT_S0);
+      if (!warp_wait(bar(F_SF0 + (it & 1)), (it >> 1) & 1, st, kFwdTimeout - 30)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      float x[128];
+      const float mx = need_mask ? fwd_scores<true, SOFTCAP>(kc, sbuf, cmin, cmax, x)
+                                 : fwd_scores<false, SOFTCAP>(kc, sbuf, cmin, cmax, x);
+      // move the reference maximum only when a score passes it by more than 8 (log2)
+      float alpha = 1.f;
+      if (it == 0) {
+        mrow = mx;
+      } else if (mx > mrow + 8.f) {
+        alpha = ex2_approx(mrow - mx);  // mrow finite here, or -inf: alpha = 0
+        mrow = mx;
+      }
+      const float muse = mrow == kNegInf ? 0.f : mrow;  // all-masked so far: P = 0
+      lrow = lrow * alpha + fwd_probs<F16>(sbuf, muse, x);
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        // O holds the products up to key tile it-1: wait for the last one, then rescale
+        if (!warp_wait(bar(F_OD), (it - 1) & 1, st, kFwdTimeout - 31)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DP / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16(t_lane + FT_O + c * 16, o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st16(t_lane + FT_O + c * 16, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(F_PF0 + (it & 1)));
+    }
+
+    // O = acc / l and LSE = (m + log2 l) * ln 2; a row with no visible key gives O = 0
+    // and LSE = +inf
+    bool have = false;
+    if (alive && total > 0) have = warp_wait(bar(F_ACC), 0, st, kFwdTimeout - 32);
+    if (have) tc_fence_after();
+    if (__all_sync(0xffffffffu, *s_abort == 0)) {
+      const bool row_ok = i < p.Sq;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (int64_t)b * p.o_sb + (int64_t)i * p.o_ss +
+                       (int64_t)h * p.o_sh;
+#pragma unroll
+      for (int c = 0; c < DP / 16; ++c) {
+        uint32_t o[16];
+        if (have) {
+          tmem_ld16(t_lane + FT_O + c * 16, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = 0u;
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          pk[e] = pack_h2<F16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+        if (row_ok) {
+          if (c * 16 < p.D)
+            *reinterpret_cast<uint4*>(orow + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          if (c * 16 + 8 < p.D)
+            *reinterpret_cast<uint4*>(orow + c * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      if (row_ok) {
+        const float lse = lrow > 0.f ? (mrow + log2f(lrow)) * 0.69314718055994531f
+                                     : __int_as_float(0x7f800000);
+        p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + (int64_t)i * p.lse_ss] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+namespace {
+
+template <int DP, bool SC, bool F16>
+cudaError_t launch_fwd_one(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
+                           const OperandMaps& v, cudaStream_t s) {
+  auto kern = fwd_tc_kernel<DP, SC, F16>;
+  // at least 116 KB, so that one CTA (which allocates all 512 TMEM columns) runs per SM
+  const size_t smem = GeoF<DP>::TOTAL > 118784u ? GeoF<DP>::TOTAL : 118784u;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t ctas = (int64_t)p.Mb * p.B * p.H;
+  if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)ctas, kFwdThreads, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
+                          const OperandMaps& v, int Dp, bool softcap, bool f16, cudaStream_t s) {
+  if (p.Mb <= 0 || p.B <= 0 || p.H <= 0) return cudaSuccess;
+#define FA_FWD_TC_CASE(DPV)                                                             \
+  case DPV:                                                                             \
+    if (f16)                                                                            \
+      return softcap ? launch_fwd_one<DPV, true, true>(p, q, k, v, s)                   \
+                     : launch_fwd_one<DPV, false, true>(p, q, k, v, s);                 \
+    return softcap ? launch_fwd_one<DPV, true, false>(p, q, k, v, s)                    \
+                   : launch_fwd_one<DPV, false, false>(p, q, k, v, s);
+  switch (Dp) {
+    FA_FWD_TC_CASE(64)
+    FA_FWD_TC_CASE(80)
+    FA_FWD_TC_CASE(96)
+    FA_FWD_TC_CASE(128)
+    default: return cudaErrorInvalidValue;
+  }
+#undef FA_FWD_TC_CASE
+}
+
+}  // namespace fa

@@ -83,6 +83,23 @@ struct FwdParams {
   int softcap_on;
 };
 
+// The tcgen05 forward: one CTA per (128-query tile, batch, q-head); q, k, v reach it
+// through tensor maps, O and LSE are written with plain stores.
+struct FwdTcParams {
+  int B, H, Hk, G, Sq, Sk, D, Mb, Nb;
+  long long lo64, hi64;          // visible iff lo <= j - i <= hi (unclamped; tile ranges)
+  int lo, hi;                    // the same bounds clamped to +-2^30 (per-element mask)
+  float scale_log2;              // scale * log2(e)
+  float cap_scale;               // scale / softcap
+  float cap_log2;                // softcap * log2(e)
+  void* o;                       // (B, Sq, H, D) of the inputs' 16-bit type
+  int64_t o_sb, o_ss, o_sh;
+  float* lse;                    // (B, H, Sq) natural log
+  int64_t lse_sb, lse_sh, lse_ss;
+  int* status;                   // timeout status word, or null
+  long long wait_limit;
+};
+
 // Tensor maps for one bf16 (B, S, H, D) operand: a 64-column 128B-swizzled box and,
 // when Dp % 64 != 0, a narrower box for the remaining 16 or 32 columns.
 struct OperandMaps {
@@ -103,6 +120,8 @@ cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const
                              const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
                              int num_kv_ctas, int num_q_ctas, cudaStream_t s);
 cudaError_t launch_fwd(const FwdParams& p, int Dp, bool f16, cudaStream_t s);
+cudaError_t launch_fwd_tc(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
+                          const OperandMaps& v, int Dp, bool softcap, bool f16, cudaStream_t s);
 #ifdef FA_TRACE
 cudaError_t bwd_trace_copy(void* host, size_t bytes);
 cudaError_t split_trace_copy(void* host, size_t bytes);

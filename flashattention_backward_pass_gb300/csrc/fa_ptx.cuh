@@ -26,13 +26,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 struct AbortState {
   volatile int* cta_abort;  // shared-memory flag seen by every role of the CTA
-  int* global_status;       // workspace status word (FA_ERR_DEVICE_TIMEOUT on timeout)
+  int* global_status;       // workspace status word (FA_ERR_DEVICE_TIMEOUT on timeout), or
+                            // null: a timeout then only stops the CTA
   long long wait_limit;     // cycles
 };
 
 __device__ __forceinline__ void raise_timeout(const AbortState& st, int code) {
   *st.cta_abort = 1;
-  atomicExch(st.global_status, code);
+  if (st.global_status) atomicExch(st.global_status, code);
 }
 
 // ------------------------------------------------------------------ mbarrier
@@ -112,7 +113,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     if (*cta_abort) return false;
     if (clock64() - t0 > limit) {
       *cta_abort = 1;
-      atomicExch(status, code);
+      if (status) atomicExch(status, code);
       return false;
     }
   }
