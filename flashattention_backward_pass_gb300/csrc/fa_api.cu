@@ -243,60 +243,36 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor
   if (B == 0 || Sq == 0) return FA_OK;
   long long lo, hi;
   mask_bounds(Sq, Sk, causal, window_left, window_right, &lo, &hi);
-  if (Sk > 0) {
-    // tcgen05 kernel: one CTA per (128-query tile, batch, q-head)
-    const int Dp = padded_dim(D);
-    OperandMaps mq, mk, mv;
-    if (!encode_pair(&mq, q, Dp) || !encode_pair(&mk, k, Dp) || !encode_pair(&mv, v, Dp))
-      return FA_ERR_CUDA;
-    FwdTcParams p;
-    memset(&p, 0, sizeof(p));
-    p.B = B; p.H = H; p.Hk = Hk; p.G = H / Hk; p.Sq = Sq; p.Sk = Sk; p.D = D;
-    p.Mb = (Sq + kTileQ - 1) / kTileQ;
-    p.Nb = (Sk + kTileK - 1) / kTileK;
-    p.lo64 = lo;
-    p.hi64 = hi;
-    p.lo = clamp30(lo);
-    p.hi = clamp30(hi);
-    p.scale_log2 = softmax_scale * kLog2e;
-    p.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
-    p.cap_log2 = softcap * kLog2e;
-    p.o = out->data;
-    p.o_sb = out->stride[0]; p.o_ss = out->stride[1]; p.o_sh = out->stride[2];
-    p.lse = (float*)lse->data;
-    p.lse_sb = lse->stride[0]; p.lse_sh = lse->stride[1]; p.lse_ss = lse->stride[2];
-    // optional workspace: its status word receives a device timeout (read with fa_bwd_status)
-    p.status = (workspace && workspace_bytes >= WS_HEADER_BYTES && is_aligned16(workspace))
-                   ? (int*)workspace + WS_STATUS
-                   : nullptr;
-    p.wait_limit = g_wait_limit;
-    if (launch_fwd_tc(p, mq, mk, mv, Dp, softcap > 0.f, dt == FA_DTYPE_F16, (cudaStream_t)stream) !=
-        cudaSuccess)
-      return FA_ERR_CUDA;
-    return FA_OK;
-  }
-  // Sk == 0: no key at all, every row gives O = 0 and LSE = +inf (the plain kernel writes
-  // them without tensor maps, which need a non-empty key extent)
-  FwdParams p;
+  FwdTcParams p;
   memset(&p, 0, sizeof(p));
-  p.q = (const __nv_bfloat16*)q->data;
-  p.k = (const __nv_bfloat16*)k->data;
-  p.v = (const __nv_bfloat16*)v->data;
-  p.o = (__nv_bfloat16*)out->data;
-  p.lse = (float*)lse->data;
-  p.q_sb = q->stride[0]; p.q_ss = q->stride[1]; p.q_sh = q->stride[2];
-  p.k_sb = k->stride[0]; p.k_ss = k->stride[1]; p.k_sh = k->stride[2];
-  p.v_sb = v->stride[0]; p.v_ss = v->stride[1]; p.v_sh = v->stride[2];
-  p.o_sb = out->stride[0]; p.o_ss = out->stride[1]; p.o_sh = out->stride[2];
-  p.lse_sb = lse->stride[0]; p.lse_sh = lse->stride[1]; p.lse_ss = lse->stride[2];
   p.B = B; p.H = H; p.Hk = Hk; p.G = H / Hk; p.Sq = Sq; p.Sk = Sk; p.D = D;
+  p.Mb = (Sq + kTileQ - 1) / kTileQ;
+  p.Nb = (Sk + kTileK - 1) / kTileK;
+  p.lo64 = lo;
+  p.hi64 = hi;
   p.lo = clamp30(lo);
   p.hi = clamp30(hi);
   p.scale_log2 = softmax_scale * kLog2e;
-  p.softcap_on = softcap > 0.f;
   p.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
   p.cap_log2 = softcap * kLog2e;
-  if (launch_fwd(p, padded_dim(D), dt == FA_DTYPE_F16, (cudaStream_t)stream) != cudaSuccess)
+  p.o = out->data;
+  p.o_sb = out->stride[0]; p.o_ss = out->stride[1]; p.o_sh = out->stride[2];
+  p.lse = (float*)lse->data;
+  p.lse_sb = lse->stride[0]; p.lse_sh = lse->stride[1]; p.lse_ss = lse->stride[2];
+  // optional workspace: its status word receives a device timeout (read with fa_bwd_status)
+  p.status = (workspace && workspace_bytes >= WS_HEADER_BYTES && is_aligned16(workspace))
+                 ? (int*)workspace + WS_STATUS
+                 : nullptr;
+  p.wait_limit = g_wait_limit;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (Sk == 0)  // no key: O = 0 and LSE = +inf (tensor maps need a non-empty key extent)
+    return launch_fwd_empty(p, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  // tcgen05 kernel: one CTA per (128-query tile, batch, q-head)
+  const int Dp = padded_dim(D);
+  OperandMaps mq, mk, mv;
+  if (!encode_pair(&mq, q, Dp) || !encode_pair(&mk, k, Dp) || !encode_pair(&mv, v, Dp))
+    return FA_ERR_CUDA;
+  if (launch_fwd_tc(p, mq, mk, mv, Dp, softcap > 0.f, dt == FA_DTYPE_F16, s) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }

@@ -365,6 +365,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 namespace {
 
+// Sk == 0: no row has a visible key, so O = 0 and LSE = +inf everywhere (the rows-without-
+// keys convention of the main kernel's epilogue).  One thread per (b, i, h) row.
+__global__ void __launch_bounds__(256) fwd_empty_kernel(const FwdTcParams p) {
+  const int64_t rows = (int64_t)p.B * p.Sq * p.H;
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = r / ((int64_t)p.Sq * p.H);
+    const int64_t rem = r - b * p.Sq * p.H;
+    const int64_t i = rem / p.H, h = rem - (rem / p.H) * p.H;
+    uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + b * p.o_sb + i * p.o_ss + h * p.o_sh;
+    for (int c = 0; c < p.D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
+    p.lse[b * p.lse_sb + h * p.lse_sh + i * p.lse_ss] = __int_as_float(0x7f800000);
+  }
+}
+
 template <int DP, bool SC, bool F16>
 cudaError_t launch_fwd_one(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
                            const OperandMaps& v, cudaStream_t s) {
@@ -380,6 +395,15 @@ cudaError_t launch_fwd_one(const FwdTcParams& p, const OperandMaps& q, const Ope
 }
 
 }  // namespace
+
+cudaError_t launch_fwd_empty(const FwdTcParams& p, cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.Sq * p.H;
+  if (rows <= 0) return cudaSuccess;
+  int64_t blocks = (rows + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  fwd_empty_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fwd_tc(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
                           const OperandMaps& v, int Dp, bool softcap, bool f16, cudaStream_t s) {

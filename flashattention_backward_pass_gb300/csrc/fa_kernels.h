@@ -66,22 +66,6 @@ struct BwdConvParams {
   float scale;
 };
 
-struct FwdParams {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
-  __nv_bfloat16* o;
-  float* lse;
-  int64_t q_sb, q_ss, q_sh;
-  int64_t k_sb, k_ss, k_sh;
-  int64_t v_sb, v_ss, v_sh;
-  int64_t o_sb, o_ss, o_sh;
-  int64_t lse_sb, lse_sh, lse_ss;
-  int B, H, Hk, G, Sq, Sk, D;
-  int lo, hi;
-  float scale_log2, cap_scale, cap_log2;
-  int softcap_on;
-};
 
 // The tcgen05 forward: one CTA per (128-query tile, batch, q-head); q, k, v reach it
 // through tensor maps, O and LSE are written with plain stores.
@@ -119,7 +103,7 @@ cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s)
 cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                              const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
                              int num_kv_ctas, int num_q_ctas, cudaStream_t s);
-cudaError_t launch_fwd(const FwdParams& p, int Dp, bool f16, cudaStream_t s);
+cudaError_t launch_fwd_empty(const FwdTcParams& p, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
                           const OperandMaps& v, int Dp, bool softcap, bool f16, cudaStream_t s);
 #ifdef FA_TRACE

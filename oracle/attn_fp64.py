@@ -82,7 +82,7 @@ def _head_forward(q, k, v, scale, vis, softcap):
         t = None
         z = a
     z = np.where(vis, z, -np.inf)
-    rowmax = z.max(axis=1)
+    rowmax = z.max(axis=1, initial=-np.inf)      # no key at all (Sk = 0): -inf, as masked
     has_key = np.isfinite(rowmax)
     safe_max = np.where(has_key, rowmax, 0.0)
     e = np.exp(z - safe_max[:, None])             # exp(-inf) = 0 for masked entries

@@ -308,6 +308,29 @@ def test_fully_masked_rows():
     np.testing.assert_allclose(o[:, 3:], o3, rtol=1e-14)
 
 
+def test_no_keys_at_all():
+    """Sk = 0: every row is a row with no visible key (same reading as the fully masked
+    rows above): O = 0, LSE = +inf, dQ = 0, and dK / dV are empty.  The rows must also
+    equal the fully masked rows of a problem that has keys."""
+    rng = np.random.default_rng(9)
+    q, do = _rand((2, 5, 2, 4), rng), _rand((2, 5, 2, 4), rng)
+    k = np.zeros((2, 0, 1, 4))
+    v = np.zeros((2, 0, 1, 4))
+    o, lse = attention_forward(q, k, v, 0.5)
+    dq, dk, dv = attention_backward(do, q, k, v, 0.5)
+    assert o.shape == q.shape and np.all(o == 0)
+    assert np.all(np.isposinf(lse))
+    assert dq.shape == q.shape and np.all(dq == 0)
+    assert dk.shape == (2, 0, 1, 4) and dv.shape == (2, 0, 1, 4)
+    # the rows a causal mask hides completely (Sq = 5 > Sk = 3: rows 0 and 1) are the same
+    k1, v1 = _rand((2, 3, 1, 4), rng), _rand((2, 3, 1, 4), rng)
+    o1, lse1 = attention_forward(q, k1, v1, 0.5, causal=True)
+    dq1, _, _ = attention_backward(do, q, k1, v1, 0.5, causal=True)
+    np.testing.assert_array_equal(o1[:, :2], o[:, :2])
+    np.testing.assert_array_equal(lse1[:, :, :2], lse[:, :, :2])
+    np.testing.assert_array_equal(dq1[:, :2], dq[:, :2])
+
+
 # ---------------------------------------------------------------- brute force
 
 def _brute(do, q, k, v, scale, causal, wl, wr, cap):

@@ -1,7 +1,8 @@
 """GPU parity: the CUDA forward/backward (through the C ABI) against the fp64 oracle.
 
 Small cases compare every element and cover tile tails (lengths that are not multiples
-of 128), Sq != Sk, fully masked query rows, key tiles with no visible query, causal /
+of 128), Sq != Sk, fully masked query rows, no keys at all, key tiles with no visible
+query, causal /
 sliding-window / softcap masks, GQA and MQA head sharing, padded head dims and strided
 inputs.  The five workloads run at full size in the launch configuration the benchmark
 times; the oracle recomputes sampled (batch, kv-head group) slices of them, which is
@@ -87,6 +88,7 @@ SMALL = [
     custom("gqa_window_softcap", 2, 384, 384, 8, 2, 128, window_left=100, window_right=0,
            softcap=30.0, seed=20),
     custom("d80_noncausal", 1, 129, 383, 2, 2, 80, seed=21),
+    custom("no_keys", 2, 70, 0, 4, 2, 64, seed=23),
 ]
 
 
