@@ -18,11 +18,13 @@ import math
 
 import torch
 
-from ._abi import (FaError, alloc_bwd_workspace, bwd_workspace_size, fa_bwd, fa_bwd_status,
-                   fa_fwd, load)
+from ._abi import (FaError, alloc_bwd_workspace, bwd_varlen_workspace_size, bwd_workspace_size,
+                   fa_bwd, fa_bwd_status, fa_bwd_varlen, fa_fwd, fa_fwd_varlen, load)
 
-__all__ = ["FaError", "alloc_bwd_workspace", "attention_backward", "attention_forward",
-           "bwd_workspace_size", "fa_bwd", "fa_bwd_status", "fa_fwd", "load"]
+__all__ = ["FaError", "alloc_bwd_workspace", "attention_backward", "attention_backward_varlen",
+           "attention_forward", "attention_forward_varlen", "bwd_varlen_workspace_size",
+           "bwd_workspace_size", "fa_bwd", "fa_bwd_status", "fa_bwd_varlen", "fa_fwd",
+           "fa_fwd_varlen", "load"]
 
 
 def _scale(q, softmax_scale):
@@ -45,4 +47,29 @@ def attention_backward(dout, q, k, v, out, lse, softmax_scale=None, causal=False
     dv = torch.empty_like(v)
     fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, _scale(q, softmax_scale), causal, window_left,
            window_right, softcap, deterministic, workspace)
+    return dq, dk, dv
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                             softmax_scale=None, causal=False, window_left=-1, window_right=-1,
+                             softcap=0.0):
+    """Packed sequences: q (total_q, H, D), k / v (total_k, Hk, D), int32 device offsets of
+    length batch + 1.  Returns out (total_q, H, D) and lse (H, total_q)."""
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+    fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                  _scale(q, softmax_scale), causal, window_left, window_right, softcap)
+    return out, lse
+
+
+def attention_backward_varlen(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                              max_seqlen_k, softmax_scale=None, causal=False, window_left=-1,
+                              window_right=-1, softcap=0.0, deterministic=False, workspace=None):
+    """Packed sequences (layouts of attention_forward_varlen).  Returns dq, dk, dv."""
+    dq = torch.empty_like(q)
+    dk = torch.zeros_like(k)
+    dv = torch.zeros_like(v)
+    fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                  max_seqlen_k, _scale(q, softmax_scale), causal, window_left, window_right,
+                  softcap, deterministic, workspace)
     return dq, dk, dv

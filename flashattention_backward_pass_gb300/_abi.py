@@ -80,6 +80,20 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd_set_algorithm.restype = ctypes.c_int
     lib.fa_bwd_set_algorithm.argtypes = [ctypes.c_int]
     lib.fa_bwd_get_algorithm.restype = ctypes.c_int
+    ip = ctypes.c_void_p  # device int32 offsets
+    if not hasattr(lib, "fa_fwd_varlen"):  # a library built before the packed entry points
+        _lib = lib
+        return lib
+    lib.fa_fwd_varlen.restype = ctypes.c_int
+    lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, ip, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_float, vp, sz, vp]
+    lib.fa_bwd_varlen_workspace_size.restype = sz
+    lib.fa_bwd_varlen_workspace_size.argtypes = [ctypes.c_int] * 5
+    lib.fa_bwd_varlen.restype = ctypes.c_int
+    lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, ip, ip, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_float, ctypes.c_int, vp, sz, vp]
     _lib = lib
     return lib
 
@@ -219,3 +233,49 @@ def fa_bwd_noalloc(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal=Fa
             int(window_left), int(window_right), float(softcap), int(bool(deterministic)),
             _stream_ptr(stream))
     _check(st, "fa_bwd_noalloc")
+
+
+# ------------------------------------------------------------------ packed sequences
+
+def _offsets(cu):
+    if cu.dtype != torch.int32 or not cu.is_cuda or cu.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    return ctypes.c_void_p(cu.data_ptr())
+
+
+def fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                  softmax_scale, causal=False, window_left=-1, window_right=-1, softcap=0.0,
+                  stream=None):
+    """C call `fa_fwd_varlen`: q, out (total_q, H, D), k, v (total_k, Hk, D), lse (H, total_q)."""
+    lib = load()
+    tv = [tensor_view(x) for x in (q, k, v, out, lse)]
+    st = lib.fa_fwd_varlen(*[ctypes.byref(x) for x in tv], _offsets(cu_seqlens_q),
+                           _offsets(cu_seqlens_k), cu_seqlens_q.numel() - 1, int(max_seqlen_q),
+                           int(max_seqlen_k), float(softmax_scale), int(bool(causal)),
+                           int(window_left), int(window_right), float(softcap), None, 0,
+                           _stream_ptr(stream))
+    _check(st, "fa_fwd_varlen")
+
+
+def bwd_varlen_workspace_size(batch, H, total_q, D, deterministic=False) -> int:
+    return int(load().fa_bwd_varlen_workspace_size(batch, H, total_q, D, int(bool(deterministic))))
+
+
+def fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                  max_seqlen_k, softmax_scale, causal=False, window_left=-1, window_right=-1,
+                  softcap=0.0, deterministic=False, workspace=None, stream=None):
+    """C call `fa_bwd_varlen` (dq, dk, dv written in place).  Returns the workspace used."""
+    lib = load()
+    batch = cu_seqlens_q.numel() - 1
+    if workspace is None:
+        n = bwd_varlen_workspace_size(batch, q.shape[1], q.shape[0], q.shape[2], deterministic)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    st = lib.fa_bwd_varlen(*[ctypes.byref(x) for x in tv], _offsets(cu_seqlens_q),
+                           _offsets(cu_seqlens_k), batch, int(max_seqlen_q), int(max_seqlen_k),
+                           float(softmax_scale), int(bool(causal)), int(window_left),
+                           int(window_right), float(softcap), int(bool(deterministic)),
+                           ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                           _stream_ptr(stream))
+    _check(st, "fa_bwd_varlen")
+    return workspace

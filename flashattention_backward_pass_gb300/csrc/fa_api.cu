@@ -76,7 +76,41 @@ bool bwd_layout(int B, int H, int Sq, int D, BwdLayout* L) {
   return true;
 }
 
+// Packed sequences: per head T = total_q / 128 + batch slots of 128 query rows (each
+// sequence's query tiles take consecutive slots; fa_tiles.h), with the same regions as
+// the batched layout.
+bool bwd_layout_varlen(int batch, int H, int total_q, int D, BwdLayout* L) {
+  if (batch < 0 || H <= 0 || total_q < 0 || D <= 0) return false;
+  L->Dp = padded_dim(D);
+  const size_t T = (size_t)slot_count(total_q, batch);
+  L->Mb = 0;
+  L->Sq_r = 0;
+  const size_t rows = (size_t)H * T * kTileQ;
+  size_t off = WS_HEADER_BYTES;
+  L->off_lse2 = off;
+  off = align_up(off + rows * 4, 256);
+  L->off_dsum = off;
+  off = align_up(off + rows * 4, 256);
+  L->off_accum = off;
+  const size_t accum = rows * L->Dp * 4;
+  off += accum;
+  L->off_sems = off;
+  const size_t sems = align_up((size_t)H * T * 4, 16);
+  off += sems;
+  L->accum_bytes = accum;
+  L->sems_bytes = sems;
+  L->total = align_up(off, 256);
+  return true;
+}
+
 bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Packed-sequence arguments of the varlen entry points.
+struct VarlenArgs {
+  const int* cu_q;
+  const int* cu_k;
+  int batch, max_q, max_k;
+};
 
 // A (B, S, H, D) view of 16-bit elements of type `dtype` (FA_DTYPE_BF16 or FA_DTYPE_F16).
 int check_h16_4d(const fa_tensor* t, int dtype, int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
@@ -154,6 +188,25 @@ void mask_bounds(int Sq, int Sk, int causal, int wl, int wr, long long* lo, long
 int clamp30(long long x) {
   const long long lim = 1ll << 30;
   return (int)(x < -lim ? -lim : (x > lim ? lim : x));
+}
+
+// A packed (total, H, D) tensor of a variable-length call as a (1, total, H, D) view, and
+// a (H, total) LSE as (1, H, total): the batched validation and tensor-map code then
+// apply unchanged, with the sequence offsets added to the row coordinate.
+int packed_view(const fa_tensor* t, int want_ndim, fa_tensor* out) {
+  if (!t) return FA_ERR_NULL;
+  if (t->ndim != want_ndim) return FA_ERR_SHAPE;
+  memset(out, 0, sizeof(*out));
+  out->data = t->data;
+  out->dtype = t->dtype;
+  out->ndim = want_ndim + 1;
+  out->shape[0] = 1;
+  out->stride[0] = t->shape[0] * t->stride[0];
+  for (int d = 0; d < want_ndim; ++d) {
+    out->shape[d + 1] = t->shape[d];
+    out->stride[d + 1] = t->stride[d];
+  }
+  return FA_OK;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -277,6 +330,67 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor
   return FA_OK;
 }
 
+int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out,
+                  fa_tensor* lse, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  int max_seqlen_q, int max_seqlen_k, float softmax_scale, int causal,
+                  int window_left, int window_right, float softcap, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  fa_tensor q4, k4, v4, o4, l3;
+  int st;
+  if ((st = packed_view(q, 3, &q4)) || (st = packed_view(k, 3, &k4)) || (st = packed_view(v, 3, &v4)) ||
+      (st = packed_view(out, 3, &o4)) || (st = packed_view(lse, 2, &l3)))
+    return st;
+  int B1, Tq, Tk, H, Hk, D, dt;
+  if ((st = check_qkv(&q4, &k4, &v4, &B1, &Tq, &Tk, &H, &Hk, &D, &dt))) return st;
+  if ((st = check_h16_4d(&o4, dt, 1, Tq, H, D))) return st;
+  if ((st = check_lse(&l3, 1, H, Tq))) return st;
+  if ((st = check_scalars(softmax_scale, softcap))) return st;
+  if (batch < 0 || batch > 65535) return batch < 0 ? FA_ERR_ARG : FA_ERR_UNSUPPORTED;
+  if (max_seqlen_q < 0 || max_seqlen_k < 0 || max_seqlen_q > Tq || max_seqlen_k > Tk)
+    return FA_ERR_ARG;
+  if (batch == 0 || Tq == 0 || max_seqlen_q == 0) return FA_OK;
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
+  FwdTcParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = batch; p.H = H; p.Hk = Hk; p.G = H / Hk; p.D = D;
+  p.Sq = max_seqlen_q; p.Sk = max_seqlen_k;
+  p.Mb = (max_seqlen_q + kTileQ - 1) / kTileQ;
+  p.Nb = (max_seqlen_k + kTileK - 1) / kTileK;
+  p.scale_log2 = softmax_scale * kLog2e;
+  p.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
+  p.cap_log2 = softcap * kLog2e;
+  p.o = o4.data;
+  p.o_sb = o4.stride[0]; p.o_ss = o4.stride[1]; p.o_sh = o4.stride[2];
+  p.lse = (float*)l3.data;
+  p.lse_sb = l3.stride[0]; p.lse_sh = l3.stride[1]; p.lse_ss = l3.stride[2];
+  p.status = (workspace && workspace_bytes >= WS_HEADER_BYTES && is_aligned16(workspace))
+                 ? (int*)workspace + WS_STATUS
+                 : nullptr;
+  p.wait_limit = g_wait_limit;
+  p.varlen = 1;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = Tq;
+  p.total_k = Tk;
+  p.causal = causal ? 1 : 0;
+  p.window_left = window_left;
+  p.window_right = window_right;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (Tk == 0 || max_seqlen_k == 0) {  // no sequence has a key: O = 0, LSE = +inf
+    FwdTcParams e = p;
+    e.B = 1; e.Sq = Tq;
+    e.o_sb = 0; e.lse_sb = 0;
+    return launch_fwd_empty(e, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+  const int Dp = padded_dim(D);
+  OperandMaps mq, mk, mv;
+  if (!encode_pair(&mq, &q4, Dp) || !encode_pair(&mk, &k4, Dp) || !encode_pair(&mv, &v4, Dp))
+    return FA_ERR_CUDA;
+  if (launch_fwd_tc(p, mq, mk, mv, Dp, softcap > 0.f, dt == FA_DTYPE_F16, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int deterministic) {
   (void)Hk; (void)Sk; (void)deterministic;
   BwdLayout L;
@@ -284,11 +398,14 @@ size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int de
   return L.total;
 }
 
-int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
-           const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq, fa_tensor* dk,
-           fa_tensor* dv, float softmax_scale, int causal, int window_left, int window_right,
-           float softcap, int deterministic, void* workspace, size_t workspace_bytes,
-           void* stream) {
+// The backward for a batch (vl == nullptr) or for packed sequences (vl: the tensors are
+// (1, total, H, D) views and LSE a (1, H, total_q) view).
+static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
+                      const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
+                      fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, float softmax_scale, int causal,
+                      int window_left, int window_right, float softcap, int deterministic,
+                      void* workspace, size_t workspace_bytes, void* stream,
+                      const VarlenArgs* vl) {
   int B, Sq, Sk, H, Hk, D, dt;
   int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &dt);
   if (st) return st;
@@ -298,13 +415,28 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   if ((st = check_h16_4d(dk, dt, B, Sk, Hk, D))) return st;
   if ((st = check_h16_4d(dv, dt, B, Sk, Hk, D))) return st;
   const bool f16 = dt == FA_DTYPE_F16;
-  // the split algorithm is built for bf16 only
-  if (f16 && g_bwd_algorithm == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;
+  // the split algorithm is built for batched bf16 only
+  if ((f16 || vl) && g_bwd_algorithm == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;
   if ((st = check_lse(lse, B, H, Sq))) return st;
   if ((st = check_scalars(softmax_scale, softcap))) return st;
+  const int total_q = Sq, total_k = Sk;  // packed: the row extents of the views
+  if (vl) {
+    if (vl->batch < 0 || vl->max_q < 0 || vl->max_k < 0 || vl->max_q > total_q ||
+        vl->max_k > total_k)
+      return FA_ERR_ARG;
+    if (vl->batch > 65535) return FA_ERR_UNSUPPORTED;
+    if (vl->batch == 0 || total_q == 0 || vl->max_q == 0) return FA_OK;
+    if (!vl->cu_q || !vl->cu_k) return FA_ERR_NULL;
+    B = vl->batch;
+    Sq = vl->max_q;
+    Sk = vl->max_k;
+  }
   if (B == 0 || Sq == 0) return FA_OK;
   BwdLayout L;
-  if (!bwd_layout(B, H, Sq, D, &L)) return FA_ERR_SHAPE;
+  if (vl ? !bwd_layout_varlen(B, H, total_q, D, &L) : !bwd_layout(B, H, Sq, D, &L))
+    return FA_ERR_SHAPE;
+  if (vl) L.Mb = (Sq + kTileQ - 1) / kTileQ;  // query tiles of the longest sequence
+  const long long T = vl ? slot_count(total_q, B) : 0;
   if (!workspace || workspace_bytes < L.total) return FA_ERR_WORKSPACE;
   if (!is_aligned16(workspace)) return FA_ERR_ALIGNMENT;
   cudaStream_t s = (cudaStream_t)stream;
@@ -326,6 +458,12 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   pre.o_sb = out->stride[0]; pre.o_ss = out->stride[1]; pre.o_sh = out->stride[2];
   pre.lse_sb = lse->stride[0]; pre.lse_sh = lse->stride[1]; pre.lse_ss = lse->stride[2];
   pre.B = B; pre.H = H; pre.Sq = Sq; pre.Sq_r = L.Sq_r; pre.D = D;
+  if (vl) {
+    pre.varlen = 1;
+    pre.cu_q = vl->cu_q;
+    pre.total_q = total_q;
+    pre.T = T;
+  }
   pre.lse2 = (float*)(ws + L.off_lse2);
   pre.dsum = (float*)(ws + L.off_dsum);
   // the accumulator and the counters are adjacent and cleared together
@@ -377,6 +515,16 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
     p.dq = (__nv_bfloat16*)dq->data;
     p.dq_sb = dq->stride[0]; p.dq_ss = dq->stride[1]; p.dq_sh = dq->stride[2];
     p.wait_limit = g_wait_limit;
+    if (vl) {
+      p.cu_q = vl->cu_q;
+      p.cu_k = vl->cu_k;
+      p.total_q = total_q;
+      p.total_k = total_k;
+      p.T = T;
+      p.causal = causal ? 1 : 0;
+      p.window_left = window_left;
+      p.window_right = window_right;
+    }
     if (split) {
       if (launch_bwd_split(p, mq, mk, mv, mdo, Dp, softcap > 0.f, num_ctas, 0, s) != cudaSuccess)
         return FA_ERR_CUDA;
@@ -393,7 +541,8 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return FA_ERR_CUDA;
     const int grid = num_ctas < sms ? num_ctas : sms;
-    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, f16, grid, s) != cudaSuccess)
+    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, f16, vl != nullptr, grid, s) !=
+        cudaSuccess)
       return FA_ERR_CUDA;
   }
 
@@ -405,9 +554,52 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
   cp.dq_sb = dq->stride[0]; cp.dq_ss = dq->stride[1]; cp.dq_sh = dq->stride[2];
   cp.B = B; cp.H = H; cp.Sq = Sq; cp.D = D; cp.Dp = Dp; cp.Mb = L.Mb;
   cp.scale = softmax_scale;
+  if (vl) {
+    cp.varlen = 1;
+    cp.cu_q = vl->cu_q;
+    cp.total_q = total_q;
+    cp.T = T;
+  }
   if (launch_bwd_convert(cp, f16, s) != cudaSuccess) return FA_ERR_CUDA;
   prof_record(3, s);
   return FA_OK;
+}
+
+int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+           const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq, fa_tensor* dk,
+           fa_tensor* dv, float softmax_scale, int causal, int window_left, int window_right,
+           float softcap, int deterministic, void* workspace, size_t workspace_bytes,
+           void* stream) {
+  return bwd_common(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal, window_left,
+                    window_right, softcap, deterministic, workspace, workspace_bytes, stream,
+                    nullptr);
+}
+
+size_t fa_bwd_varlen_workspace_size(int batch, int H, int total_q, int D, int deterministic) {
+  (void)deterministic;
+  BwdLayout L;
+  if (!bwd_layout_varlen(batch, H, total_q, D, &L)) return 0;
+  return L.total;
+}
+
+int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
+                  const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq,
+                  fa_tensor* dk, fa_tensor* dv, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  int batch, int max_seqlen_q, int max_seqlen_k, float softmax_scale, int causal,
+                  int window_left, int window_right, float softcap, int deterministic,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  fa_tensor d4, q4, k4, v4, o4, l3, dq4, dk4, dv4;
+  int st;
+  if ((st = packed_view(dout, 3, &d4)) || (st = packed_view(q, 3, &q4)) ||
+      (st = packed_view(k, 3, &k4)) || (st = packed_view(v, 3, &v4)) ||
+      (st = packed_view(out, 3, &o4)) || (st = packed_view(lse, 2, &l3)) ||
+      (st = packed_view(dq, 3, &dq4)) || (st = packed_view(dk, 3, &dk4)) ||
+      (st = packed_view(dv, 3, &dv4)))
+    return st;
+  VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k};
+  return bwd_common(&d4, &q4, &k4, &v4, &o4, &l3, &dq4, &dk4, &dv4, softmax_scale, causal,
+                    window_left, window_right, softcap, deterministic, workspace,
+                    workspace_bytes, stream, &vl);
 }
 
 int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* device_status) {

@@ -11,6 +11,7 @@
 //   dQ = bf16(scale * accumulator), cropped to Sq rows and D columns.
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
+#include "fa_tiles.h"
 
 #include <math.h>
 
@@ -40,20 +41,39 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;  // row within the warp's group of 4
   const int l8 = lane & 7;    // 16-column slice of the row
-  const int64_t nrows = (int64_t)p.B * p.H * p.Sq_r;
+  const int64_t nrows = p.varlen ? (int64_t)p.H * p.T * 128 : (int64_t)p.B * p.H * p.Sq_r;
   const int64_t warps_total = (int64_t)row_blocks * (blockDim.x >> 5);
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
 
   for (int64_t r4 = wid; 4 * r4 < nrows; r4 += warps_total) {
     const int64_t r = 4 * r4 + sub;
     float acc = 0.f;
-    int64_t bh = 0, i = 0;
+    // the row's (batch coordinate, row coordinate, head) in dO / O / LSE, and whether it
+    // is a query row at all (rather than padding of its last tile)
+    int64_t b = 0, i = 0, h = 0;
+    bool real = false;
     const bool valid_row = r < nrows;
     if (valid_row) {
-      bh = r / p.Sq_r;
-      i = r - bh * p.Sq_r;
-      if (i < p.Sq) {
-        const int64_t b = bh / p.H, h = bh - (bh / p.H) * p.H;
+      if (p.varlen) {
+        // per head T slots of 128 rows; slot t belongs to sequence slot_owner(t)
+        const int64_t tile = r >> 7;
+        h = tile / p.T;
+        const int64_t t = tile - h * p.T;
+        const int sb = slot_owner(p.cu_q, p.B, p.total_q, t);
+        int64_t q0, sq;
+        seq_rows(p.cu_q, sb, p.total_q, &q0, &sq);
+        const int64_t il = (t - first_slot(p.cu_q, sb, p.total_q)) * 128 + (r & 127);
+        real = il >= 0 && il < sq;  // (il < 0 only for malformed offsets)
+        i = q0 + il;
+      } else {
+        const int64_t bh = r / p.Sq_r;
+        const int64_t il = r - bh * p.Sq_r;
+        real = il < p.Sq;
+        b = bh / p.H;
+        h = bh - b * p.H;
+        i = il;
+      }
+      if (real) {
         const __nv_bfloat16* a = p.dout + b * p.do_sb + i * p.do_ss + h * p.do_sh;
         const __nv_bfloat16* o = p.out + b * p.o_sb + i * p.o_ss + h * p.o_sh;
         uint4 av[2], ov[2];
@@ -81,8 +101,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
     for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (valid_row && l8 == 0) {
       float l2 = INFINITY;
-      if (i < p.Sq) {
-        const int64_t b = bh / p.H, h = bh - (bh / p.H) * p.H;
+      if (real) {
         const float l = p.lse[b * p.lse_sb + h * p.lse_sh + i * p.lse_ss];
         l2 = l * kLog2e;
       }
@@ -102,21 +121,46 @@ constexpr int kConvRows = 4;
 template <bool F16>
 __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p) {
   const int o = threadIdx.x;  // 8-column group
-  const int nrb = (p.Sq + 16 * kConvRows - 1) / (16 * kConvRows);   // row blocks per (b, h)
-  const int bh = (int)(blockIdx.x / (unsigned)nrb);
-  const int rb = (int)(blockIdx.x - (unsigned)bh * (unsigned)nrb);
-  const bool active = o * 8 < p.D;
-  const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
-  const int row0 = rb * (16 * kConvRows);   // inside one 128-row tile
-  const size_t tile_id = (size_t)bh * p.Mb + (row0 >> 7);
+  bool active = o * 8 < p.D;
+  // this block's 64 rows: tile (its index in the accumulator), first local row inside the
+  // tile, and the (batch coordinate, first row coordinate, head, rows that exist) in dQ
+  size_t tile_id;
+  int row0, b, h, nvalid;
+  int64_t i0;
+  if (p.varlen) {
+    // per head T slots of 128 rows, two blocks per slot
+    tile_id = blockIdx.x >> 1;
+    row0 = (blockIdx.x & 1) * (16 * kConvRows);
+    h = (int)(tile_id / (size_t)p.T);
+    const int64_t t = (int64_t)tile_id - (int64_t)h * p.T;
+    const int sb = slot_owner(p.cu_q, p.B, p.total_q, t);
+    int64_t q0, sq;
+    seq_rows(p.cu_q, sb, p.total_q, &q0, &sq);
+    const int64_t il = (t - first_slot(p.cu_q, sb, p.total_q)) * 128 + row0;
+    b = 0;
+    i0 = q0 + il;
+    // (il < 0 only for malformed offsets: write nothing then)
+    nvalid = (int)(il < 0 || sq - il < 0 ? 0 : (sq - il > 16 * kConvRows ? 16 * kConvRows : sq - il));
+  } else {
+    const int nrb = (p.Sq + 16 * kConvRows - 1) / (16 * kConvRows);   // row blocks per (b, h)
+    const int bh = (int)(blockIdx.x / (unsigned)nrb);
+    const int rb = (int)(blockIdx.x - (unsigned)bh * (unsigned)nrb);
+    b = bh / p.H;
+    h = bh - b * p.H;
+    const int r0 = rb * (16 * kConvRows);
+    row0 = r0 & 127;
+    tile_id = (size_t)bh * p.Mb + (r0 >> 7);
+    i0 = r0;
+    nvalid = p.Sq - r0 < 16 * kConvRows ? p.Sq - r0 : 16 * kConvRows;
+  }
   const float* tile = p.dq_accum + tile_id * (size_t)(128 * p.Dp);
   float4 lo[kConvRows], hi[kConvRows];
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
-    const int i = row0 + r * 16 + threadIdx.y;
-    const int q = i & 127;
+    const int rl = r * 16 + threadIdx.y;  // row within the block
+    const int q = row0 + rl;              // row within the tile
     lo[r] = hi[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active && i < p.Sq) {
+    if (active && rl < nvalid) {
       lo[r] = __ldcs(reinterpret_cast<const float4*>(tile + ((size_t)(2 * o) * 128 + q) * 4));
       hi[r] = __ldcs(reinterpret_cast<const float4*>(tile + ((size_t)(2 * o + 1) * 128 + q) * 4));
     }
@@ -124,11 +168,11 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p)
   const float s = p.scale;
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
-    const int i = row0 + r * 16 + threadIdx.y;
-    if (!active || i >= p.Sq) break;
+    const int rl = r * 16 + threadIdx.y;
+    if (!active || rl >= nvalid) break;
     const uint4 v = make_uint4(pack_h2<F16>(lo[r].x * s, lo[r].y * s), pack_h2<F16>(lo[r].z * s, lo[r].w * s),
                                pack_h2<F16>(hi[r].x * s, hi[r].y * s), pack_h2<F16>(hi[r].z * s, hi[r].w * s));
-    *reinterpret_cast<uint4*>(p.dq + (int64_t)b * p.dq_sb + (int64_t)i * p.dq_ss +
+    *reinterpret_cast<uint4*>(p.dq + (int64_t)b * p.dq_sb + (i0 + rl) * p.dq_ss +
                               (int64_t)h * p.dq_sh + o * 8) = v;
   }
   // The block's 64 accumulator rows are dead now (every load above has been consumed by
@@ -139,7 +183,7 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p)
   const int tid = threadIdx.y * 16 + threadIdx.x;
   for (int l = tid; l < nlines; l += 256) {
     const int cg = l >> 3, ro = l & 7;
-    const float* line = tile + ((size_t)cg * 128 + (row0 & 127) + ro * 8) * 4;
+    const float* line = tile + ((size_t)cg * 128 + row0 + ro * 8) * 4;
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
   }
 }
@@ -150,7 +194,8 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t 
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t row_quads = ((int64_t)p.B * p.H * p.Sq_r + 3) / 4;
+  const int64_t nrows = p.varlen ? (int64_t)p.H * p.T * 128 : (int64_t)p.B * p.H * p.Sq_r;
+  const int64_t row_quads = (nrows + 3) / 4;
   int64_t row_blocks = (row_quads + 7) / 8;                 // 8 warps per block
   const int64_t row_cap = (int64_t)sms * 8;
   if (row_blocks > row_cap) row_blocks = row_cap;
@@ -167,7 +212,8 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t 
 
 cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s) {
   if (p.Sq == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
-  const int64_t blocks = (int64_t)((p.Sq + 16 * kConvRows - 1) / (16 * kConvRows)) * p.B * p.H;
+  const int64_t blocks = p.varlen ? (int64_t)p.H * p.T * (128 / (16 * kConvRows))
+                                  : (int64_t)((p.Sq + 16 * kConvRows - 1) / (16 * kConvRows)) * p.B * p.H;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)blocks);
   if (f16)

@@ -73,6 +73,7 @@ constexpr uint32_t SM_TMEM = 256;       // TMEM base address slot
 constexpr uint32_t SM_ABORT = 260;
 constexpr uint32_t SM_TILE = 264;       // drain scratch words
 constexpr uint32_t SM_RING = 512;       // 2 tile descriptors x 32 B
+constexpr uint32_t SM_VRING = 576;      // packed sequences: 2 sequence descriptors x 32 B
 constexpr uint32_t SM_LSE = 1024;       // 2 stages x 128 fp32
 constexpr uint32_t SM_DSUM = 2048;      // 2 stages x 128 fp32
 
@@ -92,6 +93,32 @@ constexpr int kTileConsumers = 14;
 struct TileDesc {
   int valid, n, b, hk, m_begin, m_count, total, pad;
 };
+
+// With packed sequences, the tile's sequence: its first query / key row in the packed
+// tensors, its lengths, its mask bounds (clamped to +-2^30, which keeps the predicate for
+// lengths up to 2^30) and the slot of its first query tile (fa_tiles.h).
+struct SeqDesc {
+  int q_off, k_off, Sq, Sk, lo, hi;
+  long long slot0;
+};
+
+__device__ __forceinline__ MaskGeom seq_geom(const SeqDesc& v) {
+  MaskGeom g;
+  g.Sq = v.Sq;
+  g.Sk = v.Sk;
+  g.lo = v.lo;
+  g.hi = v.hi;
+  g.tm = kTileQ;
+  g.tn = kTileK;
+  g.Mb = (v.Sq + kTileQ - 1) / kTileQ;
+  g.Nb = (v.Sk + kTileK - 1) / kTileK;
+  return g;
+}
+
+__device__ __forceinline__ int clamp_pm30(long long x) {
+  const long long lim = 1ll << 30;
+  return (int)(x < -lim ? -lim : (x > lim ? lim : x));
+}
 
 // tensor-memory columns
 constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_S = 256, TM_DP = 384;
@@ -243,7 +270,9 @@ __device__ __forceinline__ void mma_dq(uint32_t d, DescWords ds, const TileDescs
 }
 
 // F16: the operands, P^T / dS and the dK / dV outputs are f16 (else bf16).
-template <int DP, bool SOFTCAP, bool F16>
+// VARLEN: packed sequences (per-sequence offsets, lengths and mask bounds from cu_q /
+// cu_k; tiles indexed by slot).  The batched instantiations are unchanged by it.
+template <int DP, bool SOFTCAP, bool F16, bool VARLEN>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ BwdMainParams p,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tq_t,
@@ -334,6 +363,7 @@ __global__ void __launch_bounds__(512, 1)
   // accumulators are handed over between tiles with their own barriers, counted over the
   // tiles that have work (`kt`).
   TileDesc* ring = reinterpret_cast<TileDesc*>(small + SM_RING);
+  SeqDesc* vring = reinterpret_cast<SeqDesc*>(small + SM_VRING);
   auto read_tile = [&](int t, TileDesc& d) -> bool {
     const bool ok = mbar_wait(bar(B_TILEF0 + (t & 1)), (t >> 1) & 1, st, kTimeoutBase - 40);
     if (ok) d = ring[t & 1];
@@ -398,7 +428,24 @@ __global__ void __launch_bounds__(512, 1)
         if (d.valid) {
           const TileCoord c = decode_tile(p, ticket);
           int64_t mb64, me64;
-          m_range(gm, c.n, &mb64, &me64);
+          if constexpr (VARLEN) {
+            int64_t q0, sq, k0, sk;
+            seq_rows(p.cu_q, c.b, p.total_q, &q0, &sq);
+            seq_rows(p.cu_k, c.b, p.total_k, &k0, &sk);
+            const MaskGeom g = make_geom(sq, sk, p.causal, p.window_left, p.window_right, kTileQ, kTileK);
+            m_range(g, c.n, &mb64, &me64);
+            SeqDesc v;
+            v.q_off = (int)q0;
+            v.k_off = (int)k0;
+            v.Sq = (int)sq;
+            v.Sk = (int)sk;
+            v.lo = clamp_pm30(g.lo);
+            v.hi = clamp_pm30(g.hi);
+            v.slot0 = first_slot(p.cu_q, c.b, p.total_q);
+            vring[k] = v;
+          } else {
+            m_range(gm, c.n, &mb64, &me64);
+          }
           d.n = c.n;
           d.b = c.b;
           d.hk = c.hk;
@@ -429,37 +476,47 @@ __global__ void __launch_bounds__(512, 1)
       for (int t = 0; alive; ++t) {
         TileDesc d;
         if (!read_tile_ool(t, d)) break;
+        // map coordinates: batch, first query row, first key row (packed: 0, offsets)
+        int tb = d.b, q_off = 0, k_off = 0;
+        long long slot0 = 0;
+        if constexpr (VARLEN) {
+          const SeqDesc v = vring[t & 1];
+          tb = 0;
+          q_off = v.q_off;
+          k_off = v.k_off;
+          slot0 = v.slot0;
+        }
         mbar_arrive(bar(B_TILEE0 + (t & 1)));
         if (d.total == 0) {
           mbar_arrive(bar(B_NEXT));
           continue;
         }
-        const int n0 = d.n * kTileK;
+        const int n0 = k_off + d.n * kTileK;
         auto load_k = [&]() {
           ++nk;
           mbar_arrive_expect_tx(bar(B_K), G::TILE_BYTES);
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
-            tma_load_4d(sbase + G::OFF_K + pnl * G::FULL_BYTES, &tk, pnl * 64, d.hk, n0, d.b, bar(B_K));
-          if (G::TAIL) tma_load_4d(sbase + G::OFF_K + G::TAIL_OFF, &tk_t, G::NFULL * 64, d.hk, n0, d.b, bar(B_K));
+            tma_load_4d(sbase + G::OFF_K + pnl * G::FULL_BYTES, &tk, pnl * 64, d.hk, n0, tb, bar(B_K));
+          if (G::TAIL) tma_load_4d(sbase + G::OFF_K + G::TAIL_OFF, &tk_t, G::NFULL * 64, d.hk, n0, tb, bar(B_K));
         };
         auto load_v = [&]() {
           ++nv;
           mbar_arrive_expect_tx(bar(B_V), G::TILE_BYTES);
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
-            tma_load_4d(sbase + G::OFF_V + pnl * G::FULL_BYTES, &tv, pnl * 64, d.hk, n0, d.b, bar(B_V));
-          if (G::TAIL) tma_load_4d(sbase + G::OFF_V + G::TAIL_OFF, &tv_t, G::NFULL * 64, d.hk, n0, d.b, bar(B_V));
+            tma_load_4d(sbase + G::OFF_V + pnl * G::FULL_BYTES, &tv, pnl * 64, d.hk, n0, tb, bar(B_V));
+          if (G::TAIL) tma_load_4d(sbase + G::OFF_V + G::TAIL_OFF, &tv_t, G::NFULL * 64, d.hk, n0, tb, bar(B_V));
         };
         const bool kv_busy = nk > 0;  // the previous tile may still be reading K and V
         if (kv_busy) {
           // warm L2 with this tile's K and V so that the loads below, which must wait for
           // the previous tile's last MMAs, hit L2
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl) {
-            tma_prefetch_4d(&tk, pnl * 64, d.hk, n0, d.b);
-            tma_prefetch_4d(&tv, pnl * 64, d.hk, n0, d.b);
+            tma_prefetch_4d(&tk, pnl * 64, d.hk, n0, tb);
+            tma_prefetch_4d(&tv, pnl * 64, d.hk, n0, tb);
           }
           if (G::TAIL) {
-            tma_prefetch_4d(&tk_t, G::NFULL * 64, d.hk, n0, d.b);
-            tma_prefetch_4d(&tv_t, G::NFULL * 64, d.hk, n0, d.b);
+            tma_prefetch_4d(&tk_t, G::NFULL * 64, d.hk, n0, tb);
+            tma_prefetch_4d(&tv_t, G::NFULL * 64, d.hk, n0, tb);
           }
         } else {
           load_k();
@@ -482,9 +539,10 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t qdst = sbase + G::OFF_Q + s * G::TILE_BYTES;
           mbar_arrive_expect_tx(bar(B_QF0 + s), G::TILE_BYTES + 2 * 512);
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
-            tma_load_4d(qdst + pnl * G::FULL_BYTES, &tq, pnl * 64, h, m0, d.b, bar(B_QF0 + s));
-          if (G::TAIL) tma_load_4d(qdst + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, m0, d.b, bar(B_QF0 + s));
-          const size_t row = ((size_t)d.b * p.H + h) * p.Sq_r + m0;
+            tma_load_4d(qdst + pnl * G::FULL_BYTES, &tq, pnl * 64, h, q_off + m0, tb, bar(B_QF0 + s));
+          if (G::TAIL) tma_load_4d(qdst + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, q_off + m0, tb, bar(B_QF0 + s));
+          size_t row = ((size_t)d.b * p.H + h) * p.Sq_r + m0;
+          if constexpr (VARLEN) row = ((size_t)h * p.T + slot0 + m) * kTileQ;
           bulk_load(sbase + SM_LSE + s * 512, p.lse2 + row, 512, bar(B_QF0 + s));
           bulk_load(sbase + SM_DSUM + s * 512, p.dsum + row, 512, bar(B_QF0 + s));
           FA_TR(10, git);
@@ -506,8 +564,8 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t ddst = sbase + G::OFF_DO;
           mbar_arrive_expect_tx(bar(B_DOF0), G::TILE_BYTES);
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
-            tma_load_4d(ddst + pnl * G::FULL_BYTES, &tdo, pnl * 64, h, m0, d.b, bar(B_DOF0));
-          if (G::TAIL) tma_load_4d(ddst + G::TAIL_OFF, &tdo_t, G::NFULL * 64, h, m0, d.b, bar(B_DOF0));
+            tma_load_4d(ddst + pnl * G::FULL_BYTES, &tdo, pnl * 64, h, q_off + m0, tb, bar(B_DOF0));
+          if (G::TAIL) tma_load_4d(ddst + G::TAIL_OFF, &tdo_t, G::NFULL * 64, h, q_off + m0, tb, bar(B_DOF0));
           if (it == 0 && kv_busy) {
             if (!mbar_wait_ool(bar(B_KEMPTY), (nk - 1) & 1, st, kTimeoutBase - 5)) {
               ++git;
@@ -660,6 +718,10 @@ __global__ void __launch_bounds__(512, 1)
     for (int t = 0;; ++t) {
       TileDesc d;
       const bool have_tile = __all_sync(0xffffffffu, read_tile(t, d));
+      SeqDesc vd{};
+      if constexpr (VARLEN) {
+        if (have_tile) vd = vring[t & 1];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_TILEE0 + (t & 1)));
       if (!have_tile) break;
@@ -690,7 +752,8 @@ __global__ void __launch_bounds__(512, 1)
           if (lane == 0) mbar_arrive(bar(B_DQEMPTY));
         }
         if (threadIdx.x == 128) FA_TR(9, git);
-        const size_t tile_id = ((size_t)d.b * p.H + h) * p.Mb + m;
+        size_t tile_id = ((size_t)d.b * p.H + h) * p.Mb + m;
+        if constexpr (VARLEN) tile_id = (size_t)h * p.T + vd.slot0 + m;
         float* dst = p.dq_accum + tile_id * (size_t)(128 * DP);
         int* sem = p.sems + tile_id;
         if (p.deterministic) {
@@ -701,7 +764,10 @@ __global__ void __launch_bounds__(512, 1)
             int stop = (*s_abort) || !ok;
             if (!stop) {
               int64_t nb, ne;
-              n_range(gm, m, &nb, &ne);
+              if constexpr (VARLEN)
+                n_range(seq_geom(vd), m, &nb, &ne);
+              else
+                n_range(gm, m, &nb, &ne);
               const int want = d.n - (int)nb;
               long long t0 = clock64();
               while (true) {
@@ -784,22 +850,37 @@ __global__ void __launch_bounds__(512, 1)
     for (int t = 0; alive; ++t) {
       TileDesc d;
       const bool have_tile = __all_sync(0xffffffffu, read_tile(t, d));
+      // the tile's mask geometry, mask bounds and first key row in dK / dV (packed
+      // sequences: the sequence's own; else the call's)
+      MaskGeom tg = gm;
+      int t_lo = p.lo, t_hi = p.hi, t_sk = p.Sk, k_row0 = 0, tb = d.b;
+      if constexpr (VARLEN) {
+        if (have_tile) {
+          const SeqDesc v = vring[t & 1];
+          tg = seq_geom(v);
+          t_lo = v.lo;
+          t_hi = v.hi;
+          t_sk = v.Sk;
+          k_row0 = v.k_off;
+          tb = 0;
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_TILEE0 + (t & 1)));
       if (!have_tile) break;
       const int j = d.n * kTileK + jl;
-      const bool row_ok = j < p.Sk;
+      const bool row_ok = j < t_sk;
 
       for (int it = 0; it < d.total; ++it, ++git) {
         const int s = git & 1;
         const int g = it / d.m_count;
         const int m = d.m_begin + (it - g * d.m_count);
         const int m0 = m * kTileQ;
-        const bool need_mask = !tile_full(gm, m, d.n);
+        const bool need_mask = !tile_full(tg, m, d.n);
         // visible columns: lo <= (j - i) <= hi with i = m0 + col0 + ql  <=>  ql in [qmin, qmax]
         const int base = j - m0 - col0;
-        const int qmin = row_ok ? max(base - p.hi, -1) : 1 << 20;
-        const int qmax = row_ok ? min(base - p.lo, 1 << 20) : -1;
+        const int qmin = row_ok ? max(base - t_hi, -1) : 1 << 20;
+        const int qmax = row_ok ? min(base - t_lo, 1 << 20) : -1;
         const float* lse = s_lse + s * 128 + col0;
         const float* dsum = s_dsum + s * 128 + col0;
         // Without softcap each lane holds the LSE2 / D of columns lane and 32 + lane of its
@@ -900,8 +981,8 @@ __global__ void __launch_bounds__(512, 1)
         const bool store = acc_ok && *s_abort == 0 && row_ok;
         const uint32_t tcol = which ? TM_DK : TM_DV;
         const float sc = which ? p.dk_scale : 1.f;
-        __nv_bfloat16* row = which ? p.dk + (int64_t)d.b * p.dk_sb + (int64_t)j * p.dk_ss + (int64_t)d.hk * p.dk_sh
-                                   : p.dv + (int64_t)d.b * p.dv_sb + (int64_t)j * p.dv_ss + (int64_t)d.hk * p.dv_sh;
+        __nv_bfloat16* row = which ? p.dk + (int64_t)tb * p.dk_sb + (int64_t)(k_row0 + j) * p.dk_ss + (int64_t)d.hk * p.dk_sh
+                                   : p.dv + (int64_t)tb * p.dv_sb + (int64_t)(k_row0 + j) * p.dv_ss + (int64_t)d.hk * p.dv_sh;
         constexpr int NCH = DP / 16;          // 16-column chunks per accumulator row
         constexpr int NCH0 = (NCH + 1) / 2;   // chunks of warpgroup 0
         const int c0 = wg ? NCH0 : 0;
@@ -984,11 +1065,11 @@ size_t bwd_main_smem_bytes(int Dp) {
   }
 }
 
-template <int DP, bool SC, bool F16>
+template <int DP, bool SC, bool F16, bool VL>
 static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                               const OperandMaps& v, const OperandMaps& d, int num_ctas,
                               cudaStream_t s) {
-  auto kern = bwd_main_kernel<DP, SC, F16>;
+  auto kern = bwd_main_kernel<DP, SC, F16, VL>;
   const size_t smem = Geo<DP>::TOTAL;
   // The in-kernel register split assumes exactly 128 registers per thread at launch.
   cudaFuncAttributes attr;
@@ -1003,15 +1084,20 @@ static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, cons
 
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& d, int Dp, bool softcap,
-                            bool f16, int num_ctas, cudaStream_t s) {
+                            bool f16, bool varlen, int num_ctas, cudaStream_t s) {
   if (num_ctas <= 0) return cudaSuccess;
+#define FA_CASE_VL(DPV, VL)                                                             \
+  if (f16)                                                                              \
+    return softcap ? launch_one<DPV, true, true, VL>(p, q, k, v, d, num_ctas, s)        \
+                   : launch_one<DPV, false, true, VL>(p, q, k, v, d, num_ctas, s);      \
+  return softcap ? launch_one<DPV, true, false, VL>(p, q, k, v, d, num_ctas, s)         \
+                 : launch_one<DPV, false, false, VL>(p, q, k, v, d, num_ctas, s);
 #define FA_CASE(DPV)                                                                    \
   case DPV:                                                                             \
-    if (f16)                                                                            \
-      return softcap ? launch_one<DPV, true, true>(p, q, k, v, d, num_ctas, s)          \
-                     : launch_one<DPV, false, true>(p, q, k, v, d, num_ctas, s);        \
-    return softcap ? launch_one<DPV, true, false>(p, q, k, v, d, num_ctas, s)           \
-                   : launch_one<DPV, false, false>(p, q, k, v, d, num_ctas, s);
+    if (varlen) {                                                                       \
+      FA_CASE_VL(DPV, true)                                                             \
+    }                                                                                   \
+    FA_CASE_VL(DPV, false)
   switch (Dp) {
     FA_CASE(64)
     FA_CASE(80)
@@ -1020,6 +1106,7 @@ cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const 
     default: return cudaErrorInvalidValue;
   }
 #undef FA_CASE
+#undef FA_CASE_VL
 }
 
 }  // namespace fa

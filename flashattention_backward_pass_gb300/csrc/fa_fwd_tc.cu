@@ -157,16 +157,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int h = bh - b * p.H;
   const int hk = h / p.G;
   MaskGeom gm;
-  gm.Sq = p.Sq;
-  gm.Sk = p.Sk;
-  gm.lo = p.lo64;
-  gm.hi = p.hi64;
-  gm.tm = kTileQ;
-  gm.tn = kTileK;
-  gm.Mb = p.Mb;
-  gm.Nb = p.Nb;
-  int64_t nb64, ne64;
-  n_range(gm, m, &nb64, &ne64);
+  int q_off = 0, k_off = 0, tb = b, lo = p.lo, hi = p.hi;  // tb: batch coordinate of the maps
+  if (p.varlen) {
+    // sequence b: rows [cu[b], cu[b+1]) clamped into the packed tensors, so that malformed
+    // offsets cannot move a load or a store outside them
+    const int q0 = min(max(p.cu_q[b], 0), p.total_q), q1 = min(max(p.cu_q[b + 1], q0), p.total_q);
+    const int k0 = min(max(p.cu_k[b], 0), p.total_k), k1 = min(max(p.cu_k[b + 1], k0), p.total_k);
+    q_off = q0;
+    k_off = k0;
+    tb = 0;
+    gm = make_geom(q1 - q0, k1 - k0, p.causal, p.window_left, p.window_right, kTileQ, kTileK);
+    lo = (int)max64(min64(gm.lo, 1ll << 30), -(1ll << 30));
+    hi = (int)max64(min64(gm.hi, 1ll << 30), -(1ll << 30));
+  } else {
+    gm.Sq = p.Sq;
+    gm.Sk = p.Sk;
+    gm.lo = p.lo64;
+    gm.hi = p.hi64;
+    gm.tm = kTileQ;
+    gm.tn = kTileK;
+    gm.Mb = p.Mb;
+    gm.Nb = p.Nb;
+  }
+  const int Sq = (int)gm.Sq, Sk = (int)gm.Sk;
+  int64_t nb64 = 0, ne64 = 0;
+  if (m < gm.Mb) n_range(gm, m, &nb64, &ne64);  // a shorter sequence may have no tile m
   const int n_begin = (int)nb64;
   const int total = (*s_abort) ? 0 : (int)(ne64 - nb64);
   const int m0 = m * kTileQ;
@@ -181,11 +196,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (total > 0) {
         mbar_arrive_expect_tx(bar(F_Q), G::TILE_BYTES);
         for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, h, m0, b, bar(F_Q));
-        if (G::TAIL) tma_load_4d(sbase + G::OFF_Q + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, m0, b, bar(F_Q));
+          tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, h, q_off + m0, tb, bar(F_Q));
+        if (G::TAIL) tma_load_4d(sbase + G::OFF_Q + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, q_off + m0, tb, bar(F_Q));
       }
       for (int it = 0; it < total; ++it) {
-        const int n0 = (n_begin + it) * kTileK;
+        const int n0 = k_off + (n_begin + it) * kTileK;
         const int ks = it % G::KST;
         if (it >= G::KST &&
             !mbar_wait(bar(F_KE0 + ks), ((it - G::KST) / G::KST) & 1, st, kFwdTimeout - 1))
@@ -193,8 +208,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t kdst = sbase + G::OFF_K + ks * G::TILE_BYTES;
         mbar_arrive_expect_tx(bar(F_KF0 + ks), G::TILE_BYTES);
         for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(kdst + pn * G::FULL_BYTES, &tk, pn * 64, hk, n0, b, bar(F_KF0 + ks));
-        if (G::TAIL) tma_load_4d(kdst + G::TAIL_OFF, &tk_t, G::NFULL * 64, hk, n0, b, bar(F_KF0 + ks));
+          tma_load_4d(kdst + pn * G::FULL_BYTES, &tk, pn * 64, hk, n0, tb, bar(F_KF0 + ks));
+        if (G::TAIL) tma_load_4d(kdst + G::TAIL_OFF, &tk_t, G::NFULL * 64, hk, n0, tb, bar(F_KF0 + ks));
         issued_k[ks] = it / G::KST + 1;
         const int vs = it % G::VST;
         if (it >= G::VST &&
@@ -203,8 +218,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t vdst = sbase + G::OFF_V + vs * G::TILE_BYTES;
         mbar_arrive_expect_tx(bar(F_VF0 + vs), G::TILE_BYTES);
         for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(vdst + pn * G::FULL_BYTES, &tv, pn * 64, hk, n0, b, bar(F_VF0 + vs));
-        if (G::TAIL) tma_load_4d(vdst + G::TAIL_OFF, &tv_t, G::NFULL * 64, hk, n0, b, bar(F_VF0 + vs));
+          tma_load_4d(vdst + pn * G::FULL_BYTES, &tv, pn * 64, hk, n0, tb, bar(F_VF0 + vs));
+        if (G::TAIL) tma_load_4d(vdst + G::TAIL_OFF, &tv_t, G::NFULL * 64, hk, n0, tb, bar(F_VF0 + vs));
         issued_v[vs] = it / G::VST + 1;
       }
       // every copy this thread started must land before the CTA may exit
@@ -274,8 +289,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int kb = n * kTileK;  // key index of column 0
       const bool need_mask = !tile_full(gm, m, n);
       // visible columns: lo <= key - i <= hi and key < Sk  <=>  c in [cmin, cmax]
-      const int cmin = max(i + p.lo - kb, -1);
-      const int cmax = min(min(i + p.hi - kb, p.Sk - 1 - kb), 1 << 20);
+      const int cmin = max(i + lo - kb, -1);
+      const int cmax = min(min(i + hi - kb, Sk - 1 - kb), 1 << 20);
       const uint32_t sbuf = t_lane + ((it & 1) ? FT_S1 : FT_S0);
       if (!warp_wait(bar(F_SF0 + (it & 1)), (it >> 1) & 1, st, kFwdTimeout - 30)) {
         alive = false;
@@ -323,10 +338,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (alive && total > 0) have = warp_wait(bar(F_ACC), 0, st, kFwdTimeout - 32);
     if (have) tc_fence_after();
     if (__all_sync(0xffffffffu, *s_abort == 0)) {
-      const bool row_ok = i < p.Sq;
+      const bool row_ok = i < Sq;
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (int64_t)b * p.o_sb + (int64_t)i * p.o_ss +
-                       (int64_t)h * p.o_sh;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (int64_t)tb * p.o_sb +
+                       (int64_t)(q_off + i) * p.o_ss + (int64_t)h * p.o_sh;
 #pragma unroll
       for (int c = 0; c < DP / 16; ++c) {
         uint32_t o[16];
@@ -350,7 +365,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (row_ok) {
         const float lse = lrow > 0.f ? (mrow + log2f(lrow)) * 0.69314718055994531f
                                      : __int_as_float(0x7f800000);
-        p.lse[(int64_t)b * p.lse_sb + (int64_t)h * p.lse_sh + (int64_t)i * p.lse_ss] = lse;
+        p.lse[(int64_t)tb * p.lse_sb + (int64_t)h * p.lse_sh + (int64_t)(q_off + i) * p.lse_ss] = lse;
       }
     }
   }

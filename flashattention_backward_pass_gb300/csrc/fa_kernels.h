@@ -28,6 +28,12 @@ struct BwdPreParams {
   float4* zero_ptr;              // dQ accumulator + counters, zeroed here
   int64_t zero_count;            // in float4 units
   int* header;                   // status word + tile ticket, zeroed here
+  // packed sequences (varlen != 0): dout / out / lse are (1, total_q, H, D) / (1, H,
+  // total_q) views, B sequences, rows laid out per head in T slots of 128 (fa_tiles.h)
+  int varlen;
+  const int* cu_q;
+  int total_q;
+  int64_t T;
 };
 
 struct BwdMainParams {
@@ -56,6 +62,14 @@ struct BwdMainParams {
   __nv_bfloat16* dq;
   int64_t dq_sb, dq_ss, dq_sh;
   long long wait_limit;
+  // packed sequences (the VARLEN kernel): q, k, v, dout, dk, dv are (1, total, H, D)
+  // views; B sequences; Nb / Mb count the tiles of the longest one; dQ tiles, LSE2 / D
+  // rows and counters are indexed per head by slot (fa_tiles.h: first_slot, T slots)
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
+  long long T;
+  int causal, window_left, window_right;
 };
 
 struct BwdConvParams {
@@ -64,6 +78,11 @@ struct BwdConvParams {
   int64_t dq_sb, dq_ss, dq_sh;
   int B, H, Sq, D, Dp, Mb;
   float scale;
+  // packed sequences (varlen != 0): dq is a (1, total_q, H, D) view; tiles by slot
+  int varlen;
+  const int* cu_q;
+  int total_q;
+  int64_t T;
 };
 
 
@@ -82,6 +101,16 @@ struct FwdTcParams {
   int64_t lse_sb, lse_sh, lse_ss;
   int* status;                   // timeout status word, or null
   long long wait_limit;
+  // Packed variable-length sequences (varlen != 0): q, k, v and o are (1, total, H, D)
+  // views, B is the number of sequences and sequence b owns rows [cu_q[b], cu_q[b+1]) of
+  // q / o and [cu_k[b], cu_k[b+1]) of k / v; Mb counts the query tiles of the longest
+  // sequence.  The mask is bottom-right aligned per sequence, so lo / hi are derived per
+  // sequence from causal and the window sizes.
+  int varlen;
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
+  int causal, window_left, window_right;
 };
 
 // Tensor maps for one bf16 (B, S, H, D) operand: a 64-column 128B-swizzled box and,
@@ -93,10 +122,10 @@ struct OperandMaps {
 
 size_t bwd_main_smem_bytes(int Dp);
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t s);
-// f16: the 16-bit operands and outputs are f16 (else bf16)
+// f16: the 16-bit operands and outputs are f16 (else bf16); varlen: packed sequences
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
-                            bool f16, int num_ctas, cudaStream_t s);
+                            bool f16, bool varlen, int num_ctas, cudaStream_t s);
 cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s);
 // dK/dV kernel (num_kv_ctas = key tiles x batch x kv-heads) then dQ kernel (num_q_ctas =
 // query tiles x batch x q-heads), both on stream s.

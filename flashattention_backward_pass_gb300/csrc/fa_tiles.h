@@ -106,4 +106,42 @@ FA_HD bool tile_full(const MaskGeom& g, int64_t m, int64_t n) {
   return dmin >= g.lo && dmax <= g.hi && (n * g.tn + g.tn) <= g.Sk;
 }
 
+// ------------------------------------------------------------------ packed sequences
+//
+// A variable-length batch packs B sequences along the row axis: sequence b owns query
+// rows [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]).  Offsets are clamped into
+// [0, total] before use, so malformed offsets cannot address rows outside the tensors.
+FA_HD int64_t clamp_row(int64_t x, int64_t total) { return x < 0 ? 0 : (x > total ? total : x); }
+
+FA_HD void seq_rows(const int* cu, int b, int64_t total, int64_t* start, int64_t* len) {
+  const int64_t a = clamp_row(cu[b], total), e = clamp_row(cu[b + 1], total);
+  *start = a;
+  *len = e > a ? e - a : 0;
+}
+
+// The backward's per-head tile layout for packed sequences: the 128-row query tiles of
+// sequence b take the slots [first_slot(b), first_slot(b) + ceil(Sq_b / 128)), with
+// first_slot(b) = floor(cu_q[b] / 128) + b.  For non-decreasing offsets the ranges of
+// different sequences never overlap (floor((a + s) / 128) >= floor(a / 128) +
+// floor(s / 128) and ceil(s / 128) <= floor(s / 128) + 1), and slot_count slots cover
+// all of them; with clamped offsets every slot index stays below slot_count even when
+// the offsets are malformed.
+FA_HD int64_t first_slot(const int* cu_q, int b, int64_t total_q) {
+  return clamp_row(cu_q[b], total_q) / 128 + b;
+}
+FA_HD int64_t slot_count(int64_t total_q, int64_t B) { return total_q / 128 + B; }
+
+// The sequence whose slot range starts at or before slot t (the largest such b).
+FA_HD int slot_owner(const int* cu_q, int B, int64_t total_q, int64_t t) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (first_slot(cu_q, mid, total_q) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
 }  // namespace fa

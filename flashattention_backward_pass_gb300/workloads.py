@@ -9,6 +9,7 @@ definition.
 
 from __future__ import annotations
 
+import itertools
 import math
 from dataclasses import dataclass, field
 
@@ -101,3 +102,23 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None, dtype=torch.
 
 def custom(name, B, Sq, Sk, H, Hk, D, **kw) -> Workload:
     return Workload(name, B, Sq, Sk, H, Hk, D, **kw)
+
+
+def make_varlen_inputs(lengths_q, lengths_k, H, Hk, D, seed=0, device="cpu", dtype=torch.bfloat16,
+                       do_std=1.0):
+    """Packed sequences: q, do (sum(lengths_q), H, D), k, v (sum(lengths_k), Hk, D), drawn
+    like make_inputs (N(0, 1), dO scaled by do_std) from a seeded CPU generator, and the
+    int32 offsets cu_q, cu_k (length batch + 1, starting at 0)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    tq, tk = int(sum(lengths_q)), int(sum(lengths_k))
+    q = torch.randn(tq, H, D, generator=g, dtype=torch.float32)
+    k = torch.randn(tk, Hk, D, generator=g, dtype=torch.float32)
+    v = torch.randn(tk, Hk, D, generator=g, dtype=torch.float32)
+    do = torch.randn(tq, H, D, generator=g, dtype=torch.float32) * do_std
+    cu_q = torch.tensor([0] + list(itertools.accumulate(lengths_q)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(itertools.accumulate(lengths_k)), dtype=torch.int32)
+    out = [t.to(dtype) for t in (q, k, v, do)] + [cu_q, cu_k]
+    if device != "cpu":
+        out = [t.to(device) for t in out]
+    return out

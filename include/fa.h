@@ -88,7 +88,11 @@ const char* fa_status_string(int status);
 
 /*
  * Workspace the forward needs, in bytes (0 for this build: the forward keeps its
- * statistics in registers and writes O and LSE directly).
+ * statistics in registers and tensor memory and writes O and LSE directly).  A caller
+ * may still pass a workspace of at least 256 bytes (16-byte aligned): a device-side wait
+ * of the forward that runs out of time then records FA_ERR_DEVICE_TIMEOUT in its status
+ * word, which fa_bwd_status reads and clears.  Without one, such a timeout only stops
+ * the affected CTAs.
  */
 size_t fa_fwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D);
 
@@ -103,6 +107,32 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
            fa_tensor* out, fa_tensor* lse,
            float softmax_scale, int causal, int window_left, int window_right,
            float softcap, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_fwd_varlen — the forward over a batch of packed sequences of different lengths
+ * (the Triton page's `flash_attn_varlen_func` / `set_varlen_params`: cu_seqlens_q,
+ * cu_seqlens_k, max_seqlen_q, max_seqlen_k).  Sequence b owns rows
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q / out and [cu_seqlens_k[b], cu_seqlens_k[b+1])
+ * of k / v, and is computed exactly as a batch of one of that length (the mask is
+ * bottom-right aligned per sequence).
+ *   q, out (total_q, H, D) and k, v (total_k, Hk, D): ndim 3, same 16-bit type;
+ *   lse (H, total_q) fp32, natural log (+inf for a row with no visible key);
+ *   cu_seqlens_q / cu_seqlens_k: DEVICE int32 arrays of batch + 1 non-decreasing offsets
+ *     starting at 0 (caller-owned; read by the kernels, not by the host);
+ *   max_seqlen_q / max_seqlen_k: at least the longest sequence (rows of a longer one are
+ *     not computed) and at most total_q / total_k.
+ * Offsets outside [0, total] are clamped into the tensors, so malformed offsets cannot
+ * make the kernels access memory outside them (their results are then undefined).
+ * batch == 0, total_q == 0 or max_seqlen_q == 0 returns FA_OK without a launch.  Errors
+ * as fa_fwd, plus FA_ERR_ARG for batch < 0 or max lengths outside [0, total] and
+ * FA_ERR_UNSUPPORTED for batch > 65535.
+ */
+int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+                  fa_tensor* out, fa_tensor* lse,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  int max_seqlen_q, int max_seqlen_k,
+                  float softmax_scale, int causal, int window_left, int window_right,
+                  float softcap, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Workspace the backward needs, in bytes, for the given problem.  It holds the fp32
@@ -138,6 +168,33 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
            fa_tensor* dq, fa_tensor* dk, fa_tensor* dv,
            float softmax_scale, int causal, int window_left, int window_right, float softcap,
            int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace of fa_bwd_varlen, in bytes: per q-head, total_q / 128 + batch tiles of 128
+ * query rows (each sequence's query tiles are consecutive; the slack is at most one
+ * partial tile per sequence) for the fp32 dQ accumulator, D and LSE2, plus counters and
+ * the status word.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_varlen_workspace_size(int batch, int H, int total_q, int D, int deterministic);
+
+/*
+ * fa_bwd_varlen — the backward over packed sequences (the layouts and sequence offsets of
+ * fa_fwd_varlen): dout, out, dq (total_q, H, D); k, v, dk, dv (total_k, Hk, D); lse
+ * (H, total_q) fp32 natural log as fa_fwd_varlen writes it.  Every sequence is computed
+ * exactly as a batch of one of its length (bottom-right aligned mask per sequence).  The
+ * fused algorithm only (FA_ERR_UNSUPPORTED while the split one is selected); the
+ * workspace must hold fa_bwd_varlen_workspace_size bytes.  Offset clamping, argument
+ * errors and the status word as in fa_fwd_varlen and fa_bwd.  dK / dV rows of key rows
+ * that no sequence owns are left untouched.
+ */
+int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
+                  const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
+                  fa_tensor* dq, fa_tensor* dk, fa_tensor* dv,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  int max_seqlen_q, int max_seqlen_k,
+                  float softmax_scale, int causal, int window_left, int window_right,
+                  float softcap, int deterministic, void* workspace, size_t workspace_bytes,
+                  void* stream);
 
 /*
  * fa_bwd_status — waits for `stream`, then reads the device status word that the last

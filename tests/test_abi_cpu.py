@@ -149,3 +149,51 @@ def test_fwd_validation_codes(lib):
     l0 = _view((1, 2, 0), dtype=1)
     assert lib.fa_fwd(ctypes.byref(q0), ctypes.byref(k), ctypes.byref(v), ctypes.byref(o0), ctypes.byref(l0),
                       ctypes.c_float(0.1), 0, -1, -1, ctypes.c_float(0), None, 0, None) == 0
+
+
+def _varlen_fwd(lib, q=None, lse=None, cu=4096, batch=2, mq=100, mk=100, **kw):
+    tq, H, D = 300, 2, 64
+    qv = q or _view((tq, H, D))
+    kv = _view((250, H, D))
+    out = _view((tq, H, D))
+    lv = lse or _view((H, tq), dtype=1)
+    return lib.fa_fwd_varlen(ctypes.byref(qv), ctypes.byref(kv), ctypes.byref(kv), ctypes.byref(out),
+                             ctypes.byref(lv), cu, cu, batch, mq, mk, 0.125, 0, -1, -1, 0.0,
+                             None, 0, None)
+
+
+def test_varlen_validation(lib):
+    assert _varlen_fwd(lib, q=_view((1, 300, 2, 64))) == -2            # q must be (total, H, D)
+    assert _varlen_fwd(lib, lse=_view((1, 2, 300), dtype=1)) == -2     # lse must be (H, total)
+    assert _varlen_fwd(lib, lse=_view((2, 299), dtype=1)) == -2        # lse rows != total_q
+    assert _varlen_fwd(lib, batch=-1) == -9                            # negative batch
+    assert _varlen_fwd(lib, mq=301) == -9                              # max_seqlen_q > total_q
+    assert _varlen_fwd(lib, mk=-1) == -9
+    assert _varlen_fwd(lib, batch=70000) == -8                         # above the grid limit
+    assert _varlen_fwd(lib, cu=None) == -1                             # offsets missing
+    assert _varlen_fwd(lib, batch=0) == 0                              # nothing to do, no launch
+    assert _varlen_fwd(lib, mq=0) == 0
+    # the backward: split algorithm refused for packed sequences, before any launch
+    tq, tk, H, D = 300, 250, 2, 64
+    a = [_view((tq, H, D)), _view((tq, H, D)), _view((tk, H, D)), _view((tk, H, D)),
+         _view((tq, H, D)), _view((H, tq), dtype=1), _view((tq, H, D)), _view((tk, H, D)),
+         _view((tk, H, D))]
+    args = [ctypes.byref(x) for x in a]
+    assert lib.fa_bwd_set_algorithm(0) == 0
+    try:
+        assert lib.fa_bwd_varlen(*args, 4096, 4096, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
+                                 ctypes.c_void_p(4096), 1 << 30, None) == -8
+    finally:
+        assert lib.fa_bwd_set_algorithm(1) == 0
+    assert lib.fa_bwd_varlen(*args, 4096, 4096, 0, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
+                             ctypes.c_void_p(4096), 1 << 30, None) == 0           # batch 0
+    assert lib.fa_bwd_varlen(*args, 4096, 4096, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
+                             ctypes.c_void_p(4096), 16, None) == -7               # workspace
+    # workspace: per head total_q // 128 + batch slots of 128 rows
+    f = lib.fa_bwd_varlen_workspace_size
+    f.restype = ctypes.c_size_t
+    T = 300 // 128 + 2
+    rows = H * T * 128
+    want = 256 + rows * 4 + rows * 4 + rows * 64 * 4 + ((H * T * 4 + 15) // 16) * 16
+    want = (want + 255) // 256 * 256
+    assert f(2, H, 300, 64, 0) == want

@@ -71,3 +71,67 @@ def test_tile_ranges_brute_force(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "bad=0" in r.stdout
+
+
+SLOTS_HARNESS = r'''
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+#include "fa_tiles.h"
+using namespace fa;
+// Packed sequences: every query tile of every sequence gets its own slot below
+// slot_count, and slot_owner maps each used slot back to its sequence.  Also run with
+// malformed (decreasing, negative, too large) offsets, where only the bound must hold.
+int main() {
+  long bad = 0, cases = 0;
+  srand(7);
+  for (int trial = 0; trial < 3000; ++trial) {
+    const int B = 1 + rand() % 12;
+    std::vector<int> cu(B + 1, 0);
+    const bool malformed = trial % 5 == 4;
+    for (int b = 0; b < B; ++b) {
+      int len = rand() % 4 == 0 ? 0 : rand() % 700;
+      if (rand() % 6 == 0) len = 128 * (1 + rand() % 3);
+      cu[b + 1] = cu[b] + len;
+    }
+    long total = cu[B];
+    if (malformed) {
+      for (int b = 0; b <= B; ++b) cu[b] = rand() % 1500 - 300;
+      total = rand() % 1200;
+    }
+    const long T = slot_count(total, B);
+    std::vector<int> owner(T, -1);
+    for (int b = 0; b < B; ++b) {
+      long s0, len;
+      seq_rows(cu.data(), b, total, &s0, &len);
+      if (s0 < 0 || s0 + len > total) ++bad;
+      const long fs = first_slot(cu.data(), b, total);
+      for (long m = 0; m * 128 < len; ++m) {
+        const long t = fs + m;
+        ++cases;
+        if (t < 0 || t >= T) { ++bad; continue; }
+        if (malformed) continue;
+        if (owner[t] != -1) ++bad;
+        owner[t] = b;
+        if (slot_owner(cu.data(), B, total, t) != b) ++bad;
+      }
+    }
+  }
+  printf("cases=%ld bad=%ld\n", cases, bad);
+  return bad != 0;
+}
+'''
+
+
+def test_packed_sequence_slots(tmp_path):
+    gxx = shutil.which("g++") or shutil.which("c++")
+    if gxx is None:
+        pytest.skip("no C++ compiler")
+    src = tmp_path / "slots.cpp"
+    src.write_text(SLOTS_HARNESS)
+    exe = tmp_path / "slots"
+    inc = os.path.join(ROOT, "flashattention_backward_pass_gb300", "csrc")
+    subprocess.run([gxx, "-O2", "-std=c++17", "-I", inc, str(src), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "bad=0" in r.stdout
