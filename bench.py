@@ -6,6 +6,7 @@ workload B=4, Sq=Sk=2048, H=32, Hk=8, D=128), inputs resident in HBM, L2 flushed
 (256 MiB write) between steps outside the timed events.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py --varlen [--workload NAME]   (packed sequences of mixed lengths; own line)
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
 same workload (one batch x one kv-head group per step).  Under torchrun (N > 1) every
@@ -348,6 +349,104 @@ def run_reference(args, ws_, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+VARLEN_MIX = (0.375, 0.25, 0.125, 0.125, 0.0625, 0.03125, 0.03125)
+
+
+def _mix(total):
+    lens = [int(total * f) for f in VARLEN_MIX]
+    lens[0] += total - sum(lens)
+    return lens
+
+
+def run_varlen(args, ws_, local):
+    """fa_bwd_varlen over the workload's tokens packed as sequences of mixed lengths
+    (VARLEN_MIX of B*Sq query and B*Sk key rows; each sequence its own bottom-right mask)."""
+    import torch
+    import flashattention_backward_pass_gb300 as fa
+    from flashattention_backward_pass_gb300 import _abi
+    from flashattention_backward_pass_gb300.workloads import WORKLOADS, Workload, make_varlen_inputs
+
+    w = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load()
+    lq, lk = _mix(w.B * w.Sq), _mix(w.B * w.Sk)
+    q, k, v, do, cu_q, cu_k = make_varlen_inputs(lq, lk, w.H, w.Hk, w.D, seed=w.seed, device=dev,
+                                                 do_std=w.do_std)
+    kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right,
+              softcap=w.softcap)
+    mq, mk = max(lq), max(lk)
+    out, lse = fa.attention_forward_varlen(q, k, v, cu_q, cu_k, mq, mk, w.scale, **kw)
+    dq, dk, dv = torch.empty_like(q), torch.zeros_like(k), torch.zeros_like(v)
+    wsp = torch.empty(fa.bwd_varlen_workspace_size(len(lq), w.H, q.shape[0], w.D, args.deterministic),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    seqs = [Workload("seq", 1, a, b, w.H, w.Hk, w.D, w.causal, w.window_left, w.window_right,
+                     w.softcap) for a, b in zip(lq, lk)]
+    nominal = sum(x.nominal_flops for x in seqs)
+    algorithmic = sum(x.algorithmic_flops for x in seqs)
+
+    def step():
+        fa.fa_bwd_varlen(do, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, mq, mk, w.scale,
+                         deterministic=args.deterministic, workspace=wsp, **kw)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert fa.fa_bwd_status(wsp) == 0
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    status = fa.fa_bwd_status(wsp)
+    _abi.profile_enable(True)
+    split = []
+    for _ in range(min(args.steps, 20)):
+        flush.zero_()
+        step()
+        split.append(_abi.profile_read())
+    _abi.profile_enable(False)
+    fwd = []
+    for _ in range(min(args.steps, 20)):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fa.fa_fwd_varlen(q, k, v, out, lse, cu_q, cu_k, mq, mk, w.scale, **kw)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        fwd.append(e0.elapsed_time(e1))
+    t = sum(ms) / len(ms)
+    main_ms = statistics.mean(x[1] for x in split)
+    peaks, _ = _peaks()
+    return {"metric": METRIC, "value": round(nominal / (t * 1e-3) / 1e12, 3), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, packed sequences)",
+            "config": dict(w.describe(), workload=w.name + "+varlen", lengths_q=lq, lengths_k=lk,
+                           deterministic=bool(args.deterministic),
+                           l2="flushed between steps (256 MiB write, outside the timed events)",
+                           flop_convention="per sequence 10*H*Sq*Sk*D, halved for causal"),
+            "main_kernel": {"ms": round(main_ms, 4),
+                            "achieved_tflops": round(algorithmic / (main_ms * 1e-3) / 1e12, 2),
+                            "frac_of_peak": round(algorithmic / (main_ms * 1e-3) / 1e12
+                                                  / float(peaks["bf16_tflops"]), 4)},
+            "kernel_ms": {"preprocess": round(statistics.mean(x[0] for x in split), 4),
+                          "main": round(main_ms, 4),
+                          "convert": round(statistics.mean(x[2] for x in split), 4)},
+            "forward_ms": round(statistics.median(fwd), 4),
+            "forward_tflops": round(0.4 * algorithmic / (statistics.median(fwd) * 1e-3) / 1e12, 2),
+            "device_status": status}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -359,9 +458,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--varlen", action="store_true",
+                    help="time fa_bwd_varlen on the workload's tokens packed as a length mix "
+                         "(a separate line, not the headline)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws_, rank, local = _dist()
+
+    if args.varlen:
+        if rank == 0:
+            print(json.dumps(run_varlen(args, ws_, local)), flush=True)
+        return
 
     if args.impl == "reference":
         if rank != 0:

@@ -26,8 +26,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // lane in flight.  Blocks [row_blocks, gridDim.x) clear the accumulator and the counters
 // with 16-byte stores.  The two kinds of blocks run side by side, so the latency-bound row
 // reductions overlap the bandwidth-bound clearing.
-// F16: dO and O are f16 (else bf16).
-template <bool F16>
+// F16: dO and O are f16 (else bf16).  VARLEN: packed sequences (rows by slot).
+template <bool F16, bool VARLEN>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p, int row_blocks) {
   if (blockIdx.x == 0 && threadIdx.x < 4) p.header[threadIdx.x] = 0;
   if ((int)blockIdx.x >= row_blocks) {
@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;  // row within the warp's group of 4
   const int l8 = lane & 7;    // 16-column slice of the row
-  const int64_t nrows = p.varlen ? (int64_t)p.H * p.T * 128 : (int64_t)p.B * p.H * p.Sq_r;
+  const int64_t nrows = VARLEN ? (int64_t)p.H * p.T * 128 : (int64_t)p.B * p.H * p.Sq_r;
   const int64_t warps_total = (int64_t)row_blocks * (blockDim.x >> 5);
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
 
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
     bool real = false;
     const bool valid_row = r < nrows;
     if (valid_row) {
-      if (p.varlen) {
+      if constexpr (VARLEN) {
         // per head T slots of 128 rows; slot t belongs to sequence slot_owner(t)
         const int64_t tile = r >> 7;
         h = tile / p.T;
@@ -203,10 +203,18 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t 
   int64_t zero_blocks = (p.zero_count + 255) / 256;
   const int64_t zero_cap = (int64_t)sms * 8;
   if (zero_blocks > zero_cap) zero_blocks = zero_cap;
-  if (f16)
-    bwd_preprocess_kernel<true><<<(unsigned)(row_blocks + zero_blocks), 256, 0, s>>>(p, (int)row_blocks);
-  else
-    bwd_preprocess_kernel<false><<<(unsigned)(row_blocks + zero_blocks), 256, 0, s>>>(p, (int)row_blocks);
+  const unsigned grid = (unsigned)(row_blocks + zero_blocks);
+  if (p.varlen) {
+    if (f16)
+      bwd_preprocess_kernel<true, true><<<grid, 256, 0, s>>>(p, (int)row_blocks);
+    else
+      bwd_preprocess_kernel<false, true><<<grid, 256, 0, s>>>(p, (int)row_blocks);
+  } else {
+    if (f16)
+      bwd_preprocess_kernel<true, false><<<grid, 256, 0, s>>>(p, (int)row_blocks);
+    else
+      bwd_preprocess_kernel<false, false><<<grid, 256, 0, s>>>(p, (int)row_blocks);
+  }
   return cudaGetLastError();
 }
 
