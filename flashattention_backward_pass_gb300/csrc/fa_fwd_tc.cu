@@ -10,8 +10,10 @@
 //   S = Q K^T        (M = 128 queries, N = 128 keys, K = Dp; both operands K-major)
 //   P = exp2(z * log2e - m)  written as 16-bit pairs over the S columns already read
 //   O (+)= P V       (A = P from tensor memory, B = V read MN-major, N = Dp)
-// Each softmax thread owns one query row (= TMEM lane) and all 128 columns of the score
-// tile, so the row maximum and row sum need no exchange between threads.
+// Two softmax warpgroups split the 128 key columns of the score tile: thread (warpgroup
+// w, TMEM lane r) owns query row r and columns [64w, 64w + 64).  The two halves of a
+// row's maximum meet through shared memory once per key tile; each warpgroup keeps the
+// row sum of its own columns and the two are added at the end.
 //
 // The running maximum m is only moved (and O, l rescaled by exp2(m_old - m_new)) when
 // a new score exceeds it by more than 8 in log2 units; otherwise the stale m is kept and
@@ -19,10 +21,10 @@
 // the same m, so the result is exact up to rounding either way.  After the first key
 // tiles a rescale is rare.
 //
-// Warp roles (8 warps): warp 0 TMA producer (Q once, K and V per key tile into 3- and
-// 2-stage rings); warp 1 TMEM allocator and single MMA-issuing thread; warps 4-7 softmax
-// and epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31).  Warps 2-3 only join the CTA
-// barriers.
+// Warp roles (12 warps): warp 0 TMA producer of Q (once) and of the 3-stage K ring;
+// warp 2 TMA producer of the 2-stage V ring; warp 1 TMEM allocator and single
+// MMA-issuing thread; warps 4-11 two softmax / epilogue warpgroups (warp w reads TMEM
+// lanes 32 (w % 4) .. +31).  Warp 3 only joins the CTA barriers.
 //
 // Tensor memory: S double buffer [0, 128) and [128, 256) (P written over its first 32
 // columns of each 64-column half), O accumulator [256, 256 + Dp).
@@ -34,13 +36,15 @@ namespace fa {
 
 namespace {
 
-constexpr int kFwdThreads = 256;
+constexpr int kFwdThreads = 384;
 constexpr int kFwdTimeout = -1400;
 
 constexpr uint32_t FSM_BAR = 0;     // mbarriers
 constexpr uint32_t FSM_TMEM = 256;  // TMEM base address slot
 constexpr uint32_t FSM_ABORT = 260;
-constexpr uint32_t FSMALL = 1024;
+constexpr uint32_t FSM_MAX = 1024;  // [2 parities][2 warpgroups][128 rows] fp32 row maxima
+constexpr uint32_t FSM_L = 3072;    // [2 warpgroups][128 rows] fp32 row sums (epilogue)
+constexpr uint32_t FSMALL = 4096;
 
 template <int DP>
 struct GeoF : Panels<DP> {
@@ -64,51 +68,49 @@ constexpr uint32_t FT_S0 = 0, FT_S1 = 128, FT_O = 256;
 
 constexpr float kNegInf = -__builtin_huge_valf();
 
-// Scores of one row of the tile in log2 units (scale * s * log2e, or with softcap
-// c * log2e * tanh(scale * s / c)); masked columns (MASK: visible iff cmin <= column <=
-// cmax) are -inf.  Returns the row maximum.
+// Scores of this thread's 64 columns of its row in log2 units (scale * s * log2e, or
+// with softcap c * log2e * tanh(scale * s / c)); `sbuf` addresses column col0 of the
+// row; masked columns (MASK: visible iff cmin <= column <= cmax, columns of the whole
+// tile) are -inf.  Returns the maximum over the 64.
 template <bool MASK, bool SOFTCAP>
-__device__ __forceinline__ float fwd_scores(const SoftmaxConsts& kc, uint32_t sbuf, int cmin,
-                                            int cmax, float (&x)[128]) {
+__device__ __forceinline__ float fwd_scores(const SoftmaxConsts& kc, uint32_t sbuf, int col0,
+                                            int cmin, int cmax, float (&x)[64]) {
   float mx = kNegInf;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint32_t r[32];
     tmem_ld32(sbuf + c * 32, r);
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      const int col = c * 32 + e;
+      const int col = col0 + c * 32 + e;
       const float s = __uint_as_float(r[e]);
       float v = SOFTCAP ? kc.cap_log2 * tanh_exp2(s * kc.cap_scale) : s * kc.scale_log2;
       if (MASK) v = (col >= cmin && col <= cmax) ? v : kNegInf;
-      x[col] = v;
+      x[c * 32 + e] = v;
       mx = fmaxf(mx, v);
     }
   }
   return mx;
 }
 
-// P = exp2(x - m) as 16-bit pairs over the S columns: columns [0, 64) of the row go to
-// TMEM columns [0, 32), columns [64, 128) to [64, 96) (the A layout the P V product
-// reads).  Returns the row sum of P (fp32, before rounding).
+// P = exp2(x - m) for the thread's 64 columns as 16-bit pairs over the first 32 of them
+// (`sbuf` = column col0): columns [0, 64) of the row land in TMEM columns [0, 32),
+// columns [64, 128) in [64, 96), the A layout the P V product reads.  Returns the sum of
+// the 64 P values (fp32, before rounding).
 template <bool F16>
-__device__ __forceinline__ float fwd_probs(uint32_t sbuf, float m, const float (&x)[128]) {
+__device__ __forceinline__ float fwd_probs(uint32_t sbuf, float m, const float (&x)[64]) {
   float sum = 0.f;
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
+  for (int q = 0; q < 2; ++q) {
+    uint32_t pk[16];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int col = hh * 64 + q * 32 + 2 * e;
-        const float p0 = ex2_approx(x[col] - m);
-        const float p1 = ex2_approx(x[col + 1] - m);
-        sum += p0 + p1;
-        pk[e] = pack_h2<F16>(p0, p1);
-      }
-      tmem_st16(sbuf + hh * 64 + q * 16, pk);
+    for (int e = 0; e < 16; ++e) {
+      const float p0 = ex2_approx(x[q * 32 + 2 * e] - m);
+      const float p1 = ex2_approx(x[q * 32 + 2 * e + 1] - m);
+      sum += p0 + p1;
+      pk[e] = pack_h2<F16>(p0, p1);
     }
+    tmem_st16(sbuf + q * 16, pk);
   }
   return sum;
 }
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (p.status) atomicExch(p.status, kFwdTimeout - 99);
       *s_abort = 1;
     }
-    for (int i = 0; i < F_COUNT; ++i) mbar_init(bar(i), (i == F_PF0 || i == F_PF1) ? 4 : 1);
+    for (int i = 0; i < F_COUNT; ++i) mbar_init(bar(i), (i == F_PF0 || i == F_PF1) ? 8 : 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -186,14 +188,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int total = (*s_abort) ? 0 : (int)(ne64 - nb64);
   const int m0 = m * kTileQ;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 0 loads Q and the K ring, warp 2 the V ring: each refills a stage as soon as
+    // its own last reader is done (K: the stage's S product, V: its P V product), so a K
+    // load never waits behind a V stage that is still being read.
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      int issued_k[G::KST] = {}, issued_v[G::VST] = {};
-      if (total > 0) {
+      const bool kside = warp == 0;
+      const CUtensorMap* tm = kside ? &tk : &tv;
+      const CUtensorMap* tm_t = kside ? &tk_t : &tv_t;
+      const int nst = kside ? G::KST : G::VST;
+      const uint32_t base = sbase + (kside ? G::OFF_K : G::OFF_V);
+      const int full0 = kside ? F_KF0 : F_VF0, empty0 = kside ? F_KE0 : F_VE0;
+      tma_prefetch_desc(tm);
+      int issued[G::KST] = {};
+      if (kside && total > 0) {
+        tma_prefetch_desc(&tq);
         mbar_arrive_expect_tx(bar(F_Q), G::TILE_BYTES);
         for (int pn = 0; pn < G::NFULL; ++pn)
           tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, h, q_off + m0, tb, bar(F_Q));
@@ -201,35 +211,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       for (int it = 0; it < total; ++it) {
         const int n0 = k_off + (n_begin + it) * kTileK;
-        const int ks = it % G::KST;
-        if (it >= G::KST &&
-            !mbar_wait(bar(F_KE0 + ks), ((it - G::KST) / G::KST) & 1, st, kFwdTimeout - 1))
+        const int ks = it % nst;
+        if (it >= nst && !mbar_wait(bar(empty0 + ks), ((it - nst) / nst) & 1, st, kFwdTimeout - 1))
           break;
-        const uint32_t kdst = sbase + G::OFF_K + ks * G::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(F_KF0 + ks), G::TILE_BYTES);
+        const uint32_t dst = base + ks * G::TILE_BYTES;
+        mbar_arrive_expect_tx(bar(full0 + ks), G::TILE_BYTES);
         for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(kdst + pn * G::FULL_BYTES, &tk, pn * 64, hk, n0, tb, bar(F_KF0 + ks));
-        if (G::TAIL) tma_load_4d(kdst + G::TAIL_OFF, &tk_t, G::NFULL * 64, hk, n0, tb, bar(F_KF0 + ks));
-        issued_k[ks] = it / G::KST + 1;
-        const int vs = it % G::VST;
-        if (it >= G::VST &&
-            !mbar_wait(bar(F_VE0 + vs), ((it - G::VST) / G::VST) & 1, st, kFwdTimeout - 2))
-          break;
-        const uint32_t vdst = sbase + G::OFF_V + vs * G::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(F_VF0 + vs), G::TILE_BYTES);
-        for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(vdst + pn * G::FULL_BYTES, &tv, pn * 64, hk, n0, tb, bar(F_VF0 + vs));
-        if (G::TAIL) tma_load_4d(vdst + G::TAIL_OFF, &tv_t, G::NFULL * 64, hk, n0, tb, bar(F_VF0 + vs));
-        issued_v[vs] = it / G::VST + 1;
+          tma_load_4d(dst + pn * G::FULL_BYTES, tm, pn * 64, hk, n0, tb, bar(full0 + ks));
+        if (G::TAIL) tma_load_4d(dst + G::TAIL_OFF, tm_t, G::NFULL * 64, hk, n0, tb, bar(full0 + ks));
+        issued[ks] = it / nst + 1;
       }
       // every copy this thread started must land before the CTA may exit
       volatile int no_abort = 0;
       AbortState dr{&no_abort, p.status, p.wait_limit};
-      if (total > 0) mbar_wait(bar(F_Q), 0, dr, kFwdTimeout - 3);
-      for (int s = 0; s < G::KST; ++s)
-        if (issued_k[s]) mbar_wait(bar(F_KF0 + s), (issued_k[s] - 1) & 1, dr, kFwdTimeout - 3);
-      for (int s = 0; s < G::VST; ++s)
-        if (issued_v[s]) mbar_wait(bar(F_VF0 + s), (issued_v[s] - 1) & 1, dr, kFwdTimeout - 3);
+      if (kside && total > 0) mbar_wait(bar(F_Q), 0, dr, kFwdTimeout - 3);
+      for (int s2 = 0; s2 < nst; ++s2)
+        if (issued[s2]) mbar_wait(bar(full0 + s2), (issued[s2] - 1) & 1, dr, kFwdTimeout - 3);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -276,14 +273,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + epilogue
+    const int wg = (warp - 4) >> 2;        // key half of the score tile (columns 64 wg ..)
     const int qd = warp & 3;               // TMEM lane quadrant
     const int r = qd * 32 + lane;          // query row inside the tile = TMEM lane
+    const int col0 = wg * 64;
     const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
     const int i = m0 + r;
     const SoftmaxConsts kc{p.scale_log2, p.cap_scale, p.cap_log2};
+    float* s_max = reinterpret_cast<float*>(smem_raw + FSM_MAX);
+    float* s_l = reinterpret_cast<float*>(smem_raw + FSM_L);
+    // O columns this warpgroup rescales and stores: 16-column chunks [c_lo, c_hi)
+    constexpr int NCH = DP / 16;
+    constexpr int NCH0 = (NCH + 1) / 2;
+    const int c_lo = wg ? NCH0 : 0, c_hi = wg ? NCH : NCH0;
     float mrow = kNegInf;  // running maximum (log2 units); moved only by more than 8
-    float lrow = 0.f;      // running sum of P relative to mrow
-    bool alive = true;
+    float lrow = 0.f;      // running sum of this warpgroup's P relative to mrow
     for (int it = 0; it < total; ++it) {
       const int n = n_begin + it;
       const int kb = n * kTileK;  // key index of column 0
@@ -291,16 +295,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // visible columns: lo <= key - i <= hi and key < Sk  <=>  c in [cmin, cmax]
       const int cmin = max(i + lo - kb, -1);
       const int cmax = min(min(i + hi - kb, Sk - 1 - kb), 1 << 20);
-      const uint32_t sbuf = t_lane + ((it & 1) ? FT_S1 : FT_S0);
-      if (!warp_wait(bar(F_SF0 + (it & 1)), (it >> 1) & 1, st, kFwdTimeout - 30)) {
-        alive = false;
-        break;
+      const uint32_t sbuf = t_lane + ((it & 1) ? FT_S1 : FT_S0) + col0;
+      const bool ok = warp_wait(bar(F_SF0 + (it & 1)), (it >> 1) & 1, st, kFwdTimeout - 30);
+      float x[64];
+      float mx = kNegInf;
+      if (ok) {
+        tc_fence_after();
+        mx = need_mask ? fwd_scores<true, SOFTCAP>(kc, sbuf, col0, cmin, cmax, x)
+                       : fwd_scores<false, SOFTCAP>(kc, sbuf, col0, cmin, cmax, x);
       }
-      tc_fence_after();
-      float x[128];
-      const float mx = need_mask ? fwd_scores<true, SOFTCAP>(kc, sbuf, cmin, cmax, x)
-                                 : fwd_scores<false, SOFTCAP>(kc, sbuf, cmin, cmax, x);
-      // move the reference maximum only when a score passes it by more than 8 (log2)
+      // the row maximum over both halves; both warpgroups always reach this barrier, and
+      // after it both see the abort flag that a failed wait of either one has raised
+      s_max[((it & 1) * 2 + wg) * 128 + r] = mx;
+      named_bar_sync(1, 256);
+      if (*s_abort) break;
+      mx = fmaxf(mx, s_max[((it & 1) * 2 + (wg ^ 1)) * 128 + r]);
+      // move the reference maximum only when a score passes it by more than 8 (log2);
+      // both warpgroups take the same decision for a row
       float alpha = 1.f;
       if (it == 0) {
         mrow = mx;
@@ -312,18 +323,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       lrow = lrow * alpha + fwd_probs<F16>(sbuf, muse, x);
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
         // O holds the products up to key tile it-1: wait for the last one, then rescale
-        if (!warp_wait(bar(F_OD), (it - 1) & 1, st, kFwdTimeout - 31)) {
-          alive = false;
-          break;
-        }
+        // this warpgroup's columns of it (on a failed wait the next barrier ends the loop)
+        if (!warp_wait(bar(F_OD), (it - 1) & 1, st, kFwdTimeout - 31)) continue;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < DP / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld16(t_lane + FT_O + c * 16, o);
+        for (int c = 0; c < NCH0; ++c) {
+          if (c_lo + c < c_hi) {
+            uint32_t o[16];
+            tmem_ld16(t_lane + FT_O + (c_lo + c) * 16, o);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st16(t_lane + FT_O + c * 16, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(t_lane + FT_O + (c_lo + c) * 16, o);
+          }
         }
       }
       tmem_wait_st();
@@ -332,38 +343,44 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (lane == 0) mbar_arrive(bar(F_PF0 + (it & 1)));
     }
 
-    // O = acc / l and LSE = (m + log2 l) * ln 2; a row with no visible key gives O = 0
-    // and LSE = +inf
+    // O = acc / l and LSE = (m + log2 l) * ln 2 with l the sum of both halves; a row with
+    // no visible key gives O = 0 and LSE = +inf
     bool have = false;
-    if (alive && total > 0) have = warp_wait(bar(F_ACC), 0, st, kFwdTimeout - 32);
+    if (!*s_abort && total > 0) have = warp_wait(bar(F_ACC), 0, st, kFwdTimeout - 32);
+    s_l[wg * 128 + r] = lrow;
+    named_bar_sync(1, 256);
+    const float lsum = lrow + s_l[(wg ^ 1) * 128 + r];
     if (have) tc_fence_after();
     if (__all_sync(0xffffffffu, *s_abort == 0)) {
       const bool row_ok = i < Sq;
-      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (int64_t)tb * p.o_sb +
                        (int64_t)(q_off + i) * p.o_ss + (int64_t)h * p.o_sh;
 #pragma unroll
-      for (int c = 0; c < DP / 16; ++c) {
-        uint32_t o[16];
-        if (have) {
-          tmem_ld16(t_lane + FT_O + c * 16, o);
-        } else {
+      for (int cc = 0; cc < NCH0; ++cc) {
+        const int c = c_lo + cc;
+        if (c < c_hi) {
+          uint32_t o[16];
+          if (have) {
+            tmem_ld16(t_lane + FT_O + c * 16, o);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = 0u;
-        }
-        uint32_t pk[8];
+            for (int e = 0; e < 16; ++e) o[e] = 0u;
+          }
+          uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          pk[e] = pack_h2<F16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-        if (row_ok) {
-          if (c * 16 < p.D)
-            *reinterpret_cast<uint4*>(orow + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          if (c * 16 + 8 < p.D)
-            *reinterpret_cast<uint4*>(orow + c * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          for (int e = 0; e < 8; ++e)
+            pk[e] = pack_h2<F16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+          if (row_ok) {
+            if (c * 16 < p.D)
+              *reinterpret_cast<uint4*>(orow + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (c * 16 + 8 < p.D)
+              *reinterpret_cast<uint4*>(orow + c * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
         }
       }
-      if (row_ok) {
-        const float lse = lrow > 0.f ? (mrow + log2f(lrow)) * 0.69314718055994531f
+      if (row_ok && wg == 0) {
+        const float lse = lsum > 0.f ? (mrow + log2f(lsum)) * 0.69314718055994531f
                                      : __int_as_float(0x7f800000);
         p.lse[(int64_t)tb * p.lse_sb + (int64_t)h * p.lse_sh + (int64_t)(q_off + i) * p.lse_ss] = lse;
       }

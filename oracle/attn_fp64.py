@@ -34,6 +34,10 @@ Readings where the pages are silent (listed with reasons in the design notes):
   window_right >= 0) and j >= i + (Sk - Sq) - window_left (when window_left >= 0);
   causal forces window_right = 0.  A negative window bound is unbounded.
 * a query row with no visible key has O = 0, LSE = +inf, P = 0 and dQ = 0.
+* block sparsity (the sm90 page's `blocksparse_tensors` give, per key block, the query
+  blocks to visit): an optional (B, H, ceil(Sq/bs), ceil(Sk/bs)) boolean block mask; a
+  (query block, key block) pair with a 0 entry is masked out entirely, on top of the
+  element mask above.  All ones changes nothing.
 
 Parity of every public function here is pinned by tests/test_oracle.py against
 finite differences, closed forms, invariants and brute-force loops.
@@ -114,6 +118,27 @@ def _head_backward(do, q, k, v, scale, vis, softcap):
     return dq, dk, dv, dsum, dict(o=o, lse=lse, p=p, dp=dp, dz=dz, da=da)
 
 
+def _block_vis(vis, block_mask_bh, block_size):
+    """The element mask restricted to the kept (query block, key block) pairs."""
+    if block_mask_bh is None:
+        return vis
+    Sq, Sk = vis.shape
+    bm = np.asarray(block_mask_bh, dtype=bool)
+    rows = np.arange(Sq) // block_size
+    cols = np.arange(Sk) // block_size
+    return vis & bm[rows[:, None], cols[None, :]]
+
+
+def _check_block_mask(block_mask, B, H, Sq, Sk, block_size):
+    if block_mask is None:
+        return None
+    bm = np.asarray(block_mask, dtype=bool)
+    want = (B, H, -(-Sq // block_size), -(-Sk // block_size))
+    if bm.shape != want:
+        raise ValueError(f"block_mask must be {want}, got {bm.shape}")
+    return bm
+
+
 def _check_shapes(q, k, v):
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
         raise ValueError("q, k, v must be (B, S, H, D)")
@@ -127,7 +152,7 @@ def _check_shapes(q, k, v):
 
 
 def attention_forward(q, k, v, scale, causal=False, window_left=-1, window_right=-1,
-                      softcap=0.0):
+                      softcap=0.0, block_mask=None, block_size=128):
     """O (B,Sq,H,D) and natural-log LSE (B,H,Sq), both float64.
 
     q (B,Sq,H,D), k/v (B,Sk,Hk,D).  q-head h reads kv-head h // (H/Hk) (GQA/MQA page,
@@ -139,19 +164,21 @@ def attention_forward(q, k, v, scale, causal=False, window_left=-1, window_right
     B, Sq, Sk, H, Hk, D = _check_shapes(q, k, v)
     G = H // Hk
     vis = visible_mask(Sq, Sk, causal, window_left, window_right)
+    bm = _check_block_mask(block_mask, B, H, Sq, Sk, block_size)
     o = np.zeros((B, Sq, H, D))
     lse = np.zeros((B, H, Sq))
     for b in range(B):
         for h in range(H):
             hk = h // G
-            oh, lh, _, _ = _head_forward(q[b, :, h], k[b, :, hk], v[b, :, hk], scale, vis, softcap)
+            vbh = _block_vis(vis, None if bm is None else bm[b, h], block_size)
+            oh, lh, _, _ = _head_forward(q[b, :, h], k[b, :, hk], v[b, :, hk], scale, vbh, softcap)
             o[b, :, h] = oh
             lse[b, h] = lh
     return o, lse
 
 
 def attention_backward(do, q, k, v, scale, causal=False, window_left=-1, window_right=-1,
-                       softcap=0.0, return_dsum=False):
+                       softcap=0.0, return_dsum=False, block_mask=None, block_size=128):
     """dQ (B,Sq,H,D), dK and dV (B,Sk,Hk,D), float64; optionally D (B,H,Sq).
 
     O and P are this module's own fp64 forward (no GPU value enters).  dK/dV of a
@@ -167,6 +194,7 @@ def attention_backward(do, q, k, v, scale, causal=False, window_left=-1, window_
         raise ValueError("do must match q")
     G = H // Hk
     vis = visible_mask(Sq, Sk, causal, window_left, window_right)
+    bm = _check_block_mask(block_mask, B, H, Sq, Sk, block_size)
     dq = np.zeros((B, Sq, H, D))
     dk = np.zeros((B, Sk, Hk, D))
     dv = np.zeros((B, Sk, Hk, D))
@@ -174,8 +202,9 @@ def attention_backward(do, q, k, v, scale, causal=False, window_left=-1, window_
     for b in range(B):
         for h in range(H):
             hk = h // G
+            vbh = _block_vis(vis, None if bm is None else bm[b, h], block_size)
             dqh, dkh, dvh, dh, _ = _head_backward(do[b, :, h], q[b, :, h], k[b, :, hk],
-                                                  v[b, :, hk], scale, vis, softcap)
+                                                  v[b, :, hk], scale, vbh, softcap)
             dq[b, :, h] = dqh
             dk[b, :, hk] += dkh
             dv[b, :, hk] += dvh

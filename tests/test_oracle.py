@@ -333,7 +333,7 @@ def test_no_keys_at_all():
 
 # ---------------------------------------------------------------- brute force
 
-def _brute(do, q, k, v, scale, causal, wl, wr, cap):
+def _brute(do, q, k, v, scale, causal, wl, wr, cap, block_mask=None, bs=1):
     """Explicit scalar loops from the definition, one (b, h) at a time."""
     B, Sq, H, D = q.shape
     Sk, Hk = k.shape[1], k.shape[2]
@@ -351,6 +351,8 @@ def _brute(do, q, k, v, scale, causal, wl, wr, cap):
                     if wr >= 0 and j > i + Sk - Sq + wr:
                         continue
                     if wl >= 0 and j < i + Sk - Sq - wl:
+                        continue
+                    if block_mask is not None and not block_mask[b, h, i // bs, j // bs]:
                         continue
                     s = sum(q[b, i, h, d] * k[b, j, hk, d] for d in range(D))
                     a = scale * s
@@ -393,6 +395,80 @@ def test_brute_force_loops(var):
     np.testing.assert_allclose(dq, dQ, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(dk, dK, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(dv, dV, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- block sparsity
+
+def _bs_inputs(seed, B=1, Sq=5, Sk=7, H=2, Hk=1, D=3):
+    rng = np.random.default_rng(seed)
+    return (_rand((B, Sq, H, D), rng), _rand((B, Sk, Hk, D), rng), _rand((B, Sk, Hk, D), rng),
+            _rand((B, Sq, H, D), rng), rng)
+
+
+@pytest.mark.parametrize("var", VARIANTS[:3])
+def test_block_mask_brute_force(var):
+    """A random block mask (blocks of 2) against the scalar loops that skip the pairs
+    of removed blocks."""
+    q, k, v, do, rng = _bs_inputs(21)
+    bm = rng.random((1, 2, 3, 4)) < 0.6
+    bm[0, 1, 0, :] = False            # a query block with no key block at all
+    O, L, dQ, dK, dV = _brute(do, q, k, v, 0.7, var["causal"], var["window_left"],
+                              var["window_right"], var["softcap"], block_mask=bm, bs=2)
+    o, lse = attention_forward(q, k, v, 0.7, block_mask=bm, block_size=2, **var)
+    dq, dk, dv = attention_backward(do, q, k, v, 0.7, block_mask=bm, block_size=2, **var)
+    np.testing.assert_allclose(o, O, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, L, rtol=1e-13)
+    np.testing.assert_allclose(dq, dQ, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dk, dK, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv, dV, rtol=1e-12, atol=1e-13)
+    assert np.all(np.isposinf(lse[0, 1, :2])) and np.all(o[0, :2, 1] == 0)
+
+
+def test_block_mask_special_cases():
+    q, k, v, do, rng = _bs_inputs(22)
+    # all ones: no effect
+    ones = np.ones((1, 2, 1, 1), dtype=bool)
+    np.testing.assert_array_equal(attention_forward(q, k, v, 0.5, block_mask=ones)[0],
+                                  attention_forward(q, k, v, 0.5)[0])
+    # blocks of one element, lower-triangular (bottom-right aligned): the causal mask
+    tri = np.zeros((1, 2, 5, 7), dtype=bool)
+    for i in range(5):
+        tri[0, :, i, :i + 2 + 1] = True   # j <= i + (Sk - Sq)
+    o1, l1 = attention_forward(q, k, v, 0.5, block_mask=tri, block_size=1)
+    o2, l2 = attention_forward(q, k, v, 0.5, causal=True)
+    np.testing.assert_allclose(o1, o2, rtol=1e-14)
+    np.testing.assert_allclose(l1, l2, rtol=1e-14)
+    g1 = attention_backward(do, q, k, v, 0.5, block_mask=tri, block_size=1)
+    g2 = attention_backward(do, q, k, v, 0.5, causal=True)
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-15)
+    # nothing kept: O = 0, LSE = +inf, every gradient 0
+    none = np.zeros((1, 2, 1, 1), dtype=bool)
+    o, lse = attention_forward(q, k, v, 0.5, block_mask=none)
+    assert np.all(o == 0) and np.all(np.isposinf(lse))
+    for g in attention_backward(do, q, k, v, 0.5, block_mask=none):
+        assert np.all(g == 0)
+
+
+def test_block_mask_finite_differences():
+    """The block-masked loss L = sum(dO * O) has the oracle's gradients."""
+    q, k, v, do, rng = _bs_inputs(23, Sq=4, Sk=5)
+    bm = np.array([[[[True, False, True], [False, True, True]],
+                    [[False, True, True], [True, True, False]]]])  # (1, 2, 2, 3), blocks of 2
+    kw = dict(block_mask=bm, block_size=2, softcap=1.5)
+    loss = lambda q_, k_, v_: float((attention_forward(q_, k_, v_, 0.6, **kw)[0] * do).sum())
+    dq, dk, dv = attention_backward(do, q, k, v, 0.6, **kw)
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [xp if y is x else y for y in (q, k, v)]
+            args_m = [xm if y is x else y for y in (q, k, v)]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
 
 
 # ---------------------------------------------------------------- stored regression values
