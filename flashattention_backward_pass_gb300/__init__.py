@@ -18,13 +18,15 @@ import math
 
 import torch
 
-from ._abi import (FaError, alloc_bwd_workspace, bwd_varlen_workspace_size, bwd_workspace_size,
-                   fa_bwd, fa_bwd_status, fa_bwd_varlen, fa_fwd, fa_fwd_varlen, load)
+from ._abi import (FaError, alloc_bwd_workspace, bwd_blocksparse_workspace_size,
+                   bwd_varlen_workspace_size, bwd_workspace_size, fa_bwd, fa_bwd_blocksparse,
+                   fa_bwd_status, fa_bwd_varlen, fa_fwd, fa_fwd_blocksparse, fa_fwd_varlen, load)
 
 __all__ = ["FaError", "alloc_bwd_workspace", "attention_backward", "attention_backward_varlen",
            "attention_forward", "attention_forward_varlen", "bwd_varlen_workspace_size",
            "bwd_workspace_size", "fa_bwd", "fa_bwd_status", "fa_bwd_varlen", "fa_fwd",
-           "fa_fwd_varlen", "load"]
+           "fa_fwd_varlen", "load", "fa_fwd_blocksparse", "fa_bwd_blocksparse",
+           "bwd_blocksparse_workspace_size"]
 
 
 def _scale(q, softmax_scale):

@@ -90,6 +90,17 @@ def load(path: str = LIB_PATH):
                                   ctypes.c_float, vp, sz, vp]
     lib.fa_bwd_varlen_workspace_size.restype = sz
     lib.fa_bwd_varlen_workspace_size.argtypes = [ctypes.c_int] * 5
+    if not hasattr(lib, "fa_fwd_blocksparse"):  # a library built before block sparsity
+        _lib = lib
+        return lib
+    lib.fa_fwd_blocksparse.restype = ctypes.c_int
+    lib.fa_fwd_blocksparse.argtypes = [P, P, P, P, P, vp, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_float, vp, sz, vp]
+    lib.fa_bwd_blocksparse_workspace_size.restype = sz
+    lib.fa_bwd_blocksparse_workspace_size.argtypes = [ctypes.c_int] * 6
+    lib.fa_bwd_blocksparse.restype = ctypes.c_int
+    lib.fa_bwd_blocksparse.argtypes = [P, P, P, P, P, P, P, P, P, vp, ctypes.c_float, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, sz, vp]
     lib.fa_bwd_varlen.restype = ctypes.c_int
     lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, ip, ip, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
@@ -278,4 +289,48 @@ def fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_
                            ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                            _stream_ptr(stream))
     _check(st, "fa_bwd_varlen")
+    return workspace
+
+
+# ------------------------------------------------------------------ block sparsity
+
+def _block_mask_ptr(bm, q, k):
+    B, Sq, H = q.shape[0], q.shape[1], q.shape[2]
+    Sk = k.shape[1]
+    want = (B, H, -(-Sq // 128), -(-Sk // 128))
+    if bm.dtype != torch.uint8 or not bm.is_cuda or tuple(bm.shape) != want or not bm.is_contiguous():
+        raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor of shape {want}")
+    return ctypes.c_void_p(bm.data_ptr())
+
+
+def fa_fwd_blocksparse(q, k, v, out, lse, block_mask, softmax_scale, causal=False, window_left=-1,
+                       window_right=-1, softcap=0.0, stream=None):
+    """C call `fa_fwd_blocksparse` (block_mask: uint8 (B, H, ceil(Sq/128), ceil(Sk/128)))."""
+    lib = load()
+    tv = [tensor_view(x) for x in (q, k, v, out, lse)]
+    st = lib.fa_fwd_blocksparse(*[ctypes.byref(x) for x in tv], _block_mask_ptr(block_mask, q, k),
+                                float(softmax_scale), int(bool(causal)), int(window_left),
+                                int(window_right), float(softcap), None, 0, _stream_ptr(stream))
+    _check(st, "fa_fwd_blocksparse")
+
+
+def bwd_blocksparse_workspace_size(B, H, Hk, Sq, Sk, D) -> int:
+    return int(load().fa_bwd_blocksparse_workspace_size(B, H, Hk, Sq, Sk, D))
+
+
+def fa_bwd_blocksparse(dout, q, k, v, out, lse, dq, dk, dv, block_mask, softmax_scale, causal=False,
+                       window_left=-1, window_right=-1, softcap=0.0, workspace=None, stream=None):
+    """C call `fa_bwd_blocksparse` (dq, dk, dv written in place).  Returns the workspace."""
+    lib = load()
+    if workspace is None:
+        B, Sq, H, D = q.shape
+        n = bwd_blocksparse_workspace_size(B, H, k.shape[2], Sq, k.shape[1], D)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
+    st = lib.fa_bwd_blocksparse(*[ctypes.byref(x) for x in tv], _block_mask_ptr(block_mask, q, k),
+                                float(softmax_scale), int(bool(causal)), int(window_left),
+                                int(window_right), float(softcap),
+                                ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                _stream_ptr(stream))
+    _check(st, "fa_bwd_blocksparse")
     return workspace

@@ -284,9 +284,11 @@ size_t fa_fwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D) {
   return 0;
 }
 
-int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out,
-           fa_tensor* lse, float softmax_scale, int causal, int window_left, int window_right,
-           float softcap, void* workspace, size_t workspace_bytes, void* stream) {
+// The batched forward; block_mask (null = dense) is the (B, H, Mb, Nb) tile mask.
+static int fwd_common(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out,
+                      fa_tensor* lse, float softmax_scale, int causal, int window_left,
+                      int window_right, float softcap, void* workspace, size_t workspace_bytes,
+                      void* stream, const uint8_t* block_mask) {
   int B, Sq, Sk, H, Hk, D, dt;
   int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &dt);
   if (st) return st;
@@ -317,6 +319,7 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor
                  ? (int*)workspace + WS_STATUS
                  : nullptr;
   p.wait_limit = g_wait_limit;
+  p.block_mask = block_mask;
   const cudaStream_t s = (cudaStream_t)stream;
   if (Sk == 0)  // no key: O = 0 and LSE = +inf (tensor maps need a non-empty key extent)
     return launch_fwd_empty(p, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -328,6 +331,22 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor
   if (launch_fwd_tc(p, mq, mk, mv, Dp, softcap > 0.f, dt == FA_DTYPE_F16, s) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
+}
+
+int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out,
+           fa_tensor* lse, float softmax_scale, int causal, int window_left, int window_right,
+           float softcap, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_common(q, k, v, out, lse, softmax_scale, causal, window_left, window_right, softcap,
+                    workspace, workspace_bytes, stream, nullptr);
+}
+
+int fa_fwd_blocksparse(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+                       fa_tensor* out, fa_tensor* lse, const uint8_t* block_mask,
+                       float softmax_scale, int causal, int window_left, int window_right,
+                       float softcap, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!block_mask) return FA_ERR_NULL;
+  return fwd_common(q, k, v, out, lse, softmax_scale, causal, window_left, window_right, softcap,
+                    workspace, workspace_bytes, stream, block_mask);
 }
 
 int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out,
@@ -405,7 +424,7 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
                       fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, float softmax_scale, int causal,
                       int window_left, int window_right, float softcap, int deterministic,
                       void* workspace, size_t workspace_bytes, void* stream,
-                      const VarlenArgs* vl) {
+                      const VarlenArgs* vl, const uint8_t* block_mask) {
   int B, Sq, Sk, H, Hk, D, dt;
   int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &dt);
   if (st) return st;
@@ -415,8 +434,10 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
   if ((st = check_h16_4d(dk, dt, B, Sk, Hk, D))) return st;
   if ((st = check_h16_4d(dv, dt, B, Sk, Hk, D))) return st;
   const bool f16 = dt == FA_DTYPE_F16;
-  // the split algorithm is built for batched bf16 only
-  if ((f16 || vl) && g_bwd_algorithm == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;
+  // the split algorithm is built for batched dense bf16 only; block sparsity has no ordered
+  // (deterministic) mode
+  if ((f16 || vl || block_mask) && g_bwd_algorithm == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;
+  if (block_mask && deterministic) return FA_ERR_UNSUPPORTED;
   if ((st = check_lse(lse, B, H, Sq))) return st;
   if ((st = check_scalars(softmax_scale, softcap))) return st;
   const int total_q = Sq, total_k = Sk;  // packed: the row extents of the views
@@ -437,6 +458,17 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
     return FA_ERR_SHAPE;
   if (vl) L.Mb = (Sq + kTileQ - 1) / kTileQ;  // query tiles of the longest sequence
   const long long T = vl ? slot_count(total_q, B) : 0;
+  // block sparsity: per key-tile ticket a step count and a list of G * Mb entries after
+  // the regular regions
+  const int Nb_all = (Sk + kTileK - 1) / kTileK;
+  size_t off_sp_counts = 0, off_sp_lists = 0;
+  if (block_mask) {
+    if (L.Mb > 65535) return FA_ERR_UNSUPPORTED;  // list entries hold the query tile in 16 bits
+    const size_t tiles = (size_t)Nb_all * B * Hk;
+    off_sp_counts = L.total;
+    off_sp_lists = align_up(off_sp_counts + tiles * 4, 256);
+    L.total = align_up(off_sp_lists + tiles * (size_t)(H / Hk) * L.Mb * 4, 256);
+  }
   if (!workspace || workspace_bytes < L.total) return FA_ERR_WORKSPACE;
   if (!is_aligned16(workspace)) return FA_ERR_ALIGNMENT;
   cudaStream_t s = (cudaStream_t)stream;
@@ -541,8 +573,25 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return FA_ERR_CUDA;
     const int grid = num_ctas < sms ? num_ctas : sms;
-    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, f16, vl != nullptr, grid, s) !=
-        cudaSuccess)
+    if (block_mask) {
+      BwdSparseParams sp;
+      memset(&sp, 0, sizeof(sp));
+      sp.block_mask = block_mask;
+      sp.B = B; sp.H = H; sp.Hk = Hk; sp.G = H / Hk; sp.Sq = Sq; sp.Sk = Sk;
+      sp.Mb = L.Mb; sp.Nb = Nb;
+      sp.lo64 = lo;
+      sp.hi64 = hi;
+      sp.counts = (int*)(ws + off_sp_counts);
+      sp.lists = (int*)(ws + off_sp_lists);
+      sp.stride = (long long)(H / Hk) * L.Mb;
+      sp.num_tiles = num_ctas;
+      if (launch_bwd_sparse_lists(sp, s) != cudaSuccess) return FA_ERR_CUDA;
+      p.sp_counts = sp.counts;
+      p.sp_lists = sp.lists;
+      p.sp_stride = sp.stride;
+    }
+    const int mode = vl ? 1 : (block_mask ? 2 : 0);
+    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, f16, mode, grid, s) != cudaSuccess)
       return FA_ERR_CUDA;
   }
 
@@ -572,7 +621,26 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
            void* stream) {
   return bwd_common(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal, window_left,
                     window_right, softcap, deterministic, workspace, workspace_bytes, stream,
-                    nullptr);
+                    nullptr, nullptr);
+}
+
+size_t fa_bwd_blocksparse_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D) {
+  BwdLayout L;
+  if (Hk <= 0 || Sk < 0 || !bwd_layout(B, H, Sq, D, &L)) return 0;
+  const size_t tiles = (size_t)((Sk + kTileK - 1) / kTileK) * B * Hk;
+  const size_t lists = align_up(L.total + tiles * 4, 256);
+  return align_up(lists + tiles * (size_t)(H / Hk) * L.Mb * 4, 256);
+}
+
+int fa_bwd_blocksparse(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
+                       const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
+                       fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, const uint8_t* block_mask,
+                       float softmax_scale, int causal, int window_left, int window_right,
+                       float softcap, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!block_mask) return FA_ERR_NULL;
+  return bwd_common(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal, window_left,
+                    window_right, softcap, 0, workspace, workspace_bytes, stream, nullptr,
+                    block_mask);
 }
 
 size_t fa_bwd_varlen_workspace_size(int batch, int H, int total_q, int D, int deterministic) {
@@ -599,7 +667,7 @@ int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
   VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k};
   return bwd_common(&d4, &q4, &k4, &v4, &o4, &l3, &dq4, &dk4, &dv4, softmax_scale, causal,
                     window_left, window_right, softcap, deterministic, workspace,
-                    workspace_bytes, stream, &vl);
+                    workspace_bytes, stream, &vl, nullptr);
 }
 
 int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* device_status) {

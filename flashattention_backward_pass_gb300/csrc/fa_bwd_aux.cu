@@ -232,3 +232,64 @@ cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s)
 }
 
 }  // namespace fa
+
+namespace fa {
+
+namespace {
+
+// Block-sparse step lists: warp t handles key-tile ticket t (the main kernel's
+// key-tile-major order: n = t / (B Hk), then b, then hk).  Its candidate steps are the
+// main kernel's dense sequence — q-head g of the group outer, query tile m in the
+// element mask's range inner — and it keeps those whose block-mask byte
+// block_mask[b, hk*G + g, m, n] is set, compacted in order with warp ballots.
+__global__ void __launch_bounds__(256) bwd_sparse_lists_kernel(const BwdSparseParams p) {
+  const int t = (int)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+  const int lane = threadIdx.x & 31;
+  if (t >= p.num_tiles) return;
+  const int per_n = p.B * p.Hk;
+  const int n = t / per_n;
+  const int r = t - n * per_n;
+  const int b = r / p.Hk;
+  const int hk = r - b * p.Hk;
+  MaskGeom gm;
+  gm.Sq = p.Sq;
+  gm.Sk = p.Sk;
+  gm.lo = p.lo64;
+  gm.hi = p.hi64;
+  gm.tm = kTileQ;
+  gm.tn = kTileK;
+  gm.Mb = p.Mb;
+  gm.Nb = p.Nb;
+  int64_t mb, me;
+  m_range(gm, n, &mb, &me);
+  const int mc = (int)(me - mb);
+  const int total = mc * p.G;
+  int* out = p.lists + (size_t)t * p.stride;
+  int kept = 0;
+  for (int c0 = 0; c0 < total; c0 += 32) {
+    const int c = c0 + lane;
+    int g = 0, m = 0;
+    bool keep = false;
+    if (c < total) {
+      g = c / mc;
+      m = (int)mb + (c - g * mc);
+      const int h = hk * p.G + g;
+      keep = p.block_mask[(((size_t)b * p.H + h) * p.Mb + m) * (size_t)p.Nb + n] != 0;
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (keep) out[kept + __popc(bal & ((1u << lane) - 1u))] = (g << 16) | m;
+    kept += __popc(bal);
+  }
+  if (lane == 0) p.counts[t] = kept;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_sparse_lists(const BwdSparseParams& p, cudaStream_t s) {
+  if (p.num_tiles <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((p.num_tiles + 7) / 8);  // 8 warps per block
+  bwd_sparse_lists_kernel<<<blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -270,9 +270,11 @@ __device__ __forceinline__ void mma_dq(uint32_t d, DescWords ds, const TileDescs
 }
 
 // F16: the operands, P^T / dS and the dK / dV outputs are f16 (else bf16).
-// VARLEN: packed sequences (per-sequence offsets, lengths and mask bounds from cu_q /
-// cu_k; tiles indexed by slot).  The batched instantiations are unchanged by it.
-template <int DP, bool SOFTCAP, bool F16, bool VARLEN>
+// MODE 1 (VARLEN): packed sequences (per-sequence offsets, lengths and mask bounds from
+// cu_q / cu_k; tiles indexed by slot).  MODE 2 (SPARSE): block-sparse, a key tile's steps
+// come from its precomputed list instead of the whole (q-head, query tile) range.  The
+// batched dense instantiations (MODE 0) are unchanged by either.
+template <int DP, bool SOFTCAP, bool F16, int MODE>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ BwdMainParams p,
                     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tq_t,
@@ -281,6 +283,8 @@ __global__ void __launch_bounds__(512, 1)
                     const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tdo_t) {
   using G = Geo<DP>;
+  constexpr bool VARLEN = MODE == 1;
+  constexpr bool SPARSE = MODE == 2;
 #ifdef FA_TRACE
   const long long t_start = clock64();
 #endif
@@ -452,6 +456,10 @@ __global__ void __launch_bounds__(512, 1)
           d.m_begin = (int)mb64;
           d.m_count = (int)(me64 - mb64);
           d.total = d.m_count * p.G;  // steps (g, m), m fastest
+          if constexpr (SPARSE) {
+            d.total = p.sp_counts[ticket];  // the kept steps, listed in the same order
+            d.pad = ticket;
+          }
         }
         ring[k] = d;
         mbar_arrive(bar(B_TILEF0 + k));
@@ -527,8 +535,13 @@ __global__ void __launch_bounds__(512, 1)
         // dP), dO (its last dV), K (its last dQ).
         for (int it = 0; it < d.total; ++it, ++git) {
           const int s = git & 1;
-          const int g = it / d.m_count;
-          const int m = d.m_begin + (it - g * d.m_count);
+          int g = it / d.m_count;
+          int m = d.m_begin + (it - g * d.m_count);
+          if constexpr (SPARSE) {
+            const int e = p.sp_lists[(size_t)d.pad * p.sp_stride + it];
+            g = e >> 16;
+            m = e & 0xffff;
+          }
           const int h = d.hk * p.G + g;
           const int m0 = m * kTileQ;
           if (it == d.total - 1) mbar_arrive(bar(B_NEXT));  // time to claim the next tile
@@ -726,8 +739,13 @@ __global__ void __launch_bounds__(512, 1)
       if (lane == 0) mbar_arrive(bar(B_TILEE0 + (t & 1)));
       if (!have_tile) break;
       for (int it = 0; it < d.total; ++it, ++git) {
-        const int g = it / d.m_count;
-        const int m = d.m_begin + (it - g * d.m_count);
+        int g = it / d.m_count;
+        int m = d.m_begin + (it - g * d.m_count);
+        if constexpr (SPARSE) {
+          const int e = p.sp_lists[(size_t)d.pad * p.sp_stride + it];
+          g = e >> 16;
+          m = e & 0xffff;
+        }
         const int h = d.hk * p.G + g;
         bool ok = warp_wait(bar(B_DQFULL), git & 1, st, kTimeoutBase - 20);
         if (threadIdx.x == 128) FA_TR(8, git);
@@ -873,8 +891,8 @@ __global__ void __launch_bounds__(512, 1)
 
       for (int it = 0; it < d.total; ++it, ++git) {
         const int s = git & 1;
-        const int g = it / d.m_count;
-        const int m = d.m_begin + (it - g * d.m_count);
+        int m = d.m_begin + (it - (it / d.m_count) * d.m_count);
+        if constexpr (SPARSE) m = p.sp_lists[(size_t)d.pad * p.sp_stride + it] & 0xffff;
         const int m0 = m * kTileQ;
         const bool need_mask = !tile_full(tg, m, d.n);
         // visible columns: lo <= (j - i) <= hi with i = m0 + col0 + ql  <=>  ql in [qmin, qmax]
@@ -1065,11 +1083,11 @@ size_t bwd_main_smem_bytes(int Dp) {
   }
 }
 
-template <int DP, bool SC, bool F16, bool VL>
+template <int DP, bool SC, bool F16, int MODE>
 static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                               const OperandMaps& v, const OperandMaps& d, int num_ctas,
                               cudaStream_t s) {
-  auto kern = bwd_main_kernel<DP, SC, F16, VL>;
+  auto kern = bwd_main_kernel<DP, SC, F16, MODE>;
   const size_t smem = Geo<DP>::TOTAL;
   // The in-kernel register split assumes exactly 128 registers per thread at launch.
   cudaFuncAttributes attr;
@@ -1084,20 +1102,23 @@ static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, cons
 
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& d, int Dp, bool softcap,
-                            bool f16, bool varlen, int num_ctas, cudaStream_t s) {
+                            bool f16, int mode, int num_ctas, cudaStream_t s) {
   if (num_ctas <= 0) return cudaSuccess;
-#define FA_CASE_VL(DPV, VL)                                                             \
+#define FA_CASE_VL(DPV, MD)                                                             \
   if (f16)                                                                              \
-    return softcap ? launch_one<DPV, true, true, VL>(p, q, k, v, d, num_ctas, s)        \
-                   : launch_one<DPV, false, true, VL>(p, q, k, v, d, num_ctas, s);      \
-  return softcap ? launch_one<DPV, true, false, VL>(p, q, k, v, d, num_ctas, s)         \
-                 : launch_one<DPV, false, false, VL>(p, q, k, v, d, num_ctas, s);
+    return softcap ? launch_one<DPV, true, true, MD>(p, q, k, v, d, num_ctas, s)        \
+                   : launch_one<DPV, false, true, MD>(p, q, k, v, d, num_ctas, s);      \
+  return softcap ? launch_one<DPV, true, false, MD>(p, q, k, v, d, num_ctas, s)         \
+                 : launch_one<DPV, false, false, MD>(p, q, k, v, d, num_ctas, s);
 #define FA_CASE(DPV)                                                                    \
   case DPV:                                                                             \
-    if (varlen) {                                                                       \
-      FA_CASE_VL(DPV, true)                                                             \
+    if (mode == 1) {                                                                    \
+      FA_CASE_VL(DPV, 1)                                                                \
     }                                                                                   \
-    FA_CASE_VL(DPV, false)
+    if (mode == 2) {                                                                    \
+      FA_CASE_VL(DPV, 2)                                                                \
+    }                                                                                   \
+    FA_CASE_VL(DPV, 0)
   switch (Dp) {
     FA_CASE(64)
     FA_CASE(80)

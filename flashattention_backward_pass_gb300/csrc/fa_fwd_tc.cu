@@ -185,7 +185,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   int64_t nb64 = 0, ne64 = 0;
   if (m < gm.Mb) n_range(gm, m, &nb64, &ne64);  // a shorter sequence may have no tile m
   const int n_begin = (int)nb64;
-  const int total = (*s_abort) ? 0 : (int)(ne64 - nb64);
+  // Block sparsity: the key tiles of [n_begin, n_end) whose block-mask byte is set, in
+  // ascending order.  Every warp counts them (lanes striding the row) and every role walks
+  // them with its own cursor, so all roles agree on the sequence without exchanging it.
+  const uint8_t* brow = p.block_mask
+                            ? p.block_mask + (((size_t)b * p.H + h) * p.Mb + m) * (size_t)p.Nb
+                            : nullptr;
+  int nvis = (int)(ne64 - nb64);
+  if (brow) {
+    int c = 0;
+    for (int n = (int)nb64 + lane; n < (int)ne64; n += 32) c += brow[n] != 0;
+    nvis = __reduce_add_sync(0xffffffffu, c);
+  }
+  auto next_tile = [&](int nc) -> int {  // the visible key tile after nc
+    ++nc;
+    if (brow)
+      while (brow[nc] == 0) ++nc;
+    return nc;
+  };
+  const int total = (*s_abort) ? 0 : nvis;
   const int m0 = m * kTileQ;
 
   if (warp == 0 || warp == 2) {
@@ -209,8 +227,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, h, q_off + m0, tb, bar(F_Q));
         if (G::TAIL) tma_load_4d(sbase + G::OFF_Q + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, q_off + m0, tb, bar(F_Q));
       }
+      int ncur = n_begin - 1;
       for (int it = 0; it < total; ++it) {
-        const int n0 = k_off + (n_begin + it) * kTileK;
+        ncur = next_tile(ncur);
+        const int n0 = k_off + ncur * kTileK;
         const int ks = it % nst;
         if (it >= nst && !mbar_wait(bar(empty0 + ks), ((it - nst) / nst) & 1, st, kFwdTimeout - 1))
           break;
@@ -288,8 +308,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int c_lo = wg ? NCH0 : 0, c_hi = wg ? NCH : NCH0;
     float mrow = kNegInf;  // running maximum (log2 units); moved only by more than 8
     float lrow = 0.f;      // running sum of this warpgroup's P relative to mrow
+    int ncur = n_begin - 1;
     for (int it = 0; it < total; ++it) {
-      const int n = n_begin + it;
+      const int n = ncur = next_tile(ncur);
       const int kb = n * kTileK;  // key index of column 0
       const bool need_mask = !tile_full(gm, m, n);
       // visible columns: lo <= key - i <= hi and key < Sk  <=>  c in [cmin, cmax]

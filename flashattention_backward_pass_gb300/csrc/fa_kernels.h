@@ -70,6 +70,23 @@ struct BwdMainParams {
   int total_q, total_k;
   long long T;
   int causal, window_left, window_right;
+  // block sparsity (the SPARSE kernel): per key-tile ticket, the number of kept steps and
+  // their (q-head in group << 16 | query tile) entries at sp_lists[ticket * sp_stride + i]
+  const int* sp_counts;
+  const int* sp_lists;
+  long long sp_stride;
+};
+
+// Builds the block-sparse step lists of the main kernel from a (B, H, Mb, Nb) block mask:
+// one warp per key-tile ticket (the main kernel's ticket order).
+struct BwdSparseParams {
+  const uint8_t* block_mask;
+  int B, H, Hk, G, Sq, Sk, Mb, Nb;
+  long long lo64, hi64;
+  int* counts;
+  int* lists;
+  long long stride;    // G * Mb
+  int num_tiles;
 };
 
 struct BwdConvParams {
@@ -111,6 +128,9 @@ struct FwdTcParams {
   const int* cu_k;
   int total_q, total_k;
   int causal, window_left, window_right;
+  // Block sparsity (batched calls): (B, H, Mb, Nb) bytes, contiguous; a zero entry
+  // removes the (query tile, key tile) pair.  Null: every pair the mask allows is kept.
+  const uint8_t* block_mask;
 };
 
 // Tensor maps for one bf16 (B, S, H, D) operand: a 64-column 128B-swizzled box and,
@@ -122,10 +142,12 @@ struct OperandMaps {
 
 size_t bwd_main_smem_bytes(int Dp);
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t s);
-// f16: the 16-bit operands and outputs are f16 (else bf16); varlen: packed sequences
+// f16: the 16-bit operands and outputs are f16 (else bf16); mode: 0 batched, 1 packed
+// sequences, 2 block-sparse (step lists from launch_bwd_sparse_lists)
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
-                            bool f16, bool varlen, int num_ctas, cudaStream_t s);
+                            bool f16, int mode, int num_ctas, cudaStream_t s);
+cudaError_t launch_bwd_sparse_lists(const BwdSparseParams& p, cudaStream_t s);
 cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s);
 // dK/dV kernel (num_kv_ctas = key tiles x batch x kv-heads) then dQ kernel (num_q_ctas =
 // query tiles x batch x q-heads), both on stream s.

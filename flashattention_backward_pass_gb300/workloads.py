@@ -122,3 +122,12 @@ def make_varlen_inputs(lengths_q, lengths_k, H, Hk, D, seed=0, device="cpu", dty
     if device != "cpu":
         out = [t.to(device) for t in out]
     return out
+
+
+def make_block_mask(B, H, Sq, Sk, density=0.5, seed=0, block=128):
+    """A seeded random block mask: uint8 (B, H, ceil(Sq/block), ceil(Sk/block)), each entry
+    1 with probability `density` (1 = the query-tile / key-tile pair is kept)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, -(-Sq // block), -(-Sk // block))
+    return (torch.rand(shape, generator=g) < density).to(torch.uint8)

@@ -170,6 +170,33 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
            int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Block-sparse attention (the `flash_bwd_sm90.py` page's `blocksparse_tensors`: each key
+ * block visits only its listed query blocks).  block_mask: DEVICE bytes, contiguous
+ * (B, H, ceil(Sq/128), ceil(Sk/128)); entry [b, h, m, n] != 0 keeps the pair (query rows
+ * [128m, 128m+128), key rows [128n, 128n+128)) for q-head h, 0 removes it entirely, on
+ * top of the causal / window mask.  A row left with no visible key gives O = 0, LSE =
+ * +inf and dQ = 0, as elsewhere.  Forward and backward must get the same mask.
+ *
+ * fa_fwd_blocksparse: fa_fwd's arguments plus block_mask (NULL: FA_ERR_NULL).
+ * fa_bwd_blocksparse: fa_bwd's arguments plus block_mask, without `deterministic` (the
+ *   ordered dQ mode is not built for sparse step lists); the workspace must hold
+ *   fa_bwd_blocksparse_workspace_size bytes (fa_bwd's regions plus, per key tile, a list
+ *   of its kept (q-head, query tile) steps); the fused algorithm only
+ *   (FA_ERR_UNSUPPORTED while the split one is selected or for more than 65535 query
+ *   tiles).
+ */
+int fa_fwd_blocksparse(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+                       fa_tensor* out, fa_tensor* lse, const uint8_t* block_mask,
+                       float softmax_scale, int causal, int window_left, int window_right,
+                       float softcap, void* workspace, size_t workspace_bytes, void* stream);
+size_t fa_bwd_blocksparse_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D);
+int fa_bwd_blocksparse(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
+                       const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
+                       fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, const uint8_t* block_mask,
+                       float softmax_scale, int causal, int window_left, int window_right,
+                       float softcap, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Workspace of fa_bwd_varlen, in bytes: per q-head, total_q / 128 + batch tiles of 128
  * query rows (each sequence's query tiles are consecutive; the slack is at most one
  * partial tile per sequence) for the fp32 dQ accumulator, D and LSE2, plus counters and

@@ -197,3 +197,30 @@ def test_varlen_validation(lib):
     want = 256 + rows * 4 + rows * 4 + rows * 64 * 4 + ((H * T * 4 + 15) // 16) * 16
     want = (want + 255) // 256 * 256
     assert f(2, H, 300, 64, 0) == want
+
+
+def test_blocksparse_validation(lib):
+    a = _bwd_args()
+    order = ("dout", "q", "k", "v", "out", "lse", "dq", "dk", "dv")
+    ptrs = [ctypes.byref(a[n]) for n in order]
+    # the block mask is required
+    assert lib.fa_bwd_blocksparse(*ptrs, None, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+                                  1 << 30, None) == -1
+    fwd = [ctypes.byref(a[n]) for n in ("q", "k", "v", "out", "lse")]
+    assert lib.fa_fwd_blocksparse(*fwd, None, 0.125, 0, -1, -1, 0.0, None, 0, None) == -1
+    # split algorithm: refused before any launch
+    assert lib.fa_bwd_set_algorithm(0) == 0
+    try:
+        assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+                                      1 << 30, None) == -8
+    finally:
+        assert lib.fa_bwd_set_algorithm(1) == 0
+    # workspace: fa_bwd's plus per key tile a count and G * Mb list entries
+    f = lib.fa_bwd_blocksparse_workspace_size
+    f.restype = ctypes.c_size_t
+    g = lib.fa_bwd_workspace_size
+    g.restype = ctypes.c_size_t
+    base = g(1, 2, 2, 128, 128, 64, 0)
+    assert f(1, 2, 2, 128, 128, 64) == (((base + 2 * 4 + 255) // 256 * 256 + 2 * 1 * 1 * 4 + 255) // 256) * 256
+    assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+                                  base, None) == -7        # fa_bwd's size is not enough
