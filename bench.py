@@ -7,6 +7,7 @@ workload B=4, Sq=Sk=2048, H=32, Hk=8, D=128), inputs resident in HBM, L2 flushed
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
   python bench.py --varlen [--workload NAME]   (packed sequences of mixed lengths; own line)
+  python bench.py --block-density 0.5 [--workload NAME]   (block-sparse; own line)
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of the
 same workload (one batch x one kv-head group per step).  Under torchrun (N > 1) every
@@ -447,6 +448,83 @@ def run_varlen(args, ws_, local):
             "device_status": status}
 
 
+def run_blocksparse(args, local):
+    """fa_fwd_blocksparse + fa_bwd_blocksparse on the workload with a seeded random tile mask
+    of the given density; value = 10*D flops per (query, key) pair left visible by the
+    element mask and the tile mask together, per second of fa_bwd_blocksparse."""
+    import numpy as np
+    import torch
+    import flashattention_backward_pass_gb300 as fa
+    from flashattention_backward_pass_gb300 import _abi
+    from flashattention_backward_pass_gb300.workloads import WORKLOADS, make_block_mask, make_inputs
+
+    w = WORKLOADS[args.workload]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load()
+    q, k, v, do = make_inputs(w, dev)
+    bm_cpu = make_block_mask(w.B, w.H, w.Sq, w.Sk, args.block_density, seed=w.seed)
+    bm = bm_cpu.to(dev)
+    kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right,
+              softcap=w.softcap)
+    # visible pairs: per (query tile, key tile) pair of the element mask, summed over kept pairs
+    wr = 0 if w.causal else w.window_right
+    i = np.arange(w.Sq)[:, None]
+    j = np.arange(w.Sk)[None, :]
+    vis = np.ones((w.Sq, w.Sk), dtype=bool)
+    if wr >= 0:
+        vis &= j <= i + (w.Sk - w.Sq) + wr
+    if w.window_left >= 0:
+        vis &= j >= i + (w.Sk - w.Sq) - w.window_left
+    Mb, Nb = bm_cpu.shape[2], bm_cpu.shape[3]
+    pad = np.zeros((Mb * 128, Nb * 128), dtype=np.int64)
+    pad[:w.Sq, :w.Sk] = vis
+    per_tile = pad.reshape(Mb, 128, Nb, 128).sum(axis=(1, 3))
+    pairs = float((bm_cpu.numpy().astype(np.int64) * per_tile[None, None]).sum())
+    flops = 10.0 * w.D * pairs
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
+    fa.fa_fwd_blocksparse(q, k, v, out, lse, bm, w.scale, **kw)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsp = torch.empty(fa.bwd_blocksparse_workspace_size(w.B, w.H, w.Hk, w.Sq, w.Sk, w.D),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        ms = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ms.append(e0.elapsed_time(e1))
+        return sum(ms) / len(ms)
+
+    t = timed(lambda: fa.fa_bwd_blocksparse(do, q, k, v, out, lse, dq, dk, dv, bm, w.scale,
+                                            workspace=wsp, **kw))
+    status = fa.fa_bwd_status(wsp)
+    tf = timed(lambda: fa.fa_fwd_blocksparse(q, k, v, out, lse, bm, w.scale, **kw))
+    peaks, _ = _peaks()
+    return {"metric": METRIC, "value": round(flops / (t * 1e-3) / 1e12, 3), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, seeded random tile mask)",
+            "config": dict(w.describe(), workload=w.name + "+blocksparse",
+                           block_density=args.block_density,
+                           kept_tile_pairs=int(bm_cpu.sum()),
+                           l2="flushed between steps (256 MiB write, outside the timed events)",
+                           flop_convention="10*D per visible (query, key) pair after both masks"),
+            "pct_of_bf16_peak": round(100 * flops / (t * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 2),
+            "forward_ms": round(tf, 4),
+            "forward_tflops": round(0.4 * flops / (tf * 1e-3) / 1e12, 2),
+            "device_status": status}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -461,10 +539,17 @@ def main():
     ap.add_argument("--varlen", action="store_true",
                     help="time fa_bwd_varlen on the workload's tokens packed as a length mix "
                          "(a separate line, not the headline)")
+    ap.add_argument("--block-density", type=float, default=None,
+                    help="time fa_bwd_blocksparse with a random tile mask of this density "
+                         "(a separate line, not the headline)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws_, rank, local = _dist()
 
+    if args.block_density is not None:
+        if rank == 0:
+            print(json.dumps(run_blocksparse(args, local)), flush=True)
+        return
     if args.varlen:
         if rank == 0:
             print(json.dumps(run_varlen(args, ws_, local)), flush=True)
