@@ -5,11 +5,18 @@
 // LSE = (m + log2 l) * ln 2 — with the same mask (bottom-right aligned band lo <= j - i
 // <= hi, j < Sk) and softcap (z = c * tanh(scale * s / c)) as the backward.
 //
-// One CTA owns one 128-query tile of one (batch, q-head) and walks the key tiles with a
+// Work item: one 128-query tile of one (batch, q-head), walking the key tiles with a
 // visible entry (GQA/MQA page: the kv-head is h / (H / Hk)):
 //   S = Q K^T        (M = 128 queries, N = 128 keys, K = Dp; both operands K-major)
 //   P = exp2(z * log2e - m)  written as 16-bit pairs over the S columns already read
 //   O (+)= P V       (A = P from tensor memory, B = V read MN-major, N = Dp)
+// The grid is persistent: the CTAs take the items of a list ordered longest first (under
+// causal masking the last query tiles see the most keys) in snake order.  Consecutive
+// items overlap: the next item's Q and first K / V tiles load and its first S products
+// run while the softmax warps finish the current item and write its O, which lives in
+// the other of two TMEM accumulators.  A CTA therefore pays its set-up once, not per
+// query tile.
+//
 // Two softmax warpgroups split the 128 key columns of the score tile: thread (warpgroup
 // w, TMEM lane r) owns query row r and columns [64w, 64w + 64).  The two halves of a
 // row's maximum meet through shared memory once per key tile; each warpgroup keeps the
@@ -21,13 +28,15 @@
 // the same m, so the result is exact up to rounding either way.  After the first key
 // tiles a rescale is rare.
 //
-// Warp roles (12 warps): warp 0 TMA producer of Q (once) and of the 3-stage K ring;
-// warp 2 TMA producer of the 2-stage V ring; warp 1 TMEM allocator and single
-// MMA-issuing thread; warps 4-11 two softmax / epilogue warpgroups (warp w reads TMEM
-// lanes 32 (w % 4) .. +31).  Warp 3 only joins the CTA barriers.
+// Warp roles (12 warps): warp 0 TMA producer of Q (two buffers) and of the K ring; warp 2
+// TMA producer of the V ring; warp 1 TMEM allocator and MMA issue (one lane issues);
+// warps 4-11 two softmax / epilogue warpgroups (warp w reads TMEM lanes 32 (w % 4) ..
+// +31).  Warp 3 only joins the CTA barriers.  Every role walks the same item list and
+// counts key tiles and items with work the same way, so the ring and buffer phases agree
+// without any exchange.
 //
-// Tensor memory: S double buffer [0, 128) and [128, 256) (P written over its first 32
-// columns of each 64-column half), O accumulator [256, 256 + Dp).
+// Tensor memory: S buffers [0, 128) and [128, 256) (P written over the first 32 columns
+// of each 64-column half), O accumulators [256, 256 + Dp) and [384, 384 + Dp).
 #include "fa_bwd_common.cuh"
 
 #include <math.h>
@@ -43,28 +52,30 @@ constexpr uint32_t FSM_BAR = 0;     // mbarriers
 constexpr uint32_t FSM_TMEM = 256;  // TMEM base address slot
 constexpr uint32_t FSM_ABORT = 260;
 constexpr uint32_t FSM_MAX = 1024;  // [2 parities][2 warpgroups][128 rows] fp32 row maxima
-constexpr uint32_t FSM_L = 3072;    // [2 warpgroups][128 rows] fp32 row sums (epilogue)
-constexpr uint32_t FSMALL = 4096;
+constexpr uint32_t FSM_L = 3072;    // [2 item parities][2 warpgroups][128 rows] fp32 row sums
+constexpr uint32_t FSMALL = 6144;
 
 template <int DP>
 struct GeoF : Panels<DP> {
   using Panels<DP>::TILE_BYTES;
-  static constexpr int KST = 3;  // K ring stages
+  static constexpr int KST = 2;  // K ring stages
   static constexpr int VST = 2;  // V ring stages
-  static constexpr uint32_t OFF_Q = FSMALL;
-  static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr uint32_t OFF_Q = FSMALL;  // 2 buffers (this item and the next)
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES;
   static constexpr uint32_t TOTAL = OFF_V + VST * TILE_BYTES;
   static_assert(TOTAL <= 232448, "fits the 227 KB opt-in shared memory");
 };
 
+// Barriers.  Sx / Px / PDx by score buffer, Qx / ACCx / OEx by item parity (items with
+// work), K / V by ring stage.
 enum FBar : int {
-  F_Q = 0, F_KF0, F_KF1, F_KF2, F_KE0, F_KE1, F_KE2, F_VF0, F_VF1, F_VE0, F_VE1,
-  F_SF0, F_SF1, F_PF0, F_PF1, F_OD, F_ACC, F_DRAIN, F_COUNT
+  F_QF0 = 0, F_QF1, F_QE0, F_QE1, F_KF0, F_KF1, F_KE0, F_KE1, F_VF0, F_VF1, F_VE0, F_VE1,
+  F_SF0, F_SF1, F_PF0, F_PF1, F_PD0, F_PD1, F_ACC0, F_ACC1, F_OE0, F_OE1, F_DRAIN, F_COUNT
 };
 static_assert(F_COUNT <= 32, "barrier area holds 32 mbarriers");
 
-constexpr uint32_t FT_S0 = 0, FT_S1 = 128, FT_O = 256;
+constexpr uint32_t FT_S0 = 0, FT_O0 = 256;
 
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -115,6 +126,76 @@ __device__ __forceinline__ float fwd_probs(uint32_t sbuf, float m, const float (
   return sum;
 }
 
+
+// One work item as every role sees it: the query tile, its (batch, head), the sequence's
+// geometry and offsets, and the visible key tiles (the element mask's range, filtered by
+// the block mask).  Must be called by a whole warp (the block-mask count is a warp sum).
+struct FwdItem {
+  int m, b, h, hk, tb, q_off, k_off, lo, hi, Sq, Sk, n_begin, nvis;
+  MaskGeom gm;
+  const uint8_t* brow;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const FwdTcParams& p, int idx, int lane) {
+  FwdItem it;
+  const int per_m = p.B * p.H;
+  it.m = p.Mb - 1 - idx / per_m;  // longest first
+  const int bh = idx - (p.Mb - 1 - it.m) * per_m;
+  it.b = bh / p.H;
+  it.h = bh - it.b * p.H;
+  it.hk = it.h / p.G;
+  it.q_off = 0;
+  it.k_off = 0;
+  it.tb = it.b;
+  it.lo = p.lo;
+  it.hi = p.hi;
+  if (p.varlen) {
+    // sequence b: rows [cu[b], cu[b+1]) clamped into the packed tensors, so that malformed
+    // offsets cannot move a load or a store outside them
+    const int q0 = min(max(p.cu_q[it.b], 0), p.total_q);
+    const int q1 = min(max(p.cu_q[it.b + 1], q0), p.total_q);
+    const int k0 = min(max(p.cu_k[it.b], 0), p.total_k);
+    const int k1 = min(max(p.cu_k[it.b + 1], k0), p.total_k);
+    it.q_off = q0;
+    it.k_off = k0;
+    it.tb = 0;
+    it.gm = make_geom(q1 - q0, k1 - k0, p.causal, p.window_left, p.window_right, kTileQ, kTileK);
+    it.lo = (int)max64(min64(it.gm.lo, 1ll << 30), -(1ll << 30));
+    it.hi = (int)max64(min64(it.gm.hi, 1ll << 30), -(1ll << 30));
+  } else {
+    it.gm.Sq = p.Sq;
+    it.gm.Sk = p.Sk;
+    it.gm.lo = p.lo64;
+    it.gm.hi = p.hi64;
+    it.gm.tm = kTileQ;
+    it.gm.tn = kTileK;
+    it.gm.Mb = p.Mb;
+    it.gm.Nb = p.Nb;
+  }
+  it.Sq = (int)it.gm.Sq;
+  it.Sk = (int)it.gm.Sk;
+  int64_t nb = 0, ne = 0;
+  if (it.m < it.gm.Mb) n_range(it.gm, it.m, &nb, &ne);  // a shorter sequence may have no tile m
+  it.n_begin = (int)nb;
+  it.nvis = (int)(ne - nb);
+  it.brow = p.block_mask ? p.block_mask + (((size_t)it.b * p.H + it.h) * p.Mb + it.m) * (size_t)p.Nb
+                         : nullptr;
+  if (it.brow) {
+    int c = 0;
+    for (int n = (int)nb + lane; n < (int)ne; n += 32) c += it.brow[n] != 0;
+    it.nvis = __reduce_add_sync(0xffffffffu, c);
+  }
+  return it;
+}
+
+// The visible key tile after nc (block sparsity skips the removed ones).
+__device__ __forceinline__ int fwd_next_tile(const FwdItem& it, int nc) {
+  ++nc;
+  if (it.brow)
+    while (it.brow[nc] == 0) ++nc;
+  return nc;
+}
+
 }  // namespace
 
 template <int DP, bool SOFTCAP, bool F16>
@@ -138,7 +219,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (p.status) atomicExch(p.status, kFwdTimeout - 99);
       *s_abort = 1;
     }
-    for (int i = 0; i < F_COUNT; ++i) mbar_init(bar(i), (i == F_PF0 || i == F_PF1) ? 8 : 1);
+    for (int i = 0; i < F_COUNT; ++i) {
+      const bool eight = (i == F_PF0 || i == F_PF1 || i == F_OE0 || i == F_OE1);
+      mbar_init(bar(i), eight ? 8 : 1);  // softmax warps arrive on P-full and O-empty
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -150,146 +234,149 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem_raw + FSM_TMEM);
   AbortState st{s_abort, p.status, p.wait_limit};
-
-  // query tiles with the most key tiles first (under causal masking: the last ones)
-  const int per_m = p.B * p.H;
-  const int m = p.Mb - 1 - (int)(blockIdx.x / (unsigned)per_m);
-  const int bh = (int)blockIdx.x - (p.Mb - 1 - m) * per_m;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
-  const int hk = h / p.G;
-  MaskGeom gm;
-  int q_off = 0, k_off = 0, tb = b, lo = p.lo, hi = p.hi;  // tb: batch coordinate of the maps
-  if (p.varlen) {
-    // sequence b: rows [cu[b], cu[b+1]) clamped into the packed tensors, so that malformed
-    // offsets cannot move a load or a store outside them
-    const int q0 = min(max(p.cu_q[b], 0), p.total_q), q1 = min(max(p.cu_q[b + 1], q0), p.total_q);
-    const int k0 = min(max(p.cu_k[b], 0), p.total_k), k1 = min(max(p.cu_k[b + 1], k0), p.total_k);
-    q_off = q0;
-    k_off = k0;
-    tb = 0;
-    gm = make_geom(q1 - q0, k1 - k0, p.causal, p.window_left, p.window_right, kTileQ, kTileK);
-    lo = (int)max64(min64(gm.lo, 1ll << 30), -(1ll << 30));
-    hi = (int)max64(min64(gm.hi, 1ll << 30), -(1ll << 30));
-  } else {
-    gm.Sq = p.Sq;
-    gm.Sk = p.Sk;
-    gm.lo = p.lo64;
-    gm.hi = p.hi64;
-    gm.tm = kTileQ;
-    gm.tn = kTileK;
-    gm.Mb = p.Mb;
-    gm.Nb = p.Nb;
-  }
-  const int Sq = (int)gm.Sq, Sk = (int)gm.Sk;
-  int64_t nb64 = 0, ne64 = 0;
-  if (m < gm.Mb) n_range(gm, m, &nb64, &ne64);  // a shorter sequence may have no tile m
-  const int n_begin = (int)nb64;
-  // Block sparsity: the key tiles of [n_begin, n_end) whose block-mask byte is set, in
-  // ascending order.  Every warp counts them (lanes striding the row) and every role walks
-  // them with its own cursor, so all roles agree on the sequence without exchanging it.
-  const uint8_t* brow = p.block_mask
-                            ? p.block_mask + (((size_t)b * p.H + h) * p.Mb + m) * (size_t)p.Nb
-                            : nullptr;
-  int nvis = (int)(ne64 - nb64);
-  if (brow) {
-    int c = 0;
-    for (int n = (int)nb64 + lane; n < (int)ne64; n += 32) c += brow[n] != 0;
-    nvis = __reduce_add_sync(0xffffffffu, c);
-  }
-  auto next_tile = [&](int nc) -> int {  // the visible key tile after nc
-    ++nc;
-    if (brow)
-      while (brow[nc] == 0) ++nc;
-    return nc;
+  const int num_items = p.Mb * p.B * p.H;
+  // The items are ordered longest first; round k gives CTA c item k * grid + c on even
+  // rounds and k * grid + (grid - 1 - c) on odd ones, so a CTA that got a long item in
+  // one round gets a short one in the next (snake order) and the sums even out.
+  auto item_of = [&](int k) -> int {
+    const int c = (k & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    return k * (int)gridDim.x + c;
   };
-  const int total = (*s_abort) ? 0 : nvis;
-  const int m0 = m * kTileQ;
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ TMA producers
-    // Warp 0 loads Q and the K ring, warp 2 the V ring: each refills a stage as soon as
-    // its own last reader is done (K: the stage's S product, V: its P V product), so a K
-    // load never waits behind a V stage that is still being read.
+    // Warp 0 loads each item's Q (two buffers, so the next item's Q lands while this one
+    // runs) and the K ring, warp 2 the V ring; each refills a stage as soon as its own last
+    // reader is done (Q: the item's last MMA, K: its S product, V: its P V product).
+    const bool kside = warp == 0;
+    const CUtensorMap* tm = kside ? &tk : &tv;
+    const CUtensorMap* tm_t = kside ? &tk_t : &tv_t;
+    const int nst = kside ? G::KST : G::VST;
+    const uint32_t base = sbase + (kside ? G::OFF_K : G::OFF_V);
+    const int full0 = kside ? F_KF0 : F_VF0, empty0 = kside ? F_KE0 : F_VE0;
     if (lane == 0) {
-      const bool kside = warp == 0;
-      const CUtensorMap* tm = kside ? &tk : &tv;
-      const CUtensorMap* tm_t = kside ? &tk_t : &tv_t;
-      const int nst = kside ? G::KST : G::VST;
-      const uint32_t base = sbase + (kside ? G::OFF_K : G::OFF_V);
-      const int full0 = kside ? F_KF0 : F_VF0, empty0 = kside ? F_KE0 : F_VE0;
       tma_prefetch_desc(tm);
-      int issued[G::KST] = {};
-      if (kside && total > 0) {
-        tma_prefetch_desc(&tq);
-        mbar_arrive_expect_tx(bar(F_Q), G::TILE_BYTES);
-        for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, h, q_off + m0, tb, bar(F_Q));
-        if (G::TAIL) tma_load_4d(sbase + G::OFF_Q + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, q_off + m0, tb, bar(F_Q));
+      if (kside) tma_prefetch_desc(&tq);
+    }
+    int c = 0, qn = 0, qarmed = 0;  // tiles loaded into the ring, items with work, Q loads
+    bool alive = true;
+    for (int k = 0, idx = item_of(0); alive && idx < num_items; idx = item_of(++k)) {
+      const FwdItem I = fwd_item(p, idx, lane);
+      if (*s_abort) break;
+      if (I.nvis == 0) continue;
+      if (lane == 0) {
+        if (kside) {
+          const int qb = qn & 1;
+          if (qn >= 2 && !mbar_wait(bar(F_QE0 + qb), ((qn - 2) >> 1) & 1, st, kFwdTimeout - 4)) {
+            alive = false;
+          } else {
+            const uint32_t qdst = sbase + G::OFF_Q + qb * G::TILE_BYTES;
+            mbar_arrive_expect_tx(bar(F_QF0 + qb), G::TILE_BYTES);
+            for (int pn = 0; pn < G::NFULL; ++pn)
+              tma_load_4d(qdst + pn * G::FULL_BYTES, &tq, pn * 64, I.h, I.q_off + I.m * kTileQ, I.tb, bar(F_QF0 + qb));
+            if (G::TAIL) tma_load_4d(qdst + G::TAIL_OFF, &tq_t, G::NFULL * 64, I.h, I.q_off + I.m * kTileQ, I.tb, bar(F_QF0 + qb));
+            ++qarmed;
+          }
+        }
+        int ncur = I.n_begin - 1;
+        for (int t = 0; alive && t < I.nvis; ++t, ++c) {
+          ncur = fwd_next_tile(I, ncur);
+          const int n0 = I.k_off + ncur * kTileK;
+          const int ks = c % nst;
+          if (c >= nst && !mbar_wait(bar(empty0 + ks), ((c - nst) / nst) & 1, st, kFwdTimeout - 1)) {
+            alive = false;
+            break;
+          }
+          const uint32_t dst = base + ks * G::TILE_BYTES;
+          mbar_arrive_expect_tx(bar(full0 + ks), G::TILE_BYTES);
+          for (int pn = 0; pn < G::NFULL; ++pn)
+            tma_load_4d(dst + pn * G::FULL_BYTES, tm, pn * 64, I.hk, n0, I.tb, bar(full0 + ks));
+          if (G::TAIL) tma_load_4d(dst + G::TAIL_OFF, tm_t, G::NFULL * 64, I.hk, n0, I.tb, bar(full0 + ks));
+        }
       }
-      int ncur = n_begin - 1;
-      for (int it = 0; it < total; ++it) {
-        ncur = next_tile(ncur);
-        const int n0 = k_off + ncur * kTileK;
-        const int ks = it % nst;
-        if (it >= nst && !mbar_wait(bar(empty0 + ks), ((it - nst) / nst) & 1, st, kFwdTimeout - 1))
-          break;
-        const uint32_t dst = base + ks * G::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(full0 + ks), G::TILE_BYTES);
-        for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(dst + pn * G::FULL_BYTES, tm, pn * 64, hk, n0, tb, bar(full0 + ks));
-        if (G::TAIL) tma_load_4d(dst + G::TAIL_OFF, tm_t, G::NFULL * 64, hk, n0, tb, bar(full0 + ks));
-        issued[ks] = it / nst + 1;
-      }
-      // every copy this thread started must land before the CTA may exit
+      ++qn;
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+    }
+    // every copy this thread started must land before the CTA may exit: the last phase of
+    // each stage (and of each Q buffer) that it armed
+    if (lane == 0) {
       volatile int no_abort = 0;
       AbortState dr{&no_abort, p.status, p.wait_limit};
-      if (kside && total > 0) mbar_wait(bar(F_Q), 0, dr, kFwdTimeout - 3);
-      for (int s2 = 0; s2 < nst; ++s2)
-        if (issued[s2]) mbar_wait(bar(full0 + s2), (issued[s2] - 1) & 1, dr, kFwdTimeout - 3);
+      for (int k2 = 0; k2 < nst && k2 < c; ++k2) {
+        const int last = c - 1 - ((c - 1 - k2) % nst);  // the last load into stage k2
+        mbar_wait(bar(full0 + (last % nst)), (last / nst) & 1, dr, kFwdTimeout - 3);
+      }
+      if (kside)
+        for (int k2 = 0; k2 < 2 && k2 < qarmed; ++k2) {
+          const int last = qarmed - 1 - k2;
+          mbar_wait(bar(F_QF0 + (last & 1)), (last >> 1) & 1, dr, kFwdTimeout - 3);
+        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // S_0, S_1; then per key tile j: O (+)= P_j V_j once P_j is written (and O rescaled),
-    // then S_j+2 once that product is done (P_j lives in S_j's columns, which S_j+2 reuses).
-    if (lane == 0) {
-      const TileDescs dQ_ = tile_descs<DP>(sbase + G::OFF_Q);
-      auto issue_S = [&](int it) -> bool {
-        const int ks = it % G::KST;
-        if (!mbar_wait_spin(bar(F_KF0 + ks), (it / G::KST) & 1, st, kFwdTimeout - 11)) return false;
-        tc_fence_after();
-        const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K + ks * G::TILE_BYTES);
-        mma_kmajor<DP, F16>(tmem + ((it & 1) ? FT_S1 : FT_S0), dQ_, dK_);
-        mma_commit(bar(F_SF0 + (it & 1)));
-        mma_commit(bar(F_KE0 + ks));
-        return true;
-      };
-      bool ok = total > 0 && mbar_wait_spin(bar(F_Q), 0, st, kFwdTimeout - 10);
-      const bool issued_any = ok;
-      if (ok) ok = issue_S(0);
-      if (ok && total > 1) ok = issue_S(1);
-      for (int it = 0; ok && it < total; ++it) {
-        const int sb = it & 1;
-        if (!mbar_wait_spin(bar(F_PF0 + sb), (it >> 1) & 1, st, kFwdTimeout - 12)) break;
-        const int vs = it % G::VST;
-        if (!mbar_wait_spin(bar(F_VF0 + vs), (it / G::VST) & 1, st, kFwdTimeout - 13)) break;
-        tc_fence_after();
-        const TileDescs dV_ = tile_descs<DP>(sbase + G::OFF_V + vs * G::TILE_BYTES);
-        mma_dv<DP, F16>(tmem + FT_O, tmem + (sb ? FT_S1 : FT_S0), dV_, it > 0 ? 1u : 0u);
-        mma_commit(bar(F_VE0 + vs));
-        mma_commit(bar(F_OD));
-        if (it + 2 < total) {
-          if (!mbar_wait_spin(bar(F_OD), it & 1, st, kFwdTimeout - 14)) break;
-          if (!issue_S(it + 2)) break;
+    // Per item: S_0, S_1; then per key tile j: O (+)= P_j V_j once P_j is written (and O
+    // rescaled), then S_j+2 once that product is done (P_j lives in S_j's buffer).  Key
+    // tiles are counted across items (g), so the next item's first S products only wait
+    // for the buffers, not for the softmax warps to finish the current item.
+    int g = 0, on = 0;  // key tiles issued, items with work
+    bool ok = true;
+    for (int k = 0, idx = item_of(0); ok && idx < num_items; idx = item_of(++k)) {
+      const FwdItem I = fwd_item(p, idx, lane);
+      if (*s_abort) break;
+      if (I.nvis == 0) continue;
+      if (lane == 0) {
+        const int qb = on & 1;
+        const TileDescs dQ_ = tile_descs<DP>(sbase + G::OFF_Q + qb * G::TILE_BYTES);
+        auto issue_S = [&](int x) -> bool {  // global key tile x into score buffer x % 2
+          const int ks = x % G::KST;
+          // the buffer's previous P V product (key tile x - 2) must be done
+          if (x >= 2 && !mbar_wait_spin(bar(F_PD0 + (x & 1)), ((x - 2) >> 1) & 1, st, kFwdTimeout - 14))
+            return false;
+          if (!mbar_wait_spin(bar(F_KF0 + ks), (x / G::KST) & 1, st, kFwdTimeout - 11)) return false;
+          tc_fence_after();
+          const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K + ks * G::TILE_BYTES);
+          mma_kmajor<DP, F16>(tmem + FT_S0 + (x & 1) * 128, dQ_, dK_);
+          mma_commit(bar(F_SF0 + (x & 1)));
+          mma_commit(bar(F_KE0 + ks));
+          return true;
+        };
+        ok = mbar_wait_spin(bar(F_QF0 + qb), (on >> 1) & 1, st, kFwdTimeout - 10);
+        if (ok) ok = issue_S(g);
+        if (ok && I.nvis > 1) ok = issue_S(g + 1);
+        const uint32_t o_col = FT_O0 + qb * 128;
+        for (int t = 0; ok && t < I.nvis; ++t) {
+          const int x = g + t;
+          if (!mbar_wait_spin(bar(F_PF0 + (x & 1)), (x >> 1) & 1, st, kFwdTimeout - 12)) { ok = false; break; }
+          // the first product overwrites this O buffer: the item two back must have read it
+          if (t == 0 && on >= 2 &&
+              !mbar_wait_spin(bar(F_OE0 + qb), ((on - 2) >> 1) & 1, st, kFwdTimeout - 16)) {
+            ok = false;
+            break;
+          }
+          const int vs = x % G::VST;
+          if (!mbar_wait_spin(bar(F_VF0 + vs), (x / G::VST) & 1, st, kFwdTimeout - 13)) { ok = false; break; }
+          tc_fence_after();
+          const TileDescs dV_ = tile_descs<DP>(sbase + G::OFF_V + vs * G::TILE_BYTES);
+          mma_dv<DP, F16>(tmem + o_col, tmem + FT_S0 + (x & 1) * 128, dV_, t > 0 ? 1u : 0u);
+          mma_commit(bar(F_VE0 + vs));
+          mma_commit(bar(F_PD0 + (x & 1)));
+          if (t + 2 < I.nvis && !issue_S(x + 2)) { ok = false; break; }
+        }
+        if (ok) {
+          mma_commit(bar(F_QE0 + qb));    // every S of the item has been issued
+          mma_commit(bar(F_ACC0 + qb));   // and every P V: O of this item is final
         }
       }
-      if (issued_any) {
-        mma_commit(bar(F_ACC));
-        mma_commit(bar(F_DRAIN));
-        volatile int no_abort = 0;
-        AbortState dr{&no_abort, p.status, p.wait_limit};
-        mbar_wait(bar(F_DRAIN), 0, dr, kFwdTimeout - 15);
-      }
+      g += I.nvis;
+      ++on;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (lane == 0 && g > 0) {
+      // every MMA must be complete before the CTA releases tensor memory
+      mma_commit(bar(F_DRAIN));
+      volatile int no_abort = 0;
+      AbortState dr{&no_abort, p.status, p.wait_limit};
+      mbar_wait(bar(F_DRAIN), 0, dr, kFwdTimeout - 15);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + epilogue
@@ -298,7 +385,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int r = qd * 32 + lane;          // query row inside the tile = TMEM lane
     const int col0 = wg * 64;
     const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
-    const int i = m0 + r;
     const SoftmaxConsts kc{p.scale_log2, p.cap_scale, p.cap_log2};
     float* s_max = reinterpret_cast<float*>(smem_raw + FSM_MAX);
     float* s_l = reinterpret_cast<float*>(smem_raw + FSM_L);
@@ -306,84 +392,103 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     constexpr int NCH = DP / 16;
     constexpr int NCH0 = (NCH + 1) / 2;
     const int c_lo = wg ? NCH0 : 0, c_hi = wg ? NCH : NCH0;
-    float mrow = kNegInf;  // running maximum (log2 units); moved only by more than 8
-    float lrow = 0.f;      // running sum of this warpgroup's P relative to mrow
-    int ncur = n_begin - 1;
-    for (int it = 0; it < total; ++it) {
-      const int n = ncur = next_tile(ncur);
-      const int kb = n * kTileK;  // key index of column 0
-      const bool need_mask = !tile_full(gm, m, n);
-      // visible columns: lo <= key - i <= hi and key < Sk  <=>  c in [cmin, cmax]
-      const int cmin = max(i + lo - kb, -1);
-      const int cmax = min(min(i + hi - kb, Sk - 1 - kb), 1 << 20);
-      const uint32_t sbuf = t_lane + ((it & 1) ? FT_S1 : FT_S0) + col0;
-      const bool ok = warp_wait(bar(F_SF0 + (it & 1)), (it >> 1) & 1, st, kFwdTimeout - 30);
-      float x[64];
-      float mx = kNegInf;
-      if (ok) {
-        tc_fence_after();
-        mx = need_mask ? fwd_scores<true, SOFTCAP>(kc, sbuf, col0, cmin, cmax, x)
-                       : fwd_scores<false, SOFTCAP>(kc, sbuf, col0, cmin, cmax, x);
-      }
-      // the row maximum over both halves; both warpgroups always reach this barrier, and
-      // after it both see the abort flag that a failed wait of either one has raised
-      s_max[((it & 1) * 2 + wg) * 128 + r] = mx;
-      named_bar_sync(1, 256);
-      if (*s_abort) break;
-      mx = fmaxf(mx, s_max[((it & 1) * 2 + (wg ^ 1)) * 128 + r]);
-      // move the reference maximum only when a score passes it by more than 8 (log2);
-      // both warpgroups take the same decision for a row
-      float alpha = 1.f;
-      if (it == 0) {
-        mrow = mx;
-      } else if (mx > mrow + 8.f) {
-        alpha = ex2_approx(mrow - mx);  // mrow finite here, or -inf: alpha = 0
-        mrow = mx;
-      }
-      const float muse = mrow == kNegInf ? 0.f : mrow;  // all-masked so far: P = 0
-      lrow = lrow * alpha + fwd_probs<F16>(sbuf, muse, x);
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        // O holds the products up to key tile it-1: wait for the last one, then rescale
-        // this warpgroup's columns of it (on a failed wait the next barrier ends the loop)
-        if (!warp_wait(bar(F_OD), (it - 1) & 1, st, kFwdTimeout - 31)) continue;
-        tc_fence_after();
+    // Both warpgroups meet at named barrier 1 once per key tile and once per item; they
+    // leave the item loop only on a decision taken at one of those barriers (bar.red.or
+    // of the abort flag), so neither is ever left waiting there alone.
+    int g = 0, on = 0, items = 0;  // key tiles consumed, items with work, items
+    for (int k = 0, idx = item_of(0); idx < num_items; idx = item_of(++k), ++items) {
+      const FwdItem I = fwd_item(p, idx, lane);
+      const int m0 = I.m * kTileQ;
+      const int i = m0 + r;
+      const int qb = on & 1;
+      const uint32_t o_col = FT_O0 + qb * 128;
+      float mrow = kNegInf;  // running maximum (log2 units); moved only by more than 8
+      float lrow = 0.f;      // running sum of this warpgroup's P relative to mrow
+      int ncur = I.n_begin - 1;
+      bool aborted = false;
+      for (int t = 0; t < I.nvis; ++t) {
+        const int x = g + t;
+        const int n = ncur = fwd_next_tile(I, ncur);
+        const int kb = n * kTileK;  // key index of column 0
+        const bool need_mask = !tile_full(I.gm, I.m, n);
+        // visible columns: lo <= key - i <= hi and key < Sk  <=>  c in [cmin, cmax]
+        const int cmin = max(i + I.lo - kb, -1);
+        const int cmax = min(min(i + I.hi - kb, I.Sk - 1 - kb), 1 << 20);
+        const uint32_t sbuf = t_lane + FT_S0 + (x & 1) * 128 + col0;
+        const bool ok = warp_wait(bar(F_SF0 + (x & 1)), (x >> 1) & 1, st, kFwdTimeout - 30);
+        float xs[64];
+        float mx = kNegInf;
+        if (ok) {
+          tc_fence_after();
+          mx = need_mask ? fwd_scores<true, SOFTCAP>(kc, sbuf, col0, cmin, cmax, xs)
+                         : fwd_scores<false, SOFTCAP>(kc, sbuf, col0, cmin, cmax, xs);
+        }
+        // the row maximum over both halves; both warpgroups always reach this barrier, and
+        // after it both see the abort flag that a failed wait of either one has raised
+        s_max[((x & 1) * 2 + wg) * 128 + r] = mx;
+        if (named_bar_or(1, 256, *s_abort != 0)) {
+          aborted = true;
+          break;
+        }
+        mx = fmaxf(mx, s_max[((x & 1) * 2 + (wg ^ 1)) * 128 + r]);
+        // move the reference maximum only when a score passes it by more than 8 (log2);
+        // both warpgroups take the same decision for a row
+        float alpha = 1.f;
+        if (t == 0) {
+          mrow = mx;
+        } else if (mx > mrow + 8.f) {
+          alpha = ex2_approx(mrow - mx);  // mrow finite here, or -inf: alpha = 0
+          mrow = mx;
+        }
+        const float muse = mrow == kNegInf ? 0.f : mrow;  // all-masked so far: P = 0
+        lrow = lrow * alpha + fwd_probs<F16>(sbuf, muse, xs);
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds this item's products up to key tile x-1: wait for the last one, then
+          // rescale this warpgroup's columns (a failed wait ends the loop at the next barrier)
+          if (!warp_wait(bar(F_PD0 + ((x - 1) & 1)), ((x - 1) >> 1) & 1, st, kFwdTimeout - 31)) continue;
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < NCH0; ++c) {
-          if (c_lo + c < c_hi) {
-            uint32_t o[16];
-            tmem_ld16(t_lane + FT_O + (c_lo + c) * 16, o);
+          for (int cc = 0; cc < NCH0; ++cc) {
+            if (c_lo + cc < c_hi) {
+              uint32_t o[16];
+              tmem_ld16(t_lane + o_col + (c_lo + cc) * 16, o);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st16(t_lane + FT_O + (c_lo + c) * 16, o);
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st16(t_lane + o_col + (c_lo + cc) * 16, o);
+            }
           }
         }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(F_PF0 + (x & 1)));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(F_PF0 + (it & 1)));
-    }
 
-    // O = acc / l and LSE = (m + log2 l) * ln 2 with l the sum of both halves; a row with
-    // no visible key gives O = 0 and LSE = +inf
-    bool have = false;
-    if (!*s_abort && total > 0) have = warp_wait(bar(F_ACC), 0, st, kFwdTimeout - 32);
-    s_l[wg * 128 + r] = lrow;
-    named_bar_sync(1, 256);
-    const float lsum = lrow + s_l[(wg ^ 1) * 128 + r];
-    if (have) tc_fence_after();
-    if (__all_sync(0xffffffffu, *s_abort == 0)) {
-      const bool row_ok = i < Sq;
+      // O = acc / l and LSE = (m + log2 l) * ln 2 with l the sum of both halves; a row with
+      // no visible key gives O = 0 and LSE = +inf.  The O buffer is released to the item
+      // two ahead as soon as it is in registers.
+      const bool have = I.nvis > 0;
+      bool acc_ok = !aborted;
+      if (have && acc_ok) {
+        acc_ok = warp_wait(bar(F_ACC0 + qb), (on >> 1) & 1, st, kFwdTimeout - 32);
+        if (acc_ok) tc_fence_after();
+      }
+      const int lb = items & 1;  // row-sum exchange slot: alternates item by item
+      s_l[(lb * 2 + wg) * 128 + r] = lrow;
+      const bool stop = named_bar_or(1, 256, aborted || !acc_ok || *s_abort != 0);
+      const float lsum = lrow + s_l[(lb * 2 + (wg ^ 1)) * 128 + r];
+      const bool row_ok = i < I.Sq;
+      const bool store = !stop && row_ok;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (int64_t)tb * p.o_sb +
-                       (int64_t)(q_off + i) * p.o_ss + (int64_t)h * p.o_sh;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (int64_t)I.tb * p.o_sb +
+                       (int64_t)(I.q_off + i) * p.o_ss + (int64_t)I.h * p.o_sh;
 #pragma unroll
       for (int cc = 0; cc < NCH0; ++cc) {
         const int c = c_lo + cc;
         if (c < c_hi) {
           uint32_t o[16];
-          if (have) {
-            tmem_ld16(t_lane + FT_O + c * 16, o);
+          if (have && !stop) {
+            tmem_ld16(t_lane + o_col + c * 16, o);
           } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] = 0u;
@@ -392,7 +497,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             pk[e] = pack_h2<F16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-          if (row_ok) {
+          if (store) {
             if (c * 16 < p.D)
               *reinterpret_cast<uint4*>(orow + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             if (c * 16 + 8 < p.D)
@@ -400,10 +505,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      if (row_ok && wg == 0) {
+      if (have && !stop) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(F_OE0 + qb));
+      }
+      if (store && wg == 0) {
         const float lse = lsum > 0.f ? (mrow + log2f(lsum)) * 0.69314718055994531f
                                      : __int_as_float(0x7f800000);
-        p.lse[(int64_t)tb * p.lse_sb + (int64_t)h * p.lse_sh + (int64_t)(q_off + i) * p.lse_ss] = lse;
+        p.lse[(int64_t)I.tb * p.lse_sb + (int64_t)I.h * p.lse_sh + (int64_t)(I.q_off + i) * p.lse_ss] = lse;
+      }
+      if (stop) break;
+      if (have) {
+        g += I.nvis;
+        ++on;
       }
     }
   }
@@ -441,9 +556,14 @@ cudaError_t launch_fwd_one(const FwdTcParams& p, const OperandMaps& q, const Ope
   const size_t smem = GeoF<DP>::TOTAL > 118784u ? GeoF<DP>::TOTAL : 118784u;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int64_t ctas = (int64_t)p.Mb * p.B * p.H;
-  if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)ctas, kFwdThreads, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail);
+  const int64_t items = (int64_t)p.Mb * p.B * p.H;
+  if (items > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  // persistent: at most one CTA per SM, each walking items blockIdx.x, + gridDim.x, ...
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);
+  kern<<<grid, kFwdThreads, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail);
   return cudaGetLastError();
 }
 
