@@ -7,6 +7,7 @@ Public Python surface (thin wrappers over include/fa.h):
            window_right, softcap, deterministic, workspace=None)
     attention_forward(q, k, v, ...)  -> (out, lse)            allocates outputs with torch
     attention_backward(dout, q, k, v, out, lse, ...) -> (dq, dk, dv)
+    flash_attn_func(q, k, v, ...) / flash_attn_varlen_func(...)   torch.autograd functions
 
 Layouts: q/out/dout/dq (B, Sq, H, D); k/v/dk/dv (B, Sk, Hk, D); all of one 16-bit type, bf16
 or f16; lse (B, H, Sq) fp32 natural log.  All compute runs in libfa_gb300.so.
@@ -22,7 +23,10 @@ from ._abi import (FaError, alloc_bwd_workspace, bwd_blocksparse_workspace_size,
                    bwd_varlen_workspace_size, bwd_workspace_size, fa_bwd, fa_bwd_blocksparse,
                    fa_bwd_status, fa_bwd_varlen, fa_fwd, fa_fwd_blocksparse, fa_fwd_varlen, load)
 
+from .autograd import flash_attn_func, flash_attn_varlen_func
+
 __all__ = ["FaError", "alloc_bwd_workspace", "attention_backward", "attention_backward_varlen",
+           "flash_attn_func", "flash_attn_varlen_func",
            "attention_forward", "attention_forward_varlen", "bwd_varlen_workspace_size",
            "bwd_workspace_size", "fa_bwd", "fa_bwd_status", "fa_bwd_varlen", "fa_fwd",
            "fa_fwd_varlen", "load", "fa_fwd_blocksparse", "fa_bwd_blocksparse",

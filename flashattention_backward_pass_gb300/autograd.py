@@ -1,0 +1,88 @@
+"""torch.autograd entry points over the C ABI: `flash_attn_func` and
+`flash_attn_varlen_func` (the call-trace page's `flash_attn_func` -> `_flash_attn_forward`
+/ `_flash_attn_backward` pair, and the Triton page's `flash_attn_varlen_func`).
+
+The forward saves q, k, v, out and the natural-log LSE; the backward calls fa_bwd /
+fa_bwd_varlen with them (dQ, dK, dV written by the library's kernels).  Every step runs
+in libfa_gb300.so: these classes only allocate outputs and pass tensors through.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _abi
+
+
+def _scale(q, softmax_scale):
+    return softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(q.shape[-1])
+
+
+class FlashAttnFunc(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, softmax_scale, causal, window_left, window_right, softcap,
+                deterministic):
+        q, k, v = (t if t.stride(-1) == 1 else t.contiguous() for t in (q, k, v))
+        B, Sq, H, _ = q.shape
+        out = torch.empty_like(q)
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+        _abi.fa_fwd(q, k, v, out, lse, softmax_scale, causal, window_left, window_right, softcap)
+        ctx.save_for_backward(q, k, v, out, lse)
+        ctx.args = (softmax_scale, causal, window_left, window_right, softcap, deterministic)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse = ctx.saved_tensors
+        scale, causal, wl, wr, softcap, det = ctx.args
+        dout = dout if dout.stride(-1) == 1 else dout.contiguous()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        _abi.fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, scale, causal, wl, wr, softcap, det)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def flash_attn_func(q, k, v, softmax_scale=None, causal=False, window_left=-1, window_right=-1,
+                    softcap=0.0, deterministic=False):
+    """Attention with gradients: q (B, Sq, H, D), k / v (B, Sk, Hk, D), bf16 or f16.
+    Returns out (B, Sq, H, D); its backward produces dq, dk, dv through fa_bwd."""
+    return FlashAttnFunc.apply(q, k, v, _scale(q, softmax_scale), bool(causal), int(window_left),
+                               int(window_right), float(softcap), bool(deterministic))
+
+
+class FlashAttnVarlenFunc(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                softmax_scale, causal, window_left, window_right, softcap, deterministic):
+        q, k, v = (t if t.stride(-1) == 1 else t.contiguous() for t in (q, k, v))
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+        _abi.fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                           max_seqlen_k, softmax_scale, causal, window_left, window_right,
+                           softcap)
+        ctx.save_for_backward(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k)
+        ctx.args = (max_seqlen_q, max_seqlen_k, softmax_scale, causal, window_left,
+                    window_right, softcap, deterministic)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, out, lse, cu_q, cu_k = ctx.saved_tensors
+        mq, mk, scale, causal, wl, wr, softcap, det = ctx.args
+        dout = dout if dout.stride(-1) == 1 else dout.contiguous()
+        dq, dk, dv = torch.empty_like(q), torch.zeros_like(k), torch.zeros_like(v)
+        _abi.fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, mq, mk, scale,
+                           causal, wl, wr, softcap, det)
+        return dq, dk, dv, None, None, None, None, None, None, None, None, None, None
+
+
+def flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                           softmax_scale=None, causal=False, window_left=-1, window_right=-1,
+                           softcap=0.0, deterministic=False):
+    """Packed sequences with gradients: q (total_q, H, D), k / v (total_k, Hk, D), int32
+    device offsets of length batch + 1.  Returns out (total_q, H, D)."""
+    return FlashAttnVarlenFunc.apply(q, k, v, cu_seqlens_q, cu_seqlens_k, int(max_seqlen_q),
+                                     int(max_seqlen_k), _scale(q, softmax_scale), bool(causal),
+                                     int(window_left), int(window_right), float(softcap),
+                                     bool(deterministic))
