@@ -81,12 +81,13 @@ enum Bar : int {
   B_K = 0, B_V, B_QF0, B_QF1, B_QE0, B_QE1, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
   B_SFULL, B_DPFULL, B_PFULL, B_DSFULL, B_DVDONE, B_DQFULL, B_DQEMPTY, B_DSEMPTY,
   B_ACC, B_DRAIN, B_TILEF0, B_TILEF1, B_TILEE0, B_TILEE1, B_KEMPTY, B_VEMPTY, B_DVEMPTY,
-  B_DKEMPTY, B_NEXT, B_COUNT
+  B_DKEMPTY, B_NEXT, B_TURN, B_TURNE, B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area holds 32 mbarriers");
 
 // Consumers of a published tile descriptor: producer, MMA issuer, 4 drain warps and 8
-// compute warps each arrive once on the slot's empty barrier.
+// compute warps each arrive once on the slot's empty barrier (and, in the ordered mode,
+// the ordering warp).
 constexpr int kTileConsumers = 14;
 
 // One key tile of work as the scheduler publishes it in shared memory.
@@ -168,13 +169,18 @@ struct TileCoord {
 };
 
 __device__ __forceinline__ TileCoord decode_tile(const BwdMainParams& p, int t) {
-  // key-tile-major order: all (b, hk) of key tile 0 first.  Under causal masking the low
-  // key tiles see the most query tiles, so the longest work starts first, and in the
-  // deterministic mode every tile a CTA waits for was claimed by a running CTA.
+  // Key-tile-major order.  Normally all (b, hk) of key tile 0 come first: under causal
+  // masking the low key tiles see the most query tiles, so the longest work starts first.
+  // In the ordered (deterministic) mode the last key tile comes first instead: the dQ
+  // contributions to a query tile are added from the highest key tile down, which is the
+  // order in which a key-tile-major sweep reaches them (key tile n + 1 reaches query tile
+  // m one step before key tile n), and every tile a CTA waits for was claimed earlier,
+  // by a CTA that is running or done.
   TileCoord c;
-  int per_n = p.B * p.Hk;
-  c.n = t / per_n;
-  int r = t - c.n * per_n;
+  const int per_n = p.B * p.Hk;
+  const int n0 = t / per_n;
+  const int r = t - n0 * per_n;
+  c.n = p.deterministic ? p.Nb - 1 - n0 : n0;
   c.b = r / p.Hk;
   c.hk = r - c.b * p.Hk;
   return c;
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(bar(B_DOF0 + s), 1);
       mbar_init(bar(B_DOE0 + s), 1);
       mbar_init(bar(B_TILEF0 + s), 1);
-      mbar_init(bar(B_TILEE0 + s), kTileConsumers);
+      mbar_init(bar(B_TILEE0 + s), kTileConsumers + (p.deterministic ? 1 : 0));
     }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_DPFULL), 1);
@@ -338,6 +344,8 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar(B_DVEMPTY), 8);
     mbar_init(bar(B_DKEMPTY), 8);
     mbar_init(bar(B_NEXT), 1);
+    mbar_init(bar(B_TURN), 1);
+    mbar_init(bar(B_TURNE), 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(512, 1)
   if (warp < 4) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
 #ifdef FA_TRACE
-   if (warp == 3 && lane == 0 && blockIdx.x < FA_TRACE_CTAS) {
+   if (warp == 3 && lane == 0 && blockIdx.x < FA_TRACE_CTAS && !p.deterministic) {
      // observer: poll the completion barriers in order of their phases
      const int bars[5] = {B_SFULL, B_DPFULL, B_DVDONE, -1, B_DQFULL};
      int k[5] = {0, 0, 0, 0, 0};
@@ -714,6 +722,73 @@ __global__ void __launch_bounds__(512, 1)
         mbar_wait_ool(bar(B_DRAIN), 0, dr, kTimeoutBase - 17);
       }
     }
+   } else if (warp == 3) {
+    // ------------------------------------------------------------------ ordering warp
+    // Ordered mode only.  One step ahead of the drain, lane 0 waits (bounded) until the
+    // step's dQ tile holds the contributions of every higher key tile (its counter equals
+    // this key tile's rank from the top), then hands the outcome to the drain (turn
+    // barrier) and waits until the drain has taken it (turn-empty barrier) before the next
+    // step.  The drain's TMEM read, which frees the dQ columns for the next dP product,
+    // never waits on this global-memory round trip.
+    if constexpr (!SPARSE) {
+     if (p.deterministic) {
+      volatile int* s_turn = reinterpret_cast<volatile int*>(small + SM_TILE + 8);
+      int git = 0;
+      bool alive = true;
+      for (int t = 0; alive; ++t) {
+        TileDesc d;
+        const bool have_tile = __all_sync(0xffffffffu, read_tile(t, d));
+        SeqDesc vd{};
+        if constexpr (VARLEN) {
+          if (have_tile) vd = vring[t & 1];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TILEE0 + (t & 1)));
+        if (!have_tile) break;
+        if (lane == 0) {
+          for (int it = 0; it < d.total; ++it, ++git) {
+            const int g = it / d.m_count;
+            const int m = d.m_begin + (it - g * d.m_count);
+            const int h = d.hk * p.G + g;
+            size_t tile_id = ((size_t)d.b * p.H + h) * p.Mb + m;
+            if constexpr (VARLEN) tile_id = (size_t)h * p.T + vd.slot0 + m;
+            const int* sem = p.sems + tile_id;
+            if (git > 0 &&
+                !mbar_wait_ool(bar(B_TURNE), (git - 1) & 1, st, kTimeoutBase - 22)) {
+              alive = false;
+              break;
+            }
+            int64_t nb, ne;
+            if constexpr (VARLEN)
+              n_range(seq_geom(vd), m, &nb, &ne);
+            else
+              n_range(gm, m, &nb, &ne);
+            const int want = (int)ne - 1 - d.n;  // rank from the highest key tile down
+            int stop = 0;
+            const long long t0 = clock64();
+            while (true) {
+              int cur;
+              asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cur) : "l"(sem) : "memory");
+              if (cur == want) break;
+              if (*s_abort) { stop = 1; break; }
+              if (clock64() - t0 > p.wait_limit) {
+                raise_timeout(st, kTimeoutBase - 21);
+                stop = 1;
+                break;
+              }
+            }
+            s_turn[git & 1] = stop;
+            mbar_arrive(bar(B_TURN));  // release: the drain that sees the phase sees s_turn
+            if (stop) {
+              alive = false;
+              break;
+            }
+          }
+        }
+        alive = __shfl_sync(0xffffffffu, alive, 0);
+      }
+     }
+    }
    }
   } else if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 160;" ::: "memory");
@@ -727,6 +802,21 @@ __global__ void __launch_bounds__(512, 1)
     const int q = qd * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
     volatile int* s_skip = reinterpret_cast<volatile int*>(small + SM_TILE + 4);
+    // Ordered mode: the counter of the last tile added, incremented once its bulk adds
+    // have completed.  The completion wait is deferred to the next step (or the end of
+    // the key tile), so it overlaps the next dQ product.  A key tile only waits for higher
+    // key tiles, a deferred increment only holds back lower ones, and the next key tile
+    // this CTA takes starts after the release: no cycle.
+    int* pend = nullptr;
+    auto release_pending = [&]() {
+      if (pend != nullptr) {
+        bulk_wait_all();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(pend) : "memory");
+        pend = nullptr;
+      }
+    };
     int git = 0;
     for (int t = 0;; ++t) {
       TileDesc d;
@@ -775,33 +865,21 @@ __global__ void __launch_bounds__(512, 1)
         float* dst = p.dq_accum + tile_id * (size_t)(128 * DP);
         int* sem = p.sems + tile_id;
         if (p.deterministic) {
-          // Ordered mode: contributions to one dQ tile are added in ascending key-tile
-          // order.  No drain thread leaves a step early, so the named barriers of a step
-          // are always reached by all 128 drain threads.
+          // Ordered mode: contributions to one dQ tile are added in descending key-tile
+          // order; the ordering warp has waited for this step's turn.  No drain thread
+          // leaves a step early, so the named barriers of a step are always reached by all
+          // 128 drain threads.
           if (threadIdx.x == 128) {
-            int stop = (*s_abort) || !ok;
-            if (!stop) {
-              int64_t nb, ne;
-              if constexpr (VARLEN)
-                n_range(seq_geom(vd), m, &nb, &ne);
-              else
-                n_range(gm, m, &nb, &ne);
-              const int want = d.n - (int)nb;
-              long long t0 = clock64();
-              while (true) {
-                int cur;
-                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cur) : "l"(sem) : "memory");
-                if (cur == want) {
-                  asm volatile("fence.proxy.async.global;" ::: "memory");
-                  break;
-                }
-                if (*s_abort) { stop = 1; break; }
-                if (clock64() - t0 > p.wait_limit) {
-                  raise_timeout(st, kTimeoutBase - 21);
-                  stop = 1;
-                  break;
-                }
-              }
+            release_pending();
+            volatile int* s_turn = reinterpret_cast<volatile int*>(small + SM_TILE + 8);
+            int stop = !ok;
+            if (!mbar_wait(bar(B_TURN), git & 1, st, kTimeoutBase - 23)) {
+              stop = 1;
+            } else {
+              stop = stop || s_turn[git & 1];
+              mbar_arrive(bar(B_TURNE));
+              // the bulk adds below (async proxy) come after the counter acquire
+              asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             *s_skip = stop;
           }
@@ -839,18 +917,11 @@ __global__ void __launch_bounds__(512, 1)
             bulk_commit();
           }
         }
-        if (p.deterministic) {
-          if (threadIdx.x == 128) {
-            bulk_wait_all();
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            __threadfence();
-            if (*s_skip == 0)
-              asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-          }
-        }
+        if (p.deterministic && threadIdx.x == 128 && *s_skip == 0) pend = sem;
         // no early exit: every drain thread reaches every named barrier of every step (on
         // an abort the waits return at once and the stores and bulk adds are skipped)
       }
+      if (threadIdx.x == 128) release_pending();
 
     }
     if (threadIdx.x == 128) bulk_wait_all();
