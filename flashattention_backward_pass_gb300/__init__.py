@@ -58,24 +58,32 @@ def attention_backward(dout, q, k, v, out, lse, softmax_scale=None, causal=False
 
 def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                              softmax_scale=None, causal=False, window_left=-1, window_right=-1,
-                             softcap=0.0):
+                             softcap=0.0, seqused_q=None, seqused_k=None):
     """Packed sequences: q (total_q, H, D), k / v (total_k, Hk, D), int32 device offsets of
-    length batch + 1.  Returns out (total_q, H, D) and lse (H, total_q)."""
-    out = torch.empty_like(q)
-    lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+    length batch + 1, optional int32 device used lengths (seqused_q / seqused_k, length
+    batch).  Returns out (total_q, H, D) and lse (H, total_q); rows past a sequence's used
+    length are 0 in out and +inf in lse."""
+    padded = seqused_q is not None or seqused_k is not None
+    out = torch.zeros_like(q) if padded else torch.empty_like(q)
+    lse = (torch.full if padded else torch.empty)(
+        (q.shape[1], q.shape[0]), *((float("inf"),) if padded else ()), dtype=torch.float32,
+        device=q.device)
     fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
-                  _scale(q, softmax_scale), causal, window_left, window_right, softcap)
+                  _scale(q, softmax_scale), causal, window_left, window_right, softcap,
+                  seqused_q=seqused_q, seqused_k=seqused_k)
     return out, lse
 
 
 def attention_backward_varlen(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                               max_seqlen_k, softmax_scale=None, causal=False, window_left=-1,
-                              window_right=-1, softcap=0.0, deterministic=False, workspace=None):
-    """Packed sequences (layouts of attention_forward_varlen).  Returns dq, dk, dv."""
-    dq = torch.empty_like(q)
+                              window_right=-1, softcap=0.0, deterministic=False, workspace=None,
+                              seqused_q=None, seqused_k=None):
+    """Packed sequences (layouts of attention_forward_varlen).  Returns dq, dk, dv; rows
+    past a sequence's used length are 0."""
+    dq = torch.zeros_like(q) if seqused_q is not None else torch.empty_like(q)
     dk = torch.zeros_like(k)
     dv = torch.zeros_like(v)
     fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                   max_seqlen_k, _scale(q, softmax_scale), causal, window_left, window_right,
-                  softcap, deterministic, workspace)
+                  softcap, deterministic, workspace, seqused_q=seqused_q, seqused_k=seqused_k)
     return dq, dk, dv

@@ -81,11 +81,12 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd_set_algorithm.argtypes = [ctypes.c_int]
     lib.fa_bwd_get_algorithm.restype = ctypes.c_int
     ip = ctypes.c_void_p  # device int32 offsets
-    if not hasattr(lib, "fa_fwd_varlen"):  # a library built before the packed entry points
+    if not hasattr(lib, "fa_fwd_varlen") or lib.fa_abi_version() < 2:
+        # a library built before the packed entry points took used lengths
         _lib = lib
         return lib
     lib.fa_fwd_varlen.restype = ctypes.c_int
-    lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, ip, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+    lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, ip, ip, ip, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_float, vp, sz, vp]
     lib.fa_bwd_varlen_workspace_size.restype = sz
@@ -102,7 +103,7 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd_blocksparse.argtypes = [P, P, P, P, P, P, P, P, P, vp, ctypes.c_float, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, sz, vp]
     lib.fa_bwd_varlen.restype = ctypes.c_int
-    lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, ip, ip, ctypes.c_int, ctypes.c_int,
+    lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, ip, ip, ip, ip, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, vp, sz, vp]
     _lib = lib
@@ -254,14 +255,26 @@ def _offsets(cu):
     return ctypes.c_void_p(cu.data_ptr())
 
 
+def _used(used, batch):
+    """Optional per-sequence used lengths (seqused_q / seqused_k): None or a 1-D int32 CUDA
+    tensor of `batch` entries."""
+    if used is None:
+        return None
+    if used.dtype != torch.int32 or not used.is_cuda or used.dim() != 1 or used.numel() != batch:
+        raise ValueError(f"seqused must be a 1-D int32 CUDA tensor of {batch} entries")
+    return ctypes.c_void_p(used.data_ptr())
+
+
 def fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                   softmax_scale, causal=False, window_left=-1, window_right=-1, softcap=0.0,
-                  stream=None):
+                  stream=None, seqused_q=None, seqused_k=None):
     """C call `fa_fwd_varlen`: q, out (total_q, H, D), k, v (total_k, Hk, D), lse (H, total_q)."""
     lib = load()
+    batch = cu_seqlens_q.numel() - 1
     tv = [tensor_view(x) for x in (q, k, v, out, lse)]
     st = lib.fa_fwd_varlen(*[ctypes.byref(x) for x in tv], _offsets(cu_seqlens_q),
-                           _offsets(cu_seqlens_k), cu_seqlens_q.numel() - 1, int(max_seqlen_q),
+                           _offsets(cu_seqlens_k), _used(seqused_q, batch), _used(seqused_k, batch),
+                           batch, int(max_seqlen_q),
                            int(max_seqlen_k), float(softmax_scale), int(bool(causal)),
                            int(window_left), int(window_right), float(softcap), None, 0,
                            _stream_ptr(stream))
@@ -274,7 +287,8 @@ def bwd_varlen_workspace_size(batch, H, total_q, D, deterministic=False) -> int:
 
 def fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                   max_seqlen_k, softmax_scale, causal=False, window_left=-1, window_right=-1,
-                  softcap=0.0, deterministic=False, workspace=None, stream=None):
+                  softcap=0.0, deterministic=False, workspace=None, stream=None, seqused_q=None,
+                  seqused_k=None):
     """C call `fa_bwd_varlen` (dq, dk, dv written in place).  Returns the workspace used."""
     lib = load()
     batch = cu_seqlens_q.numel() - 1
@@ -283,7 +297,8 @@ def fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
     tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
     st = lib.fa_bwd_varlen(*[ctypes.byref(x) for x in tv], _offsets(cu_seqlens_q),
-                           _offsets(cu_seqlens_k), batch, int(max_seqlen_q), int(max_seqlen_k),
+                           _offsets(cu_seqlens_k), _used(seqused_q, batch), _used(seqused_k, batch),
+                           batch, int(max_seqlen_q), int(max_seqlen_k),
                            float(softmax_scale), int(bool(causal)), int(window_left),
                            int(window_right), float(softcap), int(bool(deterministic)),
                            ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),

@@ -54,14 +54,17 @@ def flash_attn_func(q, k, v, softmax_scale=None, causal=False, window_left=-1, w
 class FlashAttnVarlenFunc(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
-                softmax_scale, causal, window_left, window_right, softcap, deterministic):
+                softmax_scale, causal, window_left, window_right, softcap, deterministic,
+                seqused_q, seqused_k):
         q, k, v = (t if t.stride(-1) == 1 else t.contiguous() for t in (q, k, v))
-        out = torch.empty_like(q)
+        padded = seqused_q is not None or seqused_k is not None
+        out = torch.zeros_like(q) if padded else torch.empty_like(q)
         lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
         _abi.fa_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                            max_seqlen_k, softmax_scale, causal, window_left, window_right,
-                           softcap)
+                           softcap, seqused_q=seqused_q, seqused_k=seqused_k)
         ctx.save_for_backward(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k)
+        ctx.used = (seqused_q, seqused_k)
         ctx.args = (max_seqlen_q, max_seqlen_k, softmax_scale, causal, window_left,
                     window_right, softcap, deterministic)
         return out
@@ -71,18 +74,22 @@ class FlashAttnVarlenFunc(torch.autograd.Function):
         q, k, v, out, lse, cu_q, cu_k = ctx.saved_tensors
         mq, mk, scale, causal, wl, wr, softcap, det = ctx.args
         dout = dout if dout.stride(-1) == 1 else dout.contiguous()
-        dq, dk, dv = torch.empty_like(q), torch.zeros_like(k), torch.zeros_like(v)
+        uq, uk = ctx.used
+        dq = torch.zeros_like(q) if uq is not None else torch.empty_like(q)
+        dk, dv = torch.zeros_like(k), torch.zeros_like(v)
         _abi.fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, mq, mk, scale,
-                           causal, wl, wr, softcap, det)
-        return dq, dk, dv, None, None, None, None, None, None, None, None, None, None
+                           causal, wl, wr, softcap, det, seqused_q=uq, seqused_k=uk)
+        return (dq, dk, dv) + (None,) * 12
 
 
 def flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                            softmax_scale=None, causal=False, window_left=-1, window_right=-1,
-                           softcap=0.0, deterministic=False):
+                           softcap=0.0, deterministic=False, seqused_q=None, seqused_k=None):
     """Packed sequences with gradients: q (total_q, H, D), k / v (total_k, Hk, D), int32
-    device offsets of length batch + 1.  Returns out (total_q, H, D)."""
+    device offsets of length batch + 1, optional int32 device used lengths of length batch
+    (rows past them are padding: out and the gradients are 0 there).  Returns out
+    (total_q, H, D)."""
     return FlashAttnVarlenFunc.apply(q, k, v, cu_seqlens_q, cu_seqlens_k, int(max_seqlen_q),
                                      int(max_seqlen_k), _scale(q, softmax_scale), bool(causal),
                                      int(window_left), int(window_right), float(softcap),
-                                     bool(deterministic))
+                                     bool(deterministic), seqused_q, seqused_k)

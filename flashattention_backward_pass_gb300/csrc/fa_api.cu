@@ -109,6 +109,8 @@ bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u)
 struct VarlenArgs {
   const int* cu_q;
   const int* cu_k;
+  const int* used_q;  // optional per-sequence used lengths (null: the whole range)
+  const int* used_k;
   int batch, max_q, max_k;
 };
 
@@ -350,7 +352,8 @@ int fa_fwd_blocksparse(const fa_tensor* q, const fa_tensor* k, const fa_tensor* 
 }
 
 int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out,
-                  fa_tensor* lse, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  fa_tensor* lse, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  const int* seqused_q, const int* seqused_k, int batch,
                   int max_seqlen_q, int max_seqlen_k, float softmax_scale, int causal,
                   int window_left, int window_right, float softcap, void* workspace,
                   size_t workspace_bytes, void* stream) {
@@ -389,6 +392,8 @@ int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa
   p.varlen = 1;
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
+  p.used_q = seqused_q;
+  p.used_k = seqused_k;
   p.total_q = Tq;
   p.total_k = Tk;
   p.causal = causal ? 1 : 0;
@@ -493,6 +498,7 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
   if (vl) {
     pre.varlen = 1;
     pre.cu_q = vl->cu_q;
+    pre.used_q = vl->used_q;
     pre.total_q = total_q;
     pre.T = T;
   }
@@ -550,6 +556,8 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
     if (vl) {
       p.cu_q = vl->cu_q;
       p.cu_k = vl->cu_k;
+      p.used_q = vl->used_q;
+      p.used_k = vl->used_k;
       p.total_q = total_q;
       p.total_k = total_k;
       p.T = T;
@@ -606,6 +614,7 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
   if (vl) {
     cp.varlen = 1;
     cp.cu_q = vl->cu_q;
+    cp.used_q = vl->used_q;
     cp.total_q = total_q;
     cp.T = T;
   }
@@ -653,7 +662,8 @@ size_t fa_bwd_varlen_workspace_size(int batch, int H, int total_q, int D, int de
 int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
                   const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq,
                   fa_tensor* dk, fa_tensor* dv, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                  int batch, int max_seqlen_q, int max_seqlen_k, float softmax_scale, int causal,
+                  const int* seqused_q, const int* seqused_k, int batch, int max_seqlen_q,
+                  int max_seqlen_k, float softmax_scale, int causal,
                   int window_left, int window_right, float softcap, int deterministic,
                   void* workspace, size_t workspace_bytes, void* stream) {
   fa_tensor d4, q4, k4, v4, o4, l3, dq4, dk4, dv4;
@@ -664,7 +674,8 @@ int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
       (st = packed_view(dq, 3, &dq4)) || (st = packed_view(dk, 3, &dk4)) ||
       (st = packed_view(dv, 3, &dv4)))
     return st;
-  VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k};
+  VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k, batch, max_seqlen_q,
+                max_seqlen_k};
   return bwd_common(&d4, &q4, &k4, &v4, &o4, &l3, &dq4, &dk4, &dv4, softmax_scale, causal,
                     window_left, window_right, softcap, deterministic, workspace,
                     workspace_bytes, stream, &vl, nullptr);

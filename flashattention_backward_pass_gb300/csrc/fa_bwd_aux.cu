@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
         const int64_t t = tile - h * p.T;
         const int sb = slot_owner(p.cu_q, p.B, p.total_q, t);
         int64_t q0, sq;
-        seq_rows(p.cu_q, sb, p.total_q, &q0, &sq);
+        seq_rows(p.cu_q, p.used_q, sb, p.total_q, &q0, &sq);
         const int64_t il = (t - first_slot(p.cu_q, sb, p.total_q)) * 128 + (r & 127);
         real = il >= 0 && il < sq;  // (il < 0 only for malformed offsets)
         i = q0 + il;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(256) bwd_convert_kernel(const BwdConvParams p)
     const int64_t t = (int64_t)tile_id - (int64_t)h * p.T;
     const int sb = slot_owner(p.cu_q, p.B, p.total_q, t);
     int64_t q0, sq;
-    seq_rows(p.cu_q, sb, p.total_q, &q0, &sq);
+    seq_rows(p.cu_q, p.used_q, sb, p.total_q, &q0, &sq);
     const int64_t il = (t - first_slot(p.cu_q, sb, p.total_q)) * 128 + row0;
     b = 0;
     i0 = q0 + il;

@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(512, 1)
           int64_t mb64, me64;
           if constexpr (VARLEN) {
             int64_t q0, sq, k0, sk;
-            seq_rows(p.cu_q, c.b, p.total_q, &q0, &sq);
-            seq_rows(p.cu_k, c.b, p.total_k, &k0, &sk);
+            seq_rows(p.cu_q, p.used_q, c.b, p.total_q, &q0, &sq);
+            seq_rows(p.cu_k, p.used_k, c.b, p.total_k, &k0, &sk);
             const MaskGeom g = make_geom(sq, sk, p.causal, p.window_left, p.window_right, kTileQ, kTileK);
             m_range(g, c.n, &mb64, &me64);
             SeqDesc v;

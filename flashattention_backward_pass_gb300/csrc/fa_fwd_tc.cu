@@ -153,9 +153,12 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdTcParams& p, int idx, int l
     // sequence b: rows [cu[b], cu[b+1]) clamped into the packed tensors, so that malformed
     // offsets cannot move a load or a store outside them
     const int q0 = min(max(p.cu_q[it.b], 0), p.total_q);
-    const int q1 = min(max(p.cu_q[it.b + 1], q0), p.total_q);
+    int q1 = min(max(p.cu_q[it.b + 1], q0), p.total_q);
     const int k0 = min(max(p.cu_k[it.b], 0), p.total_k);
-    const int k1 = min(max(p.cu_k[it.b + 1], k0), p.total_k);
+    int k1 = min(max(p.cu_k[it.b + 1], k0), p.total_k);
+    // used lengths: only the first used[b] rows of the range are computed
+    if (p.used_q != nullptr) q1 = q0 + min(max(p.used_q[it.b], 0), q1 - q0);
+    if (p.used_k != nullptr) k1 = k0 + min(max(p.used_k[it.b], 0), k1 - k0);
     it.q_off = q0;
     it.k_off = k0;
     it.tb = 0;

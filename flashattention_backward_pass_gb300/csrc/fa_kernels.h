@@ -32,6 +32,7 @@ struct BwdPreParams {
   // total_q) views, B sequences, rows laid out per head in T slots of 128 (fa_tiles.h)
   int varlen;
   const int* cu_q;
+  const int* used_q;             // per-sequence used query rows, or null
   int total_q;
   int64_t T;
 };
@@ -67,6 +68,8 @@ struct BwdMainParams {
   // rows and counters are indexed per head by slot (fa_tiles.h: first_slot, T slots)
   const int* cu_q;
   const int* cu_k;
+  const int* used_q;   // per-sequence used query / key rows, or null (fa_tiles.h seq_rows)
+  const int* used_k;
   int total_q, total_k;
   long long T;
   int causal, window_left, window_right;
@@ -98,6 +101,7 @@ struct BwdConvParams {
   // packed sequences (varlen != 0): dq is a (1, total_q, H, D) view; tiles by slot
   int varlen;
   const int* cu_q;
+  const int* used_q;   // per-sequence used query rows, or null
   int total_q;
   int64_t T;
 };
@@ -126,6 +130,10 @@ struct FwdTcParams {
   int varlen;
   const int* cu_q;
   const int* cu_k;
+  // Optional per-sequence used lengths: sequence b computes only the first used_q[b]
+  // query rows and used_k[b] key rows of its range (clamped to the range); null: all.
+  const int* used_q;
+  const int* used_k;
   int total_q, total_k;
   int causal, window_left, window_right;
   // Block sparsity (batched calls): (B, H, Mb, Nb) bytes, contiguous; a zero entry

@@ -119,6 +119,18 @@ FA_HD void seq_rows(const int* cu, int b, int64_t total, int64_t* start, int64_t
   *len = e > a ? e - a : 0;
 }
 
+// With per-sequence used lengths (`used` non-null): sequence b keeps its rows from cu but
+// computes only the first used[b] of them (clamped into [0, its row count]); the rest are
+// padding.  Null `used`: every row of the sequence is used.
+FA_HD void seq_rows(const int* cu, const int* used, int b, int64_t total, int64_t* start,
+                    int64_t* len) {
+  seq_rows(cu, b, total, start, len);
+  if (used != nullptr) {
+    const int64_t u = used[b];
+    *len = u < 0 ? 0 : (u < *len ? u : *len);
+  }
+}
+
 // The backward's per-head tile layout for packed sequences: the 128-row query tiles of
 // sequence b take the slots [first_slot(b), first_slot(b) + ceil(Sq_b / 128)), with
 // first_slot(b) = floor(cu_q[b] / 128) + b.  For non-decreasing offsets the ranges of

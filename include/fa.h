@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 1
+#define FA_ABI_VERSION 2
 
 /* Element types.  Q, K, V, O, dO, dQ, dK and dV of one call share one 16-bit type:
  * bf16, or f16 (the call-trace page's dispatch covers both, `run_mha_bwd_constexpr`);
@@ -119,17 +119,28 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
  *   lse (H, total_q) fp32, natural log (+inf for a row with no visible key);
  *   cu_seqlens_q / cu_seqlens_k: DEVICE int32 arrays of batch + 1 non-decreasing offsets
  *     starting at 0 (caller-owned; read by the kernels, not by the host);
+ *   seqused_q / seqused_k: NULL, or DEVICE int32 arrays of batch used lengths (the
+ *     optional `mSeqUsedQ` / `mSeqUsedK` kernel arguments of the `flash_bwd_sm90.py`
+ *     page, whose meaning it leaves unstated): sequence b then computes only
+ *     the first seqused_q[b] query rows and seqused_k[b] key rows of its range (each
+ *     clamped into [0, the range's length]), as a batch of one of those lengths; the rows
+ *     after them are padding.  Padding rows of out and lse are not written.  They are
+ *     read as part of a sequence's last 128-row tile, where their contribution is exactly
+ *     zero, so they must hold finite values (zeros, for instance);
  *   max_seqlen_q / max_seqlen_k: at least the longest sequence (rows of a longer one are
  *     not computed) and at most total_q / total_k.
  * Offsets outside [0, total] are clamped into the tensors, so malformed offsets cannot
- * make the kernels access memory outside them (their results are then undefined).
+ * make the kernels access memory outside them (their results are then undefined).  With
+ * no key at all (total_k == 0 or max_seqlen_k == 0) every row of out is 0 and every lse
+ * row +inf, padding included.
  * batch == 0, total_q == 0 or max_seqlen_q == 0 returns FA_OK without a launch.  Errors
  * as fa_fwd, plus FA_ERR_ARG for batch < 0 or max lengths outside [0, total] and
  * FA_ERR_UNSUPPORTED for batch > 65535.
  */
 int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
                   fa_tensor* out, fa_tensor* lse,
-                  const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  const int* seqused_q, const int* seqused_k, int batch,
                   int max_seqlen_q, int max_seqlen_k,
                   float softmax_scale, int causal, int window_left, int window_right,
                   float softcap, void* workspace, size_t workspace_bytes, void* stream);
@@ -212,12 +223,15 @@ size_t fa_bwd_varlen_workspace_size(int batch, int H, int total_q, int D, int de
  * fused algorithm only (FA_ERR_UNSUPPORTED while the split one is selected); the
  * workspace must hold fa_bwd_varlen_workspace_size bytes.  Offset clamping, argument
  * errors and the status word as in fa_fwd_varlen and fa_bwd.  dK / dV rows of key rows
- * that no sequence owns are left untouched.
+ * that no sequence owns are left untouched.  seqused_q / seqused_k as in fa_fwd_varlen
+ * (the same arrays the forward got): padding rows of dq, dk and dv are not written, and
+ * padding rows of dout, q, k, v must hold finite values.
  */
 int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
                   const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
                   fa_tensor* dq, fa_tensor* dk, fa_tensor* dv,
-                  const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  const int* seqused_q, const int* seqused_k, int batch,
                   int max_seqlen_q, int max_seqlen_k,
                   float softmax_scale, int causal, int window_left, int window_right,
                   float softcap, int deterministic, void* workspace, size_t workspace_bytes,

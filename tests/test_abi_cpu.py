@@ -27,7 +27,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.fa_abi_version() == 1
+    assert lib.fa_abi_version() == 2
     for code in range(0, -12, -1):
         s = lib.fa_status_string(code)
         assert s and s.startswith(b"FA_")
@@ -158,7 +158,7 @@ def _varlen_fwd(lib, q=None, lse=None, cu=4096, batch=2, mq=100, mk=100, **kw):
     out = _view((tq, H, D))
     lv = lse or _view((H, tq), dtype=1)
     return lib.fa_fwd_varlen(ctypes.byref(qv), ctypes.byref(kv), ctypes.byref(kv), ctypes.byref(out),
-                             ctypes.byref(lv), cu, cu, batch, mq, mk, 0.125, 0, -1, -1, 0.0,
+                             ctypes.byref(lv), cu, cu, None, None, batch, mq, mk, 0.125, 0, -1, -1, 0.0,
                              None, 0, None)
 
 
@@ -181,13 +181,13 @@ def test_varlen_validation(lib):
     args = [ctypes.byref(x) for x in a]
     assert lib.fa_bwd_set_algorithm(0) == 0
     try:
-        assert lib.fa_bwd_varlen(*args, 4096, 4096, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
+        assert lib.fa_bwd_varlen(*args, 4096, 4096, None, None, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
                                  ctypes.c_void_p(4096), 1 << 30, None) == -8
     finally:
         assert lib.fa_bwd_set_algorithm(1) == 0
-    assert lib.fa_bwd_varlen(*args, 4096, 4096, 0, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
+    assert lib.fa_bwd_varlen(*args, 4096, 4096, None, None, 0, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
                              ctypes.c_void_p(4096), 1 << 30, None) == 0           # batch 0
-    assert lib.fa_bwd_varlen(*args, 4096, 4096, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
+    assert lib.fa_bwd_varlen(*args, 4096, 4096, None, None, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
                              ctypes.c_void_p(4096), 16, None) == -7               # workspace
     # workspace: per head total_q // 128 + batch slots of 128 rows
     f = lib.fa_bwd_varlen_workspace_size

@@ -80,8 +80,9 @@ SLOTS_HARNESS = r'''
 #include "fa_tiles.h"
 using namespace fa;
 // Packed sequences: every query tile of every sequence gets its own slot below
-// slot_count, and slot_owner maps each used slot back to its sequence.  Also run with
-// malformed (decreasing, negative, too large) offsets, where only the bound must hold.
+// slot_count, and slot_owner maps each used slot back to its sequence; used lengths
+// (seqused) keep the first row and clamp the length.  Also run with malformed
+// (decreasing, negative, too large) offsets, where only the bound must hold.
 int main() {
   long bad = 0, cases = 0;
   srand(7);
@@ -101,10 +102,19 @@ int main() {
     }
     const long T = slot_count(total, B);
     std::vector<int> owner(T, -1);
+    std::vector<int> used(B);
+    for (int b = 0; b < B; ++b) used[b] = rand() % 900 - 100;
     for (int b = 0; b < B; ++b) {
       long s0, len;
       seq_rows(cu.data(), b, total, &s0, &len);
       if (s0 < 0 || s0 + len > total) ++bad;
+      // used lengths: the same first row and a length clamped into [0, len], so the used
+      // rows (and their slots) stay inside the sequence's own; null means all rows
+      long s1, l1, s2, l2;
+      seq_rows(cu.data(), used.data(), b, total, &s1, &l1);
+      seq_rows(cu.data(), nullptr, b, total, &s2, &l2);
+      const long want = used[b] < 0 ? 0 : (used[b] < len ? used[b] : len);
+      if (s1 != s0 || l1 != want || s2 != s0 || l2 != len) ++bad;
       const long fs = first_slot(cu.data(), b, total);
       for (long m = 0; m * 128 < len; ++m) {
         const long t = fs + m;
