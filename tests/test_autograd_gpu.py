@@ -68,3 +68,39 @@ def test_flash_attn_varlen_func_gradients(fa):
             check_close("varlen autograd dV", to64(v.grad[k0:k0 + sk])[None], dv)
         q0 += sq
         k0 += sk
+
+
+def test_flash_attn_varlen_func_seqused(fa):
+    """Used lengths through autograd: the used rows' output and gradients follow the oracle
+    for each sequence as a batch of one of its used lengths; padding rows get a zero
+    output and zero gradients."""
+    cap_q, cap_k = [200, 130, 257], [256, 64, 300]
+    used_q, used_k = [150, 0, 257], [256, 20, 299]
+    q, k, v, do, cu_q, cu_k = make_varlen_inputs(cap_q, cap_k, 4, 2, 64, seed=79, device="cuda")
+    q, k, v = (t.clone().requires_grad_(True) for t in (q, k, v))
+    uq = torch.tensor(used_q, dtype=torch.int32, device="cuda")
+    uk = torch.tensor(used_k, dtype=torch.int32, device="cuda")
+    out = fa.flash_attn_varlen_func(q, k, v, cu_q, cu_k, max(used_q), max(used_k), causal=True,
+                                    seqused_q=uq, seqused_k=uk)
+    out.backward(do)
+    scale = 64 ** -0.5
+    q0 = k0 = 0
+    for cq, ck, sq, sk in zip(cap_q, cap_k, used_q, used_k):
+        if sq:
+            qs, dos = to64(q[q0:q0 + sq])[None], to64(do[q0:q0 + sq])[None]
+            ks, vs = to64(k[k0:k0 + sk])[None], to64(v[k0:k0 + sk])[None]
+            o_ref, _ = attention_forward(qs, ks, vs, scale, causal=True)
+            dq, dk, dv = attention_backward(dos, qs, ks, vs, scale, causal=True)
+            check_close("seqused autograd O", to64(out[q0:q0 + sq].detach())[None], o_ref)
+            check_close("seqused autograd dQ", to64(q.grad[q0:q0 + sq])[None], dq)
+            check_close("seqused autograd dK", to64(k.grad[k0:k0 + sk])[None], dk)
+            check_close("seqused autograd dV", to64(v.grad[k0:k0 + sk])[None], dv)
+        else:
+            assert torch.count_nonzero(k.grad[k0:k0 + sk]) == 0
+            assert torch.count_nonzero(v.grad[k0:k0 + sk]) == 0
+        assert torch.count_nonzero(out[q0 + sq:q0 + cq].detach()) == 0
+        assert torch.count_nonzero(q.grad[q0 + sq:q0 + cq]) == 0
+        assert torch.count_nonzero(k.grad[k0 + sk:k0 + ck]) == 0
+        assert torch.count_nonzero(v.grad[k0 + sk:k0 + ck]) == 0
+        q0 += cq
+        k0 += ck
