@@ -19,7 +19,8 @@
 // applies the scale.
 //
 // The grid is persistent (at most one CTA per SM): CTAs take key tiles from a ticket
-// counter in key-tile-major order, so under causal masking the longest tiles go first.
+// counter in key-tile-major order, so under causal masking the longest tiles go first
+// (in the ordered mode the highest key tile goes first: see decode_tile).
 //
 // Warp roles (16 warps, 512 threads):
 //   warp 0      TMA producer: K, V per tile (the next tile's K/V prefetched into L2 while
@@ -28,12 +29,14 @@
 //   warp 1      TMEM allocator and MMA issue (one elected lane issues)
 //   warp 2      tile scheduler: claims the next ticket when the current tile starts its
 //               last step and publishes it in a 2-slot ring
+//   warp 3      ordered (deterministic) mode only: waits, one step ahead of the drain,
+//               for each dQ tile's turn and hands it to the drain
 //   warps 4-7   dQ drain (160 registers each via setmaxnreg): TMEM -> registers, release
 //               the TMEM columns, then two 32 KB halves through a staging buffer into
-//               cp.reduce.async.bulk fp32 adds (ordered by key tile when deterministic);
-//               at the end of each tile, the dK / dV epilogue
+//               cp.reduce.async.bulk fp32 adds (ordered by key tile when deterministic)
 //   warps 8-15  two compute warpgroups: warpgroup w handles queries [64w, 64w+64) of
-//               the tile for every key row (thread = key = TMEM lane)
+//               the tile for every key row (thread = key = TMEM lane); at the end of
+//               each tile they write dK / dV, each warpgroup half of the columns
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0, Dp)        dK accumulator          [128, 128+Dp)  dV accumulator
