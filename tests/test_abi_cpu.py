@@ -224,3 +224,17 @@ def test_blocksparse_validation(lib):
     assert f(1, 2, 2, 128, 128, 64) == (((base + 2 * 4 + 255) // 256 * 256 + 2 * 1 * 1 * 4 + 255) // 256) * 256
     assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
                                   base, None) == -7        # fa_bwd's size is not enough
+
+
+def test_binding_checks_used_lengths():
+    """The binding accepts no used lengths, or a 1-D int32 device tensor of one entry per
+    sequence, and refuses anything else before calling the library."""
+    import torch
+    from flashattention_backward_pass_gb300 import _abi
+    assert _abi._used(None, 3) is None
+    with pytest.raises(ValueError):
+        _abi._used(torch.zeros(3, dtype=torch.int32), 3)       # host tensor
+    with pytest.raises(ValueError):
+        _abi._used(torch.zeros(3, dtype=torch.int64), 3)       # wrong type
+    with pytest.raises(ValueError):
+        _abi._used(torch.zeros((3, 1), dtype=torch.int32), 3)  # not 1-D
