@@ -19,8 +19,9 @@
 //
 // Two softmax warpgroups split the 128 key columns of the score tile: thread (warpgroup
 // w, TMEM lane r) owns query row r and columns [64w, 64w + 64).  The two halves of a
-// row's maximum meet through shared memory once per key tile; each warpgroup keeps the
-// row sum of its own columns and the two are added at the end.
+// row's maximum meet through shared memory once per key tile (a barrier of the two warps
+// that own the row); each warpgroup keeps the row sum of its own columns and the two are
+// added at the end.
 //
 // The running maximum m is only moved (and O, l rescaled by exp2(m_old - m_new)) when
 // a new score exceeds it by more than 8 in log2 units; otherwise the stale m is kept and
@@ -395,9 +396,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     constexpr int NCH = DP / 16;
     constexpr int NCH0 = (NCH + 1) / 2;
     const int c_lo = wg ? NCH0 : 0, c_hi = wg ? NCH : NCH0;
-    // Both warpgroups meet at named barrier 1 once per key tile and once per item; they
-    // leave the item loop only on a decision taken at one of those barriers (bar.red.or
-    // of the abort flag), so neither is ever left waiting there alone.
+    // The two warps of a lane quadrant (one per warpgroup) meet at named barrier 2 + qd
+    // once per key tile, and all eight softmax warps at named barrier 1 once per item.
+    // A pair leaves the key-tile loop only on a decision taken at its own barrier, and
+    // every warp reaches the item barrier (bar.red.or of the abort flag), so no warp is
+    // ever left waiting at a barrier alone.
     int g = 0, on = 0, items = 0;  // key tiles consumed, items with work, items
     for (int k = 0, idx = item_of(0); idx < num_items; idx = item_of(++k), ++items) {
       const FwdItem I = fwd_item(p, idx, lane);
@@ -426,10 +429,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mx = need_mask ? fwd_scores<true, SOFTCAP>(kc, sbuf, col0, cmin, cmax, xs)
                          : fwd_scores<false, SOFTCAP>(kc, sbuf, col0, cmin, cmax, xs);
         }
-        // the row maximum over both halves; both warpgroups always reach this barrier, and
-        // after it both see the abort flag that a failed wait of either one has raised
+        // the row maximum over both halves: only the two warps that own the same rows (one
+        // per warpgroup, barrier 2 + quadrant) meet here; both always reach it, and after
+        // it both see the abort flag that a failed wait of either one has raised
         s_max[((x & 1) * 2 + wg) * 128 + r] = mx;
-        if (named_bar_or(1, 256, *s_abort != 0)) {
+        if (named_bar_or(2 + qd, 64, *s_abort != 0)) {
           aborted = true;
           break;
         }
