@@ -145,3 +145,103 @@ def test_packed_sequence_slots(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "bad=0" in r.stdout
+
+
+ORDER_HARNESS = r'''
+#include <cstdio>
+#include <vector>
+#include "fa_tiles.h"
+using namespace fa;
+// A model of the fused backward's ordered (deterministic) dQ mode: P persistent CTAs take
+// key-tile tickets (n, batch, kv-head) in claim order; a ticket's steps visit its query
+// tiles for each of its G q-heads (head-major); the step for dQ tile (b, h, m) may add
+// only when the tile's counter equals this key tile's rank, then increments it.  Ranks:
+// descending (highest key tile first, rank = n_end - 1 - n) or ascending (n - n_begin).
+// Returns 1 if every step ran, 0 on a deadlock (no CTA can move); also checks that every
+// counter ends at its query tile's number of contributing key tiles.
+static int simulate(const MaskGeom& g, int BHk, int G, int P, bool claim_desc, bool add_desc,
+                    long* bad) {
+  const long Nb = g.Nb, Mb = g.Mb, T = Nb * BHk;
+  std::vector<int> cnt((size_t)BHk * G * Mb, 0);
+  struct Cta { long t = -1; long step = 0, total = 0, n = 0, r = 0, mb = 0, mc = 0; };
+  std::vector<Cta> c(P);
+  long next = 0, done = 0;
+  auto claim = [&](Cta& x) {
+    while (next < T) {
+      const long t = next++;
+      const long n0 = t / BHk;
+      x.r = t % BHk;
+      x.n = claim_desc ? Nb - 1 - n0 : n0;
+      long mb, me; m_range(g, x.n, &mb, &me);
+      x.mb = mb; x.mc = me - mb; x.total = x.mc * G; x.step = 0; x.t = t;
+      if (x.total > 0) return;
+      ++done;  // a ticket with no step finishes at once
+    }
+    x.t = -1;
+  };
+  for (auto& x : c) claim(x);
+  while (true) {
+    bool moved = false, busy = false;
+    for (auto& x : c) {
+      if (x.t < 0) continue;
+      busy = true;
+      const long gg = x.step / x.mc, m = x.mb + x.step % x.mc;
+      long nb, ne; n_range(g, m, &nb, &ne);
+      const int want = (int)(add_desc ? ne - 1 - x.n : x.n - nb);
+      int& k = cnt[((size_t)x.r * G + gg) * Mb + m];
+      if (k != want) continue;
+      ++k;
+      moved = true;
+      if (++x.step == x.total) { ++done; claim(x); }
+    }
+    if (!busy) break;
+    if (!moved) return 0;
+  }
+  for (long r = 0; r < BHk; ++r)
+    for (long gg = 0; gg < G; ++gg)
+      for (long m = 0; m < Mb; ++m) {
+        long nb, ne; n_range(g, m, &nb, &ne);
+        if (cnt[((size_t)r * G + gg) * Mb + m] != (int)(ne - nb)) ++*bad;
+      }
+  if (done != T) ++*bad;
+  return 1;
+}
+int main() {
+  long bad = 0, runs = 0, neg_deadlocks = 0;
+  const int lens[] = {128, 300, 512, 1000};
+  const int wins[][3] = {{1, -1, -1}, {0, -1, -1}, {0, 200, 0}, {0, 100, 300}, {1, 130, -1}};
+  const int ctas[] = {1, 2, 3, 7};
+  for (int Sq : lens) for (int Sk : lens) for (auto& w : wins) for (int BHk = 1; BHk <= 3; ++BHk)
+  for (int G = 1; G <= 2; ++G) for (int P : ctas) {
+    MaskGeom g = make_geom(Sq, Sk, w[0], w[1], w[2], 128, 128);
+    // the kernel's pairing: highest key tile claimed first, contributions added from the
+    // highest key tile down; and the plain longest-first / ascending pairing
+    if (!simulate(g, BHk, G, P, true, true, &bad)) { ++bad; if (bad < 5) printf("deadlock desc Sq=%d Sk=%d c=%d P=%d\n", Sq, Sk, w[0], P); }
+    if (!simulate(g, BHk, G, P, false, false, &bad)) { ++bad; if (bad < 5) printf("deadlock asc Sq=%d Sk=%d c=%d P=%d\n", Sq, Sk, w[0], P); }
+    // longest-first claims with descending adds must be able to deadlock
+    long ignore = 0;
+    if (!simulate(g, BHk, G, P, false, true, &ignore)) ++neg_deadlocks;
+    runs += 2;
+  }
+  printf("runs=%ld bad=%ld neg_deadlocks=%ld\n", runs, bad, neg_deadlocks);
+  return (bad != 0 || neg_deadlocks == 0) ? 1 : 0;
+}
+'''
+
+
+def test_ordered_mode_schedule_never_deadlocks(tmp_path):
+    """The ordered mode's pairing (highest key tile claimed first, dQ contributions added
+    from the highest key tile down) lets every step run on any number of CTAs, and every
+    counter ends at its contributor count; the mismatched pairing does deadlock, so the
+    model can tell the two apart."""
+    gxx = shutil.which("g++") or shutil.which("c++")
+    if gxx is None:
+        pytest.skip("no C++ compiler")
+    src = tmp_path / "order.cpp"
+    src.write_text(ORDER_HARNESS)
+    exe = tmp_path / "order"
+    inc = os.path.join(ROOT, "flashattention_backward_pass_gb300", "csrc")
+    subprocess.run([gxx, "-O2", "-std=c++17", "-I", inc, str(src), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "bad=0" in r.stdout
