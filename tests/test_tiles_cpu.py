@@ -159,9 +159,14 @@ using namespace fa;
 // descending (highest key tile first, rank = n_end - 1 - n) or ascending (n - n_begin).
 // Returns 1 if every step ran, 0 on a deadlock (no CTA can move); also checks that every
 // counter ends at its query tile's number of contributing key tiles.
-static int simulate(const MaskGeom& g, int BHk, int G, int P, bool claim_desc, bool add_desc,
-                    long* bad) {
-  const long Nb = g.Nb, Mb = g.Mb, T = Nb * BHk;
+static int simulate(const std::vector<MaskGeom>& gs, int G, int P, bool claim_desc,
+                    bool add_desc, long* bad) {
+  // one geometry per (sequence, kv-head) group: packed sequences differ in length, and the
+  // tickets run over the longest one's key tiles
+  const int BHk = (int)gs.size();
+  long Nb = 0, Mb = 0;
+  for (const auto& g : gs) { Nb = g.Nb > Nb ? g.Nb : Nb; Mb = g.Mb > Mb ? g.Mb : Mb; }
+  const long T = Nb * BHk;
   std::vector<int> cnt((size_t)BHk * G * Mb, 0);
   struct Cta { long t = -1; long step = 0, total = 0, n = 0, r = 0, mb = 0, mc = 0; };
   std::vector<Cta> c(P);
@@ -172,7 +177,7 @@ static int simulate(const MaskGeom& g, int BHk, int G, int P, bool claim_desc, b
       const long n0 = t / BHk;
       x.r = t % BHk;
       x.n = claim_desc ? Nb - 1 - n0 : n0;
-      long mb, me; m_range(g, x.n, &mb, &me);
+      long mb, me; m_range(gs[x.r], x.n, &mb, &me);
       x.mb = mb; x.mc = me - mb; x.total = x.mc * G; x.step = 0; x.t = t;
       if (x.total > 0) return;
       ++done;  // a ticket with no step finishes at once
@@ -186,7 +191,7 @@ static int simulate(const MaskGeom& g, int BHk, int G, int P, bool claim_desc, b
       if (x.t < 0) continue;
       busy = true;
       const long gg = x.step / x.mc, m = x.mb + x.step % x.mc;
-      long nb, ne; n_range(g, m, &nb, &ne);
+      long nb, ne; n_range(gs[x.r], m, &nb, &ne);
       const int want = (int)(add_desc ? ne - 1 - x.n : x.n - nb);
       int& k = cnt[((size_t)x.r * G + gg) * Mb + m];
       if (k != want) continue;
@@ -199,8 +204,8 @@ static int simulate(const MaskGeom& g, int BHk, int G, int P, bool claim_desc, b
   }
   for (long r = 0; r < BHk; ++r)
     for (long gg = 0; gg < G; ++gg)
-      for (long m = 0; m < Mb; ++m) {
-        long nb, ne; n_range(g, m, &nb, &ne);
+      for (long m = 0; m < gs[r].Mb; ++m) {
+        long nb, ne; n_range(gs[r], m, &nb, &ne);
         if (cnt[((size_t)r * G + gg) * Mb + m] != (int)(ne - nb)) ++*bad;
       }
   if (done != T) ++*bad;
@@ -213,15 +218,24 @@ int main() {
   const int ctas[] = {1, 2, 3, 7};
   for (int Sq : lens) for (int Sk : lens) for (auto& w : wins) for (int BHk = 1; BHk <= 3; ++BHk)
   for (int G = 1; G <= 2; ++G) for (int P : ctas) {
-    MaskGeom g = make_geom(Sq, Sk, w[0], w[1], w[2], 128, 128);
-    // the kernel's pairing: highest key tile claimed first, contributions added from the
-    // highest key tile down; and the plain longest-first / ascending pairing
-    if (!simulate(g, BHk, G, P, true, true, &bad)) { ++bad; if (bad < 5) printf("deadlock desc Sq=%d Sk=%d c=%d P=%d\n", Sq, Sk, w[0], P); }
-    if (!simulate(g, BHk, G, P, false, false, &bad)) { ++bad; if (bad < 5) printf("deadlock asc Sq=%d Sk=%d c=%d P=%d\n", Sq, Sk, w[0], P); }
-    // longest-first claims with descending adds must be able to deadlock
-    long ignore = 0;
-    if (!simulate(g, BHk, G, P, false, true, &ignore)) ++neg_deadlocks;
-    runs += 2;
+    // batched: every group has the same lengths; packed: group r's lengths are rotated
+    // through the list (0 included: a sequence with no query or no key)
+    for (int packed = 0; packed < 2; ++packed) {
+      std::vector<MaskGeom> gs;
+      for (int r = 0; r < BHk; ++r) {
+        const int sq = packed ? (r == 2 ? 0 : lens[(r + Sq / 100) % 4]) : Sq;
+        const int sk = packed ? lens[(r + Sk / 100 + 1) % 4] : Sk;
+        gs.push_back(make_geom(sq, sk, w[0], w[1], w[2], 128, 128));
+      }
+      // the kernel's pairing: highest key tile claimed first, contributions added from
+      // the highest key tile down; and the plain longest-first / ascending pairing
+      if (!simulate(gs, G, P, true, true, &bad)) { ++bad; if (bad < 5) printf("deadlock desc Sq=%d Sk=%d c=%d P=%d packed=%d\n", Sq, Sk, w[0], P, packed); }
+      if (!simulate(gs, G, P, false, false, &bad)) { ++bad; if (bad < 5) printf("deadlock asc Sq=%d Sk=%d c=%d P=%d packed=%d\n", Sq, Sk, w[0], P, packed); }
+      // longest-first claims with descending adds must be able to deadlock
+      long ignore = 0;
+      if (!simulate(gs, G, P, false, true, &ignore)) ++neg_deadlocks;
+      runs += 2;
+    }
   }
   printf("runs=%ld bad=%ld neg_deadlocks=%ld\n", runs, bad, neg_deadlocks);
   return (bad != 0 || neg_deadlocks == 0) ? 1 : 0;
