@@ -68,7 +68,7 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                            ctypes.c_int, ctypes.c_float, ctypes.c_int, vp, sz, vp]
     lib.fa_bwd_status.restype = ctypes.c_int
-    lib.fa_bwd_status.argtypes = [vp, sz, vp, ctypes.POINTER(ctypes.c_int)]
+    lib.fa_bwd_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     lib.fa_debug_set_wait_limit.restype = ctypes.c_int
     lib.fa_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
     lib.fa_debug_poison_ordering.restype = ctypes.c_int
@@ -81,19 +81,12 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd_set_algorithm.argtypes = [ctypes.c_int]
     lib.fa_bwd_get_algorithm.restype = ctypes.c_int
     ip = ctypes.c_void_p  # device int32 offsets
-    if not hasattr(lib, "fa_fwd_varlen") or lib.fa_abi_version() < 2:
-        # a library built before the packed entry points took used lengths
-        _lib = lib
-        return lib
     lib.fa_fwd_varlen.restype = ctypes.c_int
     lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, ip, ip, ip, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_float, vp, sz, vp]
     lib.fa_bwd_varlen_workspace_size.restype = sz
     lib.fa_bwd_varlen_workspace_size.argtypes = [ctypes.c_int] * 5
-    if not hasattr(lib, "fa_fwd_blocksparse"):  # a library built before block sparsity
-        _lib = lib
-        return lib
     lib.fa_fwd_blocksparse.restype = ctypes.c_int
     lib.fa_fwd_blocksparse.argtypes = [P, P, P, P, P, vp, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_float, vp, sz, vp]
@@ -106,6 +99,13 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, ip, ip, ip, ip, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, vp, sz, vp]
+    lib.fa_bwd_noalloc.restype = ctypes.c_int
+    lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, vp]
+    lib.fa_bwd_noalloc_status.restype = ctypes.c_int
+    lib.fa_bwd_noalloc_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    if lib.fa_abi_version() != 3:
+        raise RuntimeError(f"{path} reports ABI version {lib.fa_abi_version()}, expected 3: rebuild it")
     _lib = lib
     return lib
 
@@ -189,8 +189,8 @@ def fa_bwd_status(workspace, stream=None) -> int:
     """Device status word of the last fa_bwd on `workspace` (0 = every wait completed)."""
     lib = load()
     out = ctypes.c_int(0)
-    st = lib.fa_bwd_status(ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                           _stream_ptr(stream), ctypes.byref(out))
+    st = lib.fa_bwd_status(ctypes.c_void_p(workspace.data_ptr()), _stream_ptr(stream),
+                           ctypes.byref(out))
     _check(st, "fa_bwd_status")
     return int(out.value)
 
@@ -235,16 +235,20 @@ def fa_bwd_noalloc(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal=Fa
     """C call `fa_bwd_noalloc`: the backward with the library's own fixed scratch (for
     callers that cannot allocate device memory); raises FaError on a non-zero status."""
     lib = load()
-    fn = lib.fa_bwd_noalloc
-    P = ctypes.POINTER(FaTensor)
-    fn.restype = ctypes.c_int
-    fn.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int,
-                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
     tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
-    st = fn(*[ctypes.byref(x) for x in tv], float(softmax_scale), int(bool(causal)),
+    st = lib.fa_bwd_noalloc(*[ctypes.byref(x) for x in tv], float(softmax_scale), int(bool(causal)),
             int(window_left), int(window_right), float(softcap), int(bool(deterministic)),
             _stream_ptr(stream))
     _check(st, "fa_bwd_noalloc")
+
+
+def fa_bwd_noalloc_status(stream=None) -> int:
+    """C call `fa_bwd_noalloc_status`: device status word of the last fa_bwd_noalloc on the
+    current device (0 = every bounded wait completed), read and cleared."""
+    out = ctypes.c_int(0)
+    _check(load().fa_bwd_noalloc_status(_stream_ptr(stream), ctypes.byref(out)),
+           "fa_bwd_noalloc_status")
+    return int(out.value)
 
 
 # ------------------------------------------------------------------ packed sequences

@@ -5,15 +5,29 @@
 The forward saves q, k, v, out and the natural-log LSE; the backward calls fa_bwd /
 fa_bwd_varlen with them (dQ, dK, dV written by the library's kernels).  Every step runs
 in libfa_gb300.so: these classes only allocate outputs and pass tensors through.
+
+A bounded device-side wait that runs out (FA_ERR_DEVICE_TIMEOUT) is recorded in the
+backward's workspace, not returned by the launch.  With the environment variable
+FA_CHECK_DEVICE_STATUS=1 the backward reads that status word after each call (a stream
+synchronisation) and raises FaError when it is non-zero; by default it does not check,
+so a timed-out call would leave incomplete gradients without an error.
 """
 
 from __future__ import annotations
 
 import math
+import os
 
 import torch
 
 from . import _abi
+
+
+def _check_status(workspace):
+    if os.environ.get("FA_CHECK_DEVICE_STATUS", "0") not in ("", "0"):
+        st = _abi.fa_bwd_status(workspace)
+        if st != 0:
+            raise _abi.FaError(-11, f"backward device status {st}")
 
 
 def _scale(q, softmax_scale):
@@ -39,7 +53,8 @@ class FlashAttnFunc(torch.autograd.Function):
         scale, causal, wl, wr, softcap, det = ctx.args
         dout = dout if dout.stride(-1) == 1 else dout.contiguous()
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        _abi.fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, scale, causal, wl, wr, softcap, det)
+        ws = _abi.fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, scale, causal, wl, wr, softcap, det)
+        _check_status(ws)
         return dq, dk, dv, None, None, None, None, None, None
 
 
@@ -77,8 +92,9 @@ class FlashAttnVarlenFunc(torch.autograd.Function):
         uq, uk = ctx.used
         dq = torch.zeros_like(q) if uq is not None else torch.empty_like(q)
         dk, dv = torch.zeros_like(k), torch.zeros_like(v)
-        _abi.fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, mq, mk, scale,
-                           causal, wl, wr, softcap, det, seqused_q=uq, seqused_k=uk)
+        ws = _abi.fa_bwd_varlen(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, mq, mk, scale,
+                                causal, wl, wr, softcap, det, seqused_q=uq, seqused_k=uk)
+        _check_status(ws)
         return (dq, dk, dv) + (None,) * 12
 
 

@@ -31,12 +31,19 @@ int g_poison_first_counter = 0;
 int g_bwd_algorithm = FA_BWD_ALGO_FUSED;
 
 // Optional timing of the three backward kernels: events recorded on the caller's stream
-// before the preprocess, before and after the main kernel and after the convert.
+// before the preprocess, before and after the main kernel and after the convert.  The
+// events belong to the device that was current when profiling was enabled; a call on
+// another device records nothing (and fa_profile_read then reports the last call made on
+// the profiled device).
 bool g_profile = false;
+int g_profile_dev = -1;
 cudaEvent_t g_ev[4] = {nullptr, nullptr, nullptr, nullptr};
 
 void prof_record(int i, cudaStream_t s) {
-  if (g_profile) cudaEventRecord(g_ev[i], s);
+  if (!g_profile) return;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != g_profile_dev) return;
+  cudaEventRecord(g_ev[i], s);
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -681,9 +688,8 @@ int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
                     workspace_bytes, stream, &vl, nullptr);
 }
 
-int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* device_status) {
+int fa_bwd_status(void* workspace, void* stream, int* device_status) {
   if (!workspace || !device_status) return FA_ERR_NULL;
-  if (workspace_bytes < WS_HEADER_BYTES) return FA_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   int v = 0;
   if (cudaMemcpyAsync(&v, (int*)workspace + WS_STATUS, sizeof(int), cudaMemcpyDeviceToHost, s) !=
@@ -735,9 +741,23 @@ int fa_trace_timeline(void* host, size_t bytes, int clear) {
 #endif
 
 int fa_profile_enable(int enable) {
-  if (enable && !g_ev[0]) {
-    for (int i = 0; i < 4; ++i)
-      if (cudaEventCreate(&g_ev[i]) != cudaSuccess) return FA_ERR_CUDA;
+  if (enable) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (g_ev[0] && dev != g_profile_dev) {
+      // events of another device: make new ones on this device
+      int cur = dev;
+      if (cudaSetDevice(g_profile_dev) == cudaSuccess) {
+        for (int i = 0; i < 4; ++i) cudaEventDestroy(g_ev[i]);
+      }
+      cudaSetDevice(cur);
+      for (int i = 0; i < 4; ++i) g_ev[i] = nullptr;
+    }
+    if (!g_ev[0]) {
+      for (int i = 0; i < 4; ++i)
+        if (cudaEventCreate(&g_ev[i]) != cudaSuccess) return FA_ERR_CUDA;
+      g_profile_dev = dev;
+    }
   }
   g_profile = enable != 0;
   return FA_OK;

@@ -12,7 +12,8 @@
 // The scratch is one file-scope __device__ array of FA_NOALLOC_SCRATCH_BYTES (32 MiB).
 // Every GPU that loads the library holds it until the process exits.  Problems whose
 // workspace (fa_bwd_workspace_size) is larger are rejected with FA_ERR_WORKSPACE before
-// anything is launched.
+// anything is launched.  A bounded device-side wait that runs out records its code in the
+// array's status word; fa_bwd_noalloc_status reads and clears it.
 //
 // Host code may not use the array's name as a device address (on the host it is only a
 // stand-in symbol).  The first call on each device therefore looks the address up with
@@ -61,16 +62,22 @@ extern "C" int fa_bwd_noalloc(const fa_tensor* dout, const fa_tensor* q, const f
                               fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, float softmax_scale,
                               int causal, int window_left, int window_right, float softcap,
                               int deterministic, void* stream) {
-  if (!q || !k) return FA_ERR_NULL;
-  if (q->ndim != 4 || k->ndim != 4) return FA_ERR_SHAPE;
-  const size_t need = fa_bwd_workspace_size((int)q->shape[0], (int)q->shape[2], (int)k->shape[2],
-                                            (int)q->shape[1], (int)k->shape[1], (int)q->shape[3],
-                                            deterministic);
-  if (need > (size_t)FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  // fa_bwd validates every argument and returns FA_ERR_WORKSPACE, before any launch, for a
+  // problem whose workspace does not fit the FA_NOALLOC_SCRATCH_BYTES it is given.
   void* scratch = nullptr;
   const int st = scratch_for_current_device(&scratch);
   if (st != FA_OK) return st;
   return fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal, window_left,
                 window_right, softcap, deterministic, scratch, (size_t)FA_NOALLOC_SCRATCH_BYTES,
                 stream);
+}
+
+// The status word of the last fa_bwd_noalloc on the current device lives in the scratch
+// array's header, where fa_bwd_status finds it once it has the array's device address.
+extern "C" int fa_bwd_noalloc_status(void* stream, int* device_status) {
+  if (!device_status) return FA_ERR_NULL;
+  void* scratch = nullptr;
+  const int st = scratch_for_current_device(&scratch);
+  if (st != FA_OK) return st;
+  return fa_bwd_status(scratch, stream, device_status);
 }

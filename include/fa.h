@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 2
+#define FA_ABI_VERSION 3
 
 /* Element types.  Q, K, V, O, dO, dQ, dK and dV of one call share one 16-bit type:
  * bf16, or f16 (the call-trace page's dispatch covers both, `run_mha_bwd_constexpr`);
@@ -83,7 +83,8 @@ typedef struct {
 /* Library/ABI version (FA_ABI_VERSION). */
 int fa_abi_version(void);
 
-/* Human-readable name of a status code (static storage; never NULL). */
+/* Human-readable name of a status code (static storage; never NULL).  The library's own
+ * helper: the pages raise Python / C++ exceptions instead of returning codes. */
 const char* fa_status_string(int status);
 
 /*
@@ -146,9 +147,12 @@ int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
                   float softcap, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Workspace the backward needs, in bytes, for the given problem.  It holds the fp32
- * dQ accumulator, D = rowsum(dO*O), LSE in log2 units, the deterministic-mode
- * ordering counters and a status word.  Returns 0 for invalid sizes.
+ * Workspace the backward needs, in bytes, for the given problem.  It holds what the
+ * call-trace page's `mha_bwd` allocates for itself before `run_mha_bwd` (the fp32
+ * `dq_accum` and `softmax_d` = rowsum(dO*O)), plus the LSE in log2 units that the
+ * `flash_bwd_sm90.py` page's kernel consumes, the deterministic-mode ordering counters
+ * (its `mdQ_semaphore`) and a status word.  Here the caller allocates it and passes it to
+ * fa_bwd.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int deterministic);
 
@@ -239,14 +243,18 @@ int fa_bwd_varlen(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
 
 /*
  * fa_bwd_status — waits for `stream`, then reads the device status word that the last
- * fa_bwd on this workspace left (0 when every bounded wait completed) into
- * *device_status, and clears it.  Returns FA_OK, or FA_ERR_CUDA if the copy failed.
+ * fa_bwd (or fa_fwd given this workspace) left in `workspace` (0 when every bounded wait
+ * completed, else FA_ERR_DEVICE_TIMEOUT's device-side code) into *device_status, and
+ * clears it.  The pages have no counterpart: it is this library's way of reporting a
+ * device-side wait that ran out, which the pages' kernels do not bound.  `workspace` must
+ * be a buffer that a backward call accepted (the status word sits in its first 256 bytes).
+ * Returns FA_OK, FA_ERR_NULL for a NULL pointer, or FA_ERR_CUDA if a copy failed.
  */
-int fa_bwd_status(void* workspace, size_t workspace_bytes, void* stream, int* device_status);
+int fa_bwd_status(void* workspace, void* stream, int* device_status);
 
 /*
  * fa_bwd_noalloc — the same backward as fa_bwd (same arguments, layouts, results and
- * errors) for callers that cannot allocate device memory: code running where a
+ * argument errors; a device-side timeout is read with fa_bwd_noalloc_status) for callers that cannot allocate device memory: code running where a
  * cudaMalloc is not allowed (a serving or real-time loop that must not synchronize the
  * device, a region recorded into a CUDA graph) or an embedding with a fixed memory
  * budget that has no allocator to provide fa_bwd's workspace.  The source pages have no
@@ -267,6 +275,17 @@ int fa_bwd_noalloc(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k
                    fa_tensor* dq, fa_tensor* dk, fa_tensor* dv,
                    float softmax_scale, int causal, int window_left, int window_right,
                    float softcap, int deterministic, void* stream);
+
+/*
+ * fa_bwd_noalloc_status — fa_bwd_status for fa_bwd_noalloc: waits for `stream`, then reads
+ * the status word in the current device's library-owned scratch array into
+ * *device_status (0 when every bounded wait of the last fa_bwd_noalloc on this device
+ * completed, non-zero when one ran out and the outputs are incomplete) and clears it.
+ * Allocates nothing.  Call it before the next fa_bwd_noalloc on the device, whose first
+ * kernel clears the word.  No counterpart on the pages.  Returns FA_OK, FA_ERR_NULL, or
+ * FA_ERR_CUDA if the address lookup or a copy failed.
+ */
+int fa_bwd_noalloc_status(void* stream, int* device_status);
 
 /*
  * Backward algorithm for later fa_bwd calls in this process (not thread-safe).

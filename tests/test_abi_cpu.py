@@ -27,7 +27,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.fa_abi_version() == 2
+    assert lib.fa_abi_version() == 3
     for code in range(0, -12, -1):
         s = lib.fa_status_string(code)
         assert s and s.startswith(b"FA_")
@@ -238,3 +238,42 @@ def test_binding_checks_used_lengths():
         _abi._used(torch.zeros(3, dtype=torch.int64), 3)       # wrong type
     with pytest.raises(ValueError):
         _abi._used(torch.zeros((3, 1), dtype=torch.int32), 3)  # not 1-D
+
+
+def _prototype(name):
+    """The parameter list of `name` in include/fa.h, whitespace-normalised."""
+    import re
+    from flashattention_backward_pass_gb300._abi import HEADER_PATH
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER_PATH).read(), flags=re.S)
+    m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+    assert m, name
+    return " ".join(m.group(1).split())
+
+
+def test_boundary_signatures_match_the_scope_table():
+    """The calls the hot path's boundary lists, with their argument lists as given there:
+    fa_fwd / fa_bwd take (tensors..., scalars..., workspace, workspace_bytes, stream),
+    fa_bwd_workspace_size the problem sizes, fa_bwd_status (workspace, stream, status)."""
+    assert _prototype("fa_bwd_status") == "void* workspace, void* stream, int* device_status"
+    assert _prototype("fa_bwd_workspace_size") == (
+        "int B, int H, int Hk, int Sq, int Sk, int D, int deterministic")
+    assert _prototype("fa_fwd") == (
+        "const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa_tensor* out, "
+        "fa_tensor* lse, float softmax_scale, int causal, int window_left, int window_right, "
+        "float softcap, void* workspace, size_t workspace_bytes, void* stream")
+    assert _prototype("fa_bwd") == (
+        "const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, "
+        "const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, "
+        "float softmax_scale, int causal, int window_left, int window_right, float softcap, "
+        "int deterministic, void* workspace, size_t workspace_bytes, void* stream")
+    assert _prototype("fa_status_string") == "int status"
+
+
+def test_status_readers_reject_null_pointers(lib):
+    # argument checks come before any CUDA call (there is no GPU here)
+    out = ctypes.c_int(7)
+    assert lib.fa_bwd_status(None, None, ctypes.byref(out)) == -1
+    assert lib.fa_bwd_status(ctypes.c_void_p(4096), None, None) == -1
+    assert lib.fa_bwd_noalloc_status(None, None) == -1
+    assert out.value == 7
+

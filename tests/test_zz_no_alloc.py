@@ -45,6 +45,58 @@ def test_noalloc_matches_fa_bwd_twice(fa, w):
         torch.cuda.synchronize()
         for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
             check_close(f"{w.name} noalloc {name}", to64(got), to64(want))
+        assert _abi.fa_bwd_noalloc_status() == 0
+
+
+@pytest.mark.parametrize("w", CASES[1:], ids=[w.name for w in CASES[1:]])
+def test_noalloc_deterministic_is_bit_equal_to_fa_bwd(fa, w):
+    """The ordered dQ mode on the shared scratch: its counters and accumulator must be
+    cleared by every call, so three calls in a row give fa_bwd's deterministic result
+    bit for bit."""
+    from flashattention_backward_pass_gb300 import _abi
+    q, k, v, do = make_inputs(w, "cuda")
+    out, lse = fa.attention_forward(q, k, v, w.scale, w.causal, w.window_left, w.window_right,
+                                    w.softcap)
+    ref = fa.attention_backward(do, q, k, v, out, lse, w.scale, w.causal, w.window_left,
+                                w.window_right, w.softcap, deterministic=True)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        _abi.fa_bwd_noalloc(do, q, k, v, out, lse, dq, dk, dv, w.scale, w.causal,
+                            w.window_left, w.window_right, w.softcap, deterministic=True)
+        torch.cuda.synchronize()
+        assert _abi.fa_bwd_noalloc_status() == 0
+        for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), name
+
+
+def test_noalloc_timeout_is_readable(fa):
+    """A bounded device wait that runs out inside fa_bwd_noalloc (an ordering counter no
+    contributor matches) is reported by fa_bwd_noalloc_status and cleared by it; the next
+    call on the same scratch is clean and correct."""
+    from flashattention_backward_pass_gb300 import _abi
+    w = custom("noalloc_poison", 1, 384, 384, 2, 2, 64, causal=True, seed=43)
+    q, k, v, do = make_inputs(w, "cuda")
+    out, lse = fa.attention_forward(q, k, v, w.scale, True)
+    ref = fa.attention_backward(do, q, k, v, out, lse, w.scale, True, deterministic=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _abi.set_algorithm(_abi.ALGO_FUSED)
+    _abi.set_wait_limit(20_000_000)        # ~10 ms per wait
+    _abi.poison_ordering(True)
+    try:
+        _abi.fa_bwd_noalloc(do, q, k, v, out, lse, dq, dk, dv, w.scale, True, deterministic=True)
+        torch.cuda.synchronize()
+        status = _abi.fa_bwd_noalloc_status()
+    finally:
+        _abi.poison_ordering(False)
+        _abi.set_wait_limit(2_000_000_000)
+    assert status != 0, "the poisoned ordered wait should have reported a timeout"
+    assert _abi.fa_bwd_noalloc_status() == 0   # read and cleared
+    _abi.fa_bwd_noalloc(do, q, k, v, out, lse, dq, dk, dv, w.scale, True, deterministic=True)
+    torch.cuda.synchronize()
+    assert _abi.fa_bwd_noalloc_status() == 0
+    for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), name
 
 
 def test_noalloc_rejects_oversized_problem(fa):
