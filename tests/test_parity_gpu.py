@@ -136,24 +136,27 @@ def test_mha_causal_full(fa, det):
             compare_slice(w, t, gpu, b, hk)
 
 
-def test_gqa_causal_sampled(fa):
+@pytest.mark.parametrize("det", [False, True])
+def test_gqa_causal_sampled(fa, det):
     w = WORKLOADS["gqa_causal"]
     t = make_inputs(w, "cuda")
-    gpu = run_gpu(fa, w, *t)
+    gpu = run_gpu(fa, w, *t, deterministic=det)
     for b, hk in ((0, 0), (3, 7)):
         compare_slice(w, t, gpu, b, hk)
 
 
-def test_swa_softcap_sampled(fa):
+@pytest.mark.parametrize("det", [False, True])
+def test_swa_softcap_sampled(fa, det):
     w = WORKLOADS["swa_softcap"]
     t = make_inputs(w, "cuda")
-    gpu = run_gpu(fa, w, *t)
+    gpu = run_gpu(fa, w, *t, deterministic=det)
     compare_slice(w, t, gpu, 0, 0)   # batch 0, q-heads 0..7 (kv-head 0's group)
 
 
-def test_ragged_d72_sampled(fa):
+@pytest.mark.parametrize("det", [False, True])
+def test_ragged_d72_sampled(fa, det):
     w = WORKLOADS["ragged_d72"]
     t = make_inputs(w, "cuda")
-    gpu = run_gpu(fa, w, *t)
+    gpu = run_gpu(fa, w, *t, deterministic=det)
     for b, h in ((0, 0), (7, 11), (4, 5)):
         compare_slice(w, t, gpu, b, h)
