@@ -3,7 +3,9 @@
 
 One step = one fa_bwd call over one batch of the workload (default: the GQA causal
 workload B=4, Sq=Sk=2048, H=32, Hk=8, D=128), inputs resident in HBM, L2 flushed
-(256 MiB write) between steps outside the timed events.  Prints one JSON line.
+between steps outside the timed events (a 256 MiB write, then a 256 MiB read that
+writes the flush's dirty lines back, so each step starts on a cold, clean L2).  Prints
+one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
   python bench.py --varlen [--workload NAME]   (packed sequences of mixed lengths; own line)
@@ -34,6 +36,69 @@ sys.path.insert(0, ROOT)
 METRIC = "attention-backward TFLOP/s (bf16) and % of GB300 dense BF16 peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = ("flushed between steps outside the timed events: 256 MiB write, then a 256 MiB "
+           "read that writes the dirty lines back (cold, clean L2 at each step)")
+
+
+class L2Flush:
+    """Writes a buffer larger than L2 (evicting every line the previous step left), then
+    reads a second one, so that the flush's own dirty lines are written back before the
+    timed region instead of during it."""
+
+    def __init__(self, device):
+        import torch
+        self.wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.rbuf = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.wbuf.zero_()
+        self.rbuf.sum()
+
+
+def link_bandwidth(device, nbytes=256 << 20, reps=5):
+    """Pinned host <-> device copy bandwidth (GB/s) measured with CUDA events: host to
+    device alone, device to host alone, and both at once on two streams (total bytes of
+    both directions over the time of both)."""
+    import torch
+    h_src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_dst = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s1, s2 = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s1)
+            s2.wait_event(e0)
+            fn()
+            s1.wait_stream(s2)
+            e1.record(s1)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_src, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_dst.copy_(d_b, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in, t_out, t_both = timed(h2d), timed(d2h), timed(both)
+    return {"h2d_gbs": round(nbytes / (t_in * 1e-3) / 1e9, 1),
+            "d2h_gbs": round(nbytes / (t_out * 1e-3) / 1e9, 1),
+            "both_gbs": round(2 * nbytes / (t_both * 1e-3) / 1e9, 1),
+            "bytes_each_way": nbytes}
 
 
 def _dist():
@@ -175,7 +240,7 @@ def run_ours(args, ws_, rank, local):
                                     w.softcap)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     wsp = fa.alloc_bwd_workspace(q, k, args.deterministic)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     # The timed pass runs without the library's per-kernel events: an event between the
     # main and convert kernels would keep the convert kernel from starting on the SMs
     # the main kernel leaves.  The per-kernel split comes from a separate pass below.
@@ -187,7 +252,7 @@ def run_ours(args, ws_, rank, local):
                   w.window_right, w.softcap, args.deterministic, wsp)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert fa.fa_bwd_status(wsp) == 0
@@ -201,7 +266,7 @@ def run_ours(args, ws_, rank, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -217,7 +282,7 @@ def run_ours(args, ws_, rank, local):
     _abi.profile_enable(True)
     main_ms, pre_ms, conv_ms = [], [], []
     for i in range(min(args.steps, 20)):
-        flush.zero_()
+        flush()
         step()
         a, b_, c = _abi.profile_read()
         pre_ms.append(a)
@@ -280,15 +345,27 @@ def run_ours(args, ws_, rank, local):
         e1.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws_, dev) / n_e2e
+        # the host link's ceiling for this schedule: with upload, compute and download
+        # overlapped, a step takes at least the longest of the three (each direction at
+        # its own bandwidth, and both directions together at the concurrent bandwidth)
+        link = link_bandwidth(dev)
+        floor_ms = max(h2d / (link["h2d_gbs"] * 1e9) * 1e3, d2h / (link["d2h_gbs"] * 1e9) * 1e3,
+                       (h2d + d2h) / (link["both_gbs"] * 1e9) * 1e3, total_ms / args.steps)
         e2e = {"value": round(job_tflops(w.nominal_flops, 1, ws_, e2e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 4),
-               "schedule": "upload, fa_bwd and download on three streams, double-buffered"}
+               "schedule": "upload, fa_bwd and download on three streams, double-buffered",
+               "link": link,
+               "ceiling": {"ms_per_step": round(floor_ms, 4),
+                           "value": round(job_tflops(w.nominal_flops, 1, ws_, floor_ms), 3),
+                           "frac": round(floor_ms / e2e_ms, 4),
+                           "note": "max(upload at h2d_gbs, download at d2h_gbs, both at "
+                                   "both_gbs, the device-timed step)"}}
 
     # the forward that produces O and LSE (not part of the step): timed alone, L2 flushed
     fwd_ms = []
     for i in range(3 + min(args.steps, 20)):
-        flush.zero_()
+        flush()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
@@ -310,7 +387,7 @@ def run_ours(args, ws_, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 inputs of the workload's shape)",
         "config": dict(w.describe(), deterministic=bool(args.deterministic),
-                       l2="flushed between steps (256 MiB write, outside the timed events)",
+                       l2=L2_NOTE,
                        parallelism=f"replicas x{ws_}" if ws_ > 1 else "single GPU",
                        flop_convention="10*B*H*Sq*Sk*D, halved for causal"),
         "pct_of_bf16_peak": round(100 * value / ws_ / peak, 2),
@@ -431,7 +508,7 @@ def run_varlen(args, ws_, local):
     dq, dk, dv = torch.empty_like(q), torch.zeros_like(k), torch.zeros_like(v)
     wsp = torch.empty(fa.bwd_varlen_workspace_size(len(lq), w.H, q.shape[0], w.D, args.deterministic),
                       dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     seqs = [Workload("seq", 1, a, b, w.H, w.Hk, w.D, w.causal, w.window_left, w.window_right,
                      w.softcap) for a, b in zip(lq, lk)]
@@ -443,13 +520,13 @@ def run_varlen(args, ws_, local):
                          deterministic=args.deterministic, workspace=wsp, **kw)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert fa.fa_bwd_status(wsp) == 0
     ms = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -461,13 +538,13 @@ def run_varlen(args, ws_, local):
     _abi.profile_enable(True)
     split = []
     for _ in range(min(args.steps, 20)):
-        flush.zero_()
+        flush()
         step()
         split.append(_abi.profile_read())
     _abi.profile_enable(False)
     fwd = []
     for _ in range(min(args.steps, 20)):
-        flush.zero_()
+        flush()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -484,7 +561,7 @@ def run_varlen(args, ws_, local):
             "data": "synthetic (seeded N(0,1) bf16, packed sequences)",
             "config": dict(w.describe(), workload=w.name + "+varlen", lengths_q=lq, lengths_k=lk,
                            deterministic=bool(args.deterministic),
-                           l2="flushed between steps (256 MiB write, outside the timed events)",
+                           l2=L2_NOTE,
                            flop_convention="per sequence 10*H*Sq*Sk*D, halved for causal"),
             "main_kernel": {"ms": round(main_ms, 4),
                             "achieved_tflops": round(algorithmic / (main_ms * 1e-3) / 1e12, 2),
@@ -538,13 +615,13 @@ def run_blocksparse(args, local):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     wsp = torch.empty(fa.bwd_blocksparse_workspace_size(w.B, w.H, w.Hk, w.Sq, w.Sk, w.D),
                       dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def timed(fn):
         ms = []
         for i in range(args.warmup + args.steps):
-            flush.zero_()
+            flush()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -567,7 +644,7 @@ def run_blocksparse(args, local):
             "config": dict(w.describe(), workload=w.name + "+blocksparse",
                            block_density=args.block_density,
                            kept_tile_pairs=int(bm_cpu.sum()),
-                           l2="flushed between steps (256 MiB write, outside the timed events)",
+                           l2=L2_NOTE,
                            flop_convention="10*D per visible (query, key) pair after both masks"),
             "pct_of_bf16_peak": round(100 * flops / (t * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 2),
             "forward_ms": round(tf, 4),
