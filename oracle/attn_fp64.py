@@ -34,6 +34,8 @@ Readings where the pages are silent (listed with reasons in the design notes):
   window_right >= 0) and j >= i + (Sk - Sq) - window_left (when window_left >= 0);
   causal forces window_right = 0.  A negative window bound is unbounded.
 * a query row with no visible key has O = 0, LSE = +inf, P = 0 and dQ = 0.
+* head dims: q and k share a head dim D; v may have its own head dim Dv (the sm90 page's
+  `__init__` takes `head_dim` and `head_dim_v`), which o, dO and dV then have.
 * block sparsity (the sm90 page's `blocksparse_tensors` give, per key block, the query
   blocks to visit): an optional (B, H, ceil(Sq/bs), ceil(Sk/bs)) boolean block mask; a
   (query block, key block) pair with a 0 entry is masked out entirely, on top of the
@@ -140,32 +142,34 @@ def _check_block_mask(block_mask, B, H, Sq, Sk, block_size):
 
 
 def _check_shapes(q, k, v):
+    """(B, Sq, Sk, H, Hk, D, Dv) of q (B,Sq,H,D), k (B,Sk,Hk,D) and v (B,Sk,Hk,Dv)."""
     if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
         raise ValueError("q, k, v must be (B, S, H, D)")
     B, Sq, H, D = q.shape
     Bk, Sk, Hk, Dk = k.shape
-    if v.shape != k.shape or Bk != B or Dk != D:
-        raise ValueError("k and v must be (B, Sk, Hk, D) matching q")
+    if v.shape[:3] != k.shape[:3] or Bk != B or Dk != D:
+        raise ValueError("k must be (B, Sk, Hk, D) matching q and v (B, Sk, Hk, Dv)")
     if Hk == 0 or H % Hk != 0:
         raise ValueError("H must be a multiple of Hk")
-    return B, Sq, Sk, H, Hk, D
+    return B, Sq, Sk, H, Hk, D, v.shape[3]
 
 
 def attention_forward(q, k, v, scale, causal=False, window_left=-1, window_right=-1,
                       softcap=0.0, block_mask=None, block_size=128):
-    """O (B,Sq,H,D) and natural-log LSE (B,H,Sq), both float64.
+    """O (B,Sq,H,Dv) and natural-log LSE (B,H,Sq), both float64.
 
-    q (B,Sq,H,D), k/v (B,Sk,Hk,D).  q-head h reads kv-head h // (H/Hk) (GQA/MQA page,
-    `bidh_kv = bidh / qhead_per_khead`; Triton page `off_h_k = off_h // (HQ // HK)`).
+    q (B,Sq,H,D), k (B,Sk,Hk,D), v (B,Sk,Hk,Dv).  q-head h reads kv-head h // (H/Hk)
+    (GQA/MQA page, `bidh_kv = bidh / qhead_per_khead`; Triton page
+    `off_h_k = off_h // (HQ // HK)`).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    B, Sq, Sk, H, Hk, D = _check_shapes(q, k, v)
+    B, Sq, Sk, H, Hk, D, Dv = _check_shapes(q, k, v)
     G = H // Hk
     vis = visible_mask(Sq, Sk, causal, window_left, window_right)
     bm = _check_block_mask(block_mask, B, H, Sq, Sk, block_size)
-    o = np.zeros((B, Sq, H, D))
+    o = np.zeros((B, Sq, H, Dv))
     lse = np.zeros((B, H, Sq))
     for b in range(B):
         for h in range(H):
@@ -179,25 +183,25 @@ def attention_forward(q, k, v, scale, causal=False, window_left=-1, window_right
 
 def attention_backward(do, q, k, v, scale, causal=False, window_left=-1, window_right=-1,
                        softcap=0.0, return_dsum=False, block_mask=None, block_size=128):
-    """dQ (B,Sq,H,D), dK and dV (B,Sk,Hk,D), float64; optionally D (B,H,Sq).
+    """dQ (B,Sq,H,D), dK (B,Sk,Hk,D) and dV (B,Sk,Hk,Dv), float64; optionally D (B,H,Sq).
 
-    O and P are this module's own fp64 forward (no GPU value enters).  dK/dV of a
-    kv-head are the sums of the per-q-head gradients over its H/Hk q-heads: the
-    call-trace page's `sum_out` over the reshaped (B,S,Hk,H/Hk,D) expansion.
+    do is (B,Sq,H,Dv), like O.  O and P are this module's own fp64 forward (no GPU value
+    enters).  dK/dV of a kv-head are the sums of the per-q-head gradients over its H/Hk
+    q-heads: the call-trace page's `sum_out` over the reshaped (B,S,Hk,H/Hk,D) expansion.
     """
     do = np.asarray(do, dtype=np.float64)
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    B, Sq, Sk, H, Hk, D = _check_shapes(q, k, v)
-    if do.shape != q.shape:
-        raise ValueError("do must match q")
+    B, Sq, Sk, H, Hk, D, Dv = _check_shapes(q, k, v)
+    if do.shape != (B, Sq, H, Dv):
+        raise ValueError("do must be (B, Sq, H, Dv), like O")
     G = H // Hk
     vis = visible_mask(Sq, Sk, causal, window_left, window_right)
     bm = _check_block_mask(block_mask, B, H, Sq, Sk, block_size)
     dq = np.zeros((B, Sq, H, D))
     dk = np.zeros((B, Sk, Hk, D))
-    dv = np.zeros((B, Sk, Hk, D))
+    dv = np.zeros((B, Sk, Hk, Dv))
     dsum = np.zeros((B, H, Sq))
     for b in range(B):
         for h in range(H):

@@ -336,9 +336,9 @@ def test_no_keys_at_all():
 def _brute(do, q, k, v, scale, causal, wl, wr, cap, block_mask=None, bs=1):
     """Explicit scalar loops from the definition, one (b, h) at a time."""
     B, Sq, H, D = q.shape
-    Sk, Hk = k.shape[1], k.shape[2]
+    Sk, Hk, Dv = k.shape[1], k.shape[2], v.shape[3]
     G = H // Hk
-    O = np.zeros(q.shape); L = np.zeros((B, H, Sq))
+    O = np.zeros((B, Sq, H, Dv)); L = np.zeros((B, H, Sq))
     dQ = np.zeros(q.shape); dK = np.zeros(k.shape); dV = np.zeros(v.shape)
     if causal:
         wr = 0
@@ -368,16 +368,17 @@ def _brute(do, q, k, v, scale, causal, wl, wr, cap, block_mask=None, bs=1):
                 den = sum(math.exp(x - m) for x in z.values())
                 L[b, h, i] = m + math.log(den)
                 P = {j: math.exp(z[j] - L[b, h, i]) for j in z}
-                for d in range(D):
+                for d in range(Dv):
                     O[b, i, h, d] = sum(P[j] * v[b, j, hk, d] for j in P)
-                Di = sum(do[b, i, h, d] * O[b, i, h, d] for d in range(D))
+                Di = sum(do[b, i, h, d] * O[b, i, h, d] for d in range(Dv))
                 for j in P:
-                    dp = sum(do[b, i, h, d] * v[b, j, hk, d] for d in range(D))
+                    dp = sum(do[b, i, h, d] * v[b, j, hk, d] for d in range(Dv))
                     dz = P[j] * (dp - Di)
                     da = dz * (1 - tt[j] ** 2) if cap > 0 else dz
                     for d in range(D):
                         dQ[b, i, h, d] += scale * da * k[b, j, hk, d]
                         dK[b, j, hk, d] += scale * da * q[b, i, h, d]
+                    for d in range(Dv):
                         dV[b, j, hk, d] += P[j] * do[b, i, h, d]
     return O, L, dQ, dK, dV
 
@@ -487,3 +488,124 @@ def test_golden_regression():
         np.testing.assert_allclose(lse, lse_want, rtol=1e-12)
         for n, got in (("dq", dq), ("dk", dk), ("dv", dv)):
             np.testing.assert_allclose(got, np.array(c[n]), rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- a V head dim of its own
+
+DV_SHAPES = [(4, 6), (6, 3)]   # (D of q and k, Dv of v, o, dO and dV)
+
+
+@pytest.mark.parametrize("var", VARIANTS)
+@pytest.mark.parametrize("D,Dv", DV_SHAPES)
+def test_finite_differences_own_v_dim(var, D, Dv):
+    """Central differences of L = sum(dO * O) with v's head dim different from q's and k's
+    (the sm90 page's `head_dim` / `head_dim_v`): relative error < 1e-6 for dQ, dK and dV."""
+    rng = np.random.default_rng(4321)
+    B, Sq, Sk, H, Hk = 1, 4, 6, 2, 1
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, Hk, D), rng), _rand((B, Sk, Hk, Dv), rng)
+    do = _rand((B, Sq, H, Dv), rng)
+    scale = 0.6
+    dq, dk, dv = attention_backward(do, q, k, v, scale, **var)
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+
+    def loss(qq, kk, vv):
+        o, _ = attention_forward(qq, kk, vv, scale, **var)
+        assert o.shape == (B, Sq, H, Dv)
+        return float((do * o).sum())
+
+    h = 1e-6
+    for pos, (x, g) in enumerate(((q, dq), (k, dk), (v, dv))):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args_p, args_m = [q, k, v], [q, k, v]
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args_p[pos], args_m[pos] = xp, xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(num - g).max() / max(np.abs(g).max(), 1e-300)
+        assert err < 1e-6, ("qkv"[pos], err)
+
+
+@pytest.mark.parametrize("var", VARIANTS)
+def test_torch_autograd_own_v_dim(var):
+    """torch fp64 autograd of the definition with D = 8 for q/k and Dv = 5 for v."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(17)
+    B, Sq, Sk, H, Hk, D, Dv = 2, 7, 9, 4, 2, 8, 5
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, Hk, D), rng), _rand((B, Sk, Hk, Dv), rng)
+    do = _rand((B, Sq, H, Dv), rng)
+    scale = D ** -0.5
+    vis = torch.from_numpy(visible_mask(Sq, Sk, var["causal"], var["window_left"], var["window_right"]))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    G = H // Hk
+    a = torch.einsum("bihd,bjhd->bhij", tq, tk.repeat_interleave(G, dim=2)) * scale
+    if var["softcap"] > 0:
+        a = var["softcap"] * torch.tanh(a / var["softcap"])
+    p = torch.softmax(a.masked_fill(~vis, float("-inf")), dim=-1)
+    o = torch.einsum("bhij,bjhd->bihd", p, tv.repeat_interleave(G, dim=2))
+    o.backward(torch.from_numpy(do))
+    o_ref, _ = attention_forward(q, k, v, scale, **var)
+    dq, dk, dv = attention_backward(do, q, k, v, scale, **var)
+    np.testing.assert_allclose(o_ref, o.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("var", VARIANTS)
+@pytest.mark.parametrize("D,Dv", DV_SHAPES)
+def test_brute_force_own_v_dim(var, D, Dv):
+    rng = np.random.default_rng(19)
+    B, Sq, Sk, H, Hk = 1, 3, 4, 2, 1
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, Hk, D), rng), _rand((B, Sk, Hk, Dv), rng)
+    do = _rand((B, Sq, H, Dv), rng)
+    O, L, dQ, dK, dV = _brute(do, q, k, v, 0.8, var["causal"], var["window_left"], var["window_right"], var["softcap"])
+    o, lse = attention_forward(q, k, v, 0.8, **var)
+    dq, dk, dv = attention_backward(do, q, k, v, 0.8, **var)
+    np.testing.assert_allclose(o, O, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, L, rtol=1e-13)
+    np.testing.assert_allclose(dq, dQ, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dk, dK, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv, dV, rtol=1e-12, atol=1e-13)
+
+
+def test_own_v_dim_special_cases():
+    """Sk = 1 with Dv != D: O = V, dQ = dK = 0, dV = sum_i dO_i.  GQA with Dv != D: dK / dV
+    are the sums over the q-heads of the MHA gradients with K and V replicated.  And the
+    columns of V are independent: O[..., c] depends on V[..., c] only (a split of V by
+    columns gives the matching split of O and dV, and the same dQ / dK sums)."""
+    rng = np.random.default_rng(23)
+    q, k, v, do = (_rand((2, 5, 3, 4), rng), _rand((2, 1, 3, 4), rng), _rand((2, 1, 3, 7), rng),
+                   _rand((2, 5, 3, 7), rng))
+    o, lse = attention_forward(q, k, v, 0.3)
+    np.testing.assert_allclose(o, np.broadcast_to(v, o.shape), rtol=1e-14)
+    dq, dk, dv = attention_backward(do, q, k, v, 0.3)
+    assert np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-13
+    np.testing.assert_allclose(dv, do.sum(axis=1, keepdims=True), rtol=1e-13)
+
+    B, Sq, Sk, H, Hk, D, Dv = 2, 6, 10, 8, 2, 4, 6
+    G = H // Hk
+    q, k, v = _rand((B, Sq, H, D), rng), _rand((B, Sk, Hk, D), rng), _rand((B, Sk, Hk, Dv), rng)
+    do = _rand((B, Sq, H, Dv), rng)
+    for var in VARIANTS:
+        dq, dk, dv = attention_backward(do, q, k, v, 0.6, **var)
+        dq_m, dk_m, dv_m = attention_backward(do, q, np.repeat(k, G, axis=2), np.repeat(v, G, axis=2),
+                                              0.6, **var)
+        np.testing.assert_allclose(dq, dq_m, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(dk, dk_m.reshape(B, Sk, Hk, G, D).sum(axis=3), rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(dv, dv_m.reshape(B, Sk, Hk, G, Dv).sum(axis=3), rtol=1e-13, atol=1e-14)
+        # column split of V: forward and dV split, dQ / dK add up
+        o, lse = attention_forward(q, k, v, 0.6, **var)
+        oa, la = attention_forward(q, k, v[..., :2], 0.6, **var)
+        ob, _ = attention_forward(q, k, v[..., 2:], 0.6, **var)
+        np.testing.assert_allclose(o, np.concatenate([oa, ob], axis=-1), rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(lse, la, rtol=1e-14)
+        dqa, dka, dva = attention_backward(do[..., :2], q, k, v[..., :2], 0.6, **var)
+        dqb, dkb, dvb = attention_backward(do[..., 2:], q, k, v[..., 2:], 0.6, **var)
+        np.testing.assert_allclose(dv, np.concatenate([dva, dvb], axis=-1), rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(dq, dqa + dqb, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(dk, dka + dkb, rtol=1e-11, atol=1e-13)
+    with pytest.raises(ValueError):
+        attention_backward(do[..., :3], q, k, v, 0.6)     # dO must have v's head dim
