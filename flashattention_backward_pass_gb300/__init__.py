@@ -20,7 +20,7 @@ import math
 import torch
 
 from ._abi import (FaError, alloc_bwd_workspace, bwd_blocksparse_workspace_size,
-                   bwd_varlen_workspace_size, bwd_workspace_size, fa_bwd, fa_bwd_blocksparse,
+                   bwd_varlen_workspace_size, bwd_workspace_size, bwd_workspace_size_dv, fa_bwd, fa_bwd_blocksparse,
                    fa_bwd_status, fa_bwd_varlen, fa_fwd, fa_fwd_blocksparse, fa_fwd_varlen, load)
 
 from .autograd import flash_attn_func, flash_attn_varlen_func
@@ -28,7 +28,7 @@ from .autograd import flash_attn_func, flash_attn_varlen_func
 __all__ = ["FaError", "alloc_bwd_workspace", "attention_backward", "attention_backward_varlen",
            "flash_attn_func", "flash_attn_varlen_func",
            "attention_forward", "attention_forward_varlen", "bwd_varlen_workspace_size",
-           "bwd_workspace_size", "fa_bwd", "fa_bwd_status", "fa_bwd_varlen", "fa_fwd",
+           "bwd_workspace_size", "bwd_workspace_size_dv", "fa_bwd", "fa_bwd_status", "fa_bwd_varlen", "fa_fwd",
            "fa_fwd_varlen", "load", "fa_fwd_blocksparse", "fa_bwd_blocksparse",
            "bwd_blocksparse_workspace_size"]
 
@@ -39,8 +39,9 @@ def _scale(q, softmax_scale):
 
 def attention_forward(q, k, v, softmax_scale=None, causal=False, window_left=-1, window_right=-1,
                       softcap=0.0):
+    """out (B, Sq, H, Dv) and lse (B, H, Sq); Dv is v's head dim (it may differ from q's)."""
     B, Sq, H, D = q.shape
-    out = torch.empty_like(q)
+    out = q.new_empty(B, Sq, H, v.shape[3])
     lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, out, lse, _scale(q, softmax_scale), causal, window_left, window_right, softcap)
     return out, lse

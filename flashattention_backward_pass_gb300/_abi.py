@@ -61,6 +61,8 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_workspace_size.argtypes = [ctypes.c_int] * 6
     lib.fa_bwd_workspace_size.restype = sz
     lib.fa_bwd_workspace_size.argtypes = [ctypes.c_int] * 7
+    lib.fa_bwd_workspace_size_dv.restype = sz
+    lib.fa_bwd_workspace_size_dv.argtypes = [ctypes.c_int] * 8
     lib.fa_fwd.restype = ctypes.c_int
     lib.fa_fwd.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                            ctypes.c_float, vp, sz, vp]
@@ -153,10 +155,17 @@ def bwd_workspace_size(B, H, Hk, Sq, Sk, D, deterministic=False) -> int:
     return int(load().fa_bwd_workspace_size(B, H, Hk, Sq, Sk, D, int(bool(deterministic))))
 
 
-def alloc_bwd_workspace(q: torch.Tensor, k: torch.Tensor, deterministic=False) -> torch.Tensor:
+def bwd_workspace_size_dv(B, H, Hk, Sq, Sk, D, Dv, deterministic=False) -> int:
+    return int(load().fa_bwd_workspace_size_dv(B, H, Hk, Sq, Sk, D, Dv, int(bool(deterministic))))
+
+
+def alloc_bwd_workspace(q: torch.Tensor, k: torch.Tensor, deterministic=False,
+                        v: torch.Tensor | None = None) -> torch.Tensor:
+    """Workspace for fa_bwd on these inputs (v: only needed when its head dim differs)."""
     B, Sq, H, D = q.shape
     Sk, Hk = k.shape[1], k.shape[2]
-    n = bwd_workspace_size(B, H, Hk, Sq, Sk, D, deterministic)
+    Dv = v.shape[3] if v is not None else D
+    n = bwd_workspace_size_dv(B, H, Hk, Sq, Sk, D, Dv, deterministic)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
 
 
@@ -176,7 +185,7 @@ def fa_bwd(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal=False, win
     """Writes dQ, dK, dV in place (C call `fa_bwd`).  Returns the workspace used."""
     lib = load()
     if workspace is None:
-        workspace = alloc_bwd_workspace(q, k, deterministic)
+        workspace = alloc_bwd_workspace(q, k, deterministic, v)
     tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
     st = lib.fa_bwd(*[ctypes.byref(x) for x in tv], float(softmax_scale), int(bool(causal)),
                     int(window_left), int(window_right), float(softcap), int(bool(deterministic)),

@@ -40,7 +40,7 @@ class FlashAttnFunc(torch.autograd.Function):
                 deterministic):
         q, k, v = (t if t.stride(-1) == 1 else t.contiguous() for t in (q, k, v))
         B, Sq, H, _ = q.shape
-        out = torch.empty_like(q)
+        out = q.new_empty(B, Sq, H, v.shape[3])
         lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
         _abi.fa_fwd(q, k, v, out, lse, softmax_scale, causal, window_left, window_right, softcap)
         ctx.save_for_backward(q, k, v, out, lse)

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
 SOURCES = ["fa_api.cu", "fa_bwd_main.cu", "fa_bwd_split.cu", "fa_bwd_aux.cu", "fa_fwd_tc.cu",
-           "fa_noalloc.cu"]
+           "fa_wide.cu", "fa_noalloc.cu"]
 HEADERS = ["fa_ptx.cuh", "fa_kernels.h", "fa_tiles.h", "fa_bwd_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -47,6 +47,7 @@ void prof_record(int i, cudaStream_t s) {
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int pad64(int d) { return (d + 63) / 64 * 64; }
 
 int padded_dim(int D) {
   if (D <= 64) return 64;
@@ -79,6 +80,29 @@ bool bwd_layout(int B, int H, int Sq, int D, BwdLayout* L) {
   off += sems;
   L->accum_bytes = accum;
   L->sems_bytes = sems;
+  L->total = align_up(off, 256);
+  return true;
+}
+
+// Head dims above 128 or Dv != D (fa_wide.cu): the same header, LSE2 and D regions, and a
+// dQ accumulator of (B, H, ceil(Sq / 64), ceil(pad64(D) / 128)) blocks of 128 x 64 fp32.
+bool bwd_layout_wide(int B, int H, int Sq, int D, BwdLayout* L) {
+  if (B < 0 || H <= 0 || Sq < 0 || D <= 0) return false;
+  L->Dp = pad64(D);
+  L->Mb = (Sq + kTileQ - 1) / kTileQ;
+  L->Sq_r = L->Mb * kTileQ;
+  const size_t rows = (size_t)B * H * L->Sq_r;
+  size_t off = WS_HEADER_BYTES;
+  L->off_lse2 = off;
+  off = align_up(off + rows * 4, 256);
+  L->off_dsum = off;
+  off = align_up(off + rows * 4, 256);
+  L->off_accum = off;
+  const size_t accum = (size_t)B * H * (size_t)((Sq + 63) / 64) * (size_t)((L->Dp + 127) / 128) * 32768u;
+  off += accum;
+  L->off_sems = off;
+  L->accum_bytes = accum;
+  L->sems_bytes = 0;
   L->total = align_up(off, 256);
   return true;
 }
@@ -148,29 +172,30 @@ int check_lse(const fa_tensor* t, int64_t B, int64_t H, int64_t Sq) {
   return FA_OK;
 }
 
-// Shapes shared by fa_fwd and fa_bwd.  Returns a status; fills the problem sizes.
-// Also returns the shared 16-bit element type of q, k and v in *dtype.
+// Shapes shared by fa_fwd and fa_bwd.  Returns a status; fills the problem sizes: D is
+// the head dim of q and k, Dv the one of v (the `flash_bwd_sm90.py` page's `head_dim` and
+// `head_dim_v`).  Also returns the shared 16-bit element type of q, k and v in *dtype.
 int check_qkv(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, int* B, int* Sq,
-              int* Sk, int* H, int* Hk, int* D, int* dtype) {
+              int* Sk, int* H, int* Hk, int* D, int* Dv, int* dtype) {
   if (!q || !k || !v) return FA_ERR_NULL;
   if (q->ndim != 4 || k->ndim != 4 || v->ndim != 4) return FA_ERR_SHAPE;
   if (q->dtype != FA_DTYPE_BF16 && q->dtype != FA_DTYPE_F16) return FA_ERR_DTYPE;
   if (k->dtype != q->dtype || v->dtype != q->dtype) return FA_ERR_DTYPE;
   const int64_t b = q->shape[0], sq = q->shape[1], h = q->shape[2], d = q->shape[3];
-  const int64_t sk = k->shape[1], hk = k->shape[2];
-  if (b < 0 || sq < 0 || sk < 0 || h <= 0 || hk <= 0 || d <= 0) return FA_ERR_SHAPE;
+  const int64_t sk = k->shape[1], hk = k->shape[2], dv = v->shape[3];
+  if (b < 0 || sq < 0 || sk < 0 || h <= 0 || hk <= 0 || d <= 0 || dv <= 0) return FA_ERR_SHAPE;
   if (k->shape[0] != b || k->shape[3] != d) return FA_ERR_SHAPE;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     if (v->shape[i] != k->shape[i]) return FA_ERR_SHAPE;
   if (h % hk != 0) return FA_ERR_SHAPE;
-  if (d % 8 != 0 || d > 128) return FA_ERR_HEADDIM;
+  if (d % 8 != 0 || d > 256 || dv % 8 != 0 || dv > 256) return FA_ERR_HEADDIM;
   // launch-grid limits: the forward's grid has B in z and H in y (each at most 65535)
   if (b > 65535 || sq > (1 << 30) || sk > (1 << 30) || h > 65535) return FA_ERR_UNSUPPORTED;
   int st = check_h16_4d(q, q->dtype, b, sq, h, d);
   if (st) return st;
   st = check_h16_4d(k, q->dtype, b, sk, hk, d);
   if (st) return st;
-  st = check_h16_4d(v, q->dtype, b, sk, hk, d);
+  st = check_h16_4d(v, q->dtype, b, sk, hk, dv);
   if (st) return st;
   *dtype = q->dtype;
   *B = (int)b;
@@ -179,8 +204,13 @@ int check_qkv(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, int* B
   *H = (int)h;
   *Hk = (int)hk;
   *D = (int)d;
+  *Dv = (int)dv;
   return FA_OK;
 }
+
+// Head dims the 128-wide kernels take (one dim for q, k and v, at most 128); every other
+// valid pair goes to the wide kernels of fa_wide.cu.
+bool is_wide(int D, int Dv) { return D != Dv || D > 128; }
 
 int check_scalars(float scale, float softcap) {
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_ARG;
@@ -232,9 +262,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tensor map over a bf16 or f16 (B, S, H, D) operand, box = (width, 1, 128, 1) at
+// Tensor map over a bf16 or f16 (B, S, H, D) operand, box = (width, 1, rows, 1) at
 // 128B/64B/32B swizzle.  Out-of-range rows and columns (S tail, D padding) read as zero.
-bool encode_operand(CUtensorMap* map, const fa_tensor* t, int width) {
+bool encode_operand(CUtensorMap* map, const fa_tensor* t, int width, int rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
@@ -242,7 +272,7 @@ bool encode_operand(CUtensorMap* map, const fa_tensor* t, int width) {
   cuuint64_t strides[3] = {(cuuint64_t)(t->shape[2] > 1 ? t->stride[2] : t->shape[3]) * 2,
                            (cuuint64_t)(t->shape[1] > 1 ? t->stride[1] : t->shape[3]) * 2,
                            (cuuint64_t)(t->shape[0] > 1 ? t->stride[0] : t->shape[3]) * 2};
-  cuuint32_t box[4] = {(cuuint32_t)width, 1, 128, 1};
+  cuuint32_t box[4] = {(cuuint32_t)width, 1, (cuuint32_t)rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMapSwizzle swz = width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                        : (width == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -276,7 +306,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_NULL: return "FA_ERR_NULL: a required pointer is NULL";
     case FA_ERR_SHAPE: return "FA_ERR_SHAPE: tensor shapes do not match";
     case FA_ERR_DTYPE: return "FA_ERR_DTYPE: unsupported dtype";
-    case FA_ERR_HEADDIM: return "FA_ERR_HEADDIM: head dim must be a multiple of 8 and <= 128";
+    case FA_ERR_HEADDIM: return "FA_ERR_HEADDIM: head dims must be multiples of 8 and <= 256";
     case FA_ERR_LAYOUT: return "FA_ERR_LAYOUT: last dimension must be contiguous";
     case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT: base or stride not 16-byte aligned";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
@@ -298,18 +328,48 @@ static int fwd_common(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v
                       fa_tensor* lse, float softmax_scale, int causal, int window_left,
                       int window_right, float softcap, void* workspace, size_t workspace_bytes,
                       void* stream, const uint8_t* block_mask) {
-  int B, Sq, Sk, H, Hk, D, dt;
-  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &dt);
+  int B, Sq, Sk, H, Hk, D, Dv, dt;
+  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &Dv, &dt);
   if (st) return st;
-  if ((st = check_h16_4d(out, dt, B, Sq, H, D))) return st;
+  if ((st = check_h16_4d(out, dt, B, Sq, H, Dv))) return st;
   if ((st = check_lse(lse, B, H, Sq))) return st;
   if ((st = check_scalars(softmax_scale, softcap))) return st;
+  const bool wide = is_wide(D, Dv);
+  if (wide && block_mask) return FA_ERR_UNSUPPORTED;  // block sparsity: 128-wide kernels only
   if (B == 0 || Sq == 0) return FA_OK;
   long long lo, hi;
   mask_bounds(Sq, Sk, causal, window_left, window_right, &lo, &hi);
+  const int* status = (workspace && workspace_bytes >= WS_HEADER_BYTES && is_aligned16(workspace))
+                          ? (int*)workspace + WS_STATUS
+                          : nullptr;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (wide && Sk > 0) {
+    WideParams w;
+    memset(&w, 0, sizeof(w));
+    w.B = B; w.H = H; w.Hk = Hk; w.G = H / Hk; w.Sq = Sq; w.Sk = Sk;
+    w.Dk = D; w.Dv = Dv; w.DPK = pad64(D); w.DPV = pad64(Dv);
+    w.Mb = (Sq + kTileQ - 1) / kTileQ;
+    w.Nb = (Sk + kTileK - 1) / kTileK;
+    w.lo64 = lo; w.hi64 = hi; w.lo = clamp30(lo); w.hi = clamp30(hi);
+    w.scale_log2 = softmax_scale * kLog2e;
+    w.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
+    w.cap_log2 = softcap * kLog2e;
+    w.o = out->data;
+    w.o_sb = out->stride[0]; w.o_ss = out->stride[1]; w.o_sh = out->stride[2];
+    w.lse = (float*)lse->data;
+    w.lse_sb = lse->stride[0]; w.lse_sh = lse->stride[1]; w.lse_ss = lse->stride[2];
+    w.status = const_cast<int*>(status);
+    w.wait_limit = g_wait_limit;
+    CUtensorMap mq, mk, mv;
+    if (!encode_operand(&mq, q, 64) || !encode_operand(&mk, k, 64) || !encode_operand(&mv, v, 64))
+      return FA_ERR_CUDA;
+    return launch_fwd_wide(w, mq, mk, mv, softcap > 0.f, dt == FA_DTYPE_F16, s) == cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+  }
   FwdTcParams p;
   memset(&p, 0, sizeof(p));
-  p.B = B; p.H = H; p.Hk = Hk; p.G = H / Hk; p.Sq = Sq; p.Sk = Sk; p.D = D;
+  p.B = B; p.H = H; p.Hk = Hk; p.G = H / Hk; p.Sq = Sq; p.Sk = Sk; p.D = Dv;
   p.Mb = (Sq + kTileQ - 1) / kTileQ;
   p.Nb = (Sk + kTileK - 1) / kTileK;
   p.lo64 = lo;
@@ -324,12 +384,9 @@ static int fwd_common(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v
   p.lse = (float*)lse->data;
   p.lse_sb = lse->stride[0]; p.lse_sh = lse->stride[1]; p.lse_ss = lse->stride[2];
   // optional workspace: its status word receives a device timeout (read with fa_bwd_status)
-  p.status = (workspace && workspace_bytes >= WS_HEADER_BYTES && is_aligned16(workspace))
-                 ? (int*)workspace + WS_STATUS
-                 : nullptr;
+  p.status = const_cast<int*>(status);
   p.wait_limit = g_wait_limit;
   p.block_mask = block_mask;
-  const cudaStream_t s = (cudaStream_t)stream;
   if (Sk == 0)  // no key: O = 0 and LSE = +inf (tensor maps need a non-empty key extent)
     return launch_fwd_empty(p, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   // tcgen05 kernel: one CTA per (128-query tile, batch, q-head)
@@ -369,8 +426,9 @@ int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa
   if ((st = packed_view(q, 3, &q4)) || (st = packed_view(k, 3, &k4)) || (st = packed_view(v, 3, &v4)) ||
       (st = packed_view(out, 3, &o4)) || (st = packed_view(lse, 2, &l3)))
     return st;
-  int B1, Tq, Tk, H, Hk, D, dt;
-  if ((st = check_qkv(&q4, &k4, &v4, &B1, &Tq, &Tk, &H, &Hk, &D, &dt))) return st;
+  int B1, Tq, Tk, H, Hk, D, Dv, dt;
+  if ((st = check_qkv(&q4, &k4, &v4, &B1, &Tq, &Tk, &H, &Hk, &D, &Dv, &dt))) return st;
+  if (is_wide(D, Dv)) return FA_ERR_UNSUPPORTED;  // packed sequences: 128-wide kernels only
   if ((st = check_h16_4d(&o4, dt, 1, Tq, H, D))) return st;
   if ((st = check_lse(&l3, 1, H, Tq))) return st;
   if ((st = check_scalars(softmax_scale, softcap))) return st;
@@ -423,10 +481,89 @@ int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int deterministic) {
+  return fa_bwd_workspace_size_dv(B, H, Hk, Sq, Sk, D, D, deterministic);
+}
+
+size_t fa_bwd_workspace_size_dv(int B, int H, int Hk, int Sq, int Sk, int D, int Dv,
+                                int deterministic) {
   (void)Hk; (void)Sk; (void)deterministic;
   BwdLayout L;
-  if (!bwd_layout(B, H, Sq, D, &L)) return 0;
+  if (Dv <= 0) return 0;
+  if (is_wide(D, Dv) ? !bwd_layout_wide(B, H, Sq, D, &L) : !bwd_layout(B, H, Sq, D, &L)) return 0;
   return L.total;
+}
+
+// The backward for head dims above 128 or Dv != D: preprocess (D over Dv columns), the
+// wide main kernel, and the convert of its transposed dQ blocks.  Batched, dense,
+// non-deterministic calls (the caller has checked that).
+static int bwd_wide(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
+                    const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq,
+                    fa_tensor* dk, fa_tensor* dv, int B, int H, int Hk, int Sq, int Sk, int D,
+                    int Dv, bool f16, float softmax_scale, int causal, int window_left,
+                    int window_right, float softcap, void* workspace, size_t workspace_bytes,
+                    cudaStream_t s) {
+  BwdLayout L;
+  if (!bwd_layout_wide(B, H, Sq, D, &L)) return FA_ERR_SHAPE;
+  if (!workspace || workspace_bytes < L.total) return FA_ERR_WORKSPACE;
+  if (!is_aligned16(workspace)) return FA_ERR_ALIGNMENT;
+  uint8_t* ws = (uint8_t*)workspace;
+  long long lo, hi;
+  mask_bounds(Sq, Sk, causal, window_left, window_right, &lo, &hi);
+
+  BwdPreParams pre;
+  memset(&pre, 0, sizeof(pre));
+  pre.dout = (const __nv_bfloat16*)dout->data;
+  pre.out = (const __nv_bfloat16*)out->data;
+  pre.lse = (const float*)lse->data;
+  pre.do_sb = dout->stride[0]; pre.do_ss = dout->stride[1]; pre.do_sh = dout->stride[2];
+  pre.o_sb = out->stride[0]; pre.o_ss = out->stride[1]; pre.o_sh = out->stride[2];
+  pre.lse_sb = lse->stride[0]; pre.lse_sh = lse->stride[1]; pre.lse_ss = lse->stride[2];
+  pre.B = B; pre.H = H; pre.Sq = Sq; pre.Sq_r = L.Sq_r; pre.D = Dv;
+  pre.lse2 = (float*)(ws + L.off_lse2);
+  pre.dsum = (float*)(ws + L.off_dsum);
+  pre.zero_ptr = (float4*)(ws + L.off_accum);
+  pre.zero_count = (int64_t)(L.accum_bytes / 16);
+  pre.header = (int*)ws;
+  prof_record(0, s);
+  if (launch_bwd_preprocess(pre, f16, s) != cudaSuccess) return FA_ERR_CUDA;
+
+  WideParams w;
+  memset(&w, 0, sizeof(w));
+  w.B = B; w.H = H; w.Hk = Hk; w.G = H / Hk; w.Sq = Sq; w.Sk = Sk;
+  w.Dk = D; w.Dv = Dv; w.DPK = pad64(D); w.DPV = pad64(Dv);
+  w.Mb = (Sq + 63) / 64;
+  w.Nb = (Sk + kTileK - 1) / kTileK;
+  w.nks = (w.DPK + 127) / 128;
+  const int nvs = (w.DPV + 127) / 128;
+  w.nslice = w.nks > nvs ? w.nks : nvs;
+  w.lo64 = lo; w.hi64 = hi; w.lo = clamp30(lo); w.hi = clamp30(hi);
+  w.scale_log2 = softmax_scale * kLog2e;
+  w.cap_scale = softcap > 0.f ? softmax_scale / softcap : 0.f;
+  w.cap_log2 = softcap * kLog2e;
+  w.dk_scale = softmax_scale;
+  w.scale = softmax_scale;
+  w.lse2 = (const float*)(ws + L.off_lse2);
+  w.dsum = (const float*)(ws + L.off_dsum);
+  w.Sq_r = L.Sq_r;
+  w.dq_accum = (float*)(ws + L.off_accum);
+  w.dk = dk->data; w.dv = dv->data; w.dq = dq->data;
+  w.dk_sb = dk->stride[0]; w.dk_ss = dk->stride[1]; w.dk_sh = dk->stride[2];
+  w.dv_sb = dv->stride[0]; w.dv_ss = dv->stride[1]; w.dv_sh = dv->stride[2];
+  w.dq_sb = dq->stride[0]; w.dq_ss = dq->stride[1]; w.dq_sh = dq->stride[2];
+  w.status = (int*)ws + WS_STATUS;
+  w.wait_limit = g_wait_limit;
+  prof_record(1, s);
+  if (Sk > 0) {
+    CUtensorMap mq, mk, mv, mdo;
+    if (!encode_operand(&mq, q, 64, 64) || !encode_operand(&mk, k, 64) ||
+        !encode_operand(&mv, v, 64) || !encode_operand(&mdo, dout, 64, 64))
+      return FA_ERR_CUDA;
+    if (launch_bwd_wide(w, mq, mk, mv, mdo, softcap > 0.f, f16, s) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  prof_record(2, s);
+  if (launch_convert_wide(w, f16, s) != cudaSuccess) return FA_ERR_CUDA;
+  prof_record(3, s);
+  return FA_OK;
 }
 
 // The backward for a batch (vl == nullptr) or for packed sequences (vl: the tensors are
@@ -437,15 +574,26 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
                       int window_left, int window_right, float softcap, int deterministic,
                       void* workspace, size_t workspace_bytes, void* stream,
                       const VarlenArgs* vl, const uint8_t* block_mask) {
-  int B, Sq, Sk, H, Hk, D, dt;
-  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &dt);
+  int B, Sq, Sk, H, Hk, D, Dv, dt;
+  int st = check_qkv(q, k, v, &B, &Sq, &Sk, &H, &Hk, &D, &Dv, &dt);
   if (st) return st;
-  if ((st = check_h16_4d(dout, dt, B, Sq, H, D))) return st;
-  if ((st = check_h16_4d(out, dt, B, Sq, H, D))) return st;
+  if ((st = check_h16_4d(dout, dt, B, Sq, H, Dv))) return st;
+  if ((st = check_h16_4d(out, dt, B, Sq, H, Dv))) return st;
   if ((st = check_h16_4d(dq, dt, B, Sq, H, D))) return st;
   if ((st = check_h16_4d(dk, dt, B, Sk, Hk, D))) return st;
-  if ((st = check_h16_4d(dv, dt, B, Sk, Hk, D))) return st;
+  if ((st = check_h16_4d(dv, dt, B, Sk, Hk, Dv))) return st;
   const bool f16 = dt == FA_DTYPE_F16;
+  if (is_wide(D, Dv)) {
+    // the wide kernels: batched, dense and non-deterministic only, whichever algorithm is
+    // selected
+    if (vl || block_mask || deterministic) return FA_ERR_UNSUPPORTED;
+    if ((st = check_lse(lse, B, H, Sq))) return st;
+    if ((st = check_scalars(softmax_scale, softcap))) return st;
+    if (B == 0 || Sq == 0) return FA_OK;
+    return bwd_wide(dout, q, k, v, out, lse, dq, dk, dv, B, H, Hk, Sq, Sk, D, Dv, f16,
+                    softmax_scale, causal, window_left, window_right, softcap, workspace,
+                    workspace_bytes, (cudaStream_t)stream);
+  }
   // the split algorithm is built for batched dense bf16 only; block sparsity has no ordered
   // (deterministic) mode
   if ((f16 || vl || block_mask) && g_bwd_algorithm == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;

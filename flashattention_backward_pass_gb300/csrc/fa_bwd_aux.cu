@@ -26,8 +26,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // lane in flight.  Blocks [row_blocks, gridDim.x) clear the accumulator and the counters
 // with 16-byte stores.  The two kinds of blocks run side by side, so the latency-bound row
 // reductions overlap the bandwidth-bound clearing.
-// F16: dO and O are f16 (else bf16).  VARLEN: packed sequences (rows by slot).
-template <bool F16, bool VARLEN>
+// F16: dO and O are f16 (else bf16).  VARLEN: packed sequences (rows by slot).  WIDE:
+// rows of up to 256 columns (two 128-column passes).
+template <bool F16, bool VARLEN, bool WIDE = false>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams p, int row_blocks) {
   if (blockIdx.x == 0 && threadIdx.x < 4) p.header[threadIdx.x] = 0;
   if ((int)blockIdx.x >= row_blocks) {
@@ -76,23 +77,26 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
       if (real) {
         const __nv_bfloat16* a = p.dout + b * p.do_sb + i * p.do_ss + h * p.do_sh;
         const __nv_bfloat16* o = p.out + b * p.o_sb + i * p.o_ss + h * p.o_sh;
-        uint4 av[2], ov[2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = l8 * 16 + u * 8;
-          av[u] = c < p.D ? *reinterpret_cast<const uint4*>(a + c) : make_uint4(0, 0, 0, 0);
-          ov[u] = c < p.D ? *reinterpret_cast<const uint4*>(o + c) : make_uint4(0, 0, 0, 0);
-        }
+        for (int ch = 0; ch < (WIDE ? 2 : 1); ++ch) {
+          uint4 av[2], ov[2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint32_t aw[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
-          const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+          for (int u = 0; u < 2; ++u) {
+            const int c = ch * 128 + l8 * 16 + u * 8;
+            av[u] = c < p.D ? *reinterpret_cast<const uint4*>(a + c) : make_uint4(0, 0, 0, 0);
+            ov[u] = c < p.D ? *reinterpret_cast<const uint4*>(o + c) : make_uint4(0, 0, 0, 0);
+          }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 af = unpack_h2<F16>(aw[e]);
-            const float2 of = unpack_h2<F16>(ow[e]);
-            acc = fmaf(af.x, of.x, acc);
-            acc = fmaf(af.y, of.y, acc);
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t aw[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
+            const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 af = unpack_h2<F16>(aw[e]);
+              const float2 of = unpack_h2<F16>(ow[e]);
+              acc = fmaf(af.x, of.x, acc);
+              acc = fmaf(af.y, of.y, acc);
+            }
           }
         }
       }
@@ -204,7 +208,13 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t 
   const int64_t zero_cap = (int64_t)sms * 8;
   if (zero_blocks > zero_cap) zero_blocks = zero_cap;
   const unsigned grid = (unsigned)(row_blocks + zero_blocks);
-  if (p.varlen) {
+  if (p.D > 128) {
+    // head dims above 128 (batched calls only)
+    if (f16)
+      bwd_preprocess_kernel<true, false, true><<<grid, 256, 0, s>>>(p, (int)row_blocks);
+    else
+      bwd_preprocess_kernel<false, false, true><<<grid, 256, 0, s>>>(p, (int)row_blocks);
+  } else if (p.varlen) {
     if (f16)
       bwd_preprocess_kernel<true, true><<<grid, 256, 0, s>>>(p, (int)row_blocks);
     else

@@ -141,6 +141,38 @@ struct FwdTcParams {
   const uint8_t* block_mask;
 };
 
+// Head dims above 128, or a V head dim different from the Q/K one (fa_wide.cu).  Both
+// padded dims are multiples of 64 and at most 256; the tensor maps use 64-column
+// 128B-swizzled boxes (128 rows for K / V and the forward's Q, 64 rows for the
+// backward's Q / dO steps).
+struct WideParams {
+  int B, H, Hk, G, Sq, Sk;
+  int Dk, Dv;                    // logical head dims of q / k and of v
+  int DPK, DPV;                  // padded to multiples of 64
+  int Mb, Nb;                    // forward: 128-query tiles; backward: 64-query blocks; 128-key tiles
+  int nslice;                    // backward: 128-column output slices (max over dK and dV)
+  int nks;                       // backward: slices that carry dK / dQ columns
+  long long lo64, hi64;          // visible iff lo <= j - i <= hi (unclamped)
+  int lo, hi;                    // clamped to +-2^30
+  float scale_log2, cap_scale, cap_log2, dk_scale;
+  void* o;                       // forward output (B, Sq, H, Dv)
+  int64_t o_sb, o_ss, o_sh;
+  float* lse;
+  int64_t lse_sb, lse_sh, lse_ss;
+  const float* lse2;             // backward: (B*H, Sq_r) from the preprocess
+  const float* dsum;
+  int Sq_r;
+  float* dq_accum;               // (B, H, Mb, nks) blocks of 128 x 64 fp32 (see fa_wide.cu)
+  void* dk;                      // (B, Sk, Hk, Dk)
+  void* dv;                      // (B, Sk, Hk, Dv)
+  int64_t dk_sb, dk_ss, dk_sh, dv_sb, dv_ss, dv_sh;
+  void* dq;                      // convert: (B, Sq, H, Dk)
+  int64_t dq_sb, dq_ss, dq_sh;
+  float scale;
+  int* status;
+  long long wait_limit;
+};
+
 // Tensor maps for one bf16 (B, S, H, D) operand: a 64-column 128B-swizzled box and,
 // when Dp % 64 != 0, a narrower box for the remaining 16 or 32 columns.
 struct OperandMaps {
@@ -165,6 +197,14 @@ cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const
 cudaError_t launch_fwd_empty(const FwdTcParams& p, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
                           const OperandMaps& v, int Dp, bool softcap, bool f16, cudaStream_t s);
+size_t wide_fwd_smem_bytes(int DPK, int DPV);
+size_t wide_bwd_smem_bytes(int DPK, int DPV);
+cudaError_t launch_fwd_wide(const WideParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, bool softcap, bool f16, cudaStream_t s);
+cudaError_t launch_bwd_wide(const WideParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const CUtensorMap& dout, bool softcap,
+                            bool f16, cudaStream_t s);
+cudaError_t launch_convert_wide(const WideParams& p, bool f16, cudaStream_t s);
 #ifdef FA_TRACE
 cudaError_t bwd_trace_copy(void* host, size_t bytes);
 cudaError_t split_trace_copy(void* host, size_t bytes);

@@ -82,9 +82,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // Bounded busy wait with the non-blocking test: no suspension, so the phase change is seen
 // within a few cycles.  For the single thread that issues the MMAs, where every cycle of
 // wake-up latency leaves the tensor pipe idle.
-// Bounded busy wait with the non-blocking test: no suspension, so the phase change is seen
-// within a few cycles.  For the single thread that issues the MMAs, where every cycle of
-// wake-up latency leaves the tensor pipe idle.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const AbortState& st,
                                                int code) {
   if (mbar_test_wait(bar, parity)) return true;

@@ -32,6 +32,11 @@ class Workload:
     do_std: float = 1.0
     seed: int = 0
     deterministic_modes: tuple = field(default=(False,))
+    Dv: int = 0          # v's head dim (0: the same as D)
+
+    @property
+    def dv(self) -> int:
+        return self.Dv or self.D
 
     @property
     def scale(self) -> float:
@@ -61,13 +66,17 @@ class Workload:
 
     @property
     def algorithmic_flops(self) -> float:
-        """10*D flops (five multiply-adds over D) per visible pair, logical D."""
-        return 10.0 * self.D * self.B * self.H * self.visible_pairs_per_head()
+        """Per visible pair, 2 flops per multiply-add of the five products: S and dK and
+        dQ over D, dP and dV over Dv (10*D when Dv == D); logical head dims."""
+        return 2.0 * (3 * self.D + 2 * self.dv) * self.B * self.H * self.visible_pairs_per_head()
 
     def describe(self) -> dict:
-        return dict(workload=self.name, B=self.B, Sq=self.Sq, Sk=self.Sk, H=self.H, Hk=self.Hk,
-                    D=self.D, causal=self.causal, window_left=self.window_left,
-                    window_right=self.window_right, softcap=self.softcap)
+        d = dict(workload=self.name, B=self.B, Sq=self.Sq, Sk=self.Sk, H=self.H, Hk=self.Hk,
+                 D=self.D, causal=self.causal, window_left=self.window_left,
+                 window_right=self.window_right, softcap=self.softcap)
+        if self.Dv:
+            d["Dv"] = self.Dv
+        return d
 
 
 WORKLOADS = {
@@ -86,14 +95,14 @@ HEADLINE = "gqa_causal"
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None, dtype=torch.bfloat16):
     """q, k, v, do as 16-bit tensors (bf16 by default, or f16) in the (B, S, H, D)
-    layout, drawn from N(0, 1) (dO from N(0, do_std^2)) with a CPU generator so that
-    every device sees the same values."""
+    layout (v and do with the workload's v head dim), drawn from N(0, 1) (dO from
+    N(0, do_std^2)) with a CPU generator so that every device sees the same values."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
     q = torch.randn(w.B, w.Sq, w.H, w.D, generator=g, dtype=torch.float32)
     k = torch.randn(w.B, w.Sk, w.Hk, w.D, generator=g, dtype=torch.float32)
-    v = torch.randn(w.B, w.Sk, w.Hk, w.D, generator=g, dtype=torch.float32)
-    do = torch.randn(w.B, w.Sq, w.H, w.D, generator=g, dtype=torch.float32) * w.do_std
+    v = torch.randn(w.B, w.Sk, w.Hk, w.dv, generator=g, dtype=torch.float32)
+    do = torch.randn(w.B, w.Sq, w.H, w.dv, generator=g, dtype=torch.float32) * w.do_std
     out = [t.to(dtype) for t in (q, k, v, do)]
     if device != "cpu":
         out = [t.to(device) for t in out]

@@ -29,8 +29,14 @@
  *   - All argument errors are detected on the host before any launch and leave the
  *     outputs untouched.  A device-side wait that runs out of time records
  *     FA_ERR_DEVICE_TIMEOUT in the workspace status word (see fa_bwd_status).
- *   - Limits of this build: D % 8 == 0 and D <= 128 (padded inside to a multiple of
- *     16); H % Hk == 0; base pointers 16-byte aligned; every non-unit stride a
+ *   - Head dims: q and k share D, v may have its own Dv (the `flash_bwd_sm90.py` page's
+ *     `head_dim` / `head_dim_v`); O, dO and dV then have Dv columns.  D % 8 == 0,
+ *     Dv % 8 == 0, both <= 256.  D == Dv <= 128 runs on the 128-wide kernels (padded
+ *     inside to a multiple of 16); every other pair runs on the wide kernels (padded to
+ *     a multiple of 64), which take batched, dense, non-deterministic calls only
+ *     (packed sequences, block masks and deterministic == 1 return FA_ERR_UNSUPPORTED
+ *     there).
+ *   - Other limits: H % Hk == 0; base pointers 16-byte aligned; every non-unit stride a
  *     multiple of 8 elements (16 bytes).
  */
 #ifndef FA_GB300_H
@@ -59,7 +65,7 @@ typedef enum {
     FA_ERR_NULL = -1,          /* a required pointer is NULL                          */
     FA_ERR_SHAPE = -2,         /* mismatched dims, K/V mismatch, H % Hk != 0, ndim    */
     FA_ERR_DTYPE = -3,         /* tensors not all bf16 or all f16 / LSE not fp32      */
-    FA_ERR_HEADDIM = -4,       /* D % 8 != 0 or D > 128                               */
+    FA_ERR_HEADDIM = -4,       /* D or Dv not a multiple of 8, or above 256           */
     FA_ERR_LAYOUT = -5,        /* last dimension not contiguous                       */
     FA_ERR_ALIGNMENT = -6,     /* base not 16-byte aligned or stride not 16-byte mult */
     FA_ERR_WORKSPACE = -7,     /* workspace NULL or smaller than the size query       */
@@ -157,7 +163,14 @@ int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
 size_t fa_bwd_workspace_size(int B, int H, int Hk, int Sq, int Sk, int D, int deterministic);
 
 /*
- * fa_bwd — dQ (B,Sq,H,D), dK and dV (B,Sk,Hk,D), bf16, written in place (the call-trace
+ * The same for a call whose v has its own head dim Dv (q / k: D); equal to
+ * fa_bwd_workspace_size when Dv == D.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size_dv(int B, int H, int Hk, int Sq, int Sk, int D, int Dv,
+                                int deterministic);
+
+/*
+ * fa_bwd — dQ (B,Sq,H,D), dK (B,Sk,Hk,D) and dV (B,Sk,Hk,Dv), written in place (the call-trace
  * page's `_flash_attn_backward` mutates dq, dk, dv).  Inputs: dout, q, k, v, out and the
  * forward's natural-log lse.  dropout is not supported (p = 0).
  *

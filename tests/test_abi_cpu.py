@@ -79,7 +79,7 @@ def test_bwd_validation_codes(lib):
     a = _bwd_args(); a["lse"] = _view((1, 2, 128), dtype=0)
     assert _call_bwd(lib, a) == -3                                       # LSE must be fp32
     assert _call_bwd(lib, _bwd_args(D=60)) == -4                         # D % 8
-    assert _call_bwd(lib, _bwd_args(D=136)) == -4                        # D > 128
+    assert _call_bwd(lib, _bwd_args(D=264)) == -4                        # D > 256
     assert _call_bwd(lib, _bwd_args(B=65536)) == -8                      # B above the grid limit
     a = _bwd_args(); a["q"] = _view((1, 128, 2, 64), strides=(128 * 2 * 64, 2 * 64, 64, 2))
     assert _call_bwd(lib, a) == -5                                       # last dim not contiguous
@@ -277,3 +277,60 @@ def test_status_readers_reject_null_pointers(lib):
     assert lib.fa_bwd_noalloc_status(None, None) == -1
     assert out.value == 7
 
+
+
+def _dv_args(D=192, Dv=128, B=1, Sq=128, Sk=128, H=2, Hk=2):
+    """fa_bwd arguments with v, O, dO and dV of head dim Dv and q, k, dQ, dK of D."""
+    return _bwd_args(B=B, Sq=Sq, Sk=Sk, H=H, Hk=Hk, D=D,
+                     dout=_view((B, Sq, H, Dv)), v=_view((B, Sk, Hk, Dv)), out=_view((B, Sq, H, Dv)),
+                     dv=_view((B, Sk, Hk, Dv)))
+
+
+def test_own_v_head_dim_validation(lib):
+    """A V head dim of its own (the sm90 page's head_dim_v): O, dO and dV follow v; every
+    dim a multiple of 8 and at most 256; the wide kernels take no deterministic mode, no
+    packed sequences and no block mask (refused before any launch)."""
+    assert _call_bwd(lib, _dv_args(Sq=0)) == 0                           # valid, empty
+    assert _call_bwd(lib, _dv_args(D=256, Dv=256, Sq=0)) == 0
+    assert _call_bwd(lib, _dv_args(Dv=60)) == -4                         # Dv % 8
+    assert _call_bwd(lib, _dv_args(Dv=264)) == -4                        # Dv > 256
+    a = _dv_args(); a["dv"] = _view((1, 128, 2, 192))
+    assert _call_bwd(lib, a) == -2                                       # dV must have Dv
+    a = _dv_args(); a["out"] = _view((1, 128, 2, 192))
+    assert _call_bwd(lib, a) == -2                                       # O must have Dv
+    a = _dv_args(); a["dq"] = _view((1, 128, 2, 128))
+    assert _call_bwd(lib, a) == -2                                       # dQ must have D
+    assert _call_bwd(lib, _dv_args(), det=1) == -8                       # no ordered mode
+    assert _call_bwd(lib, _dv_args(D=192, Dv=192), det=1) == -8
+    order = ("dout", "q", "k", "v", "out", "lse", "dq", "dk", "dv")
+    a = _dv_args()
+    ptrs = [ctypes.byref(a[n]) for n in order]
+    assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+                                  1 << 30, None) == -8
+    fwd = [ctypes.byref(a[n]) for n in ("q", "k", "v", "out", "lse")]
+    assert lib.fa_fwd_blocksparse(*fwd, 4096, 0.125, 0, -1, -1, 0.0, None, 0, None) == -8
+    tq, tk, H = 300, 250, 2
+    v3 = [_view((tq, H, 192)), _view((tk, H, 192)), _view((tk, H, 128)), _view((tq, H, 128)),
+          _view((H, tq), dtype=1)]
+    assert lib.fa_fwd_varlen(*[ctypes.byref(x) for x in v3], 4096, 4096, None, None, 2, 100, 100,
+                             0.125, 0, -1, -1, 0.0, None, 0, None) == -8
+
+
+def test_wide_workspace_size(lib):
+    """Wide head dims: LSE2 and D as before, and a dQ accumulator of (B, H, ceil(Sq/64),
+    ceil(pad64(D)/128)) blocks of 128 x 64 fp32; v's head dim does not change it."""
+    f = lib.fa_bwd_workspace_size_dv
+    f.restype = ctypes.c_size_t
+    B, H, Sq = 2, 3, 200
+    Sq_r = 256
+    rows = B * H * Sq_r
+    lse2_end = (256 + rows * 4 + 255) // 256 * 256
+    dsum_end = (lse2_end + rows * 4 + 255) // 256 * 256
+    for D, nks in ((192, 2), (256, 2), (128, 1), (72, 1)):
+        want = dsum_end + B * H * 4 * nks * 32768
+        want = (want + 255) // 256 * 256
+        assert f(B, H, 1, Sq, 77, D, 64 if D != 64 else 128, 0) == want, D
+    g = lib.fa_bwd_workspace_size
+    g.restype = ctypes.c_size_t
+    assert g(B, H, 1, Sq, 77, 256, 0) == f(B, H, 1, Sq, 77, 256, 256, 0)
+    assert g(B, H, 1, Sq, 77, 128, 0) == f(B, H, 1, Sq, 77, 128, 128, 0)
