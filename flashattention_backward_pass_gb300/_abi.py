@@ -96,7 +96,8 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd_blocksparse_workspace_size.argtypes = [ctypes.c_int] * 6
     lib.fa_bwd_blocksparse.restype = ctypes.c_int
     lib.fa_bwd_blocksparse.argtypes = [P, P, P, P, P, P, P, P, P, vp, ctypes.c_float, ctypes.c_int,
-                                       ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, sz, vp]
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                       vp, sz, vp]
     lib.fa_bwd_varlen.restype = ctypes.c_int
     lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, ip, ip, ip, ip, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
@@ -206,11 +207,14 @@ def fa_bwd_status(workspace, stream=None) -> int:
 
 ALGO_SPLIT = 0
 ALGO_FUSED = 1
+ALGO_AUTO = 2
 
 
 def set_algorithm(algo: int):
     """Backward algorithm for later fa_bwd calls: ALGO_SPLIT (dK/dV kernel + dQ kernel, no
-    atomics) or ALGO_FUSED (one kernel, fp32 dQ accumulator, ordered when deterministic)."""
+    atomics), ALGO_FUSED (one kernel, fp32 dQ accumulator, ordered when deterministic) or
+    ALGO_AUTO (the default: split for deterministic batched bf16 square causal calls, fused
+    otherwise)."""
     _check(load().fa_bwd_set_algorithm(int(algo)), "fa_bwd_set_algorithm")
 
 
@@ -347,7 +351,8 @@ def bwd_blocksparse_workspace_size(B, H, Hk, Sq, Sk, D) -> int:
 
 
 def fa_bwd_blocksparse(dout, q, k, v, out, lse, dq, dk, dv, block_mask, softmax_scale, causal=False,
-                       window_left=-1, window_right=-1, softcap=0.0, workspace=None, stream=None):
+                       window_left=-1, window_right=-1, softcap=0.0, workspace=None, stream=None,
+                       deterministic=False):
     """C call `fa_bwd_blocksparse` (dq, dk, dv written in place).  Returns the workspace."""
     lib = load()
     if workspace is None:
@@ -357,7 +362,7 @@ def fa_bwd_blocksparse(dout, q, k, v, out, lse, dq, dk, dv, block_mask, softmax_
     tv = [tensor_view(x) for x in (dout, q, k, v, out, lse, dq, dk, dv)]
     st = lib.fa_bwd_blocksparse(*[ctypes.byref(x) for x in tv], _block_mask_ptr(block_mask, q, k),
                                 float(softmax_scale), int(bool(causal)), int(window_left),
-                                int(window_right), float(softcap),
+                                int(window_right), float(softcap), int(bool(deterministic)),
                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                                 _stream_ptr(stream))
     _check(st, "fa_bwd_blocksparse")

@@ -28,7 +28,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // must run out and report FA_ERR_DEVICE_TIMEOUT).
 long long g_wait_limit = 2000000000ll;
 int g_poison_first_counter = 0;
-int g_bwd_algorithm = FA_BWD_ALGO_FUSED;
+int g_bwd_algorithm = FA_BWD_ALGO_AUTO;
 
 // Optional timing of the three backward kernels: events recorded on the caller's stream
 // before the preprocess, before and after the main kernel and after the convert.  The
@@ -98,11 +98,14 @@ bool bwd_layout_wide(int B, int H, int Sq, int D, BwdLayout* L) {
   L->off_dsum = off;
   off = align_up(off + rows * 4, 256);
   L->off_accum = off;
-  const size_t accum = (size_t)B * H * (size_t)((Sq + 63) / 64) * (size_t)((L->Dp + 127) / 128) * 32768u;
+  const size_t blocks = (size_t)B * H * (size_t)((Sq + 63) / 64) * (size_t)((L->Dp + 127) / 128);
+  const size_t accum = blocks * 32768u;
   off += accum;
   L->off_sems = off;
+  const size_t sems = align_up(blocks * 4, 16);  // ordering counters (deterministic mode)
+  off += sems;
   L->accum_bytes = accum;
-  L->sems_bytes = 0;
+  L->sems_bytes = sems;
   L->total = align_up(off, 256);
   return true;
 }
@@ -494,14 +497,14 @@ size_t fa_bwd_workspace_size_dv(int B, int H, int Hk, int Sq, int Sk, int D, int
 }
 
 // The backward for head dims above 128 or Dv != D: preprocess (D over Dv columns), the
-// wide main kernel, and the convert of its transposed dQ blocks.  Batched, dense,
-// non-deterministic calls (the caller has checked that).
+// wide main kernel, and the convert of its transposed dQ blocks.  Batched, dense calls
+// (the caller has checked that).
 static int bwd_wide(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k,
                     const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse, fa_tensor* dq,
                     fa_tensor* dk, fa_tensor* dv, int B, int H, int Hk, int Sq, int Sk, int D,
                     int Dv, bool f16, float softmax_scale, int causal, int window_left,
-                    int window_right, float softcap, void* workspace, size_t workspace_bytes,
-                    cudaStream_t s) {
+                    int window_right, float softcap, int deterministic, void* workspace,
+                    size_t workspace_bytes, cudaStream_t s) {
   BwdLayout L;
   if (!bwd_layout_wide(B, H, Sq, D, &L)) return FA_ERR_SHAPE;
   if (!workspace || workspace_bytes < L.total) return FA_ERR_WORKSPACE;
@@ -521,11 +524,18 @@ static int bwd_wide(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* 
   pre.B = B; pre.H = H; pre.Sq = Sq; pre.Sq_r = L.Sq_r; pre.D = Dv;
   pre.lse2 = (float*)(ws + L.off_lse2);
   pre.dsum = (float*)(ws + L.off_dsum);
+  // the accumulator and the counters are adjacent and cleared together
   pre.zero_ptr = (float4*)(ws + L.off_accum);
-  pre.zero_count = (int64_t)(L.accum_bytes / 16);
+  pre.zero_count = (int64_t)((L.accum_bytes + L.sems_bytes) / 16);
   pre.header = (int*)ws;
   prof_record(0, s);
   if (launch_bwd_preprocess(pre, f16, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (g_poison_first_counter && deterministic) {
+    const int poison = -1000000;
+    if (cudaMemcpyAsync(ws + L.off_sems, &poison, sizeof(int), cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+  }
 
   WideParams w;
   memset(&w, 0, sizeof(w));
@@ -552,6 +562,9 @@ static int bwd_wide(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* 
   w.dq_sb = dq->stride[0]; w.dq_ss = dq->stride[1]; w.dq_sh = dq->stride[2];
   w.status = (int*)ws + WS_STATUS;
   w.wait_limit = g_wait_limit;
+  w.deterministic = deterministic ? 1 : 0;
+  w.ticket = (int*)ws + WS_TICKET;
+  w.sems = (int*)(ws + L.off_sems);
   prof_record(1, s);
   if (Sk > 0) {
     CUtensorMap mq, mk, mv, mdo;
@@ -583,21 +596,28 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
   if ((st = check_h16_4d(dk, dt, B, Sk, Hk, D))) return st;
   if ((st = check_h16_4d(dv, dt, B, Sk, Hk, Dv))) return st;
   const bool f16 = dt == FA_DTYPE_F16;
+  // The algorithm of this call.  AUTO: the split algorithm for deterministic batched bf16
+  // calls on a square causal shape (no waits; the fused ordered mode must claim the short
+  // key tiles first there), the fused one otherwise.
+  int algo = g_bwd_algorithm;
+  if (algo == FA_BWD_ALGO_AUTO) {
+    const bool square_causal = (causal || window_right == 0) && window_left < 0 && Sq == Sk;
+    algo = (deterministic && !f16 && !vl && !block_mask && square_causal) ? FA_BWD_ALGO_SPLIT
+                                                                         : FA_BWD_ALGO_FUSED;
+  }
   if (is_wide(D, Dv)) {
-    // the wide kernels: batched, dense and non-deterministic only, whichever algorithm is
-    // selected
-    if (vl || block_mask || deterministic) return FA_ERR_UNSUPPORTED;
+    // the wide kernels: batched and dense calls only, whichever algorithm is selected
+    if (vl || block_mask) return FA_ERR_UNSUPPORTED;
     if ((st = check_lse(lse, B, H, Sq))) return st;
     if ((st = check_scalars(softmax_scale, softcap))) return st;
     if (B == 0 || Sq == 0) return FA_OK;
     return bwd_wide(dout, q, k, v, out, lse, dq, dk, dv, B, H, Hk, Sq, Sk, D, Dv, f16,
-                    softmax_scale, causal, window_left, window_right, softcap, workspace,
-                    workspace_bytes, (cudaStream_t)stream);
+                    softmax_scale, causal, window_left, window_right, softcap, deterministic,
+                    workspace, workspace_bytes, (cudaStream_t)stream);
   }
   // the split algorithm is built for batched dense bf16 only; block sparsity has no ordered
   // (deterministic) mode
-  if ((f16 || vl || block_mask) && g_bwd_algorithm == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;
-  if (block_mask && deterministic) return FA_ERR_UNSUPPORTED;
+  if ((f16 || vl || block_mask) && algo == FA_BWD_ALGO_SPLIT) return FA_ERR_UNSUPPORTED;
   if ((st = check_lse(lse, B, H, Sq))) return st;
   if ((st = check_scalars(softmax_scale, softcap))) return st;
   const int total_q = Sq, total_k = Sk;  // packed: the row extents of the views
@@ -639,7 +659,7 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
   const int Dp = L.Dp;
   // The split algorithm needs key tiles to build its tensor maps; with Sk == 0 (every dQ
   // row is zero, dK/dV are empty) the fused path's convert writes the zero dQ.
-  const bool split = g_bwd_algorithm == FA_BWD_ALGO_SPLIT && Sk > 0;
+  const bool split = algo == FA_BWD_ALGO_SPLIT && Sk > 0;
 
   BwdPreParams pre;
   memset(&pre, 0, sizeof(pre));
@@ -748,9 +768,11 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
       sp.lists = (int*)(ws + off_sp_lists);
       sp.stride = (long long)(H / Hk) * L.Mb;
       sp.num_tiles = num_ctas;
+      sp.deterministic = deterministic ? 1 : 0;
       if (launch_bwd_sparse_lists(sp, s) != cudaSuccess) return FA_ERR_CUDA;
       p.sp_counts = sp.counts;
       p.sp_lists = sp.lists;
+      p.block_mask = block_mask;
       p.sp_stride = sp.stride;
     }
     const int mode = vl ? 1 : (block_mask ? 2 : 0);
@@ -800,11 +822,12 @@ int fa_bwd_blocksparse(const fa_tensor* dout, const fa_tensor* q, const fa_tenso
                        const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
                        fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, const uint8_t* block_mask,
                        float softmax_scale, int causal, int window_left, int window_right,
-                       float softcap, void* workspace, size_t workspace_bytes, void* stream) {
+                       float softcap, int deterministic, void* workspace, size_t workspace_bytes,
+                       void* stream) {
   if (!block_mask) return FA_ERR_NULL;
   return bwd_common(dout, q, k, v, out, lse, dq, dk, dv, softmax_scale, causal, window_left,
-                    window_right, softcap, 0, workspace, workspace_bytes, stream, nullptr,
-                    block_mask);
+                    window_right, softcap, deterministic, workspace, workspace_bytes, stream,
+                    nullptr, block_mask);
 }
 
 size_t fa_bwd_varlen_workspace_size(int batch, int H, int total_q, int D, int deterministic) {
@@ -854,7 +877,9 @@ int fa_bwd_status(void* workspace, void* stream, int* device_status) {
 }
 
 int fa_bwd_set_algorithm(int algorithm) {
-  if (algorithm != FA_BWD_ALGO_SPLIT && algorithm != FA_BWD_ALGO_FUSED) return FA_ERR_ARG;
+  if (algorithm != FA_BWD_ALGO_SPLIT && algorithm != FA_BWD_ALGO_FUSED &&
+      algorithm != FA_BWD_ALGO_AUTO)
+    return FA_ERR_ARG;
   g_bwd_algorithm = algorithm;
   return FA_OK;
 }

@@ -248,7 +248,8 @@ namespace fa {
 namespace {
 
 // Block-sparse step lists: warp t handles key-tile ticket t (the main kernel's
-// key-tile-major order: n = t / (B Hk), then b, then hk).  Its candidate steps are the
+// key-tile-major order: n = t / (B Hk), or Nb - 1 - t / (B Hk) in the ordered mode, then
+// b, then hk).  Its candidate steps are the
 // main kernel's dense sequence — q-head g of the group outer, query tile m in the
 // element mask's range inner — and it keeps those whose block-mask byte
 // block_mask[b, hk*G + g, m, n] is set, compacted in order with warp ballots.
@@ -257,8 +258,9 @@ __global__ void __launch_bounds__(256) bwd_sparse_lists_kernel(const BwdSparsePa
   const int lane = threadIdx.x & 31;
   if (t >= p.num_tiles) return;
   const int per_n = p.B * p.Hk;
-  const int n = t / per_n;
-  const int r = t - n * per_n;
+  const int n0 = t / per_n;
+  const int n = p.deterministic ? p.Nb - 1 - n0 : n0;
+  const int r = t - n0 * per_n;
   const int b = r / p.Hk;
   const int hk = r - b * p.Hk;
   MaskGeom gm;

@@ -791,6 +791,60 @@ __global__ void __launch_bounds__(512, 1)
         alive = __shfl_sync(0xffffffffu, alive, 0);
       }
      }
+    } else {
+     // Block-sparse steps: the contributors of a query tile are the key tiles in its
+     // element-mask range that the block mask keeps, and this key tile's rank is the
+     // number of kept ones above it (counted by the whole warp with a ballot sum; the
+     // list builder and the scheduler give key tiles out highest first, as above).
+     if (p.deterministic) {
+      volatile int* s_turn = reinterpret_cast<volatile int*>(small + SM_TILE + 8);
+      int git = 0;
+      bool alive = true;
+      for (int t = 0; alive; ++t) {
+        TileDesc d;
+        const bool have_tile = __all_sync(0xffffffffu, read_tile(t, d));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TILEE0 + (t & 1)));
+        if (!have_tile) break;
+        for (int it = 0; alive && it < d.total; ++it, ++git) {
+          const int e = p.sp_lists[(size_t)d.pad * p.sp_stride + it];
+          const int g = e >> 16;
+          const int m = e & 0xffff;
+          const int h = d.hk * p.G + g;
+          const size_t tile_id = ((size_t)d.b * p.H + h) * p.Mb + m;
+          int64_t nb, ne;
+          n_range(gm, m, &nb, &ne);
+          const uint8_t* brow = p.block_mask + tile_id * (size_t)p.Nb;
+          int cnt = 0;
+          for (int n2 = d.n + 1 + lane; n2 < (int)ne; n2 += 32) cnt += brow[n2] != 0;
+          const int want = __reduce_add_sync(0xffffffffu, cnt);
+          int stop = 0;
+          if (lane == 0) {
+            const int* sem = p.sems + tile_id;
+            if (git > 0 && !mbar_wait_ool(bar(B_TURNE), (git - 1) & 1, st, kTimeoutBase - 22)) {
+              stop = 2;  // the drain is gone: no turn to hand over
+            } else {
+              const long long t0 = clock64();
+              while (true) {
+                int cur;
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cur) : "l"(sem) : "memory");
+                if (cur == want) break;
+                if (*s_abort) { stop = 1; break; }
+                if (clock64() - t0 > p.wait_limit) {
+                  raise_timeout(st, kTimeoutBase - 21);
+                  stop = 1;
+                  break;
+                }
+              }
+              s_turn[git & 1] = stop;
+              mbar_arrive(bar(B_TURN));  // release: the drain that sees the phase sees s_turn
+            }
+          }
+          stop = __shfl_sync(0xffffffffu, stop, 0);
+          if (stop) alive = false;
+        }
+      }
+     }
     }
    }
   } else if (warp < 8) {

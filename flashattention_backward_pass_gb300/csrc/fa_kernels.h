@@ -78,6 +78,9 @@ struct BwdMainParams {
   const int* sp_counts;
   const int* sp_lists;
   long long sp_stride;
+  // and the (B, H, Mb, Nb) block mask itself: the ordered mode counts, for a step's query
+  // tile, the kept key tiles above this one
+  const uint8_t* block_mask;
 };
 
 // Builds the block-sparse step lists of the main kernel from a (B, H, Mb, Nb) block mask:
@@ -90,6 +93,7 @@ struct BwdSparseParams {
   int* lists;
   long long stride;    // G * Mb
   int num_tiles;
+  int deterministic;   // the main kernel's ticket order: highest key tile first
 };
 
 struct BwdConvParams {
@@ -171,6 +175,12 @@ struct WideParams {
   float scale;
   int* status;
   long long wait_limit;
+  // deterministic mode: tiles are claimed from *ticket highest key tile first, and the dQ
+  // partials of a block are added in descending key-tile order through sems (one counter
+  // per accumulator block)
+  int deterministic;
+  int* ticket;
+  int* sems;
 };
 
 // Tensor maps for one bf16 (B, S, H, D) operand: a 64-column 128B-swizzled box and,

@@ -17,7 +17,9 @@
 // moved only when a score passes it by more than 8 in log2 units, as in fa_fwd_tc.cu).
 // Tensor memory: S buffers [0, 128) and [128, 256), O [256, 256 + DPV).
 //
-// Backward (one CTA per (128-key tile, batch, kv-head, output slice)): slice s owns the
+// Backward (one CTA per (128-key tile, batch, kv-head, output slice); in the deterministic
+// mode the CTAs claim the tiles from a ticket counter, highest key tile first, and add the
+// dQ partials of a block from the highest key tile down): slice s owns the
 // dK / dQ columns [128 s, 128 s + 128) of DPK and the dV columns [128 s, 128 s + 128) of
 // DPV; every slice recomputes the scores over the full head dims.  Per (q-head of the
 // group, 64-query block):
@@ -392,7 +394,7 @@ enum WBBar : int {
   WB_KV = 0, WB_QF, WB_QE, WB_DOF, WB_DOE, WB_SF, WB_DPF, WB_PF, WB_DSF, WB_DQF, WB_DQE,
   WB_DSE, WB_ACC, WB_DRAIN, WB_COUNT
 };
-constexpr uint32_t WB_TMEM = 512, WB_ABORT = 516, WB_LSE = 1024, WB_DSUM = 1536;
+constexpr uint32_t WB_TMEM = 512, WB_ABORT = 516, WB_TICKET = 520, WB_LSE = 1024, WB_DSUM = 1536;
 constexpr uint32_t WBT_DK = 0, WBT_DV = 128, WBT_S = 256, WBT_DP = 320, WBT_DQ = 384;
 
 }  // namespace
@@ -416,25 +418,11 @@ __global__ void __launch_bounds__(512, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + 8u * (uint32_t)i; };
   const WideBwdGeo geo = wide_bwd_geo(p.DPK, p.DPV);
 
-  // the tile: key-tile major (under causal masking the low key tiles see the most queries)
-  const int per_n = p.B * p.Hk * p.nslice;
-  const int n = (int)(blockIdx.x / (unsigned)per_n);
-  int rem = (int)(blockIdx.x % (unsigned)per_n);
-  const int s = rem % p.nslice;
-  rem /= p.nslice;
-  const int hk = rem % p.Hk;
-  const int b = rem / p.Hk;
-  const int kcols = min(max(p.DPK - 128 * s, 0), 128);  // dK / dQ columns of this slice
-  const int vcols = min(max(p.DPV - 128 * s, 0), 128);  // dV columns of this slice
-  MaskGeom gm;  // 64-query blocks x 128-key tiles
-  gm.Sq = p.Sq; gm.Sk = p.Sk; gm.lo = p.lo64; gm.hi = p.hi64;
-  gm.tm = 64; gm.tn = 128; gm.Mb = p.Mb; gm.Nb = p.Nb;
-  int64_t mb64 = 0, me64 = 0;
-  m_range(gm, n, &mb64, &me64);
-  const int m_begin = (int)mb64, m_count = (int)(me64 - mb64);
-  const int total = m_count * p.G;  // steps (g, m), m fastest
-
   if (threadIdx.x == 0) {
+    // the tile index: the block index, or in the ordered mode a ticket, so that every key
+    // tile whose dQ partials this one must wait for was claimed by a CTA already running
+    *reinterpret_cast<volatile int*>(smem_raw + WB_TICKET) =
+        p.deterministic ? atomicAdd(p.ticket, 1) : (int)blockIdx.x;
     *s_abort = 0;
     if ((sbase & 1023u) != 0) {
       atomicExch(p.status, kWideTimeout - 98);
@@ -455,6 +443,28 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem_raw + WB_TMEM);
   AbortState st{s_abort, p.status, p.wait_limit};
+
+  // the tile: key-tile major (under causal masking the low key tiles see the most queries;
+  // in the ordered mode the highest key tile comes first, since dQ partials are added from
+  // the highest key tile down), then batch, kv-head, slice
+  const int tix = *reinterpret_cast<volatile int*>(smem_raw + WB_TICKET);
+  const int per_n = p.B * p.Hk * p.nslice;
+  const int n0t = tix / per_n;
+  const int n = p.deterministic ? p.Nb - 1 - n0t : n0t;
+  int rem = tix - n0t * per_n;
+  const int s = rem % p.nslice;
+  rem /= p.nslice;
+  const int hk = rem % p.Hk;
+  const int b = rem / p.Hk;
+  const int kcols = min(max(p.DPK - 128 * s, 0), 128);  // dK / dQ columns of this slice
+  const int vcols = min(max(p.DPV - 128 * s, 0), 128);  // dV columns of this slice
+  MaskGeom gm;  // 64-query blocks x 128-key tiles
+  gm.Sq = p.Sq; gm.Sk = p.Sk; gm.lo = p.lo64; gm.hi = p.hi64;
+  gm.tm = 64; gm.tn = 128; gm.Mb = p.Mb; gm.Nb = p.Nb;
+  int64_t mb64 = 0, me64 = 0;
+  m_range(gm, n, &mb64, &me64);
+  const int m_begin = (int)mb64, m_count = (int)(me64 - mb64);
+  const int total = m_count * p.G;  // steps (g, m), m fastest
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -600,6 +610,28 @@ __global__ void __launch_bounds__(512, 1)
         }
         const size_t blk = (((size_t)b * p.H + h) * p.Mb + mb) * (size_t)p.nks + s;
         float* dst = p.dq_accum + blk * 8192;
+        // ordered mode: the block takes this key tile's partial once every higher key tile
+        // that reaches it has added its own (its counter equals this tile's rank from the
+        // top); a wait that runs out stops the CTA
+        if (p.deterministic && threadIdx.x == 128 && ok) {
+          int64_t nb = 0, ne = 0;
+          n_range(gm, mb, &nb, &ne);
+          const int want = (int)ne - 1 - n;
+          const int* sem = p.sems + blk;
+          const long long t0 = clock64();
+          while (true) {
+            int cur;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(cur) : "l"(sem) : "memory");
+            if (cur == want) break;
+            if (*s_abort) break;
+            if (clock64() - t0 > p.wait_limit) {
+              raise_timeout(st, kWideTimeout - 21);
+              break;
+            }
+          }
+          // the bulk adds (async proxy) come after the acquire
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         // two halves of 64 rows each through the 16 KB staging buffer; every drain thread
         // reaches every named barrier
 #pragma unroll 1
@@ -619,6 +651,13 @@ __global__ void __launch_bounds__(512, 1)
             bulk_reduce_add_f32(dst + hf * 64 * 64, stg, 16384);
             bulk_commit();
           }
+        }
+        // ordered mode: hand the block on once the adds have landed
+        if (p.deterministic && threadIdx.x == 128 && *s_abort == 0) {
+          bulk_wait_all();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.sems + blk) : "memory");
         }
       }
     }

@@ -45,11 +45,16 @@ class Workload:
 
     @property
     def nominal_flops(self) -> float:
-        """Backward FLOPs by the stated convention: 10*B*H*Sq*Sk*D, halved when causal.
-        A window with window_right == 0 is causal (no key after the diagonal) and is
-        counted as such."""
-        f = 10.0 * self.B * self.H * self.Sq * self.Sk * self.D
+        """Backward FLOPs by the stated convention: 10*B*H*Sq*Sk*D, halved when causal
+        (with a v head dim of its own: 2*(3*D + 2*Dv) in place of 10*D).  A window with
+        window_right == 0 is causal (no key after the diagonal) and is counted as such."""
+        f = 2.0 * (3 * self.D + 2 * self.dv) * self.B * self.H * self.Sq * self.Sk
         return f / 2 if (self.causal or self.window_right == 0) else f
+
+    @property
+    def forward_flops(self) -> float:
+        """Forward FLOPs per visible pair: S = QK^T over D and O += PV over Dv."""
+        return 2.0 * (self.D + self.dv) * self.B * self.H * self.visible_pairs_per_head()
 
     def visible_pairs_per_head(self) -> int:
         """Number of (query, key) pairs the mask keeps (closed form per row)."""
@@ -91,6 +96,16 @@ WORKLOADS = {
 }
 
 HEADLINE = "gqa_causal"
+
+# Wider heads (the wide kernels): the headline's GQA causal shape with head dims 256 and
+# (192 for q / k, 128 for v).  Bench lines of their own; parity cases live in the tests.
+EXTRA_WORKLOADS = {
+    "gqa_causal_d256": Workload("gqa_causal_d256", 2, 2048, 2048, 16, 4, 256, causal=True,
+                                do_std=0.1, seed=5),
+    "gqa_causal_d192_dv128": Workload("gqa_causal_d192_dv128", 4, 2048, 2048, 32, 8, 192,
+                                      causal=True, do_std=0.1, seed=6, Dv=128),
+}
+ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 
 
 def make_inputs(w: Workload, device="cpu", seed: int | None = None, dtype=torch.bfloat16):

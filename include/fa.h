@@ -33,9 +33,8 @@
  *     `head_dim` / `head_dim_v`); O, dO and dV then have Dv columns.  D % 8 == 0,
  *     Dv % 8 == 0, both <= 256.  D == Dv <= 128 runs on the 128-wide kernels (padded
  *     inside to a multiple of 16); every other pair runs on the wide kernels (padded to
- *     a multiple of 64), which take batched, dense, non-deterministic calls only
- *     (packed sequences, block masks and deterministic == 1 return FA_ERR_UNSUPPORTED
- *     there).
+ *     a multiple of 64), which take batched, dense calls only (packed sequences and block
+ *     masks return FA_ERR_UNSUPPORTED there).
  *   - Other limits: H % Hk == 0; base pointers 16-byte aligned; every non-unit stride a
  *     multiple of 8 elements (16 bytes).
  */
@@ -206,12 +205,13 @@ int fa_bwd(const fa_tensor* dout, const fa_tensor* q, const fa_tensor* k, const 
  * +inf and dQ = 0, as elsewhere.  Forward and backward must get the same mask.
  *
  * fa_fwd_blocksparse: fa_fwd's arguments plus block_mask (NULL: FA_ERR_NULL).
- * fa_bwd_blocksparse: fa_bwd's arguments plus block_mask, without `deterministic` (the
- *   ordered dQ mode is not built for sparse step lists); the workspace must hold
+ * fa_bwd_blocksparse: fa_bwd's arguments plus block_mask; the workspace must hold
  *   fa_bwd_blocksparse_workspace_size bytes (fa_bwd's regions plus, per key tile, a list
  *   of its kept (q-head, query tile) steps); the fused algorithm only
  *   (FA_ERR_UNSUPPORTED while the split one is selected or for more than 65535 query
- *   tiles).
+ *   tiles).  deterministic != 0 adds the dQ contributions of the kept key tiles of a
+ *   query tile in descending key-tile order, as fa_bwd's ordered mode does (bitwise
+ *   reproducible).
  */
 int fa_fwd_blocksparse(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
                        fa_tensor* out, fa_tensor* lse, const uint8_t* block_mask,
@@ -222,7 +222,8 @@ int fa_bwd_blocksparse(const fa_tensor* dout, const fa_tensor* q, const fa_tenso
                        const fa_tensor* v, const fa_tensor* out, const fa_tensor* lse,
                        fa_tensor* dq, fa_tensor* dk, fa_tensor* dv, const uint8_t* block_mask,
                        float softmax_scale, int causal, int window_left, int window_right,
-                       float softcap, void* workspace, size_t workspace_bytes, void* stream);
+                       float softcap, int deterministic, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /*
  * Workspace of fa_bwd_varlen, in bytes: per q-head, total_q / 128 + batch tiles of 128
@@ -304,9 +305,20 @@ int fa_bwd_noalloc_status(void* stream, int* device_status);
  * Backward algorithm for later fa_bwd calls in this process (not thread-safe).
  * fa_bwd_set_algorithm returns FA_ERR_ARG for an unknown value; fa_bwd_get_algorithm
  * returns the current one.
+ *   FA_BWD_ALGO_AUTO (default): the fused algorithm, except for deterministic batched
+ *     bf16 calls without a block mask on a square causal shape (Sq == Sk, causal, no left
+ *     window), which run the split algorithm: there it needs no waits, while the fused
+ *     ordered mode must claim the shortest key tiles first.  Both results are bitwise
+ *     reproducible, but they are not the same bits, so on those shapes a deterministic
+ *     batched call no longer matches the fused ordered mode (which fa_bwd_varlen always
+ *     uses) bit for bit; select FA_BWD_ALGO_FUSED for that.
+ *   FA_BWD_ALGO_FUSED / FA_BWD_ALGO_SPLIT: always that algorithm (the split one refuses
+ *     f16, packed sequences and block masks with FA_ERR_UNSUPPORTED).
+ * Wide head dims (D > 128 or Dv != D) have a kernel of their own whatever is selected.
  */
 #define FA_BWD_ALGO_SPLIT 0
 #define FA_BWD_ALGO_FUSED 1
+#define FA_BWD_ALGO_AUTO 2
 int fa_bwd_set_algorithm(int algorithm);
 int fa_bwd_get_algorithm(void);
 

@@ -51,4 +51,4 @@ def algorithm_fixture_body(request):
     _abi.load()
     _abi.set_algorithm(request.param)
     yield request.param
-    _abi.set_algorithm(_abi.ALGO_FUSED)
+    _abi.set_algorithm(_abi.ALGO_AUTO)

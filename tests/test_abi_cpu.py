@@ -117,7 +117,7 @@ def test_f16_validation(lib):
     try:
         assert _call_bwd(lib, _f16_args()) == -8                         # FA_ERR_UNSUPPORTED
     finally:
-        assert lib.fa_bwd_set_algorithm(1) == 0
+        assert lib.fa_bwd_set_algorithm(2) == 0
 
 
 def test_empty_problems_launch_nothing(lib):
@@ -184,7 +184,7 @@ def test_varlen_validation(lib):
         assert lib.fa_bwd_varlen(*args, 4096, 4096, None, None, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
                                  ctypes.c_void_p(4096), 1 << 30, None) == -8
     finally:
-        assert lib.fa_bwd_set_algorithm(1) == 0
+        assert lib.fa_bwd_set_algorithm(2) == 0
     assert lib.fa_bwd_varlen(*args, 4096, 4096, None, None, 0, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
                              ctypes.c_void_p(4096), 1 << 30, None) == 0           # batch 0
     assert lib.fa_bwd_varlen(*args, 4096, 4096, None, None, 2, 100, 100, 0.125, 0, -1, -1, 0.0, 0,
@@ -204,17 +204,17 @@ def test_blocksparse_validation(lib):
     order = ("dout", "q", "k", "v", "out", "lse", "dq", "dk", "dv")
     ptrs = [ctypes.byref(a[n]) for n in order]
     # the block mask is required
-    assert lib.fa_bwd_blocksparse(*ptrs, None, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+    assert lib.fa_bwd_blocksparse(*ptrs, None, 0.125, 0, -1, -1, 0.0, 0, ctypes.c_void_p(4096),
                                   1 << 30, None) == -1
     fwd = [ctypes.byref(a[n]) for n in ("q", "k", "v", "out", "lse")]
     assert lib.fa_fwd_blocksparse(*fwd, None, 0.125, 0, -1, -1, 0.0, None, 0, None) == -1
     # split algorithm: refused before any launch
     assert lib.fa_bwd_set_algorithm(0) == 0
     try:
-        assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+        assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, 0, ctypes.c_void_p(4096),
                                       1 << 30, None) == -8
     finally:
-        assert lib.fa_bwd_set_algorithm(1) == 0
+        assert lib.fa_bwd_set_algorithm(2) == 0
     # workspace: fa_bwd's plus per key tile a count and G * Mb list entries
     f = lib.fa_bwd_blocksparse_workspace_size
     f.restype = ctypes.c_size_t
@@ -222,7 +222,7 @@ def test_blocksparse_validation(lib):
     g.restype = ctypes.c_size_t
     base = g(1, 2, 2, 128, 128, 64, 0)
     assert f(1, 2, 2, 128, 128, 64) == (((base + 2 * 4 + 255) // 256 * 256 + 2 * 1 * 1 * 4 + 255) // 256) * 256
-    assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+    assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, 0, ctypes.c_void_p(4096),
                                   base, None) == -7        # fa_bwd's size is not enough
 
 
@@ -288,8 +288,8 @@ def _dv_args(D=192, Dv=128, B=1, Sq=128, Sk=128, H=2, Hk=2):
 
 def test_own_v_head_dim_validation(lib):
     """A V head dim of its own (the sm90 page's head_dim_v): O, dO and dV follow v; every
-    dim a multiple of 8 and at most 256; the wide kernels take no deterministic mode, no
-    packed sequences and no block mask (refused before any launch)."""
+    dim a multiple of 8 and at most 256; the wide kernels take no packed sequences and no
+    block mask (refused before any launch)."""
     assert _call_bwd(lib, _dv_args(Sq=0)) == 0                           # valid, empty
     assert _call_bwd(lib, _dv_args(D=256, Dv=256, Sq=0)) == 0
     assert _call_bwd(lib, _dv_args(Dv=60)) == -4                         # Dv % 8
@@ -300,12 +300,10 @@ def test_own_v_head_dim_validation(lib):
     assert _call_bwd(lib, a) == -2                                       # O must have Dv
     a = _dv_args(); a["dq"] = _view((1, 128, 2, 128))
     assert _call_bwd(lib, a) == -2                                       # dQ must have D
-    assert _call_bwd(lib, _dv_args(), det=1) == -8                       # no ordered mode
-    assert _call_bwd(lib, _dv_args(D=192, Dv=192), det=1) == -8
     order = ("dout", "q", "k", "v", "out", "lse", "dq", "dk", "dv")
     a = _dv_args()
     ptrs = [ctypes.byref(a[n]) for n in order]
-    assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, ctypes.c_void_p(4096),
+    assert lib.fa_bwd_blocksparse(*ptrs, 4096, 0.125, 0, -1, -1, 0.0, 0, ctypes.c_void_p(4096),
                                   1 << 30, None) == -8
     fwd = [ctypes.byref(a[n]) for n in ("q", "k", "v", "out", "lse")]
     assert lib.fa_fwd_blocksparse(*fwd, 4096, 0.125, 0, -1, -1, 0.0, None, 0, None) == -8
@@ -317,8 +315,9 @@ def test_own_v_head_dim_validation(lib):
 
 
 def test_wide_workspace_size(lib):
-    """Wide head dims: LSE2 and D as before, and a dQ accumulator of (B, H, ceil(Sq/64),
-    ceil(pad64(D)/128)) blocks of 128 x 64 fp32; v's head dim does not change it."""
+    """Wide head dims: LSE2 and D as before, a dQ accumulator of (B, H, ceil(Sq/64),
+    ceil(pad64(D)/128)) blocks of 128 x 64 fp32 and one ordering counter per block; v's
+    head dim does not change it."""
     f = lib.fa_bwd_workspace_size_dv
     f.restype = ctypes.c_size_t
     B, H, Sq = 2, 3, 200
@@ -327,10 +326,24 @@ def test_wide_workspace_size(lib):
     lse2_end = (256 + rows * 4 + 255) // 256 * 256
     dsum_end = (lse2_end + rows * 4 + 255) // 256 * 256
     for D, nks in ((192, 2), (256, 2), (128, 1), (72, 1)):
-        want = dsum_end + B * H * 4 * nks * 32768
+        blocks = B * H * 4 * nks
+        want = dsum_end + blocks * 32768 + (blocks * 4 + 15) // 16 * 16   # + ordering counters
         want = (want + 255) // 256 * 256
         assert f(B, H, 1, Sq, 77, D, 64 if D != 64 else 128, 0) == want, D
     g = lib.fa_bwd_workspace_size
     g.restype = ctypes.c_size_t
     assert g(B, H, 1, Sq, 77, 256, 0) == f(B, H, 1, Sq, 77, 256, 256, 0)
     assert g(B, H, 1, Sq, 77, 128, 0) == f(B, H, 1, Sq, 77, 128, 128, 0)
+
+
+def test_algorithm_selection(lib):
+    """AUTO (2) is the default; 0, 1 and 2 are accepted, anything else is FA_ERR_ARG."""
+    assert lib.fa_bwd_get_algorithm() == 2
+    try:
+        for a in (0, 1, 2):
+            assert lib.fa_bwd_set_algorithm(a) == 0
+            assert lib.fa_bwd_get_algorithm() == a
+        assert lib.fa_bwd_set_algorithm(3) == -9
+        assert lib.fa_bwd_set_algorithm(-1) == -9
+    finally:
+        lib.fa_bwd_set_algorithm(2)

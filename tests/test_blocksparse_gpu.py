@@ -27,7 +27,8 @@ def fa():
     from flashattention_backward_pass_gb300 import _abi
     fa.load()
     _abi.set_algorithm(_abi.ALGO_FUSED)
-    return fa
+    yield fa
+    _abi.set_algorithm(_abi.ALGO_AUTO)
 
 
 CASES = [
@@ -38,7 +39,7 @@ CASES = [
 ]
 
 
-def run(fa, w, bm_cpu):
+def run(fa, w, bm_cpu, deterministic=False):
     q, k, v, do = make_inputs(w, "cuda")
     bm = bm_cpu.cuda()
     kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right,
@@ -47,7 +48,8 @@ def run(fa, w, bm_cpu):
     lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device="cuda")
     fa.fa_fwd_blocksparse(q, k, v, out, lse, bm, w.scale, **kw)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = fa.fa_bwd_blocksparse(do, q, k, v, out, lse, dq, dk, dv, bm, w.scale, **kw)
+    ws = fa.fa_bwd_blocksparse(do, q, k, v, out, lse, dq, dk, dv, bm, w.scale,
+                               deterministic=deterministic, **kw)
     torch.cuda.synchronize()
     assert fa.fa_bwd_status(ws) == 0
     return (q, k, v, do), (out, lse, dq, dk, dv), kw
@@ -66,14 +68,42 @@ def compare(w, bm_cpu, tensors, gpu, kw):
     check_close(w.name + " dV", to64(dv), dv_ref)
 
 
+@pytest.mark.parametrize("det", [False, True], ids=["unordered", "ordered"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0].name for c in CASES])
-def test_blocksparse_matches_oracle(fa, case):
+def test_blocksparse_matches_oracle(fa, case, det):
     w, density = case
     bm = make_block_mask(w.B, w.H, w.Sq, w.Sk, density, seed=w.seed)
     bm[0, 0, 0, :] = 0     # a query tile with no key tile at all
     bm[0, -1, :, -1] = 0   # a key tile no query tile of that head visits
-    tensors, gpu, kw = run(fa, w, bm)
+    tensors, gpu, kw = run(fa, w, bm, deterministic=det)
     compare(w, bm, tensors, gpu, kw)
+
+
+def test_blocksparse_deterministic_bitwise(fa):
+    """Ordered mode on step lists: ten runs, identical bits."""
+    w, density = CASES[1]
+    bm = make_block_mask(w.B, w.H, w.Sq, w.Sk, density, seed=w.seed + 100)
+    _, first, _ = run(fa, w, bm, deterministic=True)
+    first = [x.view(torch.int16).clone() for x in first[2:]]
+    for _ in range(9):
+        _, again, _ = run(fa, w, bm, deterministic=True)
+        for a, b in zip(first, again[2:]):
+            assert torch.equal(a, b.view(torch.int16))
+
+
+def test_blocksparse_all_kept_ordered_equals_dense_ordered(fa):
+    """With every tile pair kept the step lists are the dense steps in the dense order, so
+    the ordered sparse backward gives the fused ordered dense backward's bits."""
+    from flashattention_backward_pass_gb300 import _abi
+    w = custom("bs_all_ordered", 2, 384, 520, 4, 2, 64, causal=True, seed=65)
+    ones = make_block_mask(w.B, w.H, w.Sq, w.Sk, 1.0)
+    tensors, gpu, kw = run(fa, w, ones, deterministic=True)
+    q, k, v, do = tensors
+    _abi.set_algorithm(_abi.ALGO_FUSED)
+    ref = fa.attention_backward(do, q, k, v, gpu[0], gpu[1], w.scale, deterministic=True, **kw)
+    torch.cuda.synchronize()
+    for a, b in zip(gpu[2:], ref):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 def test_blocksparse_all_and_nothing(fa):

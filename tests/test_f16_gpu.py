@@ -28,7 +28,8 @@ def fa():
     from flashattention_backward_pass_gb300 import _abi
     fa.load()
     _abi.set_algorithm(_abi.ALGO_FUSED)
-    return fa
+    yield fa
+    _abi.set_algorithm(_abi.ALGO_AUTO)
 
 
 def run_f16(fa, w, deterministic=False):

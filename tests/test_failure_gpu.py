@@ -22,6 +22,7 @@ def fa():
     yield fa
     _abi.poison_ordering(False)
     _abi.set_wait_limit(2_000_000_000)
+    _abi.set_algorithm(_abi.ALGO_AUTO)
 
 
 def test_ordered_wait_times_out_and_recovers(fa):

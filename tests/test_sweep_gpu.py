@@ -66,7 +66,7 @@ def test_sweep(fa, w, algo):
         torch.cuda.synchronize()
         assert fa.fa_bwd_status(ws) == 0
     finally:
-        _abi.set_algorithm(_abi.ALGO_FUSED)
+        _abi.set_algorithm(_abi.ALGO_AUTO)
     qs, ks, vs, dos = (to64(t) for t in (q, k, v, do))
     o_ref, lse_ref = attention_forward(qs, ks, vs, w.scale, **kw)
     dq_ref, dk_ref, dv_ref = attention_backward(dos, qs, ks, vs, w.scale, **kw)

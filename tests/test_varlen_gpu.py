@@ -29,7 +29,8 @@ def fa():
     from flashattention_backward_pass_gb300 import _abi
     fa.load()
     _abi.set_algorithm(_abi.ALGO_FUSED)
-    return fa
+    yield fa
+    _abi.set_algorithm(_abi.ALGO_AUTO)
 
 
 CASES = [

@@ -88,3 +88,60 @@ def test_wide_twice_same_workspace(fa):
     torch.cuda.synchronize()
     for a, b in zip(first, second):
         check_close("twice", to64(b), to64(a), rel=1e-2, abs_=1e-3)
+
+
+@pytest.mark.parametrize("w", [CASES[0], CASES[2], CASES[6]], ids=[CASES[i].name for i in (0, 2, 6)])
+def test_wide_deterministic(fa, w):
+    """The ordered mode of the wide backward: oracle parity, and ten runs with identical
+    bits."""
+    q, k, v, do = make_inputs(w, "cuda")
+    kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right,
+              softcap=w.softcap)
+    out, lse = fa.attention_forward(q, k, v, w.scale, **kw)
+    ws = fa.alloc_bwd_workspace(q, k, True, v)
+    first = None
+    for _ in range(10):
+        res = fa.attention_backward(do, q, k, v, out, lse, w.scale, deterministic=True,
+                                    workspace=ws, **kw)
+        torch.cuda.synchronize()
+        assert fa.fa_bwd_status(ws) == 0
+        bits = [x.view(torch.int16).clone() for x in res]
+        if first is None:
+            first = bits
+            dq_ref, dk_ref, dv_ref = attention_backward(to64(do), to64(q), to64(k), to64(v),
+                                                        w.scale, **kw)
+            check_close(w.name + " det dQ", to64(res[0]), dq_ref)
+            check_close(w.name + " det dK", to64(res[1]), dk_ref)
+            check_close(w.name + " det dV", to64(res[2]), dv_ref)
+        else:
+            for a, b in zip(first, bits):
+                assert torch.equal(a, b)
+
+
+def test_wide_ordered_wait_times_out_and_recovers(fa):
+    """A poisoned ordering counter makes the wide kernel's bounded wait run out: the status
+    word reports it, and a clean call afterwards is correct."""
+    from flashattention_backward_pass_gb300 import _abi
+    w = custom("wide_poison", 1, 256, 256, 2, 1, 192, causal=True, seed=86)
+    q, k, v, do = make_inputs(w, "cuda")
+    out, lse = fa.attention_forward(q, k, v, w.scale, True)
+    ws = fa.alloc_bwd_workspace(q, k, True, v)
+    _abi.set_wait_limit(20_000_000)        # ~10 ms per wait
+    _abi.poison_ordering(True)
+    try:
+        fa.attention_backward(do, q, k, v, out, lse, w.scale, True, deterministic=True, workspace=ws)
+        torch.cuda.synchronize()
+        status = fa.fa_bwd_status(ws)
+    finally:
+        _abi.poison_ordering(False)
+        _abi.set_wait_limit(2_000_000_000)
+    assert status != 0
+    dq, dk, dv = fa.attention_backward(do, q, k, v, out, lse, w.scale, True, deterministic=True,
+                                       workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.fa_bwd_status(ws) == 0
+    dq_ref, dk_ref, dv_ref = attention_backward(to64(do), to64(q), to64(k), to64(v), w.scale,
+                                                causal=True)
+    check_close("wide recovered dQ", to64(dq), dq_ref)
+    check_close("wide recovered dK", to64(dk), dk_ref)
+    check_close("wide recovered dV", to64(dv), dv_ref)

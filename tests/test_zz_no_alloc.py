@@ -78,22 +78,25 @@ def test_noalloc_timeout_is_readable(fa):
     w = custom("noalloc_poison", 1, 384, 384, 2, 2, 64, causal=True, seed=43)
     q, k, v, do = make_inputs(w, "cuda")
     out, lse = fa.attention_forward(q, k, v, w.scale, True)
-    ref = fa.attention_backward(do, q, k, v, out, lse, w.scale, True, deterministic=True)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    _abi.set_algorithm(_abi.ALGO_FUSED)
-    _abi.set_wait_limit(20_000_000)        # ~10 ms per wait
-    _abi.poison_ordering(True)
+    _abi.set_algorithm(_abi.ALGO_FUSED)    # the ordered dQ wait belongs to the fused path
     try:
+        ref = fa.attention_backward(do, q, k, v, out, lse, w.scale, True, deterministic=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        _abi.set_wait_limit(20_000_000)        # ~10 ms per wait
+        _abi.poison_ordering(True)
+        try:
+            _abi.fa_bwd_noalloc(do, q, k, v, out, lse, dq, dk, dv, w.scale, True, deterministic=True)
+            torch.cuda.synchronize()
+            status = _abi.fa_bwd_noalloc_status()
+        finally:
+            _abi.poison_ordering(False)
+            _abi.set_wait_limit(2_000_000_000)
+        assert status != 0, "the poisoned ordered wait should have reported a timeout"
+        assert _abi.fa_bwd_noalloc_status() == 0   # read and cleared
         _abi.fa_bwd_noalloc(do, q, k, v, out, lse, dq, dk, dv, w.scale, True, deterministic=True)
         torch.cuda.synchronize()
-        status = _abi.fa_bwd_noalloc_status()
     finally:
-        _abi.poison_ordering(False)
-        _abi.set_wait_limit(2_000_000_000)
-    assert status != 0, "the poisoned ordered wait should have reported a timeout"
-    assert _abi.fa_bwd_noalloc_status() == 0   # read and cleared
-    _abi.fa_bwd_noalloc(do, q, k, v, out, lse, dq, dk, dv, w.scale, True, deterministic=True)
-    torch.cuda.synchronize()
+        _abi.set_algorithm(_abi.ALGO_AUTO)
     assert _abi.fa_bwd_noalloc_status() == 0
     for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert torch.equal(got.view(torch.int16), want.view(torch.int16)), name
