@@ -134,12 +134,18 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def _kernel_source_hash():
-    """Hash of the main kernel's sources with comments and whitespace removed, so that the
-    committed DRAM-traffic capture stays valid across comment-only edits."""
+KERNEL_SOURCES = {
+    "fa_bwd_main": ("fa_bwd_main.cu", "fa_bwd_common.cuh", "fa_ptx.cuh", "fa_kernels.h", "fa_tiles.h"),
+    "fa_bwd_wide": ("fa_wide.cu", "fa_bwd_common.cuh", "fa_ptx.cuh", "fa_kernels.h", "fa_tiles.h"),
+}
+
+
+def _kernel_source_hash(kernel="fa_bwd_main"):
+    """Hash of a backward kernel's sources with comments and whitespace removed, so that
+    the committed DRAM-traffic capture stays valid across comment-only edits."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flashattention_backward_pass_gb300", "csrc")
-    for f in ("fa_bwd_main.cu", "fa_bwd_common.cuh", "fa_ptx.cuh", "fa_kernels.h", "fa_tiles.h"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f)) as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -148,14 +154,14 @@ def _kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def _traffic(workload):
+def _traffic(workload, kernel="fa_bwd_main"):
     """DRAM bytes per main-kernel launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", f"fa_bwd_main.{workload}.traffic.json")
+    p = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        if d.get("kernel_source_hash") == _kernel_source_hash():
+        if d.get("kernel_source_hash") == _kernel_source_hash(kernel):
             return d.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -229,9 +235,9 @@ def run_ours(args, ws_, rank, local):
     import torch
     import flashattention_backward_pass_gb300 as fa
     from flashattention_backward_pass_gb300 import _abi
-    from flashattention_backward_pass_gb300.workloads import WORKLOADS, make_inputs
+    from flashattention_backward_pass_gb300.workloads import ALL_WORKLOADS, make_inputs
 
-    w = WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     fa.load()
@@ -239,7 +245,7 @@ def run_ours(args, ws_, rank, local):
     out, lse = fa.attention_forward(q, k, v, w.scale, w.causal, w.window_left, w.window_right,
                                     w.softcap)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    wsp = fa.alloc_bwd_workspace(q, k, args.deterministic)
+    wsp = fa.alloc_bwd_workspace(q, k, args.deterministic, v)
     flush = L2Flush(dev)
     # The timed pass runs without the library's per-kernel events: an event between the
     # main and convert kernels would keep the convert kernel from starting on the SMs
@@ -381,6 +387,9 @@ def run_ours(args, ws_, rank, local):
     main_avg = statistics.mean(main_ms)
     achieved = w.algorithmic_flops / (main_avg * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
+    wide = w.D != w.dv or w.D > 128
+    main_kernel = "fa::bwd_wide_kernel" if wide else "fa::bwd_main_kernel"
+    fwd_kernel = "fa::fwd_wide_kernel" if wide else "fa::fwd_tc_kernel"
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -389,24 +398,25 @@ def run_ours(args, ws_, rank, local):
         "config": dict(w.describe(), deterministic=bool(args.deterministic),
                        l2=L2_NOTE,
                        parallelism=f"replicas x{ws_}" if ws_ > 1 else "single GPU",
-                       flop_convention="10*B*H*Sq*Sk*D, halved for causal"),
+                       flop_convention="10*B*H*Sq*Sk*D (2*(3D+2Dv) for Dv != D), halved for causal"),
         "pct_of_bf16_peak": round(100 * value / ws_ / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic(args.workload), "kernel": "fa::bwd_main_kernel",
+                     "traffic": _traffic(args.workload, "fa_bwd_wide" if wide else "fa_bwd_main"),
+                     "kernel": main_kernel,
                      "flops_per_launch": w.algorithmic_flops,
                      "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4)},
         "kernel_ms": {"preprocess": round(statistics.mean(pre_ms), 4), "main": round(main_avg, 4),
                       "convert": round(statistics.mean(conv_ms), 4)},
-        "forward": {"kernel": "fa::fwd_tc_kernel", "ms": round(statistics.median(fwd_ms), 4),
-                    "flops_per_launch": 0.4 * w.algorithmic_flops,
-                    "achieved_tflops": round(0.4 * w.algorithmic_flops
+        "forward": {"kernel": fwd_kernel, "ms": round(statistics.median(fwd_ms), 4),
+                    "flops_per_launch": w.forward_flops,
+                    "achieved_tflops": round(w.forward_flops
                                              / (statistics.median(fwd_ms) * 1e-3) / 1e12, 2),
-                    "frac_of_peak": round(0.4 * w.algorithmic_flops
+                    "frac_of_peak": round(w.forward_flops
                                           / (statistics.median(fwd_ms) * 1e-3) / 1e12 / peak, 4),
-                    "note": "fa_fwd (O, LSE) timed alone between L2 flushes; 4*D flops per "
-                            "visible pair; not part of the timed step"},
+                    "note": "fa_fwd (O, LSE) timed alone between L2 flushes; 2*(D + Dv) flops "
+                            "per visible pair; not part of the timed step"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "e2e": e2e,
@@ -450,8 +460,8 @@ def cpu_baseline(w, budget_s=15.0):
 
 
 def run_reference(args, ws_, rank):
-    from flashattention_backward_pass_gb300.workloads import WORKLOADS, make_inputs
-    w = WORKLOADS[args.workload]
+    from flashattention_backward_pass_gb300.workloads import ALL_WORKLOADS, make_inputs
+    w = ALL_WORKLOADS[args.workload]
     q, k, v, do = (t.float().numpy() for t in make_inputs(w, "cpu"))
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     for i in range(args.warmup):
@@ -633,7 +643,7 @@ def run_blocksparse(args, local):
         return sum(ms) / len(ms)
 
     t = timed(lambda: fa.fa_bwd_blocksparse(do, q, k, v, out, lse, dq, dk, dv, bm, w.scale,
-                                            workspace=wsp, **kw))
+                                            workspace=wsp, deterministic=args.deterministic, **kw))
     status = fa.fa_bwd_status(wsp)
     tf = timed(lambda: fa.fa_fwd_blocksparse(q, k, v, out, lse, bm, w.scale, **kw))
     peaks, _ = _peaks()
@@ -643,6 +653,7 @@ def run_blocksparse(args, local):
             "data": "synthetic (seeded N(0,1) bf16, seeded random tile mask)",
             "config": dict(w.describe(), workload=w.name + "+blocksparse",
                            block_density=args.block_density,
+                           deterministic=bool(args.deterministic),
                            kept_tile_pairs=int(bm_cpu.sum()),
                            l2=L2_NOTE,
                            flop_convention="10*D per visible (query, key) pair after both masks"),
@@ -657,7 +668,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gqa_causal")
+    ap.add_argument("--workload", default="gqa_causal",
+                    help="one of the five workloads (default: the GQA causal headline), or "
+                         "gqa_causal_d256 / gqa_causal_d192_dv128 (the wide kernels)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
