@@ -34,7 +34,9 @@
 // and the dQ partial is added into an fp32 accumulator with bulk reductions.  Tensor
 // memory: dK_s [0, 128), dV_s [128, 256), S^T [256, 320), dP^T [320, 384), dQ^T
 // [384, 448).  Shared memory at DPK = DPV = 256: K 64 KB, V 64 KB, Q 32 KB, dO 32 KB,
-// dS^T 16 KB and a 16 KB staging buffer, 227 KB in all, so Q and dO have one buffer each.
+// dS^T 16 KB and a 16 KB staging buffer, 227 KB in all, so Q and dO have one buffer each
+// there; where two fit (smaller head dims), Q and dO are double-buffered and the MMAs of
+// consecutive steps overlap.
 //
 // dQ accumulator layout: per (b, h, 64-query block, slice) one block of 128 head-dim rows
 // x 64 queries fp32 (32 KB); in row d, the 16-byte chunk of queries 4c..4c+3 sits at
@@ -372,6 +374,7 @@ namespace {
 
 struct WideBwdGeo {
   uint32_t off_k, off_v, off_q, off_do, off_ds, off_stg, total, kb, vb, qb, dob;
+  int nst;  // Q / dO stages: 2 when they fit in shared memory, else 1
 };
 
 __host__ __device__ inline WideBwdGeo wide_bwd_geo(int DPK, int DPV) {
@@ -383,17 +386,20 @@ __host__ __device__ inline WideBwdGeo wide_bwd_geo(int DPK, int DPV) {
   g.off_k = 3072;
   g.off_v = g.off_k + g.kb;
   g.off_q = g.off_v + g.vb;
-  g.off_do = g.off_q + g.qb;
-  g.off_ds = g.off_do + g.dob;
+  g.nst = (g.off_q + 2u * (g.qb + g.dob) + 32768u <= 232448u) ? 2 : 1;
+  g.off_do = g.off_q + (uint32_t)g.nst * g.qb;
+  g.off_ds = g.off_do + (uint32_t)g.nst * g.dob;
   g.off_stg = g.off_ds + 16384;
   g.total = g.off_stg + 16384;
   return g;
 }
 
 enum WBBar : int {
-  WB_KV = 0, WB_QF, WB_QE, WB_DOF, WB_DOE, WB_SF, WB_DPF, WB_PF, WB_DSF, WB_DQF, WB_DQE,
-  WB_DSE, WB_ACC, WB_DRAIN, WB_COUNT
+  WB_KV = 0, WB_QF0, WB_QF1, WB_QE0, WB_QE1, WB_DOF0, WB_DOF1, WB_DOE0, WB_DOE1, WB_SF, WB_DPF,
+  WB_PF, WB_DSF, WB_DQF, WB_DQE, WB_DSE, WB_ACC, WB_DRAIN, WB_COUNT
 };
+// small region: barriers, TMEM slot, abort flag, ticket, and per Q stage the step's LSE2 and
+// D (64 fp32 each)
 constexpr uint32_t WB_TMEM = 512, WB_ABORT = 516, WB_TICKET = 520, WB_LSE = 1024, WB_DSUM = 1536;
 constexpr uint32_t WBT_DK = 0, WBT_DV = 128, WBT_S = 256, WBT_DP = 320, WBT_DQ = 384;
 
@@ -413,10 +419,9 @@ __global__ void __launch_bounds__(512, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem_raw + WB_ABORT);
-  const float* s_lse = reinterpret_cast<const float*>(smem_raw + WB_LSE);
-  const float* s_dsum = reinterpret_cast<const float*>(smem_raw + WB_DSUM);
   auto bar = [&](int i) -> uint32_t { return sbase + 8u * (uint32_t)i; };
   const WideBwdGeo geo = wide_bwd_geo(p.DPK, p.DPV);
+  const int nst = geo.nst;
 
   if (threadIdx.x == 0) {
     // the tile index: the block index, or in the ordered mode a ticket, so that every key
@@ -482,32 +487,48 @@ __global__ void __launch_bounds__(512, 1)
         const int mb = m_begin + (it - g * m_count);
         const int h = hk * p.G + g;
         const int q0 = mb * 64;
-        // Q, LSE2 and D of step it may land once step it-1's dK (their last reader) is done
-        if (it >= 1 && !mbar_wait(bar(WB_QE), (it - 1) & 1, st, kWideTimeout - 41)) break;
-        mbar_arrive_expect_tx(bar(WB_QF), geo.qb + 512);
+        const int sq = it % nst;
+        // Q, LSE2 and D of step it go to stage it % nst once that stage's last reader (the
+        // dK product nst steps back) is done
+        if (it >= nst && !mbar_wait(bar(WB_QE0 + sq), ((it - nst) / nst) & 1, st, kWideTimeout - 41)) break;
+        mbar_arrive_expect_tx(bar(WB_QF0 + sq), geo.qb + 512);
         for (int pn = 0; pn < npk; ++pn)
-          tma_load_4d(sbase + geo.off_q + pn * W_PANEL64, &tq, pn * 64, h, q0, b, bar(WB_QF));
+          tma_load_4d(sbase + geo.off_q + sq * geo.qb + pn * W_PANEL64, &tq, pn * 64, h, q0, b,
+                      bar(WB_QF0 + sq));
         const size_t row = ((size_t)b * p.H + h) * p.Sq_r + q0;
-        bulk_load(sbase + WB_LSE, p.lse2 + row, 256, bar(WB_QF));
-        bulk_load(sbase + WB_DSUM, p.dsum + row, 256, bar(WB_QF));
+        bulk_load(sbase + WB_LSE + sq * 256, p.lse2 + row, 256, bar(WB_QF0 + sq));
+        bulk_load(sbase + WB_DSUM + sq * 256, p.dsum + row, 256, bar(WB_QF0 + sq));
         ++nq;
-        // dO of step it may land once step it-1's dV is done
-        if (it >= 1 && !mbar_wait(bar(WB_DOE), (it - 1) & 1, st, kWideTimeout - 42)) break;
-        mbar_arrive_expect_tx(bar(WB_DOF), geo.dob);
+        // dO of step it once the dV product nst steps back is done
+        if (it >= nst && !mbar_wait(bar(WB_DOE0 + sq), ((it - nst) / nst) & 1, st, kWideTimeout - 42)) break;
+        mbar_arrive_expect_tx(bar(WB_DOF0 + sq), geo.dob);
         for (int pn = 0; pn < npv; ++pn)
-          tma_load_4d(sbase + geo.off_do + pn * W_PANEL64, &tdo, pn * 64, h, q0, b, bar(WB_DOF));
+          tma_load_4d(sbase + geo.off_do + sq * geo.dob + pn * W_PANEL64, &tdo, pn * 64, h, q0, b,
+                      bar(WB_DOF0 + sq));
         ++ndo;
       }
+      // every copy started here must land before the CTA may exit: the last load of each
+      // stage
       volatile int no_abort = 0;
       AbortState dr{&no_abort, p.status, p.wait_limit};
       mbar_wait(bar(WB_KV), 0, dr, kWideTimeout - 43);
-      if (nq > 0) mbar_wait(bar(WB_QF), (nq - 1) & 1, dr, kWideTimeout - 43);
-      if (ndo > 0) mbar_wait(bar(WB_DOF), (ndo - 1) & 1, dr, kWideTimeout - 43);
+      for (int k2 = 0; k2 < nst && k2 < nq; ++k2) {
+        const int last = nq - 1 - ((nq - 1 - k2) % nst);
+        mbar_wait(bar(WB_QF0 + last % nst), (last / nst) & 1, dr, kWideTimeout - 43);
+      }
+      for (int k2 = 0; k2 < nst && k2 < ndo; ++k2) {
+        const int last = ndo - 1 - ((ndo - 1 - k2) % nst);
+        mbar_wait(bar(WB_DOF0 + last % nst), (last / nst) & 1, dr, kWideTimeout - 43);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // Per step: S^T, dP^T; dV (after P^T); dK (after dS^T) -> Q free; dQ^T (after the
-    // previous dQ^T is drained) -> dq_full; dS free.
+    // Per step i: S^T, dP^T; dV (after P^T) -> dO free; dK (after dS^T) -> Q free; dQ^T
+    // (after the previous dQ^T is drained) -> dq_full; dS free.  With two Q / dO stages
+    // the next step's S^T follows dV_i and its dP^T follows dK_i (they overwrite P^T_i and
+    // dS^T_i, which those products read: issue order), so the compute warps find the next
+    // scores ready; with one stage the next Q can only land after dK_i, so the steps run
+    // one after another.
     if (total > 0) {
       const bool leader = elect_one();
       auto wspin = [&](uint32_t bb, uint32_t par, int code) -> bool {
@@ -519,48 +540,64 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t idQ = idesc_h<F16>(128, 64, true, true);
       const DescWords aK = desc_words(sbase + geo.off_k, 16, 1024, SWZ_128B);
       const DescWords aV = desc_words(sbase + geo.off_v, 16, 1024, SWZ_128B);
-      const DescWords bQ = desc_words(sbase + geo.off_q, 16, 1024, SWZ_128B);
-      const DescWords bDO = desc_words(sbase + geo.off_do, 16, 1024, SWZ_128B);
-      const DescWords bQs = desc_words(sbase + geo.off_q + 2 * s * W_PANEL64, W_PANEL64, 1024, SWZ_128B);
-      const DescWords bDOs = desc_words(sbase + geo.off_do + 2 * s * W_PANEL64, W_PANEL64, 1024, SWZ_128B);
       const DescWords aKt = desc_words(sbase + geo.off_k + 2 * s * W_PANEL128, W_PANEL128, 1024, SWZ_128B);
       const DescWords bDS = desc_words(sbase + geo.off_ds, W_PANEL64, 1024, SWZ_128B);
-      bool ok = wspin(bar(WB_KV), 0, kWideTimeout - 10);
-      for (int it = 0; ok && it < total; ++it) {
-        const uint32_t ph = it & 1;
-        if (!wspin(bar(WB_QF), ph, kWideTimeout - 11)) { ok = false; break; }
+      auto do_S = [&](int i) -> bool {
+        const int sq = i % nst;
+        if (!wspin(bar(WB_QF0 + sq), (i / nst) & 1, kWideTimeout - 11)) return false;
         tc_fence_after();
+        const DescWords bQ = desc_words(sbase + geo.off_q + sq * geo.qb, 16, 1024, SWZ_128B);
         if (leader) mma_kk(tmem + WBT_S, aK, W_PANEL128 >> 4, bQ, W_PANEL64 >> 4, p.DPK / 16, idS);
         if (leader) mma_commit(bar(WB_SF));
-        if (!wspin(bar(WB_DOF), ph, kWideTimeout - 12)) { ok = false; break; }
+        return true;
+      };
+      auto do_dP = [&](int i) -> bool {
+        const int sq = i % nst;
+        if (!wspin(bar(WB_DOF0 + sq), (i / nst) & 1, kWideTimeout - 12)) return false;
         tc_fence_after();
+        const DescWords bDO = desc_words(sbase + geo.off_do + sq * geo.dob, 16, 1024, SWZ_128B);
         if (leader) mma_kk(tmem + WBT_DP, aV, W_PANEL128 >> 4, bDO, W_PANEL64 >> 4, p.DPV / 16, idS);
         if (leader) mma_commit(bar(WB_DPF));
-        // dV_s += P^T dO_s: A = P^T (queries [0, 32) as pairs in columns [0, 16) of S^T,
-        // [32, 64) in [32, 48)), K = 64 queries in 4 steps
-        if (!wspin(bar(WB_PF), ph, kWideTimeout - 13)) { ok = false; break; }
+        return true;
+      };
+      // dV_s += P^T dO_s: A = P^T (queries [0, 32) as pairs in columns [0, 16) of S^T,
+      // [32, 64) in [32, 48)), K = 64 queries in 4 steps
+      auto do_dV = [&](int i) -> bool {
+        const int sq = i % nst;
+        if (!wspin(bar(WB_PF), i & 1, kWideTimeout - 13)) return false;
         tc_fence_after();
+        const DescWords bDOs =
+            desc_words(sbase + geo.off_do + sq * geo.dob + 2 * s * W_PANEL64, W_PANEL64, 1024, SWZ_128B);
         if (leader && vcols > 0) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_ts_wp(tmem + WBT_DV, tmem + WBT_S + (ks >> 1) * 32 + (ks & 1) * 8, bDOs, ks * 128, idV,
-                      (it > 0 || ks > 0) ? 1u : 0u);
+                      (i > 0 || ks > 0) ? 1u : 0u);
         }
-        if (leader) mma_commit(bar(WB_DOE));
-        // dK_s += dS^T Q_s: A = dS^T over the dP^T columns, same layout
-        if (!wspin(bar(WB_DSF), ph, kWideTimeout - 14)) { ok = false; break; }
+        if (leader) mma_commit(bar(WB_DOE0 + sq));
+        return true;
+      };
+      // dK_s += dS^T Q_s: A = dS^T over the dP^T columns, same layout
+      auto do_dK = [&](int i) -> bool {
+        const int sq = i % nst;
+        if (!wspin(bar(WB_DSF), i & 1, kWideTimeout - 14)) return false;
         tc_fence_after();
+        const DescWords bQs =
+            desc_words(sbase + geo.off_q + sq * geo.qb + 2 * s * W_PANEL64, W_PANEL64, 1024, SWZ_128B);
         if (leader && kcols > 0) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_ts_wp(tmem + WBT_DK, tmem + WBT_DP + (ks >> 1) * 32 + (ks & 1) * 8, bQs, ks * 128, idK,
-                      (it > 0 || ks > 0) ? 1u : 0u);
+                      (i > 0 || ks > 0) ? 1u : 0u);
         }
-        if (leader) mma_commit(bar(WB_QE));
-        // dQ_s^T = K_s^T dS^T: A = the K tile's slice panels read MN-major (M = 128 head-dim
-        // rows), B = dS^T from shared memory (N = 64 queries), K = 128 keys in 8 steps
+        if (leader) mma_commit(bar(WB_QE0 + sq));
+        return true;
+      };
+      // dQ_s^T = K_s^T dS^T: A = the K tile's slice panels read MN-major (M = 128 head-dim
+      // rows), B = dS^T from shared memory (N = 64 queries), K = 128 keys in 8 steps
+      auto do_dQ = [&](int i) -> bool {
         if (kcols > 0) {
-          if (it >= 1 && !wspin(bar(WB_DQE), (it - 1) & 1, kWideTimeout - 15)) { ok = false; break; }
+          if (i >= 1 && !wspin(bar(WB_DQE), (i - 1) & 1, kWideTimeout - 15)) return false;
           tc_fence_after();
           if (leader) {
 #pragma unroll
@@ -574,6 +611,19 @@ __global__ void __launch_bounds__(512, 1)
           if (leader) mma_commit(bar(WB_DQF));
         }
         if (leader) mma_commit(bar(WB_DSE));
+        return true;
+      };
+      bool ok = wspin(bar(WB_KV), 0, kWideTimeout - 10);
+      if (nst == 1) {
+        for (int it = 0; ok && it < total; ++it)
+          ok = do_S(it) && do_dP(it) && do_dV(it) && do_dK(it) && do_dQ(it);
+      } else {
+        ok = ok && do_S(0) && do_dP(0);
+        for (int it = 0; ok && it < total; ++it) {
+          const bool more = it + 1 < total;
+          ok = do_dV(it) && (!more || do_S(it + 1)) && do_dK(it) && (!more || do_dP(it + 1)) &&
+               do_dQ(it);
+        }
       }
       if (ok && leader) mma_commit(bar(WB_ACC));
       if (leader) mma_commit(bar(WB_DRAIN));
@@ -684,6 +734,8 @@ __global__ void __launch_bounds__(512, 1)
       const int qmax = row_ok ? min(base - p.lo, 1 << 20) : -1;
       if (!warp_wait(bar(WB_SF), it & 1, st, kWideTimeout - 30)) { alive = false; break; }
       tc_fence_after();
+      const float* s_lse = reinterpret_cast<const float*>(smem_raw + WB_LSE + (it % nst) * 256);
+      const float* s_dsum = reinterpret_cast<const float*>(smem_raw + WB_DSUM + (it % nst) * 256);
       uint32_t r[32];
       tmem_ld32(t_lane + WBT_S + col0, r);
       float pc[32];  // P (times 1 - tanh^2 under softcap), kept for dS

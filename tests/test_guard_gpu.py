@@ -130,3 +130,31 @@ def test_packed_outputs_stay_in_bounds(fa):
     assert torch.equal(lse, lse2)
     for got, want in zip((dq, dk, dv), ref):
         assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+@pytest.mark.parametrize("D,Dv", [(192, 128), (256, 256)])
+def test_wide_outputs_stay_in_bounds(fa, D, Dv):
+    """The wide kernels (head dims above 128, or Dv != D) write O, LSE, dQ, dK and dV only
+    inside their views, and the views equal contiguous outputs bit for bit (ordered mode)."""
+    w = custom(f"guard_wide_{D}_{Dv}", 1, 200, 330, 4, 2, D, causal=True, seed=64, Dv=Dv)
+    q, k, v, do = make_inputs(w, "cuda")
+    ob, o, om = guarded16((w.B, w.Sq, w.H, Dv))
+    lb, lse, lm = guarded_lse((w.B, w.H, w.Sq))
+    fa.fa_fwd(q, k, v, o, lse, w.scale, True)
+    qb, dq, qm = guarded16((w.B, w.Sq, w.H, D))
+    kb, dk, km = guarded16((w.B, w.Sk, w.Hk, D))
+    vb, dv, vm = guarded16((w.B, w.Sk, w.Hk, Dv))
+    ws = fa.alloc_bwd_workspace(q, k, True, v)
+    fa.fa_bwd(do, q, k, v, o, lse, dq, dk, dv, w.scale, True, deterministic=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.fa_bwd_status(ws) == 0
+    for name, big, mask in (("O", ob, om), ("LSE", lb, lm), ("dQ", qb, qm), ("dK", kb, km),
+                            ("dV", vb, vm)):
+        assert_intact(f"{w.name} {name}", big, mask)
+    o2, lse2 = fa.attention_forward(q, k, v, w.scale, True)
+    ref = fa.attention_backward(do, q, k, v, o2, lse2, w.scale, True, deterministic=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse, lse2)
+    for got, want in zip((dq, dk, dv), ref):
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
