@@ -597,13 +597,14 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
   if ((st = check_h16_4d(dv, dt, B, Sk, Hk, Dv))) return st;
   const bool f16 = dt == FA_DTYPE_F16;
   // The algorithm of this call.  AUTO: the split algorithm for deterministic batched bf16
-  // calls on a square causal shape (no waits; the fused ordered mode must claim the short
-  // key tiles first there), the fused one otherwise.
+  // calls on a square shape (its two kernels never wait; on square causal and windowed
+  // shapes the fused ordered mode is slower, since deadlock freedom makes it claim the
+  // short key tiles first), the fused one otherwise (rectangular shapes, whose few query
+  // tiles per key tile make the split algorithm's recomputation costly).
   int algo = g_bwd_algorithm;
   if (algo == FA_BWD_ALGO_AUTO) {
-    const bool square_causal = (causal || window_right == 0) && window_left < 0 && Sq == Sk;
-    algo = (deterministic && !f16 && !vl && !block_mask && square_causal) ? FA_BWD_ALGO_SPLIT
-                                                                         : FA_BWD_ALGO_FUSED;
+    algo = (deterministic && !f16 && !vl && !block_mask && Sq == Sk) ? FA_BWD_ALGO_SPLIT
+                                                                   : FA_BWD_ALGO_FUSED;
   }
   if (is_wide(D, Dv)) {
     // the wide kernels: batched and dense calls only, whichever algorithm is selected

@@ -245,6 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   counts[KB_DSFULL] = 8;
   int tile;
   const uint32_t tmem = cta_setup(smem_raw, sbase, KB_COUNT, counts, p.ticket, p.status, &tile);
+  // the dQ kernel reads nothing this kernel writes: let it start filling the SMs that this
+  // kernel's last CTAs leave
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   AbortState st{s_abort, p.status, p.wait_limit};
 
   // key-tile-major order: under causal masking the low key tiles see the most query tiles
@@ -757,6 +760,30 @@ cudaError_t launch_kernel(Kern kern, size_t smem, const BwdMainParams& p, const 
   return cudaGetLastError();
 }
 
+// The dQ kernel as a programmatic dependent of the dK / dV kernel before it on the stream:
+// it may start once every dK / dV CTA has started (they signal it at once), and needs no
+// result of theirs.
+template <typename Kern>
+cudaError_t launch_dependent(Kern kern, size_t smem, const BwdMainParams& p, const OperandMaps& q,
+                             const OperandMaps& k, const OperandMaps& v, const OperandMaps& d,
+                             int num_ctas, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p, q.full, q.tail, k.full, k.tail, v.full, v.tail, d.full, d.tail);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
@@ -772,10 +799,10 @@ cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const
                                   num_kv_ctas, s);                                             \
     if (e != cudaSuccess) return e;                                                            \
     if (num_q_ctas > 0)                                                                        \
-      e = softcap ? launch_kernel(bwd_dq_kernel<DPV, true>, GeoQ<DPV>::TOTAL, p, q, k, v, d,    \
-                                  num_q_ctas, s)                                               \
-                  : launch_kernel(bwd_dq_kernel<DPV, false>, GeoQ<DPV>::TOTAL, p, q, k, v, d,   \
-                                  num_q_ctas, s);                                              \
+      e = softcap ? launch_dependent(bwd_dq_kernel<DPV, true>, GeoQ<DPV>::TOTAL, p, q, k, v, d, \
+                                     num_q_ctas, s)                                            \
+                  : launch_dependent(bwd_dq_kernel<DPV, false>, GeoQ<DPV>::TOTAL, p, q, k, v,  \
+                                     d, num_q_ctas, s);                                        \
     return e;                                                                                  \
   }
   switch (Dp) {

@@ -105,6 +105,8 @@ EXTRA_WORKLOADS = {
     "gqa_causal_d192_dv128": Workload("gqa_causal_d192_dv128", 4, 2048, 2048, 32, 8, 192,
                                       causal=True, do_std=0.1, seed=6, Dv=128),
 }
+# A non-causal square shape (for the choice between the deterministic algorithms).
+EXTRA_WORKLOADS["mha_full"] = Workload("mha_full", 2, 2048, 2048, 16, 16, 128, seed=7)
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 
 

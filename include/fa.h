@@ -306,12 +306,12 @@ int fa_bwd_noalloc_status(void* stream, int* device_status);
  * fa_bwd_set_algorithm returns FA_ERR_ARG for an unknown value; fa_bwd_get_algorithm
  * returns the current one.
  *   FA_BWD_ALGO_AUTO (default): the fused algorithm, except for deterministic batched
- *     bf16 calls without a block mask on a square causal shape (Sq == Sk, causal, no left
- *     window), which run the split algorithm: there it needs no waits, while the fused
- *     ordered mode must claim the shortest key tiles first.  Both results are bitwise
- *     reproducible, but they are not the same bits, so on those shapes a deterministic
- *     batched call no longer matches the fused ordered mode (which fa_bwd_varlen always
- *     uses) bit for bit; select FA_BWD_ALGO_FUSED for that.
+ *     bf16 calls without a block mask on a square shape (Sq == Sk), which run the split
+ *     algorithm: there it needs no waits, while the fused ordered mode must claim the
+ *     shortest key tiles first.  Both results are bitwise reproducible, but they are not
+ *     the same bits, so on those shapes a deterministic batched call no longer matches the
+ *     fused ordered mode (which fa_bwd_varlen always uses) bit for bit; select
+ *     FA_BWD_ALGO_FUSED for that.
  *   FA_BWD_ALGO_FUSED / FA_BWD_ALGO_SPLIT: always that algorithm (the split one refuses
  *     f16, packed sequences and block masks with FA_ERR_UNSUPPORTED).
  * Wide head dims (D > 128 or Dv != D) have a kernel of their own whatever is selected.

@@ -1,7 +1,6 @@
 """The default backward algorithm (FA_BWD_ALGO_AUTO): deterministic batched bf16 calls on a
-square causal shape run the split algorithm (bit for bit what FA_BWD_ALGO_SPLIT gives);
-every other call runs the fused algorithm (bit for bit its ordered mode when
-deterministic)."""
+square shape run the split algorithm (bit for bit what FA_BWD_ALGO_SPLIT gives); every
+other call runs the fused algorithm (bit for bit its ordered mode when deterministic)."""
 
 import pytest
 import torch
@@ -51,18 +50,21 @@ def test_auto_is_the_default(fa):
     assert _abi.get_algorithm() == _abi.ALGO_AUTO
 
 
-def test_auto_square_causal_runs_split(fa):
+@pytest.mark.parametrize("w", [
+    custom("auto_square", 2, 640, 640, 8, 2, 128, causal=True, seed=81),
+    custom("auto_window", 1, 640, 640, 4, 2, 128, window_left=200, window_right=0, seed=82),
+    custom("auto_noncausal", 1, 384, 384, 2, 2, 64, seed=84),
+], ids=["causal", "window", "noncausal"])
+def test_auto_square_runs_split(fa, w):
     from flashattention_backward_pass_gb300 import _abi
-    w = custom("auto_square", 2, 640, 640, 8, 2, 128, causal=True, seed=81)
     assert _equal(_det_bits(fa, w, _abi.ALGO_AUTO), _det_bits(fa, w, _abi.ALGO_SPLIT))
 
 
 @pytest.mark.parametrize("w", [
-    custom("auto_window", 1, 640, 640, 4, 2, 128, window_left=200, window_right=0, seed=82),
     custom("auto_rect", 1, 256, 640, 4, 4, 64, causal=True, seed=83),
-    custom("auto_noncausal", 1, 384, 384, 2, 2, 64, seed=84),
-], ids=["window", "rectangular", "noncausal"])
-def test_auto_other_shapes_run_fused(fa, w):
+    custom("auto_rect_tall", 1, 640, 300, 4, 2, 128, causal=True, seed=87),
+], ids=["rectangular", "tall"])
+def test_auto_rectangular_runs_fused(fa, w):
     from flashattention_backward_pass_gb300 import _abi
     assert _equal(_det_bits(fa, w, _abi.ALGO_AUTO), _det_bits(fa, w, _abi.ALGO_FUSED))
 
