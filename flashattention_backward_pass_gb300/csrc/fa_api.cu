@@ -288,11 +288,11 @@ bool encode_operand(CUtensorMap* map, const fa_tensor* t, int width, int rows = 
   return r == CUDA_SUCCESS;
 }
 
-bool encode_pair(OperandMaps* m, const fa_tensor* t, int Dp) {
+bool encode_pair(OperandMaps* m, const fa_tensor* t, int Dp, int rows = 128) {
   memset(m, 0, sizeof(*m));
-  if (!encode_operand(&m->full, t, 64)) return false;
+  if (!encode_operand(&m->full, t, 64, rows)) return false;
   const int tail = Dp % 64;
-  if (tail) return encode_operand(&m->tail, t, tail);
+  if (tail) return encode_operand(&m->tail, t, tail, rows);
   m->tail = m->full;
   return true;
 }
@@ -777,7 +777,12 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
       p.sp_stride = sp.stride;
     }
     const int mode = vl ? 1 : (block_mask ? 2 : 0);
-    if (launch_bwd_main(p, mq, mk, mv, mdo, Dp, softcap > 0.f, f16, mode, grid, s) != cudaSuccess)
+    // dK / dV leave through tensor copies where the outputs' layout has tensor maps (the
+    // alignment checks above make that the rule); otherwise each thread stores its row
+    OperandMaps mdk, mdv;
+    p.tma_epilogue = encode_pair(&mdk, dk, Dp, 32) && encode_pair(&mdv, dv, Dp, 32) ? 1 : 0;
+    if (launch_bwd_main(p, mq, mk, mv, mdo, mdk, mdv, Dp, softcap > 0.f, f16, mode, grid, s) !=
+        cudaSuccess)
       return FA_ERR_CUDA;
   }
 

@@ -66,9 +66,127 @@ struct Geo : Panels<DP> {
   static constexpr uint32_t DS_BYTES = 128u * 128u * 2u;
   static constexpr uint32_t OFF_STG = OFF_DS + DS_BYTES;           // dQ reduction staging
   static constexpr uint32_t STG_BYTES = 128u * 64u * 4u;           // 64 fp32 columns
-  static constexpr uint32_t TOTAL = OFF_STG + STG_BYTES;
+  // dV staging for the tensor-copy epilogue where it fits (Dp < 128); at Dp = 128 dV is
+  // staged after dK's last reader, in the dS buffer
+  static constexpr uint32_t OFF_EPI = OFF_STG + STG_BYTES;
+  static constexpr uint32_t EPI_BYTES = DP < 128 ? TILE_BYTES : 0;
+  static constexpr uint32_t TOTAL = OFF_EPI + EPI_BYTES;
   static_assert(TOTAL <= 232448, "fits the 227 KB opt-in shared memory");
 };
+
+// ---------------------------------------------------------------- dK / dV epilogue units
+// The accumulators leave tensor memory in units of (accumulator, column range) per warp:
+// warpgroup 0 writes dV columns [0, 64) and dK columns [64, Dp), warpgroup 1 dK columns
+// [0, 64) and dV columns [64, Dp), so that every unit is one 64-column operand panel or
+// the 16 / 32-column tail panel and both warpgroups move Dp columns.  A unit of a warp's
+// 32 key rows is rounded to the 16-bit type, written into a shared-memory box laid out
+// like the operand panels (rows of 2W bytes, 128B / 64B / 32B swizzle for W = 64 / 32 /
+// 16) and stored by lane 0 with one tensor copy; the tensor map clips rows past the key
+// length and columns past the head dim.  Without a tensor map (or for a packed sequence's
+// last rows, which the next sequence follows) the lanes store their rows directly.
+
+// W columns from this warp's 32 TMEM lanes, times sc, as 16-bit pairs in pk[0, W / 2)
+// (zeros when the tile has no visible query).
+template <int W, bool F16>
+__device__ __forceinline__ void epi_load(uint32_t taddr, float sc, bool valid, uint32_t (&pk)[32]) {
+  if constexpr (W == 16) {
+    uint32_t r[16];
+    if (valid) {
+      tmem_ld16(taddr, r);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) r[e] = 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      pk[e] = pack_h2<F16>(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
+  } else {
+#pragma unroll
+    for (int h = 0; h < W / 32; ++h) {
+      uint32_t r[32];
+      if (valid) {
+        tmem_ld32(taddr + h * 32, r);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pk[h * 16 + e] =
+            pack_h2<F16>(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
+    }
+  }
+}
+
+// Row `lane` of a W-column box at sbox (1024-byte aligned): 16-byte chunk c sits at
+// chunk c ^ (address bits 7.. of the row) within the row, the tensor map's swizzle.
+template <int W>
+__device__ __forceinline__ void epi_stage(uint32_t sbox, int lane, const uint32_t (&pk)[32]) {
+  constexpr int ROWB = 2 * W;
+  constexpr int NCH = ROWB / 16;
+  const uint32_t row = sbox + (uint32_t)(lane * ROWB);
+  const uint32_t sw = (uint32_t)((lane * ROWB) >> 7) & (uint32_t)(NCH - 1);
+#pragma unroll
+  for (int c = 0; c < NCH; ++c)
+    st_shared_v4(row + (((uint32_t)c ^ sw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                 pk[4 * c + 3]);
+}
+
+// The direct form: this lane's row from column col0 on, the first ncols columns of it.
+template <int W>
+__device__ __forceinline__ void epi_store_row(__nv_bfloat16* row, int ncols,
+                                              const uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int g = 0; g < W / 8; ++g)
+    if (g * 8 < ncols)
+      *reinterpret_cast<uint4*>(row + g * 8) =
+          make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+}
+
+// One unit of the calling warp (tma, store: warp-uniform).  The box is reused only once
+// the issuing lane's earlier copies have read their sources.
+template <int W>
+__device__ __forceinline__ void epi_put(const uint32_t (&pk)[32], bool tma, bool store,
+                                        uint32_t box, int lane, const CUtensorMap* map,
+                                        int col, int h, int row, int b, __nv_bfloat16* grow,
+                                        bool row_ok, int ncols) {
+  if (!store) return;
+  if (tma) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+    epi_stage<W>(box, lane, pk);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_4d(map, col, h, row, b, box);
+      bulk_commit();
+    }
+  } else if (row_ok) {
+    epi_store_row<W>(grow, ncols, pk);
+  }
+}
+
+// Releases the accumulator's columns (after the calling warp's tensor-memory reads) to the
+// next tile.
+__device__ __forceinline__ void epi_release(bool valid, int lane, uint32_t bar) {
+  if (valid) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  }
+}
+
+// A whole unit: load, release, store.
+template <int W, bool F16>
+__device__ __forceinline__ void epi_unit(uint32_t taddr, float sc, bool valid, uint32_t release,
+                                         bool tma, bool store, uint32_t box, int lane,
+                                         const CUtensorMap* map, int col, int h, int row, int b,
+                                         __nv_bfloat16* grow, bool row_ok, int ncols) {
+  uint32_t pk[32];
+  epi_load<W, F16>(taddr, sc, valid, pk);
+  epi_release(valid, lane, release);
+  epi_put<W>(pk, tma, store, box, lane, map, col, h, row, b, grow, row_ok, ncols);
+}
 
 // small-region layout
 constexpr uint32_t SM_BAR = 0;          // 32 barriers x 8 B
@@ -146,7 +264,7 @@ __device__ long long g_fa_trace[FA_TRACE_CTAS][FA_TRACE_ITERS][FA_TRACE_EV];
 // warp 3: S, dP, dV, dK, dQ.
 __device__ long long g_fa_mma_done[FA_TRACE_CTAS][FA_TRACE_ITERS][5];
 // Whole-kernel tile timeline (global timer, ns): per CTA and per tile it ran.
-constexpr int FA_TL_CTAS = 160, FA_TL_TILES = 24, FA_TL_EV = 8;
+constexpr int FA_TL_CTAS = 160, FA_TL_TILES = 24, FA_TL_EV = 12;
 __device__ long long g_fa_tl[FA_TL_CTAS][FA_TL_TILES][FA_TL_EV];
 __device__ __forceinline__ long long gtimer() {
   long long t;
@@ -290,7 +408,10 @@ __global__ void __launch_bounds__(512, 1)
                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tk_t,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tv_t,
                     const __grid_constant__ CUtensorMap tdo,
-                    const __grid_constant__ CUtensorMap tdo_t) {
+                    const __grid_constant__ CUtensorMap tdo_t,
+                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdk_t,
+                    const __grid_constant__ CUtensorMap tdv,
+                    const __grid_constant__ CUtensorMap tdv_t) {
   using G = Geo<DP>;
   constexpr bool VARLEN = MODE == 1;
   constexpr bool SPARSE = MODE == 2;
@@ -596,6 +717,7 @@ __global__ void __launch_bounds__(512, 1)
               alive = false;
               break;
             }
+            FA_TL(t, 8, gtimer());
             load_k();
           }
         }
@@ -1038,6 +1160,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!warp_wait(bar(B_SFULL), git & 1, st, kTimeoutBase - 30)) { alive = false; break; }
         tc_fence_after();
         if (threadIdx.x == 256) FA_TR(4, git);
+        if (it == 0 && threadIdx.x == 256) FA_TL(t, 10, gtimer());
         float lreg[2] = {0.f, 0.f};
         if (!SOFTCAP) {
           lreg[0] = lse[lane];
@@ -1053,6 +1176,7 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_PFULL));
         if (threadIdx.x == 256) FA_TR(5, git);
+        if (it == 0 && threadIdx.x == 256) FA_TL(t, 9, gtimer());
         if (threadIdx.x == 384) FA_TR(11, git);
 
         if (!warp_wait(bar(B_DPFULL), git & 1, st, kTimeoutBase - 31)) { alive = false; break; }
@@ -1066,6 +1190,11 @@ __global__ void __launch_bounds__(512, 1)
         if (!SOFTCAP) {
           dreg[0] = dsum[lane];
           dreg[1] = dsum[32 + lane];
+        }
+        if (it == 0) {
+          // the previous epilogue's tensor copies may still read this warp's dS rows
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
         }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -1109,62 +1238,84 @@ __global__ void __launch_bounds__(512, 1)
       if (!alive) break;
 
       // ---------------------------------------------------------------- dK / dV epilogue
-      // Each warpgroup writes half of the columns of both accumulators for its key row.
-      // dV is final as soon as the tile's last dV is complete, so it is read out while
-      // the last dK / dQ still run; dK follows once every MMA of the tile is complete.
-      // Each accumulator's columns are released to the next tile as soon as they are in
+      // dV is final as soon as the tile's last dV is complete, so its unit is read out
+      // (and, where it has its own staging buffer, stored) while the last dK / dQ still
+      // run; dK follows once every MMA of the tile is complete and is staged in this
+      // warp's own rows of the dS buffer, which no MMA reads any more.  Each
+      // accumulator's columns are released to the next tile as soon as they are in
       // registers.
       const bool have = d.total > 0;
+      constexpr int W1 = DP - 64;            // the second unit's width: 0, 16, 32 or 64
+      const int krow = k_row0 + d.n * kTileK + qd * 32;
+      const bool tma = p.tma_epilogue != 0 && (!VARLEN || d.n * kTileK + qd * 32 + 32 <= t_sk);
+      const uint32_t slot = sbase + G::OFF_DS + wg * 16384 + qd * 4096;
+      __nv_bfloat16* dv_row = p.dv + (int64_t)tb * p.dv_sb + (int64_t)(k_row0 + j) * p.dv_ss +
+                              (int64_t)d.hk * p.dv_sh;
+      __nv_bfloat16* dk_row = p.dk + (int64_t)tb * p.dk_sb + (int64_t)(k_row0 + j) * p.dk_ss +
+                              (int64_t)d.hk * p.dk_sh;
       bool acc_ok = true;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
+      if (have) {
+        acc_ok = warp_wait(bar(B_DVDONE), (git - 1) & 1, st, kTimeoutBase - 34);
+        if (acc_ok) tc_fence_after();
+      }
+      const bool valid_v = have && acc_ok;
+      if constexpr (DP == 128) {
+        // warpgroup w: dV columns [64w, 64w + 64), dK columns [64 - 64w, 128 - 64w); dV
+        // waits in registers until dK's last reader is done with the dS buffer
+        uint32_t vpk[32];
+        epi_load<64, F16>(t_lane + TM_DV + wg * 64, 1.f, valid_v, vpk);
+        epi_release(valid_v, lane, bar(B_DVEMPTY));
         if (have) {
-          acc_ok = acc_ok && (which ? warp_wait(bar(B_ACC), kt & 1, st, kTimeoutBase - 33)
-                                    : warp_wait(bar(B_DVDONE), (git - 1) & 1, st, kTimeoutBase - 34));
+          acc_ok = acc_ok && warp_wait(bar(B_ACC), kt & 1, st, kTimeoutBase - 33);
           if (acc_ok) tc_fence_after();
-          if (which && threadIdx.x == 256) FA_TL(t, 5, gtimer());
+          if (threadIdx.x == 256) FA_TL(t, 5, gtimer());
         }
-        const bool store = acc_ok && *s_abort == 0 && row_ok;
-        const uint32_t tcol = which ? TM_DK : TM_DV;
-        const float sc = which ? p.dk_scale : 1.f;
-        __nv_bfloat16* row = which ? p.dk + (int64_t)tb * p.dk_sb + (int64_t)(k_row0 + j) * p.dk_ss + (int64_t)d.hk * p.dk_sh
-                                   : p.dv + (int64_t)tb * p.dv_sb + (int64_t)(k_row0 + j) * p.dv_ss + (int64_t)d.hk * p.dv_sh;
-        constexpr int NCH = DP / 16;          // 16-column chunks per accumulator row
-        constexpr int NCH0 = (NCH + 1) / 2;   // chunks of warpgroup 0
-        const int c0 = wg ? NCH0 : 0;
-        const int nch = wg ? NCH - NCH0 : NCH0;
-#pragma unroll 1
-        for (int cc = 0; cc < NCH0; ++cc) {
-          if (cc < nch) {
-            const int c = c0 + cc;
-            uint32_t r[16];
-            if (have && acc_ok) {
-              tmem_ld16(t_lane + tcol + c * 16, r);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) r[e] = 0u;  // no visible query: zero rows
-            }
-            uint32_t pk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              pk[e] = pack_h2<F16>(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
-            if (store) {
-              if (c * 16 < p.D)
-                *reinterpret_cast<uint4*>(row + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              if (c * 16 + 8 < p.D)
-                *reinterpret_cast<uint4*>(row + c * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
-          }
-          if (cc == NCH0 - 1 && have && acc_ok) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(which ? B_DKEMPTY : B_DVEMPTY));
-          }
+        const bool store = acc_ok && __shfl_sync(0xffffffffu, *s_abort == 0, 0);
+        epi_put<64>(vpk, tma, store, slot, lane, &tdv, wg * 64, d.hk, krow, tb, dv_row + wg * 64,
+                    row_ok, p.D - wg * 64);
+        epi_unit<64, F16>(t_lane + TM_DK + (1 - wg) * 64, p.dk_scale, have && acc_ok,
+                          bar(B_DKEMPTY), tma, store, slot, lane, &tdk, (1 - wg) * 64, d.hk, krow,
+                          tb, dk_row + (1 - wg) * 64, row_ok, p.D - (1 - wg) * 64);
+      } else {
+        // dV has a staging buffer of its own and leaves at once
+        const bool store_v = acc_ok && __shfl_sync(0xffffffffu, *s_abort == 0, 0);
+        const uint32_t vbox = sbase + G::OFF_EPI + (wg == 0 ? qd * 4096 : 16384 + qd * 64 * W1);
+        if (wg == 0) {
+          epi_unit<64, F16>(t_lane + TM_DV, 1.f, valid_v, bar(B_DVEMPTY), tma, store_v, vbox,
+                            lane, &tdv, 0, d.hk, krow, tb, dv_row, row_ok, p.D);
+        } else {
+          if constexpr (W1 > 0)
+            epi_unit<W1, F16>(t_lane + TM_DV + 64, 1.f, valid_v, bar(B_DVEMPTY), tma, store_v,
+                              vbox, lane, &tdv_t, 64, d.hk, krow, tb, dv_row + 64, row_ok,
+                              p.D - 64);
+          else
+            epi_release(valid_v, lane, bar(B_DVEMPTY));
+        }
+        if (have) {
+          acc_ok = acc_ok && warp_wait(bar(B_ACC), kt & 1, st, kTimeoutBase - 33);
+          if (acc_ok) tc_fence_after();
+          if (threadIdx.x == 256) FA_TL(t, 5, gtimer());
+        }
+        const bool store = acc_ok && __shfl_sync(0xffffffffu, *s_abort == 0, 0);
+        const bool valid_k = have && acc_ok;
+        if (wg == 1) {
+          epi_unit<64, F16>(t_lane + TM_DK, p.dk_scale, valid_k, bar(B_DKEMPTY), tma, store,
+                            slot, lane, &tdk, 0, d.hk, krow, tb, dk_row, row_ok, p.D);
+        } else {
+          if constexpr (W1 > 0)
+            epi_unit<W1, F16>(t_lane + TM_DK + 64, p.dk_scale, valid_k, bar(B_DKEMPTY), tma,
+                              store, slot, lane, &tdk_t, 64, d.hk, krow, tb, dk_row + 64, row_ok,
+                              p.D - 64);
+          else
+            epi_release(valid_k, lane, bar(B_DKEMPTY));
         }
       }
       if (have) ++kt;
       if (threadIdx.x == 256) FA_TL(t, 6, gtimer());
     }
+    // the epilogue's last tensor copies complete before the CTA (and its shared memory) ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1213,8 +1364,8 @@ size_t bwd_main_smem_bytes(int Dp) {
 
 template <int DP, bool SC, bool F16, int MODE>
 static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
-                              const OperandMaps& v, const OperandMaps& d, int num_ctas,
-                              cudaStream_t s) {
+                              const OperandMaps& v, const OperandMaps& d, const OperandMaps& dk,
+                              const OperandMaps& dv, int num_ctas, cudaStream_t s) {
   auto kern = bwd_main_kernel<DP, SC, F16, MODE>;
   const size_t smem = Geo<DP>::TOTAL;
   // The in-kernel register split assumes exactly 128 registers per thread at launch.
@@ -1224,20 +1375,22 @@ static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, cons
   if (attr.numRegs != 128) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_ctas, 512, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail, d.full, d.tail);
+  kern<<<num_ctas, 512, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail, d.full, d.tail,
+                                   dk.full, dk.tail, dv.full, dv.tail);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
-                            const OperandMaps& v, const OperandMaps& d, int Dp, bool softcap,
-                            bool f16, int mode, int num_ctas, cudaStream_t s) {
+                            const OperandMaps& v, const OperandMaps& d, const OperandMaps& dk,
+                            const OperandMaps& dv, int Dp, bool softcap, bool f16, int mode,
+                            int num_ctas, cudaStream_t s) {
   if (num_ctas <= 0) return cudaSuccess;
 #define FA_CASE_VL(DPV, MD)                                                             \
   if (f16)                                                                              \
-    return softcap ? launch_one<DPV, true, true, MD>(p, q, k, v, d, num_ctas, s)        \
-                   : launch_one<DPV, false, true, MD>(p, q, k, v, d, num_ctas, s);      \
-  return softcap ? launch_one<DPV, true, false, MD>(p, q, k, v, d, num_ctas, s)         \
-                 : launch_one<DPV, false, false, MD>(p, q, k, v, d, num_ctas, s);
+    return softcap ? launch_one<DPV, true, true, MD>(p, q, k, v, d, dk, dv, num_ctas, s)        \
+                   : launch_one<DPV, false, true, MD>(p, q, k, v, d, dk, dv, num_ctas, s);      \
+  return softcap ? launch_one<DPV, true, false, MD>(p, q, k, v, d, dk, dv, num_ctas, s)         \
+                 : launch_one<DPV, false, false, MD>(p, q, k, v, d, dk, dv, num_ctas, s);
 #define FA_CASE(DPV)                                                                    \
   case DPV:                                                                             \
     if (mode == 1) {                                                                    \

@@ -80,7 +80,9 @@ struct BwdMainParams {
   long long sp_stride;
   // and the (B, H, Mb, Nb) block mask itself: the ordered mode counts, for a step's query
   // tile, the kept key tiles above this one
-  const uint8_t* block_mask;
+  const uint8_t* block_mask;  // dK / dV leave through tensor copies of 32-row boxes (tensor maps of dk and dv passed
+  // to the main kernel); 0: every row is stored by its thread
+  int tma_epilogue;
 };
 
 // Builds the block-sparse step lists of the main kernel from a (B, H, Mb, Nb) block mask:
@@ -194,9 +196,11 @@ size_t bwd_main_smem_bytes(int Dp);
 cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t s);
 // f16: the 16-bit operands and outputs are f16 (else bf16); mode: 0 batched, 1 packed
 // sequences, 2 block-sparse (step lists from launch_bwd_sparse_lists)
+// dk, dv: tensor maps of the outputs with 32-row boxes (used when p.tma_epilogue is set)
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
-                            const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
-                            bool f16, int mode, int num_ctas, cudaStream_t s);
+                            const OperandMaps& v, const OperandMaps& dout, const OperandMaps& dk,
+                            const OperandMaps& dv, int Dp, bool softcap, bool f16, int mode,
+                            int num_ctas, cudaStream_t s);
 cudaError_t launch_bwd_sparse_lists(const BwdSparseParams& p, cudaStream_t s);
 cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s);
 // dK/dV kernel (num_kv_ctas = key tiles x batch x kv-heads) then dQ kernel (num_q_ctas =

@@ -165,6 +165,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// 4-D tiled store of a shared-memory box (written through the generic proxy and fenced
+// with fence_proxy_async_smem by its writers) to global memory; elements outside the
+// tensor's extents are not written.  Tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_4d(const void* tmap, int c0, int c1, int c2, int c3,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+      : "memory");
+}
+
 // Prefetch of one 4-D tile into L2 (no shared-memory destination, no completion signal).
 __device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
   asm volatile(
