@@ -23,9 +23,10 @@
 // (in the ordered mode the highest key tile goes first: see decode_tile).
 //
 // Warp roles (16 warps, 512 threads):
-//   warp 0      TMA producer: K, V per tile (the next tile's K/V prefetched into L2 while
-//               the current one finishes); Q+LSE2+D and dO per step (2-stage Q ring,
-//               one dO buffer)
+//   warp 0      TMA producer: K, V per tile (the next tile's V, and at Dp = 96 / 128 its
+//               K, prefetched into L2 while the current one finishes; at Dp <= 80 K has
+//               two stages and the next tile's K is loaded at once); Q+LSE2+D and dO per
+//               step (2-stage Q ring, one dO buffer)
 //   warp 1      TMEM allocator and MMA issue (one elected lane issues)
 //   warp 2      tile scheduler: claims the next ticket when the current tile starts its
 //               last step and publishes it in a 2-slot ring
@@ -36,7 +37,8 @@
 //               cp.reduce.async.bulk fp32 adds (ordered by key tile when deterministic)
 //   warps 8-15  two compute warpgroups: warpgroup w handles queries [64w, 64w+64) of
 //               the tile for every key row (thread = key = TMEM lane); at the end of
-//               each tile they write dK / dV, each warpgroup half of the columns
+//               each tile they stage dK / dV in shared memory, each warpgroup Dp of the
+//               2 Dp columns, and tensor stores write them out
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0, Dp)        dK accumulator          [128, 128+Dp)  dV accumulator
@@ -45,8 +47,8 @@
 //
 // Shared memory (1024-byte aligned tiles, 128B swizzle for 64-column panels, 32B/64B
 // swizzle for a 16/32-column tail panel when Dp % 64 != 0):
-//   K, V, Q[2], dO (128 rows x Dp bf16 each), dS^T (128 keys x 128 queries bf16),
-//   dQ staging (128 x 64 fp32)
+//   K (two stages at Dp <= 80), V, Q[2], dO (128 rows x Dp bf16 each), dS^T (128 keys x
+//   128 queries bf16), dQ staging (128 x 64 fp32), dV staging (Dp < 128)
 #include "fa_bwd_common.cuh"
 
 namespace fa {
@@ -58,8 +60,11 @@ struct Geo : Panels<DP> {
   using Panels<DP>::TILE_BYTES;
   // shared-memory layout (offsets from a 1024-aligned base)
   static constexpr uint32_t SMALL = 3072;
+  // K has two stages where they fit beside the dV staging (Dp <= 80): the next tile's K
+  // then lands while the current tile's last products still read the other stage
+  static constexpr int KST = DP <= 80 ? 2 : 1;
   static constexpr uint32_t OFF_K = SMALL;
-  static constexpr uint32_t OFF_V = OFF_K + TILE_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KST * TILE_BYTES;
   static constexpr uint32_t OFF_Q = OFF_V + TILE_BYTES;            // 2 stages
   static constexpr uint32_t OFF_DO = OFF_Q + 2 * TILE_BYTES;       // 1 stage
   static constexpr uint32_t OFF_DS = OFF_DO + TILE_BYTES;
@@ -84,6 +89,11 @@ struct Geo : Panels<DP> {
 // 16) and stored by lane 0 with one tensor copy; the tensor map clips rows past the key
 // length and columns past the head dim.  Without a tensor map (or for a packed sequence's
 // last rows, which the next sequence follows) the lanes store their rows directly.
+
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
 
 // W columns from this warp's 32 TMEM lanes, times sc, as 16-bit pairs in pk[0, W / 2)
 // (zeros when the tile has no visible query).
@@ -195,6 +205,7 @@ constexpr uint32_t SM_ABORT = 260;
 constexpr uint32_t SM_TILE = 264;       // drain scratch words
 constexpr uint32_t SM_RING = 512;       // 2 tile descriptors x 32 B
 constexpr uint32_t SM_VRING = 576;      // packed sequences: 2 sequence descriptors x 32 B
+constexpr uint32_t SM_BAR2 = 640;       // mbarriers 32.. x 8 B
 constexpr uint32_t SM_LSE = 1024;       // 2 stages x 128 fp32
 constexpr uint32_t SM_DSUM = 2048;      // 2 stages x 128 fp32
 
@@ -202,9 +213,9 @@ enum Bar : int {
   B_K = 0, B_V, B_QF0, B_QF1, B_QE0, B_QE1, B_DOF0, B_DOF1, B_DOE0, B_DOE1,
   B_SFULL, B_DPFULL, B_PFULL, B_DSFULL, B_DVDONE, B_DQFULL, B_DQEMPTY, B_DSEMPTY,
   B_ACC, B_DRAIN, B_TILEF0, B_TILEF1, B_TILEE0, B_TILEE1, B_KEMPTY, B_VEMPTY, B_DVEMPTY,
-  B_DKEMPTY, B_NEXT, B_TURN, B_TURNE, B_COUNT
+  B_DKEMPTY, B_NEXT, B_TURN, B_TURNE, B_K1, B_KEMPTY1, B_COUNT
 };
-static_assert(B_COUNT <= 32, "barrier area holds 32 mbarriers");
+static_assert(B_COUNT <= 40, "barrier areas hold 32 + 8 mbarriers");
 
 // Consumers of a published tile descriptor: producer, MMA issuer, 4 drain warps and 8
 // compute warps each arrive once on the slot's empty barrier (and, in the ordered mode,
@@ -428,7 +439,9 @@ __global__ void __launch_bounds__(512, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(small + SM_TMEM);
   const float* s_lse = reinterpret_cast<const float*>(small + SM_LSE);
   const float* s_dsum = reinterpret_cast<const float*>(small + SM_DSUM);
-  auto bar = [&](int i) -> uint32_t { return sbase + SM_BAR + 8u * i; };
+  auto bar = [&](int i) -> uint32_t {
+    return sbase + (i < 32 ? SM_BAR + 8u * i : SM_BAR2 + 8u * (i - 32));
+  };
 
 #ifdef FA_TRACE
   if (threadIdx.x == 0) {
@@ -444,6 +457,7 @@ __global__ void __launch_bounds__(512, 1)
       *s_abort = 1;
     }
     mbar_init(bar(B_K), 1);
+    mbar_init(bar(B_K1), 1);
     mbar_init(bar(B_V), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_QF0 + s), 1);
@@ -464,6 +478,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar(B_ACC), 1);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_KEMPTY), 1);
+    mbar_init(bar(B_KEMPTY1), 1);
     mbar_init(bar(B_VEMPTY), 1);
     mbar_init(bar(B_DVEMPTY), 8);
     mbar_init(bar(B_DKEMPTY), 8);
@@ -633,11 +648,14 @@ __global__ void __launch_bounds__(512, 1)
         }
         const int n0 = k_off + d.n * kTileK;
         auto load_k = [&]() {
+          const int ks = G::KST == 2 ? (nk & 1) : 0;
+          const uint32_t kb = bar(ks ? B_K1 : B_K);
+          const uint32_t kdst = sbase + G::OFF_K + ks * G::TILE_BYTES;
           ++nk;
-          mbar_arrive_expect_tx(bar(B_K), G::TILE_BYTES);
+          mbar_arrive_expect_tx(kb, G::TILE_BYTES);
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
-            tma_load_4d(sbase + G::OFF_K + pnl * G::FULL_BYTES, &tk, pnl * 64, d.hk, n0, tb, bar(B_K));
-          if (G::TAIL) tma_load_4d(sbase + G::OFF_K + G::TAIL_OFF, &tk_t, G::NFULL * 64, d.hk, n0, tb, bar(B_K));
+            tma_load_4d(kdst + pnl * G::FULL_BYTES, &tk, pnl * 64, d.hk, n0, tb, kb);
+          if (G::TAIL) tma_load_4d(kdst + G::TAIL_OFF, &tk_t, G::NFULL * 64, d.hk, n0, tb, kb);
         };
         auto load_v = [&]() {
           ++nv;
@@ -647,15 +665,22 @@ __global__ void __launch_bounds__(512, 1)
           if (G::TAIL) tma_load_4d(sbase + G::OFF_V + G::TAIL_OFF, &tv_t, G::NFULL * 64, d.hk, n0, tb, bar(B_V));
         };
         const bool kv_busy = nk > 0;  // the previous tile may still be reading K and V
+        if (G::KST == 2 && kv_busy) {
+          // the stage this K goes to was last read two tiles back
+          if (nk >= 2 && !mbar_wait_ool(bar((nk & 1) ? B_KEMPTY1 : B_KEMPTY), ((nk >> 1) - 1) & 1,
+                                        st, kTimeoutBase - 5))
+            break;
+          load_k();
+        }
         if (kv_busy) {
           // warm L2 with this tile's K and V so that the loads below, which must wait for
           // the previous tile's last MMAs, hit L2
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl) {
-            tma_prefetch_4d(&tk, pnl * 64, d.hk, n0, tb);
+            if (G::KST == 1) tma_prefetch_4d(&tk, pnl * 64, d.hk, n0, tb);
             tma_prefetch_4d(&tv, pnl * 64, d.hk, n0, tb);
           }
           if (G::TAIL) {
-            tma_prefetch_4d(&tk_t, G::NFULL * 64, d.hk, n0, tb);
+            if (G::KST == 1) tma_prefetch_4d(&tk_t, G::NFULL * 64, d.hk, n0, tb);
             tma_prefetch_4d(&tv_t, G::NFULL * 64, d.hk, n0, tb);
           }
         } else {
@@ -711,7 +736,7 @@ __global__ void __launch_bounds__(512, 1)
           _Pragma("unroll 1") for (int pnl = 0; pnl < G::NFULL; ++pnl)
             tma_load_4d(ddst + pnl * G::FULL_BYTES, &tdo, pnl * 64, h, q_off + m0, tb, bar(B_DOF0));
           if (G::TAIL) tma_load_4d(ddst + G::TAIL_OFF, &tdo_t, G::NFULL * 64, h, q_off + m0, tb, bar(B_DOF0));
-          if (it == 0 && kv_busy) {
+          if (G::KST == 1 && it == 0 && kv_busy) {
             if (!mbar_wait_ool(bar(B_KEMPTY), (nk - 1) & 1, st, kTimeoutBase - 5)) {
               ++git;
               alive = false;
@@ -727,7 +752,14 @@ __global__ void __launch_bounds__(512, 1)
       // barrier can still be pending.
       volatile int no_abort = 0;
       AbortState dr{&no_abort, p.status, p.wait_limit};
-      if (nk > 0) mbar_wait_ool(bar(B_K), (nk - 1) & 1, dr, kTimeoutBase - 3);
+      if (G::KST == 1) {
+        if (nk > 0) mbar_wait_ool(bar(B_K), (nk - 1) & 1, dr, kTimeoutBase - 3);
+      } else {
+        for (int ks = 0; ks < 2; ++ks) {
+          const int nks = (nk - ks + 1) / 2;  // loads issued into K stage ks
+          if (nks > 0) mbar_wait_ool(bar(ks ? B_K1 : B_K), (nks - 1) & 1, dr, kTimeoutBase - 3);
+        }
+      }
       if (nv > 0) mbar_wait_ool(bar(B_V), (nv - 1) & 1, dr, kTimeoutBase - 3);
       for (int s = 0; s < 2; ++s) {
         const int nq = (git - s + 1) / 2;  // loads issued into Q stage s
@@ -751,7 +783,9 @@ __global__ void __launch_bounds__(512, 1)
       auto wspin = [&](uint32_t b, uint32_t par, int code) -> bool {
         return __all_sync(0xffffffffu, mbar_wait_spin(b, par, st, code));
       };
-      const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K), dV_ = tile_descs<DP>(sbase + G::OFF_V);
+      const TileDescs dK0 = tile_descs<DP>(sbase + G::OFF_K), dV_ = tile_descs<DP>(sbase + G::OFF_V);
+      const TileDescs dK1 = tile_descs<DP>(sbase + G::OFF_K + (G::KST - 1) * G::TILE_BYTES);
+      int kst = 0;  // K stage of the current tile
       const TileDescs dDO = tile_descs<DP>(sbase + G::OFF_DO);
       const TileDescs dQ0 = tile_descs<DP>(sbase + G::OFF_Q), dQ1 = tile_descs<DP>(sbase + G::OFF_Q + G::TILE_BYTES);
       const DescWords dsK = desc_words(sbase + G::OFF_DS, 16, 1024, SWZ_128B);      // dS^T, K-major
@@ -761,7 +795,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!wspin(bar(B_QF0 + s), (g >> 1) & 1, kTimeoutBase - 11)) return false;
         tc_fence_after();
         if (leader) FA_TR(0, g);
-        if (leader) mma_kmajor<DP, F16>(tmem + TM_S, dK_, s ? dQ1 : dQ0);
+        if (leader) mma_kmajor<DP, F16>(tmem + TM_S, kst ? dK1 : dK0, s ? dQ1 : dQ0);
         if (leader) mma_commit(bar(B_SFULL));
         return true;
       };
@@ -782,7 +816,8 @@ __global__ void __launch_bounds__(512, 1)
         if (d.total == 0) continue;
         // the previous tile's last P^T and dQ columns must be consumed before S_0 / dP_0
         if (git > 0 && !wspin(bar(B_DVDONE), (git - 1) & 1, kTimeoutBase - 12)) break;
-        if (!wspin(bar(B_K), kt & 1, kTimeoutBase - 10)) break;
+        kst = G::KST == 2 ? (kt & 1) : 0;
+        if (!wspin(bar(kst ? B_K1 : B_K), (G::KST == 2 ? kt >> 1 : kt) & 1, kTimeoutBase - 10)) break;
         if (leader) FA_TL(t, 2, gtimer());
         if (leader) FA_TL(t, 7, d.total);
         if (!issue_S(git)) break;
@@ -823,7 +858,7 @@ __global__ void __launch_bounds__(512, 1)
           if (leader) FA_TR(3, git);
           if (leader) mma_dk<DP, F16>(tmem + TM_DK, dsK, s ? dQ1 : dQ0, acc);
           if (leader) mma_commit(bar(B_QE0 + s));
-          if (leader) mma_dq<DP, F16>(tmem + TM_DP, dsM, dK_);  // the dQ tile goes where dP^T was
+          if (leader) mma_dq<DP, F16>(tmem + TM_DP, dsM, kst ? dK1 : dK0);  // the dQ tile goes where dP^T was
           if (leader) mma_commit(bar(B_DQFULL));
           if (leader) mma_commit(bar(B_DSEMPTY));
           acc = 1;
@@ -836,7 +871,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!ok) break;
         if (leader) FA_TL(t, 4, gtimer());
         if (leader) mma_commit(bar(B_ACC));     // this tile's dK / dV are final
-        if (leader) mma_commit(bar(B_KEMPTY));  // and its K buffer may be refilled
+        if (leader) mma_commit(bar(kst ? B_KEMPTY1 : B_KEMPTY));  // and its K stage may be refilled
         ++kt;
       }
       if (git > 0 || kt > 0) {
@@ -1259,23 +1294,32 @@ __global__ void __launch_bounds__(512, 1)
         if (acc_ok) tc_fence_after();
       }
       const bool valid_v = have && acc_ok;
-      if constexpr (DP == 128) {
-        // warpgroup w: dV columns [64w, 64w + 64), dK columns [64 - 64w, 128 - 64w); dV
-        // waits in registers until dK's last reader is done with the dS buffer
-        uint32_t vpk[32];
-        epi_load<64, F16>(t_lane + TM_DV + wg * 64, 1.f, valid_v, vpk);
-        epi_release(valid_v, lane, bar(B_DVEMPTY));
-        if (have) {
-          acc_ok = acc_ok && warp_wait(bar(B_ACC), kt & 1, st, kTimeoutBase - 33);
-          if (acc_ok) tc_fence_after();
-          if (threadIdx.x == 256) FA_TL(t, 5, gtimer());
-        }
-        const bool store = acc_ok && __shfl_sync(0xffffffffu, *s_abort == 0, 0);
-        epi_put<64>(vpk, tma, store, slot, lane, &tdv, wg * 64, d.hk, krow, tb, dv_row + wg * 64,
-                    row_ok, p.D - wg * 64);
-        epi_unit<64, F16>(t_lane + TM_DK + (1 - wg) * 64, p.dk_scale, have && acc_ok,
-                          bar(B_DKEMPTY), tma, store, slot, lane, &tdk, (1 - wg) * 64, d.hk, krow,
-                          tb, dk_row + (1 - wg) * 64, row_ok, p.D - (1 - wg) * 64);
+      if constexpr (G::EPI_BYTES == 0) {
+        // dV waits in registers until dK's last reader is done with the dS buffer, then
+        // both units of the warp go through its rows there, one after the other
+        auto late = [&](auto wv, auto wk) {
+          constexpr int WV = decltype(wv)::value, WK = decltype(wk)::value;
+          const int cv = wg == 0 ? 0 : 64, ck = wg == 0 ? 64 : 0;
+          uint32_t vpk[32];
+          epi_load<WV, F16>(t_lane + TM_DV + cv, 1.f, valid_v, vpk);
+          epi_release(valid_v, lane, bar(B_DVEMPTY));
+          if (have) {
+            acc_ok = acc_ok && warp_wait(bar(B_ACC), kt & 1, st, kTimeoutBase - 33);
+            if (acc_ok) tc_fence_after();
+            if (threadIdx.x == 256) FA_TL(t, 5, gtimer());
+          }
+          const bool store = acc_ok && __shfl_sync(0xffffffffu, *s_abort == 0, 0);
+          epi_put<WV>(vpk, tma, store, slot, lane, WV == 64 ? &tdv : &tdv_t, cv, d.hk, krow, tb,
+                      dv_row + cv, row_ok, p.D - cv);
+          epi_unit<WK, F16>(t_lane + TM_DK + ck, p.dk_scale, have && acc_ok, bar(B_DKEMPTY), tma,
+                            store, slot, lane, WK == 64 ? &tdk : &tdk_t, ck, d.hk, krow, tb,
+                            dk_row + ck, row_ok, p.D - ck);
+        };
+        // warpgroup 0: dV columns [0, 64) and dK columns [64, Dp); warpgroup 1 the others
+        if (wg == 0)
+          late(IntC<64>{}, IntC<W1>{});
+        else
+          late(IntC<W1>{}, IntC<64>{});
       } else {
         // dV has a staging buffer of its own and leaves at once
         const bool store_v = acc_ok && __shfl_sync(0xffffffffu, *s_abort == 0, 0);
