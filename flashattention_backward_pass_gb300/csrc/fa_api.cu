@@ -394,10 +394,12 @@ static int fwd_common(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v
     return launch_fwd_empty(p, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   // tcgen05 kernel: one CTA per (128-query tile, batch, q-head)
   const int Dp = padded_dim(D);
-  OperandMaps mq, mk, mv;
+  OperandMaps mq, mk, mv, mo;
   if (!encode_pair(&mq, q, Dp) || !encode_pair(&mk, k, Dp) || !encode_pair(&mv, v, Dp))
     return FA_ERR_CUDA;
-  if (launch_fwd_tc(p, mq, mk, mv, Dp, softcap > 0.f, dt == FA_DTYPE_F16, s) != cudaSuccess)
+  // O leaves through tensor copies where its layout has tensor maps; else row stores
+  p.tma_epilogue = encode_pair(&mo, out, Dp, 32) ? 1 : 0;
+  if (launch_fwd_tc(p, mq, mk, mv, mo, Dp, softcap > 0.f, dt == FA_DTYPE_F16, s) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -475,10 +477,11 @@ int fa_fwd_varlen(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, fa
     return launch_fwd_empty(e, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
   const int Dp = padded_dim(D);
-  OperandMaps mq, mk, mv;
+  OperandMaps mq, mk, mv, mo;
   if (!encode_pair(&mq, &q4, Dp) || !encode_pair(&mk, &k4, Dp) || !encode_pair(&mv, &v4, Dp))
     return FA_ERR_CUDA;
-  if (launch_fwd_tc(p, mq, mk, mv, Dp, softcap > 0.f, dt == FA_DTYPE_F16, s) != cudaSuccess)
+  p.tma_epilogue = encode_pair(&mo, &o4, Dp, 32) ? 1 : 0;
+  if (launch_fwd_tc(p, mq, mk, mv, mo, Dp, softcap > 0.f, dt == FA_DTYPE_F16, s) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }

@@ -72,13 +72,19 @@ struct GeoF : Panels<DP> {
 // work), K / V by ring stage.
 enum FBar : int {
   F_QF0 = 0, F_QF1, F_QE0, F_QE1, F_KF0, F_KF1, F_KE0, F_KE1, F_VF0, F_VF1, F_VE0, F_VE1,
-  F_SF0, F_SF1, F_PF0, F_PF1, F_PD0, F_PD1, F_ACC0, F_ACC1, F_OE0, F_OE1, F_DRAIN, F_COUNT
+  F_SF0, F_SF1, F_PF0, F_PF1, F_PD0, F_PD1, F_ACC0, F_ACC1, F_OE0, F_OE1, F_DRAIN,
+  F_OS0, F_OS1, F_COUNT
 };
 static_assert(F_COUNT <= 32, "barrier area holds 32 mbarriers");
 
 constexpr uint32_t FT_S0 = 0, FT_O0 = 256;
 
 constexpr float kNegInf = -__builtin_huge_valf();
+
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
 
 // Scores of this thread's 64 columns of its row in log2 units (scale * s * log2e, or
 // with softcap c * log2e * tanh(scale * s / c)); `sbuf` addresses column col0 of the
@@ -207,7 +213,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_tc_kernel(const __grid_constant__ FwdTcParams p,
                   const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tq_t,
                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tk_t,
-                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tv_t) {
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tv_t,
+                  const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap to_t) {
   using G = GeoF<DP>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
@@ -224,8 +231,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       *s_abort = 1;
     }
     for (int i = 0; i < F_COUNT; ++i) {
-      const bool eight = (i == F_PF0 || i == F_PF1 || i == F_OE0 || i == F_OE1);
-      mbar_init(bar(i), eight ? 8 : 1);  // softmax warps arrive on P-full and O-empty
+      const bool eight = (i == F_PF0 || i == F_PF1 || i == F_OE0 || i == F_OE1 || i == F_OS0 ||
+                          i == F_OS1);
+      mbar_init(bar(i), eight ? 8 : 1);  // softmax warps arrive on P-full, O-empty, O-staged
     }
     fence_barrier_init();
   }
@@ -271,7 +279,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (lane == 0) {
         if (kside) {
           const int qb = qn & 1;
-          if (qn >= 2 && !mbar_wait(bar(F_QE0 + qb), ((qn - 2) >> 1) & 1, st, kFwdTimeout - 4)) {
+          // the buffer's item two back: its S products are done and its O, staged there,
+          // has been read by the tensor stores
+          if (qn >= 2 && (!mbar_wait(bar(F_QE0 + qb), ((qn - 2) >> 1) & 1, st, kFwdTimeout - 4) ||
+                          !mbar_wait(bar(F_OS0 + qb), ((qn - 2) >> 1) & 1, st, kFwdTimeout - 5))) {
             alive = false;
           } else {
             const uint32_t qdst = sbase + G::OFF_Q + qb * G::TILE_BYTES;
@@ -402,6 +413,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // every warp reaches the item barrier (bar.red.or of the abort flag), so no warp is
     // ever left waiting at a barrier alone.
     int g = 0, on = 0, items = 0;  // key tiles consumed, items with work, items
+    // Q buffer (1 + index) whose staged O this warp's tensor stores may still read; it is
+    // handed back (O-staged barrier) at the next item's first key tile or epilogue
+    int os_pend = 0;
+    auto flush_os = [&]() {
+      if (os_pend) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(F_OS0 + os_pend - 1));
+        os_pend = 0;
+      }
+    };
     for (int k = 0, idx = item_of(0); idx < num_items; idx = item_of(++k), ++items) {
       const FwdItem I = fwd_item(p, idx, lane);
       const int m0 = I.m * kTileQ;
@@ -469,6 +491,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(F_PF0 + (x & 1)));
+        if (t == 0) flush_os();
       }
 
       // O = acc / l and LSE = (m + log2 l) * ln 2 with l the sum of both halves; a row with
@@ -489,13 +512,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (int64_t)I.tb * p.o_sb +
                        (int64_t)(I.q_off + i) * p.o_ss + (int64_t)I.h * p.o_sh;
+      flush_os();
+      // Warpgroup 0 writes O columns [0, 64), warpgroup 1 columns [64, Dp): each a 64-column
+      // panel or the 16 / 32-column tail panel.  Staged in the item's Q buffer (free once
+      // the item's products are done) in the tensor map's swizzled layout, a warp's 32 rows
+      // leave with one tensor store; the map clips rows past Sq and columns past D.  A
+      // packed sequence's last rows (the next sequence follows) are stored row by row.
+      const bool tma = p.tma_epilogue != 0 && have && !stop &&
+                       (!p.varlen || m0 + qd * 32 + 32 <= I.Sq);
+      auto out_unit = [&](auto wc) {
+        constexpr int W = decltype(wc)::value;
+        constexpr int ROWB = 2 * W;
+        constexpr int NCW = ROWB / 16;
+        const int c0 = wg == 0 ? 0 : 64;
+        const uint32_t box =
+            sbase + G::OFF_Q + qb * G::TILE_BYTES + (wg == 0 ? qd * 4096 : 16384 + qd * 32 * ROWB);
+        const uint32_t srow = box + (uint32_t)(lane * ROWB);
+        const uint32_t sw = (uint32_t)((lane * ROWB) >> 7) & (uint32_t)(NCW - 1);
 #pragma unroll
-      for (int cc = 0; cc < NCH0; ++cc) {
-        const int c = c_lo + cc;
-        if (c < c_hi) {
+        for (int gq = 0; gq < W / 16; ++gq) {
           uint32_t o[16];
           if (have && !stop) {
-            tmem_ld16(t_lane + o_col + c * 16, o);
+            tmem_ld16(t_lane + o_col + c0 + gq * 16, o);
           } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] = 0u;
@@ -504,18 +542,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             pk[e] = pack_h2<F16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-          if (store) {
-            if (c * 16 < p.D)
-              *reinterpret_cast<uint4*>(orow + c * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            if (c * 16 + 8 < p.D)
-              *reinterpret_cast<uint4*>(orow + c * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          const int c = c0 + gq * 16;
+          if (tma) {
+            st_shared_v4(srow + (((uint32_t)(2 * gq) ^ sw) << 4), pk[0], pk[1], pk[2], pk[3]);
+            st_shared_v4(srow + (((uint32_t)(2 * gq + 1) ^ sw) << 4), pk[4], pk[5], pk[6], pk[7]);
+          } else if (store) {
+            if (c < p.D)
+              *reinterpret_cast<uint4*>(orow + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (c + 8 < p.D)
+              *reinterpret_cast<uint4*>(orow + c + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
+        if (tma) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(wg == 0 ? &to : &to_t, c0, I.h, I.q_off + m0 + qd * 32, I.tb, box);
+            bulk_commit();
+          }
+        }
+      };
+      if (wg == 0) {
+        out_unit(IntC<64>{});
+      } else {
+        if constexpr (DP > 64) out_unit(IntC<DP - 64>{});
       }
       if (have && !stop) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(F_OE0 + qb));
+        os_pend = qb + 1;  // the Q buffer goes back to the producer once the stores read it
       }
       if (store && wg == 0) {
         const float lse = lsum > 0.f ? (mrow + log2f(lsum)) * 0.69314718055994531f
@@ -528,6 +584,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++on;
       }
     }
+    flush_os();
+    // the last tensor stores complete before the CTA (and its shared memory) ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -557,7 +617,7 @@ __global__ void __launch_bounds__(256) fwd_empty_kernel(const FwdTcParams p) {
 
 template <int DP, bool SC, bool F16>
 cudaError_t launch_fwd_one(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
-                           const OperandMaps& v, cudaStream_t s) {
+                           const OperandMaps& v, const OperandMaps& o, cudaStream_t s) {
   auto kern = fwd_tc_kernel<DP, SC, F16>;
   // at least 116 KB, so that one CTA (which allocates all 512 TMEM columns) runs per SM
   const size_t smem = GeoF<DP>::TOTAL > 118784u ? GeoF<DP>::TOTAL : 118784u;
@@ -570,7 +630,8 @@ cudaError_t launch_fwd_one(const FwdTcParams& p, const OperandMaps& q, const Ope
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned grid = (unsigned)(items < sms ? items : sms);
-  kern<<<grid, kFwdThreads, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail);
+  kern<<<grid, kFwdThreads, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail, o.full,
+                                       o.tail);
   return cudaGetLastError();
 }
 
@@ -586,15 +647,16 @@ cudaError_t launch_fwd_empty(const FwdTcParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd_tc(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
-                          const OperandMaps& v, int Dp, bool softcap, bool f16, cudaStream_t s) {
+                          const OperandMaps& v, const OperandMaps& o, int Dp, bool softcap,
+                          bool f16, cudaStream_t s) {
   if (p.Mb <= 0 || p.B <= 0 || p.H <= 0) return cudaSuccess;
 #define FA_FWD_TC_CASE(DPV)                                                             \
   case DPV:                                                                             \
     if (f16)                                                                            \
-      return softcap ? launch_fwd_one<DPV, true, true>(p, q, k, v, s)                   \
-                     : launch_fwd_one<DPV, false, true>(p, q, k, v, s);                 \
-    return softcap ? launch_fwd_one<DPV, true, false>(p, q, k, v, s)                    \
-                   : launch_fwd_one<DPV, false, false>(p, q, k, v, s);
+      return softcap ? launch_fwd_one<DPV, true, true>(p, q, k, v, o, s)                   \
+                     : launch_fwd_one<DPV, false, true>(p, q, k, v, o, s);                 \
+    return softcap ? launch_fwd_one<DPV, true, false>(p, q, k, v, o, s)                    \
+                   : launch_fwd_one<DPV, false, false>(p, q, k, v, o, s);
   switch (Dp) {
     FA_FWD_TC_CASE(64)
     FA_FWD_TC_CASE(80)

@@ -145,6 +145,9 @@ struct FwdTcParams {
   // Block sparsity (batched calls): (B, H, Mb, Nb) bytes, contiguous; a zero entry
   // removes the (query tile, key tile) pair.  Null: every pair the mask allows is kept.
   const uint8_t* block_mask;
+  // O leaves through tensor copies of 32-row boxes staged in the item's Q buffer (tensor
+  // maps of o passed to the kernel); 0: every row is stored by its thread
+  int tma_epilogue;
 };
 
 // Head dims above 128, or a V head dim different from the Q/K one (fa_wide.cu).  Both
@@ -209,8 +212,10 @@ cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const
                              const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
                              int num_kv_ctas, int num_q_ctas, cudaStream_t s);
 cudaError_t launch_fwd_empty(const FwdTcParams& p, cudaStream_t s);
+// o: tensor maps of the output with 32-row boxes (used when p.tma_epilogue is set)
 cudaError_t launch_fwd_tc(const FwdTcParams& p, const OperandMaps& q, const OperandMaps& k,
-                          const OperandMaps& v, int Dp, bool softcap, bool f16, cudaStream_t s);
+                          const OperandMaps& v, const OperandMaps& o, int Dp, bool softcap,
+                          bool f16, cudaStream_t s);
 size_t wide_fwd_smem_bytes(int DPK, int DPV);
 size_t wide_bwd_smem_bytes(int DPK, int DPV);
 cudaError_t launch_fwd_wide(const WideParams& p, const CUtensorMap& q, const CUtensorMap& k,
