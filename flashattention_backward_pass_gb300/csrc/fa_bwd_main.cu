@@ -347,14 +347,32 @@ __device__ __forceinline__ void phase_p(const SoftmaxConsts& kc, uint32_t taddr,
         for (int u = 0; u < 4; ++u) lv[u] = __shfl_sync(0xffffffffu, lreg[c], v4 * 4 + u);
       }
       float pv[4], pcv[4];
+      if (SOFTCAP) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float fac;
+          pv[u] = prob<SOFTCAP>(kc, __uint_as_float(r[v4 * 4 + u]), lv[u], &fac);
+          pcv[u] = pv[u] * fac;
+        }
+      } else {
+        // exp2(S * scale * log2e - LSE2), two columns per paired fused multiply-add
+        const uint64_t sl2 = f2_pack(kc.scale_log2, kc.scale_log2);
+#pragma unroll
+        for (int u = 0; u < 4; u += 2) {
+          const uint64_t t = f2_fma(f2_pack(__uint_as_float(r[v4 * 4 + u]), __uint_as_float(r[v4 * 4 + u + 1])),
+                                    sl2, f2_pack(-lv[u], -lv[u + 1]));
+          pv[u] = ex2_approx(f2_lo(t));
+          pv[u + 1] = ex2_approx(f2_hi(t));
+        }
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int ql = c * 32 + v4 * 4 + u;
-        float fac;
-        float pr = prob<SOFTCAP>(kc, __uint_as_float(r[v4 * 4 + u]), lv[u], &fac);
-        if (MASK) pr = (ql >= qmin && ql <= qmax) ? pr : 0.f;
-        pv[u] = pr;
-        pcv[u] = SOFTCAP ? pr * fac : pr;
+        if (MASK) {
+          pv[u] = (ql >= qmin && ql <= qmax) ? pv[u] : 0.f;
+          if (SOFTCAP) pcv[u] = (ql >= qmin && ql <= qmax) ? pcv[u] : 0.f;
+        }
+        if (!SOFTCAP) pcv[u] = pv[u];
       }
       pk[v4 * 2] = pack_h2<F16>(pv[0], pv[1]);
       pk[v4 * 2 + 1] = pack_h2<F16>(pv[2], pv[3]);
@@ -1251,11 +1269,13 @@ __global__ void __launch_bounds__(512, 1)
             }
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
+              // dS = P * (dP - D), two columns per paired subtract and multiply
               const int e = v4 * 4 + e2 * 2;
               const float2 pcv = unpack_f16(pc[c * 16 + (e >> 1)]);
-              const float d0 = pcv.x * (__uint_as_float(r[e]) - dv[2 * e2]);
-              const float d1 = pcv.y * (__uint_as_float(r[e + 1]) - dv[2 * e2 + 1]);
-              pk[e >> 1] = pack_h2<F16>(d0, d1);
+              const uint64_t d = f2_mul(f2_pack(pcv.x, pcv.y),
+                                        f2_sub(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                               f2_pack(dv[2 * e2], dv[2 * e2 + 1])));
+              pk[e >> 1] = pack_h2<F16>(f2_lo(d), f2_hi(d));
             }
           }
 #pragma unroll

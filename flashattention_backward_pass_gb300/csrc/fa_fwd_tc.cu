@@ -86,10 +86,12 @@ struct IntC {
   static constexpr int value = N;
 };
 
-// Scores of this thread's 64 columns of its row in log2 units (scale * s * log2e, or
-// with softcap c * log2e * tanh(scale * s / c)); `sbuf` addresses column col0 of the
-// row; masked columns (MASK: visible iff cmin <= column <= cmax, columns of the whole
-// tile) are -inf.  Returns the maximum over the 64.
+// Scores of this thread's 64 columns of its row (`sbuf` addresses column col0 of the row;
+// masked columns, MASK: visible iff cmin <= column <= cmax, columns of the whole tile,
+// are -inf).  Without softcap x holds the raw scores s (the scale is applied together
+// with the subtraction of the maximum in fwd_probs, one fused multiply-add); with softcap
+// c x holds z = c * log2e * tanh(scale * s / c).  Returns the maximum over the 64 in
+// log2 units (scale * log2e > 0, so the raw maximum scales to the scaled one).
 template <bool MASK, bool SOFTCAP>
 __device__ __forceinline__ float fwd_scores(const SoftmaxConsts& kc, uint32_t sbuf, int col0,
                                             int cmin, int cmax, float (&x)[64]) {
@@ -102,35 +104,38 @@ __device__ __forceinline__ float fwd_scores(const SoftmaxConsts& kc, uint32_t sb
     for (int e = 0; e < 32; ++e) {
       const int col = col0 + c * 32 + e;
       const float s = __uint_as_float(r[e]);
-      float v = SOFTCAP ? kc.cap_log2 * tanh_exp2(s * kc.cap_scale) : s * kc.scale_log2;
+      float v = SOFTCAP ? kc.cap_log2 * tanh_exp2(s * kc.cap_scale) : s;
       if (MASK) v = (col >= cmin && col <= cmax) ? v : kNegInf;
       x[c * 32 + e] = v;
       mx = fmaxf(mx, v);
     }
   }
-  return mx;
+  return SOFTCAP ? mx : mx * kc.scale_log2;
 }
 
-// P = exp2(x - m) for the thread's 64 columns as 16-bit pairs over the first 32 of them
-// (`sbuf` = column col0): columns [0, 64) of the row land in TMEM columns [0, 32),
-// columns [64, 128) in [64, 96), the A layout the P V product reads.  Returns the sum of
-// the 64 P values (fp32, before rounding).
+// P = exp2(x * mul - m) for the thread's 64 columns (mul = scale * log2e on raw scores,
+// 1 on softcapped ones) as 16-bit pairs over the first 32 of them (`sbuf` = column col0):
+// columns [0, 64) of the row land in TMEM columns [0, 32), columns [64, 128) in [64, 96),
+// the A layout the P V product reads.  Returns the sum of the 64 P values (fp32, before
+// rounding).
 template <bool F16>
-__device__ __forceinline__ float fwd_probs(uint32_t sbuf, float m, const float (&x)[64]) {
-  float sum = 0.f;
+__device__ __forceinline__ float fwd_probs(uint32_t sbuf, float mul, float m, const float (&x)[64]) {
+  const uint64_t mul2 = f2_pack(mul, mul), negm2 = f2_pack(-m, -m);
+  uint64_t sum2 = 0;  // (+0, +0)
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const float p0 = ex2_approx(x[q * 32 + 2 * e] - m);
-      const float p1 = ex2_approx(x[q * 32 + 2 * e + 1] - m);
-      sum += p0 + p1;
+      const uint64_t t = f2_fma(f2_pack(x[q * 32 + 2 * e], x[q * 32 + 2 * e + 1]), mul2, negm2);
+      const float p0 = ex2_approx(f2_lo(t));
+      const float p1 = ex2_approx(f2_hi(t));
+      sum2 = f2_add(sum2, f2_pack(p0, p1));
       pk[e] = pack_h2<F16>(p0, p1);
     }
     tmem_st16(sbuf + q * 16, pk);
   }
-  return sum;
+  return f2_lo(sum2) + f2_hi(sum2);
 }
 
 
@@ -470,7 +475,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mrow = mx;
         }
         const float muse = mrow == kNegInf ? 0.f : mrow;  // all-masked so far: P = 0
-        lrow = lrow * alpha + fwd_probs<F16>(sbuf, muse, xs);
+        lrow = lrow * alpha + fwd_probs<F16>(sbuf, SOFTCAP ? 1.f : kc.scale_log2, muse, xs);
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           // O holds this item's products up to key tile x-1: wait for the last one, then
           // rescale this warpgroup's columns (a failed wait ends the loop at the next barrier)
