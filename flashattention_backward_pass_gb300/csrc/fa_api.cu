@@ -784,8 +784,12 @@ static int bwd_common(const fa_tensor* dout, const fa_tensor* q, const fa_tensor
     // alignment checks above make that the rule); otherwise each thread stores its row
     OperandMaps mdk, mdv;
     p.tma_epilogue = encode_pair(&mdk, dk, Dp, 32) && encode_pair(&mdv, dv, Dp, 32) ? 1 : 0;
-    if (launch_bwd_main(p, mq, mk, mv, mdo, mdk, mdv, Dp, softcap > 0.f, f16, mode, grid, s) !=
-        cudaSuccess)
+    // the main kernel overlaps the preprocess's tail when nothing else was enqueued between
+    // them (block-sparse calls build their step lists in between; the counter-poisoning
+    // test hook writes a counter)
+    const bool pdl = !block_mask && !(g_poison_first_counter && deterministic);
+    if (launch_bwd_main(p, mq, mk, mv, mdo, mdk, mdv, Dp, softcap > 0.f, f16, mode, grid, pdl,
+                        s) != cudaSuccess)
       return FA_ERR_CUDA;
   }
 

@@ -37,6 +37,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdPreParams 
     for (int64_t k = (int64_t)(blockIdx.x - row_blocks) * blockDim.x + threadIdx.x;
          k < p.zero_count; k += nthreads)
       p.zero_ptr[k] = z;
+    // A clearing block that is done lets the main kernel (launched as this grid's
+    // programmatic dependent) start once every block has finished or signalled; the main
+    // kernel waits for this grid's results before it reads them.  Signalling at the start
+    // instead let the main kernel's CTAs take SMs that this grid still needed (slower).
+    pdl_launch_dependents();
     return;
   }
   const int lane = threadIdx.x & 31;

@@ -589,7 +589,19 @@ __global__ void __launch_bounds__(512, 1)
           mbar_arrive(bar(B_TILEF0 + k));
           break;
         }
-        const int ticket = (*s_abort) ? p.num_tiles : atomicAdd(p.ticket, 1);
+        // The first tile is blockIdx.x (the grid never exceeds the tile count); later ones
+        // come from the ticket counter, which the preprocess clears, so the first claim
+        // waits for that grid (a no-op unless this kernel was launched as its dependent).
+        int ticket;
+        if (*s_abort) {
+          ticket = p.num_tiles;
+        } else if (t == 0) {
+          ticket = (int)blockIdx.x;
+          if constexpr (SPARSE) pdl_wait_prior();  // the step lists come from the grid before
+        } else {
+          if (t == 1) pdl_wait_prior();
+          ticket = (int)gridDim.x + atomicAdd(p.ticket, 1);
+        }
         FA_TL(t, 0, ticket);
         FA_TL(t, 1, gtimer());
         TileDesc d{};
@@ -731,6 +743,7 @@ __global__ void __launch_bounds__(512, 1)
           if (G::TAIL) tma_load_4d(qdst + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, q_off + m0, tb, bar(B_QF0 + s));
           size_t row = ((size_t)d.b * p.H + h) * p.Sq_r + m0;
           if constexpr (VARLEN) row = ((size_t)h * p.T + slot0 + m) * kTileQ;
+          if (git == 0) pdl_wait_prior();  // LSE2 and D come from the preprocess
           bulk_load(sbase + SM_LSE + s * 512, p.lse2 + row, 512, bar(B_QF0 + s));
           bulk_load(sbase + SM_DSUM + s * 512, p.dsum + row, 512, bar(B_QF0 + s));
           FA_TR(10, git);
@@ -910,6 +923,7 @@ __global__ void __launch_bounds__(512, 1)
     // never waits on this global-memory round trip.
     if constexpr (!SPARSE) {
      if (p.deterministic) {
+      if (lane == 0) pdl_wait_prior();  // the counters are cleared by the preprocess
       volatile int* s_turn = reinterpret_cast<volatile int*>(small + SM_TILE + 8);
       int git = 0;
       bool alive = true;
@@ -972,6 +986,7 @@ __global__ void __launch_bounds__(512, 1)
      // number of kept ones above it (counted by the whole warp with a ballot sum; the
      // list builder and the scheduler give key tiles out highest first, as above).
      if (p.deterministic) {
+      if (lane == 0) pdl_wait_prior();  // the counters are cleared by the preprocess
       volatile int* s_turn = reinterpret_cast<volatile int*>(small + SM_TILE + 8);
       int git = 0;
       bool alive = true;
@@ -1145,6 +1160,7 @@ __global__ void __launch_bounds__(512, 1)
           }
           named_bar_sync(1, 128);
           if (threadIdx.x == 128 && ok) {
+            if (git == 0 && hf == 0) pdl_wait_prior();  // the preprocess clears the accumulator
             bulk_reduce_add_f32(dst + (size_t)cg0 * 128 * 4, stg, (uint32_t)ncg * 128 * 16);
             bulk_commit();
           }
@@ -1429,7 +1445,7 @@ size_t bwd_main_smem_bytes(int Dp) {
 template <int DP, bool SC, bool F16, int MODE>
 static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                               const OperandMaps& v, const OperandMaps& d, const OperandMaps& dk,
-                              const OperandMaps& dv, int num_ctas, cudaStream_t s) {
+                              const OperandMaps& dv, int num_ctas, bool pdl, cudaStream_t s) {
   auto kern = bwd_main_kernel<DP, SC, F16, MODE>;
   const size_t smem = Geo<DP>::TOTAL;
   // The in-kernel register split assumes exactly 128 registers per thread at launch.
@@ -1439,22 +1455,35 @@ static cudaError_t launch_one(const BwdMainParams& p, const OperandMaps& q, cons
   if (attr.numRegs != 128) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_ctas, 512, smem, s>>>(p, q.full, q.tail, k.full, k.tail, v.full, v.tail, d.full, d.tail,
-                                   dk.full, dk.tail, dv.full, dv.tail);
+  // pdl: a programmatic dependent of the preprocess, whose results it waits for before
+  // it reads them (its set-up and first input loads overlap the preprocess's last blocks)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_ctas);
+  cfg.blockDim = dim3(512);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = la;
+  cfg.numAttrs = pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, p, q.full, q.tail, k.full, k.tail, v.full, v.tail, d.full,
+                         d.tail, dk.full, dk.tail, dv.full, dv.tail);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& d, const OperandMaps& dk,
                             const OperandMaps& dv, int Dp, bool softcap, bool f16, int mode,
-                            int num_ctas, cudaStream_t s) {
+                            int num_ctas, bool pdl, cudaStream_t s) {
   if (num_ctas <= 0) return cudaSuccess;
 #define FA_CASE_VL(DPV, MD)                                                             \
   if (f16)                                                                              \
-    return softcap ? launch_one<DPV, true, true, MD>(p, q, k, v, d, dk, dv, num_ctas, s)        \
-                   : launch_one<DPV, false, true, MD>(p, q, k, v, d, dk, dv, num_ctas, s);      \
-  return softcap ? launch_one<DPV, true, false, MD>(p, q, k, v, d, dk, dv, num_ctas, s)         \
-                 : launch_one<DPV, false, false, MD>(p, q, k, v, d, dk, dv, num_ctas, s);
+    return softcap ? launch_one<DPV, true, true, MD>(p, q, k, v, d, dk, dv, num_ctas, pdl, s)        \
+                   : launch_one<DPV, false, true, MD>(p, q, k, v, d, dk, dv, num_ctas, pdl, s);      \
+  return softcap ? launch_one<DPV, true, false, MD>(p, q, k, v, d, dk, dv, num_ctas, pdl, s)         \
+                 : launch_one<DPV, false, false, MD>(p, q, k, v, d, dk, dv, num_ctas, pdl, s);
 #define FA_CASE(DPV)                                                                    \
   case DPV:                                                                             \
     if (mode == 1) {                                                                    \

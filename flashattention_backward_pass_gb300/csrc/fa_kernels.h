@@ -200,10 +200,12 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams& p, bool f16, cudaStream_t 
 // f16: the 16-bit operands and outputs are f16 (else bf16); mode: 0 batched, 1 packed
 // sequences, 2 block-sparse (step lists from launch_bwd_sparse_lists)
 // dk, dv: tensor maps of the outputs with 32-row boxes (used when p.tma_epilogue is set)
+// pdl: launched as a programmatic dependent of the kernel before it on the stream (the
+// preprocess), which must then be the last operation enqueued before it
 cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                             const OperandMaps& v, const OperandMaps& dout, const OperandMaps& dk,
                             const OperandMaps& dv, int Dp, bool softcap, bool f16, int mode,
-                            int num_ctas, cudaStream_t s);
+                            int num_ctas, bool pdl, cudaStream_t s);
 cudaError_t launch_bwd_sparse_lists(const BwdSparseParams& p, cudaStream_t s);
 cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s);
 // dK/dV kernel (num_kv_ctas = key tiles x batch x kv-heads) then dQ kernel (num_q_ctas =
