@@ -11,8 +11,8 @@
 // dK/dV stay in TMEM over the whole GQA group (the call-trace page's `sum_out`, done
 // in-kernel), dK gets the softmax scale once at the end.
 //
-// dQ kernel: one CTA owns a 128-query tile of one q-head and walks the key tiles with a
-// visible entry (the Triton page's `_bwd_kernel_dq` loop, recomputing P):
+// dQ kernel: persistent CTAs claim 128-query tiles of one q-head each and walk the key
+// tiles with a visible entry (the Triton page's `_bwd_kernel_dq` loop, recomputing P):
 //   S = Q K^T, dP = dO V^T, dS = P*(dP - D) -> bf16 over the S columns (A of dQ),
 //   dQ += dS K  (fp32 in TMEM across all key tiles), then dQ = bf16(scale * dQ) once.
 // Each output element is summed in one fixed order by one CTA, so the results are
@@ -35,7 +35,7 @@ constexpr int kTimeoutQ = -1300;
 constexpr uint32_t SM_BAR = 0;     // up to 32 mbarriers
 constexpr uint32_t SM_TMEM = 256;  // TMEM base address slot
 constexpr uint32_t SM_ABORT = 260;
-constexpr uint32_t SM_TILE = 264;
+constexpr uint32_t SM_TILE = 264;  // dK/dV kernel: its ticket; dQ kernel: 2-slot tile ring
 constexpr uint32_t SM_LSE = 1024;  // dK/dV kernel: 2 stages x 128 fp32
 constexpr uint32_t SM_DSUM = 2048; // dK/dV kernel: 2 stages x 128 fp32
 constexpr uint32_t SMALL = 3072;
@@ -69,7 +69,8 @@ enum KvBar : int {
 };
 enum QBar : int {
   QB_QDO = 0, QB_KF0, QB_KF1, QB_KF2, QB_KE0, QB_KE1, QB_KE2, QB_VF0, QB_VF1, QB_VE0, QB_VE1,
-  QB_SF0, QB_SF1, QB_DPFULL, QB_DPFREE, QB_DSFULL, QB_DQDONE, QB_ACC, QB_DRAIN, QB_COUNT
+  QB_SF0, QB_SF1, QB_DPFULL, QB_DPFREE, QB_DSFULL0, QB_DSFULL1, QB_DQDONE, QB_ACC, QB_DRAIN,
+  QB_QDOE, QB_TF0, QB_TF1, QB_TE0, QB_TE1, QB_COUNT
 };
 
 // tensor-memory columns
@@ -107,8 +108,8 @@ __device__ __forceinline__ MaskGeom geom_of(const BwdMainParams& p) {
   return g;
 }
 
-// Common prologue: barrier init, TMEM allocation (512 columns), ticket.  Returns the TMEM
-// base; *tile receives the ticket.
+// Common prologue: barrier init, TMEM allocation (512 columns), ticket (claimed here when
+// `ticket` is not null).  Returns the TMEM base; *tile receives the ticket.
 __device__ __forceinline__ uint32_t cta_setup(uint8_t* smem_raw, uint32_t sbase, int nbar,
                                               const uint32_t* counts, int* ticket, int* status,
                                               int* tile_out) {
@@ -121,7 +122,7 @@ __device__ __forceinline__ uint32_t cta_setup(uint8_t* smem_raw, uint32_t sbase,
       atomicExch(status, -1999);
       *s_abort = 1;
     }
-    *s_tile = atomicAdd(ticket, 1);
+    *s_tile = ticket ? atomicAdd(ticket, 1) : 0;
     for (int i = 0; i < nbar; ++i) mbar_init(sbase + SM_BAR + 8u * i, counts[i]);
     fence_barrier_init();
   }
@@ -505,6 +506,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ============================================================================ dQ
 
+// One query tile of the dQ kernel as every role decodes it from its ticket: query tiles
+// with the most key tiles first (under causal masking: the last ones).
+struct QTile {
+  int m0, b, h, hk, n_begin, total;
+};
+
+__device__ __forceinline__ QTile q_tile_of(const BwdMainParams& p, const MaskGeom& gm, int tile) {
+  QTile t;
+  const int per_m = p.B * p.H;
+  const int m = p.Mb - 1 - tile / per_m;
+  const int bh = tile - (p.Mb - 1 - m) * per_m;
+  t.b = bh / p.H;
+  t.h = bh - t.b * p.H;
+  t.hk = t.h / p.G;
+  int64_t nb64, ne64;
+  n_range(gm, m, &nb64, &ne64);
+  t.n_begin = (int)nb64;
+  t.total = (int)(ne64 - nb64);
+  t.m0 = m * kTileQ;
+  return t;
+}
+
+// Persistent: one CTA per SM claims query tiles from a ticket until none is left.  The TMA
+// producer claims each tile when it reaches it and hands the ticket to the MMA thread and
+// the compute warps through a two-slot ring (tile-full / tile-empty barriers).  Every
+// per-step barrier phase, the K / V ring stages and the S buffers follow the CTA's global
+// step count, so the next tile's Q / dO load starts as soon as the current tile's last
+// S and dP products are complete, and its K / V loads run ahead across the boundary.
 template <int DP, bool SOFTCAP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ BwdMainParams p,
@@ -520,29 +549,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem_raw + SM_ABORT);
+  volatile int* s_tiles = reinterpret_cast<volatile int*>(smem_raw + SM_TILE);  // 2 slots
   auto bar = [&](int i) -> uint32_t { return sbase + SM_BAR + 8u * i; };
 
   uint32_t counts[QB_COUNT];
   for (int i = 0; i < QB_COUNT; ++i) counts[i] = 1;
   counts[QB_DPFREE] = 8;
-  counts[QB_DSFULL] = 8;
-  int tile;
-  const uint32_t tmem = cta_setup(smem_raw, sbase, QB_COUNT, counts, p.ticket_dq, p.status, &tile);
+  counts[QB_DSFULL0] = counts[QB_DSFULL1] = 8;
+  counts[QB_TE0] = counts[QB_TE1] = 9;  // the MMA thread and the 8 compute warps
+  int unused;
+  const uint32_t tmem = cta_setup(smem_raw, sbase, QB_COUNT, counts, nullptr, p.status, &unused);
   AbortState st{s_abort, p.status, p.wait_limit};
-
-  // query tiles with the most key tiles first (under causal masking: the last ones)
-  const int per_m = p.B * p.H;
-  const int m = p.Mb - 1 - tile / per_m;
-  const int bh = tile - (p.Mb - 1 - m) * per_m;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
-  const int hk = h / p.G;
+  const int num_tiles = p.B * p.H * p.Mb;
   const MaskGeom gm = geom_of(p);
-  int64_t nb64, ne64;
-  n_range(gm, m, &nb64, &ne64);
-  const int n_begin = (int)nb64;
-  const int total = (*s_abort) ? 0 : (int)(ne64 - nb64);
-  const int m0 = m * kTileQ;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -552,43 +571,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tv);
       tma_prefetch_desc(&tdo);
       int issued_k[G::KST] = {0, 0, 0}, issued_v[2] = {0, 0};
-      const bool qd = total > 0;
-      if (qd) {
+      int q_loads = 0;  // Q / dO loads issued (tiles with a visible key tile)
+      int j = 0;        // steps (key tiles) loaded, over all tiles of the CTA
+      bool ok = true;
+      for (int T = 0; ok; ++T) {
+        const int slot = T & 1;
+        if (T >= 2 && !mbar_wait(bar(QB_TE0 + slot), ((T - 2) >> 1) & 1, st, kTimeoutQ - 4)) break;
+        int tile = *s_abort ? -1 : atomicAdd(p.ticket_dq, 1);
+        if (tile >= num_tiles) tile = -1;
+        s_tiles[slot] = tile;
+        mbar_arrive(bar(QB_TF0 + slot));  // release: the waiters see the slot
+        if (tile < 0) break;
+        const QTile q = q_tile_of(p, gm, tile);
+        if (q.total == 0) continue;
+        // Q / dO are free once the previous tile's last S and dP products are complete
+        if (q_loads > 0 && !mbar_wait(bar(QB_QDOE), (q_loads - 1) & 1, st, kTimeoutQ - 5)) break;
         mbar_arrive_expect_tx(bar(QB_QDO), 2 * G::TILE_BYTES);
         for (int pn = 0; pn < G::NFULL; ++pn) {
-          tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, h, m0, b, bar(QB_QDO));
-          tma_load_4d(sbase + G::OFF_DO + pn * G::FULL_BYTES, &tdo, pn * 64, h, m0, b, bar(QB_QDO));
+          tma_load_4d(sbase + G::OFF_Q + pn * G::FULL_BYTES, &tq, pn * 64, q.h, q.m0, q.b, bar(QB_QDO));
+          tma_load_4d(sbase + G::OFF_DO + pn * G::FULL_BYTES, &tdo, pn * 64, q.h, q.m0, q.b, bar(QB_QDO));
         }
         if (G::TAIL) {
-          tma_load_4d(sbase + G::OFF_Q + G::TAIL_OFF, &tq_t, G::NFULL * 64, h, m0, b, bar(QB_QDO));
-          tma_load_4d(sbase + G::OFF_DO + G::TAIL_OFF, &tdo_t, G::NFULL * 64, h, m0, b, bar(QB_QDO));
+          tma_load_4d(sbase + G::OFF_Q + G::TAIL_OFF, &tq_t, G::NFULL * 64, q.h, q.m0, q.b, bar(QB_QDO));
+          tma_load_4d(sbase + G::OFF_DO + G::TAIL_OFF, &tdo_t, G::NFULL * 64, q.h, q.m0, q.b, bar(QB_QDO));
+        }
+        ++q_loads;
+        for (int it = 0; it < q.total; ++it, ++j) {
+          const int n0 = (q.n_begin + it) * kTileK;
+          const int ks = j % G::KST;
+          if (j >= G::KST &&
+              !mbar_wait(bar(QB_KE0 + ks), ((j - G::KST) / G::KST) & 1, st, kTimeoutQ - 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kdst = sbase + G::OFF_K + ks * G::TILE_BYTES;
+          mbar_arrive_expect_tx(bar(QB_KF0 + ks), G::TILE_BYTES);
+          for (int pn = 0; pn < G::NFULL; ++pn)
+            tma_load_4d(kdst + pn * G::FULL_BYTES, &tk, pn * 64, q.hk, n0, q.b, bar(QB_KF0 + ks));
+          if (G::TAIL) tma_load_4d(kdst + G::TAIL_OFF, &tk_t, G::NFULL * 64, q.hk, n0, q.b, bar(QB_KF0 + ks));
+          issued_k[ks] = j / G::KST + 1;
+          ST_TR(1, 8, j);
+          const int vs = j & 1;
+          if (j >= 2 && !mbar_wait(bar(QB_VE0 + vs), ((j - 2) >> 1) & 1, st, kTimeoutQ - 2)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vdst = sbase + G::OFF_V + vs * G::TILE_BYTES;
+          mbar_arrive_expect_tx(bar(QB_VF0 + vs), G::TILE_BYTES);
+          for (int pn = 0; pn < G::NFULL; ++pn)
+            tma_load_4d(vdst + pn * G::FULL_BYTES, &tv, pn * 64, q.hk, n0, q.b, bar(QB_VF0 + vs));
+          if (G::TAIL) tma_load_4d(vdst + G::TAIL_OFF, &tv_t, G::NFULL * 64, q.hk, n0, q.b, bar(QB_VF0 + vs));
+          issued_v[vs] = j / 2 + 1;
         }
       }
-      for (int it = 0; it < total; ++it) {
-        const int n0 = (n_begin + it) * kTileK;
-        const int ks = it % G::KST;
-        if (it >= G::KST &&
-            !mbar_wait(bar(QB_KE0 + ks), ((it - G::KST) / G::KST) & 1, st, kTimeoutQ - 1))
-          break;
-        const uint32_t kdst = sbase + G::OFF_K + ks * G::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(QB_KF0 + ks), G::TILE_BYTES);
-        for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(kdst + pn * G::FULL_BYTES, &tk, pn * 64, hk, n0, b, bar(QB_KF0 + ks));
-        if (G::TAIL) tma_load_4d(kdst + G::TAIL_OFF, &tk_t, G::NFULL * 64, hk, n0, b, bar(QB_KF0 + ks));
-        issued_k[ks] = it / G::KST + 1;
-        ST_TR(1, 8, it);
-        const int vs = it & 1;
-        if (it >= 2 && !mbar_wait(bar(QB_VE0 + vs), ((it - 2) >> 1) & 1, st, kTimeoutQ - 2)) break;
-        const uint32_t vdst = sbase + G::OFF_V + vs * G::TILE_BYTES;
-        mbar_arrive_expect_tx(bar(QB_VF0 + vs), G::TILE_BYTES);
-        for (int pn = 0; pn < G::NFULL; ++pn)
-          tma_load_4d(vdst + pn * G::FULL_BYTES, &tv, pn * 64, hk, n0, b, bar(QB_VF0 + vs));
-        if (G::TAIL) tma_load_4d(vdst + G::TAIL_OFF, &tv_t, G::NFULL * 64, hk, n0, b, bar(QB_VF0 + vs));
-        issued_v[vs] = it / 2 + 1;
-      }
+      // every copy this thread issued lands before the CTA ends
       volatile int no_abort = 0;
       AbortState dr{&no_abort, p.status, p.wait_limit};
-      if (qd) mbar_wait(bar(QB_QDO), 0, dr, kTimeoutQ - 3);
+      if (q_loads) mbar_wait(bar(QB_QDO), (q_loads - 1) & 1, dr, kTimeoutQ - 3);
       for (int s = 0; s < G::KST; ++s)
         if (issued_k[s]) mbar_wait(bar(QB_KF0 + s), (issued_k[s] - 1) & 1, dr, kTimeoutQ - 3);
       for (int s = 0; s < 2; ++s)
@@ -596,31 +635,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // prologue S_0, dP_0, S_1; then per key tile i:
+    // per tile: S_0, dP_0, S_1; then per key tile i:
     //   dP_i+1 (needs dP_i read: runs while dS_i is formed) ; dQ += dS_i K_i (needs dS_i) ;
-    //   S_i+2 (needs dQ_i done: dS_i aliases S_i's columns, which S_i+2 reuses)
+    //   S_i+2 (needs dQ_i done: dS_i aliases S_i's columns, which S_i+2 reuses).
+    // Across tiles the step index j runs on: the S buffers, the dP buffer and every
+    // per-step barrier phase follow it.
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_N = idesc_bf16(128, G::NFULL * 64, false, true);
       constexpr uint32_t ID_N_T = idesc_bf16(128, G::TAIL ? G::TAIL : 16, false, true);
       const uint32_t sQ = sbase + G::OFF_Q, sDO = sbase + G::OFF_DO;
-      auto issue_S = [&](int it) -> bool {
-        const int ks = it % G::KST;
-        if (!mbar_wait_spin(bar(QB_KF0 + ks), (it / G::KST) & 1, st, kTimeoutQ - 11)) return false;
+      // j: the CTA's global step index of the product being issued
+      auto issue_S = [&](int j) -> bool {
+        const int ks = j % G::KST;
+        if (!mbar_wait_spin(bar(QB_KF0 + ks), (j / G::KST) & 1, st, kTimeoutQ - 11)) return false;
         tc_fence_after();
-        ST_TR(1, 0, it);
+        ST_TR(1, 0, j);
         const uint32_t sK = sbase + G::OFF_K + ks * G::TILE_BYTES;
-        const uint32_t dst = tmem + ((it & 1) ? QT_S1 : QT_S0);
+        const uint32_t dst = tmem + ((j & 1) ? QT_S1 : QT_S0);
         for (int k = 0; k < G::KSTEPS; ++k)
           mma_ss(dst, desc_kmajor<DP>(sQ, k), desc_kmajor<DP>(sK, k), ID_S, k > 0);
-        mma_commit(bar(QB_SF0 + (it & 1)));
+        mma_commit(bar(QB_SF0 + (j & 1)));
         return true;
       };
-      auto issue_dP = [&](int it) -> bool {
-        const int vs = it & 1;
-        if (!mbar_wait_spin(bar(QB_VF0 + vs), (it >> 1) & 1, st, kTimeoutQ - 13)) return false;
+      auto issue_dP = [&](int j) -> bool {
+        const int vs = j & 1;
+        if (!mbar_wait_spin(bar(QB_VF0 + vs), (j >> 1) & 1, st, kTimeoutQ - 13)) return false;
         tc_fence_after();
-        ST_TR(1, 1, it);
+        ST_TR(1, 1, j);
         const uint32_t sV = sbase + G::OFF_V + vs * G::TILE_BYTES;
         for (int k = 0; k < G::KSTEPS; ++k)
           mma_ss(tmem + QT_DP, desc_kmajor<DP>(sDO, k), desc_kmajor<DP>(sV, k), ID_S, k > 0);
@@ -628,37 +670,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(QB_VE0 + vs));
         return true;
       };
-      bool ok = total > 0 && mbar_wait_spin(bar(QB_QDO), 0, st, kTimeoutQ - 10);
-      const bool issued_any = ok;
-      if (ok) ok = issue_S(0) && issue_dP(0);
-      if (ok && total > 1) ok = issue_S(1);
-      for (int it = 0; ok && it < total; ++it) {
-        if (it + 1 < total) {
-          if (!mbar_wait_spin(bar(QB_DPFREE), it & 1, st, kTimeoutQ - 14)) break;
-          if (!issue_dP(it + 1)) break;
+      int j0 = 0, tq = 0;  // steps issued before this tile, tiles with work
+      bool ok = true;
+      for (int T = 0; ok; ++T) {
+        const int slot = T & 1;
+        if (!mbar_wait(bar(QB_TF0 + slot), (T >> 1) & 1, st, kTimeoutQ - 18)) break;
+        const int tile = s_tiles[slot];
+        mbar_arrive(bar(QB_TE0 + slot));
+        if (tile < 0) break;
+        const int total = q_tile_of(p, gm, tile).total;
+        if (total == 0) continue;
+        if (!mbar_wait_spin(bar(QB_QDO), tq & 1, st, kTimeoutQ - 10)) break;
+        // S_0 reuses the buffer of the previous tile's second-to-last step (its dQ product
+        // was waited for in that tile's loop) and dP_0 the dP buffer (read once the previous
+        // tile's last DPFREE phase completes), so both queue right behind the previous
+        // tile's last dQ product; S_1 waits for that product itself.
+        if (j0 > 0 && !mbar_wait_spin(bar(QB_DPFREE), (j0 - 1) & 1, st, kTimeoutQ - 14)) break;
+        ok = issue_S(j0) && issue_dP(j0);
+        if (ok && total == 1) mma_commit(bar(QB_QDOE));
+        if (ok && j0 > 0) ok = mbar_wait_spin(bar(QB_DQDONE), (j0 - 1) & 1, st, kTimeoutQ - 12);
+        if (ok && total > 1) ok = issue_S(j0 + 1);
+        for (int it = 0; ok && it < total; ++it) {
+          const int j = j0 + it;
+          if (it + 1 < total) {
+            if (!mbar_wait_spin(bar(QB_DPFREE), j & 1, st, kTimeoutQ - 14)) { ok = false; break; }
+            if (!issue_dP(j + 1)) { ok = false; break; }
+            // the tile's last S and dP products are issued: Q / dO free once they complete
+            if (it + 2 == total) mma_commit(bar(QB_QDOE));
+          }
+          // dQ += dS K : A = dS (bf16 pairs over S_j's columns), B = K_j MN-major, K = keys
+          // (one dS barrier per step parity: a warp that has finished step j may finish step
+          // j+1 (its S and dP are already issued) before a slower warp finishes step j, and
+          // an arrival for j+1 must not complete the phase of j)
+          if (!mbar_wait_spin(bar(QB_DSFULL0 + (j & 1)), (j >> 1) & 1, st, kTimeoutQ - 16)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          ST_TR(1, 2, j);
+          const int ks = j % G::KST;
+          const uint32_t sK = sbase + G::OFF_K + ks * G::TILE_BYTES;
+          const uint32_t sbuf = tmem + ((j & 1) ? QT_S1 : QT_S0);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t a_t = sbuf + (k >> 2) * 64 + (k & 3) * 8;
+            const uint32_t en = (it > 0 || k > 0) ? 1u : 0u;
+            mma_ts(tmem + QT_DQ, a_t, desc_mn_full<DP>(sK, k), ID_N, en);
+            if (G::TAIL) mma_ts(tmem + QT_DQ + G::NFULL * 64, a_t, desc_mn_tail<DP>(sK, k), ID_N_T, en);
+          }
+          mma_commit(bar(QB_KE0 + ks));
+          mma_commit(bar(QB_DQDONE));
+          // every DQDONE phase is waited for, in order, before the next dQ product issues
+          // (a tile's last one at the next tile's start)
+          if (it + 1 < total) {
+            if (!mbar_wait_spin(bar(QB_DQDONE), j & 1, st, kTimeoutQ - 12)) { ok = false; break; }
+            if (it + 2 < total && !issue_S(j + 2)) { ok = false; break; }
+          }
         }
-        // dQ += dS K : A = dS (bf16 pairs over S_it's columns), B = K_it MN-major, K = keys
-        if (!mbar_wait_spin(bar(QB_DSFULL), it & 1, st, kTimeoutQ - 16)) break;
-        tc_fence_after();
-        ST_TR(1, 2, it);
-        const int ks = it % G::KST;
-        const uint32_t sK = sbase + G::OFF_K + ks * G::TILE_BYTES;
-        const uint32_t sbuf = tmem + ((it & 1) ? QT_S1 : QT_S0);
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t a_t = sbuf + (k >> 2) * 64 + (k & 3) * 8;
-          const uint32_t en = (it > 0 || k > 0) ? 1u : 0u;
-          mma_ts(tmem + QT_DQ, a_t, desc_mn_full<DP>(sK, k), ID_N, en);
-          if (G::TAIL) mma_ts(tmem + QT_DQ + G::NFULL * 64, a_t, desc_mn_tail<DP>(sK, k), ID_N_T, en);
-        }
-        mma_commit(bar(QB_KE0 + ks));
-        mma_commit(bar(QB_DQDONE));
-        if (it + 2 < total) {
-          if (!mbar_wait_spin(bar(QB_DQDONE), it & 1, st, kTimeoutQ - 12)) break;
-          if (!issue_S(it + 2)) break;
-        }
+        if (!ok) break;
+        mma_commit(bar(QB_ACC));
+        j0 += total;
+        ++tq;
       }
-      mma_commit(bar(QB_ACC));
-      if (issued_any) {
+      if (j0 > 0 || tq > 0 || !ok) {
+        // every product issued is complete before tensor memory is released
         mma_commit(bar(QB_DRAIN));
         volatile int no_abort = 0;
         AbortState dr{&no_abort, p.status, p.wait_limit};
@@ -672,67 +746,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ql = qd * 32 + lane;         // query row inside the tile = TMEM lane
     const int col0 = wg * 64;
     const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
-    const int i = m0 + ql;
-    const bool row_ok = i < p.Sq;
-    const size_t row = ((size_t)b * p.H + h) * p.Sq_r + (size_t)(m0 + ql);
-    const float lse2 = p.lse2[row];  // +inf on padded rows, so P = 0 there
-    const float dsum = p.dsum[row];
     const SoftmaxConsts kc{p.scale_log2, p.cap_scale, p.cap_log2};
-
-    for (int it = 0; it < total; ++it) {
-      const int n = n_begin + it;
-      const int kb = n * kTileK + col0;  // key index of this thread's column 0
-      const bool need_mask = !tile_full(gm, m, n);
-      // visible columns: lo <= (key - i) <= hi and key < Sk  <=>  c in [cmin, cmax]
-      const int cmin = max(i + p.lo - kb, -1);
-      const int cmax = min(min(i + p.hi - kb, p.Sk - 1 - kb), 1 << 20);
-      const uint32_t sbuf = t_lane + ((it & 1) ? QT_S1 : QT_S0) + col0;
-
-      if (!warp_wait(bar(QB_SF0 + (it & 1)), (it >> 1) & 1, st, kTimeoutQ - 30)) break;
-      if (!warp_wait(bar(QB_DPFULL), it & 1, st, kTimeoutQ - 31)) break;
-      tc_fence_after();
-      if (threadIdx.x == 128) ST_TR(1, 4, it);
-      uint32_t dp[64];
-      {
-        uint32_t r[32];
-        tmem_ld32(t_lane + QT_DP + col0, r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) dp[e] = r[e];
-        tmem_ld32(t_lane + QT_DP + col0 + 32, r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) dp[32 + e] = r[e];
-      }
-      tc_fence_before();
+    int j0 = 0, tq = 0;  // steps before this tile, tiles with work
+    for (int T = 0;; ++T) {
+      const int slot = T & 1;
+      if (!warp_wait(bar(QB_TF0 + slot), (T >> 1) & 1, st, kTimeoutQ - 34)) break;
+      const int tile = s_tiles[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(QB_DPFREE));
-      if (threadIdx.x == 128) ST_TR(1, 5, it);
-      if (need_mask)
-        q_phase_ds<true, SOFTCAP>(kc, sbuf, lse2, dsum, cmin, cmax, dp);
-      else
-        q_phase_ds<false, SOFTCAP>(kc, sbuf, lse2, dsum, cmin, cmax, dp);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(QB_DSFULL));
-      if (threadIdx.x == 128) ST_TR(1, 7, it);
-    }
+      if (lane == 0) mbar_arrive(bar(QB_TE0 + slot));
+      if (tile < 0) break;
+      const QTile q = q_tile_of(p, gm, tile);
+      const int i = q.m0 + ql;
+      const bool row_ok = i < p.Sq;
+      const size_t row = ((size_t)q.b * p.H + q.h) * p.Sq_r + (size_t)(q.m0 + ql);
+      const float lse2 = p.lse2[row];  // +inf on padded rows, so P = 0 there
+      const float dsum = p.dsum[row];
+      bool ok = true;
+      for (int it = 0; it < q.total; ++it) {
+        const int j = j0 + it;
+        const int n = q.n_begin + it;
+        const int kb = n * kTileK + col0;  // key index of this thread's column 0
+        const bool need_mask = !tile_full(gm, q.m0 / kTileQ, n);
+        // visible columns: lo <= (key - i) <= hi and key < Sk  <=>  c in [cmin, cmax]
+        const int cmin = max(i + p.lo - kb, -1);
+        const int cmax = min(min(i + p.hi - kb, p.Sk - 1 - kb), 1 << 20);
+        const uint32_t sbuf = t_lane + ((j & 1) ? QT_S1 : QT_S0) + col0;
 
-    // ------------------------------------------------------------------ dQ epilogue
-    __nv_bfloat16* rowp = p.dq + (int64_t)b * p.dq_sb + (int64_t)i * p.dq_ss + (int64_t)h * p.dq_sh;
-    bool have = false;
-    if (total > 0) have = warp_wait(bar(QB_ACC), 0, st, kTimeoutQ - 33);
-    if (have) tc_fence_after();
-    if (__all_sync(0xffffffffu, *s_abort == 0)) {
+        if (!warp_wait(bar(QB_SF0 + (j & 1)), (j >> 1) & 1, st, kTimeoutQ - 30)) { ok = false; break; }
+        if (!warp_wait(bar(QB_DPFULL), j & 1, st, kTimeoutQ - 31)) { ok = false; break; }
+        tc_fence_after();
+        if (threadIdx.x == 128) ST_TR(1, 4, j);
+        uint32_t dp[64];
+        {
+          uint32_t r[32];
+          tmem_ld32(t_lane + QT_DP + col0, r);
 #pragma unroll
-      for (int c = wg; c < DP / 16; c += 2) {
-        uint32_t r[16];
-        if (have) {
-          tmem_ld16(t_lane + QT_DQ + c * 16, r);
-        } else {
+          for (int e = 0; e < 32; ++e) dp[e] = r[e];
+          tmem_ld32(t_lane + QT_DP + col0 + 32, r);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = 0u;
+          for (int e = 0; e < 32; ++e) dp[32 + e] = r[e];
         }
-        store_row16(rowp, c, p.D, r, p.dk_scale, row_ok);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_DPFREE));
+        if (threadIdx.x == 128) ST_TR(1, 5, j);
+        if (need_mask)
+          q_phase_ds<true, SOFTCAP>(kc, sbuf, lse2, dsum, cmin, cmax, dp);
+        else
+          q_phase_ds<false, SOFTCAP>(kc, sbuf, lse2, dsum, cmin, cmax, dp);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(QB_DSFULL0 + (j & 1)));
+        if (threadIdx.x == 128) ST_TR(1, 7, j);
+      }
+
+      // -------------------------------------------------------------- dQ epilogue
+      // (the accumulator columns are read before this warp's next dS arrival, which the
+      // next tile's first dQ product waits for)
+      __nv_bfloat16* rowp =
+          p.dq + (int64_t)q.b * p.dq_sb + (int64_t)i * p.dq_ss + (int64_t)q.h * p.dq_sh;
+      bool have = false;
+      if (ok && q.total > 0) have = warp_wait(bar(QB_ACC), tq & 1, st, kTimeoutQ - 33);
+      if (have) tc_fence_after();
+      if (__all_sync(0xffffffffu, ok && *s_abort == 0)) {
+#pragma unroll
+        for (int c = wg; c < DP / 16; c += 2) {
+          uint32_t r[16];
+          if (have) {
+            tmem_ld16(t_lane + QT_DQ + c * 16, r);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = 0u;
+          }
+          store_row16(rowp, c, p.D, r, p.dk_scale, row_ok);
+        }
+      } else {
+        break;
+      }
+      if (q.total > 0) {
+        j0 += q.total;
+        ++tq;
       }
     }
   }
@@ -789,6 +883,15 @@ cudaError_t launch_dependent(Kern kern, size_t smem, const BwdMainParams& p, con
 cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                              const OperandMaps& v, const OperandMaps& d, int Dp, bool softcap,
                              int num_kv_ctas, int num_q_ctas, cudaStream_t s) {
+  // the dQ kernel is persistent: one CTA per SM at most, each claiming query tiles
+  int q_ctas = num_q_ctas;
+  if (num_q_ctas > 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (q_ctas > sms) q_ctas = sms;
+  }
 #define FA_SPLIT_CASE(DPV)                                                                     \
   case DPV: {                                                                                  \
     cudaError_t e = cudaSuccess;                                                               \
@@ -800,9 +903,9 @@ cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const
     if (e != cudaSuccess) return e;                                                            \
     if (num_q_ctas > 0)                                                                        \
       e = softcap ? launch_dependent(bwd_dq_kernel<DPV, true>, GeoQ<DPV>::TOTAL, p, q, k, v, d, \
-                                     num_q_ctas, s)                                            \
+                                     q_ctas, s)                                                \
                   : launch_dependent(bwd_dq_kernel<DPV, false>, GeoQ<DPV>::TOTAL, p, q, k, v,  \
-                                     d, num_q_ctas, s);                                        \
+                                     d, q_ctas, s);                                            \
     return e;                                                                                  \
   }
   switch (Dp) {

@@ -209,7 +209,8 @@ cudaError_t launch_bwd_main(const BwdMainParams& p, const OperandMaps& q, const 
 cudaError_t launch_bwd_sparse_lists(const BwdSparseParams& p, cudaStream_t s);
 cudaError_t launch_bwd_convert(const BwdConvParams& p, bool f16, cudaStream_t s);
 // dK/dV kernel (num_kv_ctas = key tiles x batch x kv-heads) then dQ kernel (num_q_ctas =
-// query tiles x batch x q-heads), both on stream s.
+// query tiles x batch x q-heads, claimed by at most one persistent CTA per SM), both on
+// stream s.
 cudaError_t launch_bwd_split(const BwdMainParams& p, const OperandMaps& q, const OperandMaps& k,
                              const OperandMaps& v, const OperandMaps& dout, int Dp, bool softcap,
                              int num_kv_ctas, int num_q_ctas, cudaStream_t s);

@@ -177,9 +177,9 @@ size_t fa_bwd_workspace_size_dv(int B, int H, int Hk, int Sq, int Sk, int D, int
  * `stream`, after a preprocess kernel (D = rowsum(dO*O), LSE*log2e):
  *   FA_BWD_ALGO_SPLIT: a dK/dV kernel (one CTA per 128-key tile of one kv-head;
  *     recomputes P per 128-query tile; dK/dV accumulate in tensor memory over all q-heads
- *     of the kv-head, so the GQA reduction happens in-kernel) and a dQ kernel (one CTA per
- *     128-query tile of one q-head; recomputes P and dS over its key tiles; dQ accumulates
- *     in tensor memory and is written once).  No atomics: every output is summed in a
+ *     of the kv-head, so the GQA reduction happens in-kernel) and a dQ kernel (persistent
+ *     CTAs, at most one per SM, each claiming 128-query tiles of one q-head; recomputes P
+ *     and dS over the tile's key tiles; dQ accumulates in tensor memory and is written once).  No atomics: every output is summed in a
  *     fixed order, so results are bitwise reproducible whatever `deterministic` says.
  *   FA_BWD_ALGO_FUSED (default): one kernel computes all five products per (key tile, query tile)
  *     and adds fp32 dQ partials into an accumulator in the workspace (bulk reductions),
