@@ -335,9 +335,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // Per item: S_0, S_1; then per key tile j: O (+)= P_j V_j once P_j is written (and O
-    // rescaled), then S_j+2 once that product is done (P_j lives in S_j's buffer).  Key
-    // tiles are counted across items (g), so the next item's first S products only wait
-    // for the buffers, not for the softmax warps to finish the current item.
+    // rescaled), then S_j+2 right behind it (P_j lives in S_j's buffer; the products of
+    // this one thread run in issue order).  Key tiles are counted across items (g), so the
+    // next item's first S products do not wait for the softmax warps to finish the
+    // current item.
     int g = 0, on = 0;  // key tiles issued, items with work
     bool ok = true;
     for (int k = 0, idx = item_of(0); ok && idx < num_items; idx = item_of(++k)) {
@@ -349,9 +350,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const TileDescs dQ_ = tile_descs<DP>(sbase + G::OFF_Q + qb * G::TILE_BYTES);
         auto issue_S = [&](int x) -> bool {  // global key tile x into score buffer x % 2
           const int ks = x % G::KST;
-          // the buffer's previous P V product (key tile x - 2) must be done
-          if (x >= 2 && !mbar_wait_spin(bar(F_PD0 + (x & 1)), ((x - 2) >> 1) & 1, st, kFwdTimeout - 14))
-            return false;
+          // The buffer holds P of key tile x - 2, which that tile's P V product reads; this
+          // thread issued that product before (tcgen05.mma from one thread execute in issue
+          // order), so S_x is queued right behind it without waiting for its completion.
           if (!mbar_wait_spin(bar(F_KF0 + ks), (x / G::KST) & 1, st, kFwdTimeout - 11)) return false;
           tc_fence_after();
           const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K + ks * G::TILE_BYTES);
