@@ -65,11 +65,11 @@ struct GeoQ : Panels<DP> {
 
 enum KvBar : int {
   KB_KV = 0, KB_QF0, KB_QF1, KB_QE0, KB_QE1, KB_DOF0, KB_DOF1, KB_DOE0, KB_DOE1,
-  KB_SFULL, KB_DPFULL, KB_PFULL, KB_DSFULL, KB_DVDONE, KB_DKDONE, KB_ACC, KB_DRAIN, KB_COUNT
+  KB_SFULL, KB_DPFULL, KB_PFULL, KB_DSFULL, KB_ACC, KB_DRAIN, KB_COUNT
 };
 enum QBar : int {
   QB_QDO = 0, QB_KF0, QB_KF1, QB_KF2, QB_KE0, QB_KE1, QB_KE2, QB_VF0, QB_VF1, QB_VE0, QB_VE1,
-  QB_SF0, QB_SF1, QB_DPFULL, QB_DPFREE, QB_DSFULL0, QB_DSFULL1, QB_DQDONE, QB_ACC, QB_DRAIN,
+  QB_SF0, QB_SF1, QB_DPFULL, QB_DPFREE, QB_DSFULL0, QB_DSFULL1, QB_ACC, QB_DRAIN,
   QB_QDOE, QB_TF0, QB_TF1, QB_TE0, QB_TE1, QB_COUNT
 };
 
@@ -371,7 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         acc_v = 1;
         mma_commit(bar(KB_DOE0 + s));
-        mma_commit(bar(KB_DVDONE));
         // dK += dS^T Q : A = dS^T (bf16 pairs over the dP^T columns), K = 128 queries
         if (!mbar_wait_spin(bar(KB_DSFULL), it & 1, st, kTimeoutKV - 16)) break;
         tc_fence_after();
@@ -384,13 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         acc_k = 1;
         mma_commit(bar(KB_QE0 + s));
-        mma_commit(bar(KB_DKDONE));
         if (it + 1 < total) {
-          // dV_i completed while dK_i was being issued, and dK_i completes while S_i+1 is
-          // being issued, so neither TMEM reuse below waits on an idle pipe
-          if (!mbar_wait_spin(bar(KB_DVDONE), it & 1, st, kTimeoutKV - 12)) break;
+          // S_i+1 overwrites P^T_i (read by dV_i) and dP_i+1 overwrites dS^T_i (read by
+          // dK_i): both products were issued before by this thread, and tcgen05.mma
+          // operations from one thread execute in issue order, so they queue right behind
           if (!issue_S(it + 1)) break;
-          if (!mbar_wait_spin(bar(KB_DKDONE), it & 1, st, kTimeoutKV - 14)) break;
           if (!issue_dP(it + 1)) break;
         }
       }
@@ -637,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     // per tile: S_0, dP_0, S_1; then per key tile i:
     //   dP_i+1 (needs dP_i read: runs while dS_i is formed) ; dQ += dS_i K_i (needs dS_i) ;
-    //   S_i+2 (needs dQ_i done: dS_i aliases S_i's columns, which S_i+2 reuses).
+    //   S_i+2 (dS_i aliases S_i's columns, which S_i+2 reuses: it queues right behind
+    //   dQ_i, since tcgen05.mma operations from this one thread execute in issue order).
     // Across tiles the step index j runs on: the S buffers, the dP buffer and every
     // per-step barrier phase follow it.
     if (lane == 0) {
@@ -681,14 +679,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int total = q_tile_of(p, gm, tile).total;
         if (total == 0) continue;
         if (!mbar_wait_spin(bar(QB_QDO), tq & 1, st, kTimeoutQ - 10)) break;
-        // S_0 reuses the buffer of the previous tile's second-to-last step (its dQ product
-        // was waited for in that tile's loop) and dP_0 the dP buffer (read once the previous
-        // tile's last DPFREE phase completes), so both queue right behind the previous
-        // tile's last dQ product; S_1 waits for that product itself.
+        // S_0 / S_1 reuse the buffers of the previous tile's last two steps (issue order
+        // puts them behind those steps' dQ products) and dP_0 the dP buffer (read once the
+        // previous tile's last DPFREE phase completes).
         if (j0 > 0 && !mbar_wait_spin(bar(QB_DPFREE), (j0 - 1) & 1, st, kTimeoutQ - 14)) break;
         ok = issue_S(j0) && issue_dP(j0);
         if (ok && total == 1) mma_commit(bar(QB_QDOE));
-        if (ok && j0 > 0) ok = mbar_wait_spin(bar(QB_DQDONE), (j0 - 1) & 1, st, kTimeoutQ - 12);
         if (ok && total > 1) ok = issue_S(j0 + 1);
         for (int it = 0; ok && it < total; ++it) {
           const int j = j0 + it;
@@ -718,13 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (G::TAIL) mma_ts(tmem + QT_DQ + G::NFULL * 64, a_t, desc_mn_tail<DP>(sK, k), ID_N_T, en);
           }
           mma_commit(bar(QB_KE0 + ks));
-          mma_commit(bar(QB_DQDONE));
-          // every DQDONE phase is waited for, in order, before the next dQ product issues
-          // (a tile's last one at the next tile's start)
-          if (it + 1 < total) {
-            if (!mbar_wait_spin(bar(QB_DQDONE), j & 1, st, kTimeoutQ - 12)) { ok = false; break; }
-            if (it + 2 < total && !issue_S(j + 2)) { ok = false; break; }
-          }
+          // S_j+2 overwrites dS_j (read by dQ_j, issued just above): issue order suffices
+          if (it + 2 < total && !issue_S(j + 2)) { ok = false; break; }
         }
         if (!ok) break;
         mma_commit(bar(QB_ACC));
