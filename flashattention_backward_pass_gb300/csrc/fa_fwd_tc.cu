@@ -73,7 +73,7 @@ struct GeoF : Panels<DP> {
 enum FBar : int {
   F_QF0 = 0, F_QF1, F_QE0, F_QE1, F_KF0, F_KF1, F_KE0, F_KE1, F_VF0, F_VF1, F_VE0, F_VE1,
   F_SF0, F_SF1, F_PF0, F_PF1, F_PD0, F_PD1, F_ACC0, F_ACC1, F_OE0, F_OE1, F_DRAIN,
-  F_OS0, F_OS1, F_COUNT
+  F_OS0, F_OS1, F_DRAIN2, F_COUNT
 };
 static_assert(F_COUNT <= 32, "barrier area holds 32 mbarriers");
 
@@ -332,13 +332,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_wait(bar(F_QF0 + (last & 1)), (last >> 1) & 1, dr, kFwdTimeout - 3);
         }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    // Per item: S_0, S_1; then per key tile j: O (+)= P_j V_j once P_j is written (and O
-    // rescaled), then S_j+2 right behind it (P_j lives in S_j's buffer; the products of
-    // this one thread run in issue order).  Key tiles are counted across items (g), so the
-    // next item's first S products do not wait for the softmax warps to finish the
-    // current item.
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 1 issues the P V products, warp 3 the score products.  Per key tile j (counted
+    // across items): S_j once K_j is loaded (and, at an item's first tile, its Q) and the
+    // P V product of key tile j-2 is complete (P_j-2 lives in the buffer S_j overwrites);
+    // O (+)= P_j V_j once P_j is written (and O rescaled).  A thread's tcgen05.mma issue
+    // stalls while the products before it drain, so one thread issuing both kinds in
+    // turn held each P V product back behind the score product issued before it; with two
+    // issuers, P V starts as soon as P is ready.
+    const bool s_side = warp == 3;
     int g = 0, on = 0;  // key tiles issued, items with work
     bool ok = true;
     for (int k = 0, idx = item_of(0); ok && idx < num_items; idx = item_of(++k)) {
@@ -347,45 +350,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (I.nvis == 0) continue;
       if (lane == 0) {
         const int qb = on & 1;
-        const TileDescs dQ_ = tile_descs<DP>(sbase + G::OFF_Q + qb * G::TILE_BYTES);
-        auto issue_S = [&](int x) -> bool {  // global key tile x into score buffer x % 2
-          const int ks = x % G::KST;
-          // The buffer holds P of key tile x - 2, which that tile's P V product reads; this
-          // thread issued that product before (tcgen05.mma from one thread execute in issue
-          // order), so S_x is queued right behind it without waiting for its completion.
-          if (!mbar_wait_spin(bar(F_KF0 + ks), (x / G::KST) & 1, st, kFwdTimeout - 11)) return false;
-          tc_fence_after();
-          const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K + ks * G::TILE_BYTES);
-          mma_kmajor<DP, F16>(tmem + FT_S0 + (x & 1) * 128, dQ_, dK_);
-          mma_commit(bar(F_SF0 + (x & 1)));
-          mma_commit(bar(F_KE0 + ks));
-          return true;
-        };
-        ok = mbar_wait_spin(bar(F_QF0 + qb), (on >> 1) & 1, st, kFwdTimeout - 10);
-        if (ok) ok = issue_S(g);
-        if (ok && I.nvis > 1) ok = issue_S(g + 1);
-        const uint32_t o_col = FT_O0 + qb * 128;
-        for (int t = 0; ok && t < I.nvis; ++t) {
-          const int x = g + t;
-          if (!mbar_wait_spin(bar(F_PF0 + (x & 1)), (x >> 1) & 1, st, kFwdTimeout - 12)) { ok = false; break; }
-          // the first product overwrites this O buffer: the item two back must have read it
-          if (t == 0 && on >= 2 &&
-              !mbar_wait_spin(bar(F_OE0 + qb), ((on - 2) >> 1) & 1, st, kFwdTimeout - 16)) {
-            ok = false;
-            break;
+        if (s_side) {
+          const TileDescs dQ_ = tile_descs<DP>(sbase + G::OFF_Q + qb * G::TILE_BYTES);
+          ok = mbar_wait_spin(bar(F_QF0 + qb), (on >> 1) & 1, st, kFwdTimeout - 10);
+          for (int t = 0; ok && t < I.nvis; ++t) {
+            const int x = g + t;  // global key tile x into score buffer x % 2
+            const int ks = x % G::KST;
+            if (x >= 2 &&
+                !mbar_wait_spin(bar(F_PD0 + (x & 1)), ((x - 2) >> 1) & 1, st, kFwdTimeout - 14)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait_spin(bar(F_KF0 + ks), (x / G::KST) & 1, st, kFwdTimeout - 11)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const TileDescs dK_ = tile_descs<DP>(sbase + G::OFF_K + ks * G::TILE_BYTES);
+            mma_kmajor<DP, F16>(tmem + FT_S0 + (x & 1) * 128, dQ_, dK_);
+            mma_commit(bar(F_SF0 + (x & 1)));
+            mma_commit(bar(F_KE0 + ks));
           }
-          const int vs = x % G::VST;
-          if (!mbar_wait_spin(bar(F_VF0 + vs), (x / G::VST) & 1, st, kFwdTimeout - 13)) { ok = false; break; }
-          tc_fence_after();
-          const TileDescs dV_ = tile_descs<DP>(sbase + G::OFF_V + vs * G::TILE_BYTES);
-          mma_dv<DP, F16>(tmem + o_col, tmem + FT_S0 + (x & 1) * 128, dV_, t > 0 ? 1u : 0u);
-          mma_commit(bar(F_VE0 + vs));
-          mma_commit(bar(F_PD0 + (x & 1)));
-          if (t + 2 < I.nvis && !issue_S(x + 2)) { ok = false; break; }
-        }
-        if (ok) {
-          mma_commit(bar(F_QE0 + qb));    // every S of the item has been issued
-          mma_commit(bar(F_ACC0 + qb));   // and every P V: O of this item is final
+          if (ok) mma_commit(bar(F_QE0 + qb));  // every S of the item has been issued
+        } else {
+          const uint32_t o_col = FT_O0 + qb * 128;
+          for (int t = 0; ok && t < I.nvis; ++t) {
+            const int x = g + t;
+            if (!mbar_wait_spin(bar(F_PF0 + (x & 1)), (x >> 1) & 1, st, kFwdTimeout - 12)) { ok = false; break; }
+            // the first product overwrites this O buffer: the item two back must have read it
+            if (t == 0 && on >= 2 &&
+                !mbar_wait_spin(bar(F_OE0 + qb), ((on - 2) >> 1) & 1, st, kFwdTimeout - 16)) {
+              ok = false;
+              break;
+            }
+            const int vs = x % G::VST;
+            if (!mbar_wait_spin(bar(F_VF0 + vs), (x / G::VST) & 1, st, kFwdTimeout - 13)) { ok = false; break; }
+            tc_fence_after();
+            const TileDescs dV_ = tile_descs<DP>(sbase + G::OFF_V + vs * G::TILE_BYTES);
+            mma_dv<DP, F16>(tmem + o_col, tmem + FT_S0 + (x & 1) * 128, dV_, t > 0 ? 1u : 0u);
+            mma_commit(bar(F_VE0 + vs));
+            mma_commit(bar(F_PD0 + (x & 1)));
+          }
+          if (ok) mma_commit(bar(F_ACC0 + qb));  // every P V: O of this item is final
         }
       }
       g += I.nvis;
@@ -393,11 +399,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     if (lane == 0 && g > 0) {
-      // every MMA must be complete before the CTA releases tensor memory
-      mma_commit(bar(F_DRAIN));
+      // every product this thread issued is complete before the CTA releases tensor memory
+      const uint32_t drain = bar(s_side ? F_DRAIN2 : F_DRAIN);
+      mma_commit(drain);
       volatile int no_abort = 0;
       AbortState dr{&no_abort, p.status, p.wait_limit};
-      mbar_wait(bar(F_DRAIN), 0, dr, kFwdTimeout - 15);
+      mbar_wait(drain, 0, dr, kFwdTimeout - 15);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + epilogue
