@@ -30,11 +30,11 @@
 // tiles a rescale is rare.
 //
 // Warp roles (12 warps): warp 0 TMA producer of Q (two buffers) and of the K ring; warp 2
-// TMA producer of the V ring; warp 1 TMEM allocator and MMA issue (one lane issues);
-// warps 4-11 two softmax / epilogue warpgroups (warp w reads TMEM lanes 32 (w % 4) ..
-// +31).  Warp 3 only joins the CTA barriers.  Every role walks the same item list and
-// counts key tiles and items with work the same way, so the ring and buffer phases agree
-// without any exchange.
+// TMA producer of the V ring; warp 1 TMEM allocator and issuer of the P V products, warp
+// 3 issuer of the score products (one lane of each issues); warps 4-11 two softmax /
+// epilogue warpgroups (warp w reads TMEM lanes 32 (w % 4) .. +31).  Every role walks the
+// same item list and counts key tiles and items with work the same way, so the ring and
+// buffer phases agree without any exchange.
 //
 // Tensor memory: S buffers [0, 128) and [128, 256) (P written over the first 32 columns
 // of each 64-column half), O accumulators [256, 256 + Dp) and [384, 384 + Dp).
