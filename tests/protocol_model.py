@@ -1,0 +1,483 @@
+"""Discrete-event model of the mbarrier protocols of the split algorithm's dQ kernel and of
+the forward kernel, for the CPU tests in test_protocol_cpu.py.
+
+Each role of a kernel is a Python generator that yields the operations its CUDA code
+performs, in program order: barrier waits and arrivals, tensor-memory / shared-memory
+reads and writes, asynchronous copies (TMA) and asynchronous products (tcgen05.mma) with
+their commits.  A scheduler interleaves the roles, the copies and the products of each
+issuing thread (which execute in issue order) at random, and checks what the hardware
+does not:
+
+* a wait for phase k of a barrier passes when the barrier's phase parity differs from
+  k's (mbarrier.try_wait.parity); it is an error if that happens before phase k has
+  completed (the wait would pass early), or if phase k + 1 had already completed when the
+  wait was first reached (the parity would alias a later phase);
+* an arrival meant for phase k while the barrier is still collecting another phase is an
+  error (it would complete the wrong phase);
+* every buffer holds a tag naming the data in it; a read that finds another tag than the
+  one the code relies on is a data race;
+* no role may be left waiting (deadlock).
+
+The models restate the kernels' barrier and buffer logic; they import nothing from the
+package and run no GPU code.
+"""
+
+import itertools
+import random
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+class Sim:
+    def __init__(self, seed):
+        self.rng = random.Random(seed)
+        self.bars = {}
+        self.bufs = {}
+        self.agents = {}   # name -> [generator, pending request, first evaluation done]
+        self.pipes = {}    # issuing thread -> list of products / commits in issue order
+        self.copies = []   # asynchronous copies in flight: (barrier, phase, writes)
+        self.shared = {}   # plain shared-memory variables the roles exchange
+
+    def barrier(self, name, count=1):
+        self.bars[name] = {"count": count, "arrived": 0, "done": 0}
+
+    def add(self, name, gen):
+        self.agents[name] = [gen, None, False]
+
+    # ------------------------------------------------------------------ primitives
+    def _arrive(self, bar, k, who):
+        b = self.bars[bar]
+        if b["done"] != k:
+            raise ProtocolError(f"{who}: arrival for phase {k} of {bar} while it collects "
+                                f"phase {b['done']}")
+        b["arrived"] += 1
+        if b["arrived"] == b["count"]:
+            b["arrived"] = 0
+            b["done"] += 1
+
+    def _read(self, buf, tag, who):
+        cur = self.bufs.get(buf)
+        if cur != tag:
+            raise ProtocolError(f"{who}: reads {buf} expecting {tag}, finds {cur}")
+
+    def _wait_passes(self, bar, k):
+        return (self.bars[bar]["done"] & 1) != (k & 1)
+
+    # ------------------------------------------------------------------ roles
+    def _runnable(self, name):
+        gen, req, _ = self.agents[name]
+        if req is None:
+            return True
+        return req[0] != "wait" or self._wait_passes(req[1], req[2])
+
+    def _step_agent(self, name):
+        st = self.agents[name]
+        if st[1] is None:
+            try:
+                st[1] = next(st[0])
+            except StopIteration:
+                del self.agents[name]
+                return
+            st[2] = False
+        req = st[1]
+        kind = req[0]
+        if kind == "wait":
+            _, bar, k = req
+            done = self.bars[bar]["done"]
+            if not st[2]:
+                st[2] = True
+                if done >= k + 2:
+                    raise ProtocolError(f"{name}: waits for phase {k} of {bar}, which has "
+                                        f"completed {done} phases (parity aliases)")
+            if not self._wait_passes(bar, k):
+                return  # blocked
+            if done < k + 1:
+                raise ProtocolError(f"{name}: wait for phase {k} of {bar} passes with only "
+                                    f"{done} phases completed")
+        elif kind == "arrive":
+            self._arrive(req[1], req[2], name)
+        elif kind == "read":
+            self._read(req[1], req[2], name)
+        elif kind == "write":
+            self.bufs[req[1]] = req[2]
+        elif kind == "copy":  # (copy, barrier, phase, writes)
+            self.copies.append((req[1], req[2], req[3]))
+        elif kind in ("mma", "commit"):  # (mma, thread, reads, writes) / (commit, thread, bar, k)
+            self.pipes.setdefault(req[1], []).append(req)
+        else:
+            raise ValueError(kind)
+        st[1] = None
+
+    # ------------------------------------------------------------------ asynchronous work
+    def _step_pipe(self, thread):
+        op = self.pipes[thread].pop(0)
+        if op[0] == "mma":
+            for buf, tag in op[2]:
+                self._read(buf, tag, f"product of {thread}")
+            for buf, tag in op[3]:
+                self.bufs[buf] = tag
+        else:
+            self._arrive(op[2], op[3], f"commit of {thread}")
+
+    def _step_copy(self, i):
+        bar, k, writes = self.copies.pop(i)
+        for buf, tag in writes:
+            self.bufs[buf] = tag
+        self._arrive(bar, k, "copy")
+
+    def run(self, max_steps=2_000_000):
+        for _ in range(max_steps):
+            choices = [("a", n) for n in list(self.agents) if self._runnable(n)]
+            choices += [("p", t) for t, q in self.pipes.items() if q]
+            choices += [("c", i) for i in range(len(self.copies))]
+            if not choices:
+                if self.agents:
+                    blocked = {n: st[1] for n, st in self.agents.items()}
+                    raise ProtocolError(f"deadlock: {blocked}")
+                return
+            kind, x = self.rng.choice(choices)
+            if kind == "a":
+                self._step_agent(x)
+            elif kind == "p":
+                self._step_pipe(x)
+            else:
+                self._step_copy(x)
+        raise ProtocolError("step limit")
+
+
+# ============================================================================ dQ kernel
+
+def dq_kernel(sim, totals, warps=2, kst=3, dsfull_per_parity=True):
+    """The split algorithm's persistent dQ kernel on one CTA: `totals[t]` key tiles for the
+    t-th query tile it claims.  `warps` compute warps stand for the eight (each arrives on
+    the per-step barriers once).  dsfull_per_parity=False restores the single dS-full
+    barrier the kernel had before (one barrier for every step)."""
+    W = warps
+    for b in ["QDO", "QDOE", "DPFULL", "ACC"]:
+        sim.barrier(b)
+    sim.barrier("DPFREE", W)
+    for s in range(kst):
+        sim.barrier(f"KF{s}")
+        sim.barrier(f"KE{s}")
+    for s in range(2):
+        sim.barrier(f"VF{s}")
+        sim.barrier(f"VE{s}")
+        sim.barrier(f"SF{s}")
+        sim.barrier(f"TF{s}")
+        sim.barrier(f"TE{s}", 1 + W)
+    if dsfull_per_parity:
+        sim.barrier("DSFULL0", W)
+        sim.barrier("DSFULL1", W)
+    else:
+        sim.barrier("DSFULL", W)
+    slots = [None, None]
+    ticket = itertools.count()
+
+    def ds_bar(j):
+        return (f"DSFULL{j & 1}", j >> 1) if dsfull_per_parity else ("DSFULL", j)
+
+    def producer():
+        q_loads = 0
+        j = 0
+        for T in itertools.count():
+            slot = T & 1
+            if T >= 2:
+                yield ("wait", f"TE{slot}", (T - 2) >> 1)
+            tile = next(ticket)
+            if tile >= len(totals):
+                tile = -1
+            slots[slot] = tile
+            yield ("arrive", f"TF{slot}", T >> 1)
+            if tile < 0:
+                return
+            total = totals[tile]
+            if total == 0:
+                continue
+            if q_loads > 0:
+                yield ("wait", "QDOE", q_loads - 1)
+            yield ("copy", "QDO", q_loads, [("Q", ("Q", tile))])
+            q_loads += 1
+            for _ in range(total):
+                ks = j % kst
+                if j >= kst:
+                    yield ("wait", f"KE{ks}", (j - kst) // kst)
+                yield ("copy", f"KF{ks}", j // kst, [(f"K{ks}", ("K", j))])
+                vs = j & 1
+                if j >= 2:
+                    yield ("wait", f"VE{vs}", (j - 2) >> 1)
+                yield ("copy", f"VF{vs}", j >> 1, [(f"V{vs}", ("V", j))])
+                j += 1
+
+    def mma():
+        def issue_s(j, tile):
+            ks = j % kst
+            yield ("wait", f"KF{ks}", j // kst)
+            yield ("mma", "mma", [("Q", ("Q", tile)), (f"K{ks}", ("K", j))],
+                   [(f"S{j & 1}.{p}", ("S", j)) for p in range(W)])
+            yield ("commit", "mma", f"SF{j & 1}", j >> 1)
+
+        def issue_dp(j, tile):
+            vs = j & 1
+            yield ("wait", f"VF{vs}", j >> 1)
+            yield ("mma", "mma", [("Q", ("Q", tile)), (f"V{vs}", ("V", j))],
+                   [(f"DP.{p}", ("dP", j)) for p in range(W)])
+            yield ("commit", "mma", "DPFULL", j)
+            yield ("commit", "mma", f"VE{vs}", j >> 1)
+
+        j0 = tq = 0
+        for T in itertools.count():
+            slot = T & 1
+            yield ("wait", f"TF{slot}", T >> 1)
+            tile = slots[slot]
+            yield ("arrive", f"TE{slot}", T >> 1)
+            if tile < 0:
+                return
+            total = totals[tile]
+            if total == 0:
+                continue
+            yield ("wait", "QDO", tq)
+            if j0 > 0:
+                yield ("wait", "DPFREE", j0 - 1)
+            yield from issue_s(j0, tile)
+            yield from issue_dp(j0, tile)
+            if total == 1:
+                yield ("commit", "mma", "QDOE", tq)
+            if total > 1:
+                yield from issue_s(j0 + 1, tile)
+            for it in range(total):
+                j = j0 + it
+                if it + 1 < total:
+                    yield ("wait", "DPFREE", j)
+                    yield from issue_dp(j + 1, tile)
+                    if it + 2 == total:
+                        yield ("commit", "mma", "QDOE", tq)
+                yield ("wait",) + ds_bar(j)
+                ks = j % kst
+                reads = [(f"S{j & 1}.{p}", ("dS", j)) for p in range(W)] + [(f"K{ks}", ("K", j))]
+                if it > 0:
+                    reads += [(f"DQ.{p}", ("dQ", tile, it - 1)) for p in range(W)]
+                yield ("mma", "mma", reads, [(f"DQ.{p}", ("dQ", tile, it)) for p in range(W)])
+                yield ("commit", "mma", f"KE{ks}", j // kst)
+                if it + 2 < total:
+                    yield from issue_s(j + 2, tile)
+            yield ("commit", "mma", "ACC", tq)
+            j0 += total
+            tq += 1
+
+    def compute(p):
+        j0 = tq = 0
+        for T in itertools.count():
+            slot = T & 1
+            yield ("wait", f"TF{slot}", T >> 1)
+            tile = slots[slot]
+            yield ("arrive", f"TE{slot}", T >> 1)
+            if tile < 0:
+                return
+            total = totals[tile]
+            for it in range(total):
+                j = j0 + it
+                b = j & 1
+                yield ("wait", f"SF{b}", j >> 1)
+                yield ("wait", "DPFULL", j)
+                yield ("read", f"DP.{p}", ("dP", j))
+                yield ("arrive", "DPFREE", j)
+                yield ("read", f"S{b}.{p}", ("S", j))
+                yield ("write", f"S{b}.{p}", ("dS", j))
+                yield ("arrive",) + ds_bar(j)
+            if total > 0:
+                yield ("wait", "ACC", tq)
+                yield ("read", f"DQ.{p}", ("dQ", tile, total - 1))
+                j0 += total
+                tq += 1
+
+    sim.add("producer", producer())
+    sim.add("mma", mma())
+    for p in range(W):
+        sim.add(f"compute{p}", compute(p))
+
+
+# ============================================================================ forward kernel
+
+def forward_kernel(sim, nvis, warps=2, kst=2, vst=2, rescale=0.3, two_issuers=True,
+                   s_waits_pd=True):
+    """The forward kernel on one CTA: `nvis[i]` visible key tiles for its i-th item.
+    `warps` softmax warps stand for the eight (each arrives on the P-full, O-empty and
+    O-staged barriers once).  A softmax warp rescales its O rows before a key tile's P V
+    product with probability `rescale` (seeded), after waiting for the previous product.
+    two_issuers=False issues both kinds of product from one thread (the kernel's earlier
+    form).  s_waits_pd=False drops the score products' wait for the P V product whose P
+    they overwrite: safe for one issuing thread (issue order), a race for two."""
+    W = warps
+    rng = random.Random(sim.rng.random())
+    for s in range(2):
+        for b in ["QF", "QE", "SF", "PD", "ACC"]:
+            sim.barrier(f"{b}{s}")
+        for b in ["PF", "OE", "OS"]:
+            sim.barrier(f"{b}{s}", W)
+    for s in range(kst):
+        sim.barrier(f"KF{s}")
+        sim.barrier(f"KE{s}")
+    for s in range(vst):
+        sim.barrier(f"VF{s}")
+        sim.barrier(f"VE{s}")
+    sim.barrier("NB", W)  # the softmax warps' per-item named barrier, as a rendezvous
+    resc = {(x, p): rng.random() < rescale for x in range(sum(nvis)) for p in range(W)}
+    stores = {}  # (warp, item) -> whether its tensor store has read the staged O
+
+    def k_producer():
+        qn = c = 0
+        for item, n in enumerate(nvis):
+            if n == 0:
+                continue
+            qb = qn & 1
+            if qn >= 2:
+                yield ("wait", f"QE{qb}", (qn - 2) >> 1)
+                yield ("wait", f"OS{qb}", (qn - 2) >> 1)
+            yield ("copy", f"QF{qb}", qn >> 1, [(f"Q{qb}.{p}", ("Q", item)) for p in range(W)])
+            for _ in range(n):
+                ks = c % kst
+                if c >= kst:
+                    yield ("wait", f"KE{ks}", (c - kst) // kst)
+                yield ("copy", f"KF{ks}", c // kst, [(f"K{ks}", ("K", c))])
+                c += 1
+            qn += 1
+
+    def v_producer():
+        c = 0
+        for n in nvis:
+            for _ in range(n):
+                vs = c % vst
+                if c >= vst:
+                    yield ("wait", f"VE{vs}", (c - vst) // vst)
+                yield ("copy", f"VF{vs}", c // vst, [(f"V{vs}", ("V", c))])
+                c += 1
+
+    def issue_s(thread, x, item, qb):
+        ks = x % kst
+        yield ("wait", f"KF{ks}", x // kst)
+        yield ("mma", thread, [(f"Q{qb}.{p}", ("Q", item)) for p in range(W)] + [(f"K{ks}", ("K", x))],
+               [(f"S{x & 1}.{p}", ("S", x)) for p in range(W)])
+        yield ("commit", thread, f"SF{x & 1}", x >> 1)
+        yield ("commit", thread, f"KE{ks}", x // kst)
+
+    def issue_pv(thread, x, t, item, on, qb):
+        yield ("wait", f"PF{x & 1}", x >> 1)
+        if t == 0 and on >= 2:
+            yield ("wait", f"OE{qb}", (on - 2) >> 1)
+        vs = x % vst
+        yield ("wait", f"VF{vs}", x // vst)
+        reads = [(f"S{x & 1}.{p}", ("P", x)) for p in range(W)] + [(f"V{vs}", ("V", x))]
+        if t > 0:
+            reads += [(f"O{qb}.{p}", ("Or" if resc[(x, p)] else "O", item, t - 1)) for p in range(W)]
+        yield ("mma", thread, reads, [(f"O{qb}.{p}", ("O", item, t)) for p in range(W)])
+        yield ("commit", thread, f"VE{vs}", x // vst)
+        yield ("commit", thread, f"PD{x & 1}", x >> 1)
+
+    def s_issuer():
+        g = on = 0
+        for item, n in enumerate(nvis):
+            if n == 0:
+                continue
+            qb = on & 1
+            yield ("wait", f"QF{qb}", on >> 1)
+            for t in range(n):
+                x = g + t
+                if x >= 2 and s_waits_pd:
+                    yield ("wait", f"PD{x & 1}", (x - 2) >> 1)
+                yield from issue_s("s", x, item, qb)
+            yield ("commit", "s", f"QE{qb}", on >> 1)
+            g += n
+            on += 1
+
+    def pv_issuer():
+        g = on = 0
+        for item, n in enumerate(nvis):
+            if n == 0:
+                continue
+            qb = on & 1
+            for t in range(n):
+                yield from issue_pv("pv", g + t, t, item, on, qb)
+            yield ("commit", "pv", f"ACC{qb}", on >> 1)
+            g += n
+            on += 1
+
+    def one_issuer():
+        g = on = 0
+        for item, n in enumerate(nvis):
+            if n == 0:
+                continue
+            qb = on & 1
+
+            def s_after_pd(x):
+                if x >= 2 and s_waits_pd:
+                    yield ("wait", f"PD{x & 1}", (x - 2) >> 1)
+                yield from issue_s("mma", x, item, qb)
+
+            yield ("wait", f"QF{qb}", on >> 1)
+            yield from s_after_pd(g)
+            if n > 1:
+                yield from s_after_pd(g + 1)
+            for t in range(n):
+                x = g + t
+                yield from issue_pv("mma", x, t, item, on, qb)
+                if t + 2 < n:
+                    yield from s_after_pd(x + 2)
+            yield ("commit", "mma", f"QE{qb}", on >> 1)
+            yield ("commit", "mma", f"ACC{qb}", on >> 1)
+            g += n
+            on += 1
+
+    def softmax(p):
+        g = on = 0
+        os_pend = None  # (buffer, phase, item) whose staged O this warp's store may still read
+
+        def flush():
+            nonlocal os_pend
+            if os_pend is not None:
+                qb_, ph, it_ = os_pend
+                # bulk_wait_read_all: the store has read the staged rows
+                yield ("read", f"Q{qb_}.{p}", ("Ostage", it_))
+                stores[(p, it_)] = True
+                yield ("arrive", f"OS{qb_}", ph)
+                os_pend = None
+
+        for item, n in enumerate(nvis):
+            qb = on & 1
+            for t in range(n):
+                x = g + t
+                b = x & 1
+                yield ("wait", f"SF{b}", x >> 1)
+                yield ("read", f"S{b}.{p}", ("S", x))
+                if t > 0 and resc[(x, p)]:
+                    yield ("wait", f"PD{(x - 1) & 1}", (x - 1) >> 1)
+                    yield ("read", f"O{qb}.{p}", ("O", item, t - 1))
+                    yield ("write", f"O{qb}.{p}", ("Or", item, t - 1))
+                yield ("write", f"S{b}.{p}", ("P", x))
+                yield ("arrive", f"PF{b}", x >> 1)
+                if t == 0:
+                    yield from flush()
+            if n > 0:
+                yield ("wait", f"ACC{qb}", on >> 1)
+            yield ("arrive", "NB", item)
+            yield ("wait", "NB", item)
+            yield from flush()
+            if n > 0:
+                yield ("read", f"O{qb}.{p}", ("O", item, n - 1))
+                yield ("write", f"Q{qb}.{p}", ("Ostage", item))
+                yield ("arrive", f"OE{qb}", on >> 1)
+                os_pend = (qb, on >> 1, item)
+                g += n
+                on += 1
+        yield from flush()
+
+    sim.add("k_producer", k_producer())
+    sim.add("v_producer", v_producer())
+    if two_issuers:
+        sim.add("s_issuer", s_issuer())
+        sim.add("pv_issuer", pv_issuer())
+    else:
+        sim.add("mma", one_issuer())
+    for p in range(W):
+        sim.add(f"softmax{p}", softmax(p))
