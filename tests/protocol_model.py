@@ -481,3 +481,238 @@ def forward_kernel(sim, nvis, warps=2, kst=2, vst=2, rescale=0.3, two_issuers=Tr
         sim.add("mma", one_issuer())
     for p in range(W):
         sim.add(f"softmax{p}", softmax(p))
+
+
+# ============================================================================ main kernel
+
+def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, dv_waits_dp=True):
+    """The fused backward's main kernel on one CTA (unordered mode): `tiles[t]` steps for
+    the t-th key tile it claims.  `warps` compute warps stand for the eight and `drains`
+    dQ-drain warps for the four.  kst: K stages (1 at Dp = 96 / 128, 2 at Dp <= 80).
+    issuers=2 models a split of the MMA issue over two threads (S and dP from one, dV, dK
+    and dQ from the other) with the completion waits that split needs; dv_waits_dp=False
+    drops the one it adds (dO is read by dP_i and dV_i, issued by different threads, so
+    the dO buffer may only be handed back once both are complete)."""
+    W, D = warps, drains
+    ones = ["V", "SFULL", "DPFULL", "DVDONE", "DQFULL", "DSEMPTY", "ACC", "NEXT", "VEMPTY"]
+    for b in ones + [f"K{s}" for s in range(kst)] + [f"KEMPTY{s}" for s in range(kst)]:
+        sim.barrier(b)
+    for s in range(2):
+        sim.barrier(f"QF{s}")
+        sim.barrier(f"QE{s}")
+        sim.barrier(f"TF{s}")
+        sim.barrier(f"TE{s}", 1 + issuers + D + W)
+    sim.barrier("DOF")
+    sim.barrier("DOE")
+    for b in ["PFULL", "DSFULL", "DVEMPTY", "DKEMPTY"]:
+        sim.barrier(b, W)
+    sim.barrier("DQEMPTY", D)
+    ring = [None, None]
+    ticket = itertools.count()
+
+    def scheduler():
+        for t in itertools.count():
+            if t >= 1:
+                yield ("wait", "NEXT", t - 1)
+            if t >= 2:
+                yield ("wait", f"TE{t & 1}", (t - 2) >> 1)
+            tk = next(ticket)
+            ring[t & 1] = (tk, tiles[tk]) if tk < len(tiles) else None
+            yield ("arrive", f"TF{t & 1}", t >> 1)
+            if ring[t & 1] is None:
+                return
+
+    def k_stage(kt):
+        return (kt & 1, kt >> 1) if kst == 2 else (0, kt)
+
+    def producer():
+        git = nk = nv = 0
+        for t in itertools.count():
+            yield ("wait", f"TF{t & 1}", t >> 1)
+            d = ring[t & 1]
+            yield ("arrive", f"TE{t & 1}", t >> 1)
+            if d is None:
+                return
+            tk, total = d
+            if total == 0:
+                yield ("arrive", "NEXT", t)
+                continue
+
+            def load_k():
+                nonlocal nk
+                ks, ph = k_stage(nk)
+                nk += 1
+                yield ("copy", f"K{ks}", ph, [(f"Ks{ks}", ("K", tk))])
+
+            def load_v():
+                nonlocal nv
+                nv += 1
+                yield ("copy", "V", nv - 1, [("Vs", ("V", tk))])
+
+            kv_busy = nk > 0
+            if kst == 2 and kv_busy:
+                if nk >= 2:
+                    yield ("wait", f"KEMPTY{nk & 1}", (nk >> 1) - 1)
+                yield from load_k()
+            if not kv_busy:
+                yield from load_k()
+                yield from load_v()
+            for it in range(total):
+                s = git & 1
+                if it == total - 1:
+                    yield ("arrive", "NEXT", t)
+                if git >= 2:
+                    yield ("wait", f"QE{s}", (git - 2) >> 1)
+                yield ("copy", f"QF{s}", git >> 1, [(f"Q{s}", ("Q", git))])
+                if it == 0 and kv_busy:
+                    yield ("wait", "VEMPTY", nv - 1)
+                    yield from load_v()
+                if git >= 1:
+                    yield ("wait", "DOE", git - 1)
+                yield ("copy", "DOF", git, [("dO", ("dO", git))])
+                if kst == 1 and it == 0 and kv_busy:
+                    yield ("wait", "KEMPTY0", nk - 1)
+                    yield from load_k()
+                git += 1
+
+    def mma_s(th, git, tk, ks):
+        s = git & 1
+        yield ("wait", f"QF{s}", git >> 1)
+        yield ("mma", th, [(f"Ks{ks}", ("K", tk)), (f"Q{s}", ("Q", git))],
+               [(f"S.{p}", ("S", git)) for p in range(W)])
+        yield ("commit", th, "SFULL", git)
+
+    def mma_dp(th, git, tk):
+        yield ("wait", "DOF", git)
+        yield ("mma", th, [("Vs", ("V", tk)), ("dO", ("dO", git))],
+               [(f"DP.{p}", ("dP", git)) for p in range(W)] +
+               [(f"DP.d{q}", ("dP", git)) for q in range(D)])
+        yield ("commit", th, "DPFULL", git)
+
+    def mma(role):
+        # role: "all" (one issuer), "sdp" (S and dP), "rest" (dV, dK, dQ)
+        git = kt = 0
+        th = "mma" if role == "all" else role
+        do_s = role in ("all", "sdp")
+        do_rest = role in ("all", "rest")
+        for t in itertools.count():
+            yield ("wait", f"TF{t & 1}", t >> 1)
+            d = ring[t & 1]
+            yield ("arrive", f"TE{t & 1}", t >> 1)
+            if d is None:
+                return
+            tk, total = d
+            if total == 0:
+                continue
+            ks, kph = k_stage(kt)
+            if do_s:
+                if git > 0:
+                    yield ("wait", "DVDONE", git - 1)
+                yield ("wait", f"K{ks}", kph)
+                yield from mma_s(th, git, tk, ks)
+                if git > 0:
+                    yield ("wait", "DQEMPTY", git - 1)
+                yield ("wait", "V", kt)
+                yield from mma_dp(th, git, tk)
+                if total == 1:
+                    yield ("commit", th, "VEMPTY", kt)
+            for it in range(total):
+                s = git & 1
+                if do_rest:
+                    yield ("wait", "PFULL", git)
+                    if it == 0 and kt > 0:
+                        yield ("wait", "DVEMPTY", kt - 1)
+                    reads = [(f"S.{p}", ("P", git)) for p in range(W)] + [("dO", ("dO", git))]
+                    if it > 0:
+                        reads += [(f"DV.{p}", ("DV", kt, it - 1)) for p in range(W)]
+                    if role == "rest" and dv_waits_dp:
+                        # dO is also read by dP_git, issued by the other thread: it must be
+                        # complete before the dO buffer is handed back
+                        yield ("wait", "DPFULL", git)
+                    yield ("mma", th, reads, [(f"DV.{p}", ("DV", kt, it)) for p in range(W)])
+                    yield ("commit", th, "DOE", git)
+                    yield ("commit", th, "DVDONE", git)
+                if do_s and it + 1 < total:
+                    yield ("wait", "DVDONE", git)
+                    yield from mma_s(th, git + 1, tk, ks)
+                if do_rest:
+                    yield ("wait", "DSFULL", git)
+                    if it == 0 and kt > 0:
+                        yield ("wait", "DKEMPTY", kt - 1)
+                    reads = [(f"DS.{p}", ("dS", git)) for p in range(W)] + [(f"Q{s}", ("Q", git))]
+                    if it > 0:
+                        reads += [(f"DK.{p}", ("DK", kt, it - 1)) for p in range(W)]
+                    yield ("mma", th, reads, [(f"DK.{p}", ("DK", kt, it)) for p in range(W)])
+                    yield ("commit", th, f"QE{s}", git >> 1)
+                    # the dQ tile goes over the dP^T columns (all of them)
+                    yield ("mma", th, [(f"DS.{p}", ("dS", git)) for p in range(W)] + [(f"Ks{ks}", ("K", tk))],
+                           [(f"DP.d{q}", ("dQ", git)) for q in range(D)] +
+                           [(f"DP.{p}", ("dQ", git)) for p in range(W)])
+                    yield ("commit", th, "DQFULL", git)
+                    yield ("commit", th, "DSEMPTY", git)
+                if do_s and it + 1 < total:
+                    yield ("wait", "DQEMPTY", git)
+                    yield from mma_dp(th, git + 1, tk)
+                    if it + 2 == total:
+                        yield ("commit", th, "VEMPTY", kt)
+                git += 1
+            if do_rest:
+                yield ("commit", th, "ACC", kt)
+                yield ("commit", th, f"KEMPTY{ks}", kph)
+            kt += 1
+
+    def drain(q):
+        git = 0
+        for t in itertools.count():
+            yield ("wait", f"TF{t & 1}", t >> 1)
+            d = ring[t & 1]
+            yield ("arrive", f"TE{t & 1}", t >> 1)
+            if d is None:
+                return
+            for _ in range(d[1]):
+                yield ("wait", "DQFULL", git)
+                yield ("read", f"DP.d{q}", ("dQ", git))
+                yield ("arrive", "DQEMPTY", git)
+                git += 1
+
+    def compute(p):
+        git = kt = 0
+        for t in itertools.count():
+            yield ("wait", f"TF{t & 1}", t >> 1)
+            d = ring[t & 1]
+            yield ("arrive", f"TE{t & 1}", t >> 1)
+            if d is None:
+                return
+            total = d[1]
+            for _ in range(total):
+                yield ("wait", "SFULL", git)
+                yield ("read", f"S.{p}", ("S", git))
+                yield ("write", f"S.{p}", ("P", git))
+                yield ("arrive", "PFULL", git)
+                yield ("wait", "DPFULL", git)
+                if git > 0:
+                    yield ("wait", "DSEMPTY", git - 1)
+                yield ("read", f"DP.{p}", ("dP", git))
+                yield ("write", f"DS.{p}", ("dS", git))
+                yield ("arrive", "DSFULL", git)
+                git += 1
+            if total > 0:
+                yield ("wait", "DVDONE", git - 1)
+                yield ("read", f"DV.{p}", ("DV", kt, total - 1))
+                yield ("arrive", "DVEMPTY", kt)
+                yield ("wait", "ACC", kt)
+                yield ("read", f"DK.{p}", ("DK", kt, total - 1))
+                yield ("arrive", "DKEMPTY", kt)
+                kt += 1
+
+    sim.add("scheduler", scheduler())
+    sim.add("producer", producer())
+    if issuers == 1:
+        sim.add("mma", mma("all"))
+    else:
+        sim.add("mma_sdp", mma("sdp"))
+        sim.add("mma_rest", mma("rest"))
+    for q in range(D):
+        sim.add(f"drain{q}", drain(q))
+    for p in range(W):
+        sim.add(f"compute{p}", compute(p))

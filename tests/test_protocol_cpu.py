@@ -98,3 +98,31 @@ def test_model_flags_premature_and_aliased_waits():
     sim.add("late", late())
     with pytest.raises(pm.ProtocolError, match="parity aliases"):
         sim.run()
+
+
+@pytest.mark.parametrize("kst", [1, 2])
+@pytest.mark.parametrize("issuers", [1, 2])
+def test_main_kernel_protocol(kst, issuers):
+    """The fused main kernel as built (one MMA issuer) and the split of its MMA issue over
+    two threads (S / dP and dV / dK / dQ) with the extra completion wait that split needs."""
+    for seed in SEEDS:
+        tiles, warps = _tiles(seed, 0)
+        sim = pm.Sim(seed)
+        pm.main_kernel(sim, tiles, warps=warps, drains=2, kst=kst, issuers=issuers)
+        try:
+            sim.run()
+        except pm.ProtocolError as e:
+            raise AssertionError(f"seed {seed}, tiles {tiles}, warps {warps}: {e}") from None
+
+
+def test_main_model_catches_do_reuse_with_two_issuers():
+    caught = 0
+    for seed in SEEDS:
+        tiles, _ = _tiles(seed, 1)
+        sim = pm.Sim(seed)
+        pm.main_kernel(sim, tiles, warps=2, drains=2, issuers=2, dv_waits_dp=False)
+        try:
+            sim.run()
+        except pm.ProtocolError:
+            caught += 1
+    assert caught > 0
