@@ -485,14 +485,14 @@ def forward_kernel(sim, nvis, warps=2, kst=2, vst=2, rescale=0.3, two_issuers=Tr
 
 # ============================================================================ main kernel
 
-def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, dv_waits_dp=True):
+def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, do_waits_dp=True):
     """The fused backward's main kernel on one CTA (unordered mode): `tiles[t]` steps for
     the t-th key tile it claims.  `warps` compute warps stand for the eight and `drains`
     dQ-drain warps for the four.  kst: K stages (1 at Dp = 96 / 128, 2 at Dp <= 80).
     issuers=2 models a split of the MMA issue over two threads (S and dP from one, dV, dK
-    and dQ from the other) with the completion waits that split needs; dv_waits_dp=False
+    and dQ from the other) with the completion waits that split needs; do_waits_dp=False
     drops the one it adds (dO is read by dP_i and dV_i, issued by different threads, so
-    the dO buffer may only be handed back once both are complete)."""
+    the producer reloads the dO buffer only once dP_i, not just dV_i, is complete)."""
     W, D = warps, drains
     ones = ["V", "SFULL", "DPFULL", "DVDONE", "DQFULL", "DSEMPTY", "ACC", "NEXT", "VEMPTY"]
     for b in ones + [f"K{s}" for s in range(kst)] + [f"KEMPTY{s}" for s in range(kst)]:
@@ -569,6 +569,8 @@ def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, dv_waits_dp=Tru
                     yield from load_v()
                 if git >= 1:
                     yield ("wait", "DOE", git - 1)
+                    if issuers == 2 and do_waits_dp:
+                        yield ("wait", "DPFULL", git - 1)
                 yield ("copy", "DOF", git, [("dO", ("dO", git))])
                 if kst == 1 and it == 0 and kv_busy:
                     yield ("wait", "KEMPTY0", nk - 1)
@@ -625,10 +627,6 @@ def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, dv_waits_dp=Tru
                     reads = [(f"S.{p}", ("P", git)) for p in range(W)] + [("dO", ("dO", git))]
                     if it > 0:
                         reads += [(f"DV.{p}", ("DV", kt, it - 1)) for p in range(W)]
-                    if role == "rest" and dv_waits_dp:
-                        # dO is also read by dP_git, issued by the other thread: it must be
-                        # complete before the dO buffer is handed back
-                        yield ("wait", "DPFULL", git)
                     yield ("mma", th, reads, [(f"DV.{p}", ("DV", kt, it)) for p in range(W)])
                     yield ("commit", th, "DOE", git)
                     yield ("commit", th, "DVDONE", git)

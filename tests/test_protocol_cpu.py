@@ -120,7 +120,7 @@ def test_main_model_catches_do_reuse_with_two_issuers():
     for seed in SEEDS:
         tiles, _ = _tiles(seed, 1)
         sim = pm.Sim(seed)
-        pm.main_kernel(sim, tiles, warps=2, drains=2, issuers=2, dv_waits_dp=False)
+        pm.main_kernel(sim, tiles, warps=2, drains=2, issuers=2, do_waits_dp=False)
         try:
             sim.run()
         except pm.ProtocolError:
