@@ -714,3 +714,100 @@ def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, do_waits_dp=Tru
         sim.add(f"drain{q}", drain(q))
     for p in range(W):
         sim.add(f"compute{p}", compute(p))
+
+
+# ============================================================================ dK / dV kernel
+
+def dkdv_kernel(sim, total, warps=2, s_behind=True):
+    """The split algorithm's dK/dV kernel on one CTA (one key tile, `total` steps).
+    s_behind=True issues S_i+1 and dP_i+1 right behind dK_i (they overwrite P^T_i and
+    dS^T_i, which dV_i and dK_i read, and the products of one thread run in issue order);
+    False waits for dV_i's and dK_i's completion first (the kernel's earlier form)."""
+    W = warps
+    for b in ["KV", "SFULL", "DPFULL", "ACC", "DVDONE", "DKDONE"]:
+        sim.barrier(b)
+    for s in range(2):
+        for b in ["QF", "QE", "DOF", "DOE"]:
+            sim.barrier(f"{b}{s}")
+    sim.barrier("PFULL", W)
+    sim.barrier("DSFULL", W)
+
+    def producer():
+        if total == 0:
+            return
+        yield ("copy", "KV", 0, [("K", "K"), ("V", "V")])
+        for it in range(total):
+            s = it & 1
+            if it >= 2:
+                yield ("wait", f"QE{s}", (it - 2) >> 1)
+            yield ("copy", f"QF{s}", it >> 1, [(f"Q{s}", ("Q", it)), (f"LSE{s}", ("lse", it))])
+            if it >= 2:
+                yield ("wait", f"DOE{s}", (it - 2) >> 1)
+            yield ("copy", f"DOF{s}", it >> 1, [(f"dO{s}", ("dO", it))])
+
+    def issue_s(it):
+        s = it & 1
+        yield ("wait", f"QF{s}", it >> 1)
+        yield ("mma", "mma", [("K", "K"), (f"Q{s}", ("Q", it))], [(f"S.{p}", ("S", it)) for p in range(W)])
+        yield ("commit", "mma", "SFULL", it)
+
+    def issue_dp(it):
+        s = it & 1
+        yield ("wait", f"DOF{s}", it >> 1)
+        yield ("mma", "mma", [("V", "V"), (f"dO{s}", ("dO", it))], [(f"DP.{p}", ("dP", it)) for p in range(W)])
+        yield ("commit", "mma", "DPFULL", it)
+
+    def mma():
+        if total == 0:
+            yield ("commit", "mma", "ACC", 0)
+            return
+        yield ("wait", "KV", 0)
+        yield from issue_s(0)
+        yield from issue_dp(0)
+        for it in range(total):
+            s = it & 1
+            yield ("wait", "PFULL", it)
+            reads = [(f"S.{p}", ("P", it)) for p in range(W)] + [(f"dO{s}", ("dO", it))]
+            if it > 0:
+                reads += [(f"DV.{p}", ("DV", it - 1)) for p in range(W)]
+            yield ("mma", "mma", reads, [(f"DV.{p}", ("DV", it)) for p in range(W)])
+            yield ("commit", "mma", f"DOE{s}", it >> 1)
+            yield ("commit", "mma", "DVDONE", it)
+            yield ("wait", "DSFULL", it)
+            reads = [(f"DP.{p}", ("dS", it)) for p in range(W)] + [(f"Q{s}", ("Q", it))]
+            if it > 0:
+                reads += [(f"DK.{p}", ("DK", it - 1)) for p in range(W)]
+            yield ("mma", "mma", reads, [(f"DK.{p}", ("DK", it)) for p in range(W)])
+            yield ("commit", "mma", f"QE{s}", it >> 1)
+            yield ("commit", "mma", "DKDONE", it)
+            if it + 1 < total:
+                if not s_behind:
+                    yield ("wait", "DVDONE", it)
+                yield from issue_s(it + 1)
+                if not s_behind:
+                    yield ("wait", "DKDONE", it)
+                yield from issue_dp(it + 1)
+        yield ("commit", "mma", "ACC", 0)
+
+    def compute(p):
+        for it in range(total):
+            s = it & 1
+            yield ("wait", "SFULL", it)
+            yield ("read", f"LSE{s}", ("lse", it))
+            yield ("read", f"S.{p}", ("S", it))
+            yield ("write", f"S.{p}", ("P", it))
+            yield ("arrive", "PFULL", it)
+            yield ("wait", "DPFULL", it)
+            yield ("read", f"LSE{s}", ("lse", it))  # D shares the stage with LSE2
+            yield ("read", f"DP.{p}", ("dP", it))
+            yield ("write", f"DP.{p}", ("dS", it))
+            yield ("arrive", "DSFULL", it)
+        yield ("wait", "ACC", 0)
+        if total > 0:
+            yield ("read", f"DK.{p}", ("DK", total - 1))
+            yield ("read", f"DV.{p}", ("DV", total - 1))
+
+    sim.add("producer", producer())
+    sim.add("mma", mma())
+    for p in range(W):
+        sim.add(f"compute{p}", compute(p))

@@ -126,3 +126,18 @@ def test_main_model_catches_do_reuse_with_two_issuers():
         except pm.ProtocolError:
             caught += 1
     assert caught > 0
+
+
+@pytest.mark.parametrize("s_behind", [True, False])
+def test_dkdv_kernel_protocol(s_behind):
+    """The split algorithm's dK/dV kernel, with S_i+1 / dP_i+1 queued right behind dK_i
+    (as built) and after dV_i / dK_i have completed (its earlier form)."""
+    for seed in SEEDS:
+        r = random.Random(seed)
+        total, warps = r.randint(0, 9), r.choice([2, 3])
+        sim = pm.Sim(seed)
+        pm.dkdv_kernel(sim, total, warps=warps, s_behind=s_behind)
+        try:
+            sim.run()
+        except pm.ProtocolError as e:
+            raise AssertionError(f"seed {seed}, steps {total}, warps {warps}: {e}") from None
