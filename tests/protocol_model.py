@@ -485,14 +485,18 @@ def forward_kernel(sim, nvis, warps=2, kst=2, vst=2, rescale=0.3, two_issuers=Tr
 
 # ============================================================================ main kernel
 
-def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, do_waits_dp=True):
+def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, do_waits_dp=True,
+                ordered=False):
     """The fused backward's main kernel on one CTA (unordered mode): `tiles[t]` steps for
     the t-th key tile it claims.  `warps` compute warps stand for the eight and `drains`
     dQ-drain warps for the four.  kst: K stages (1 at Dp = 96 / 128, 2 at Dp <= 80).
     issuers=2 models a split of the MMA issue over two threads (S and dP from one, dV, dK
     and dQ from the other) with the completion waits that split needs; do_waits_dp=False
     drops the one it adds (dO is read by dP_i and dV_i, issued by different threads, so
-    the producer reloads the dO buffer only once dP_i, not just dV_i, is complete)."""
+    the producer reloads the dO buffer only once dP_i, not just dV_i, is complete).
+    ordered=True adds the ordered mode's hand-over between the ordering warp and the
+    drain (turn / turn-empty barriers and a two-slot turn word; the cross-CTA counter the
+    ordering warp polls is outside a one-CTA model)."""
     W, D = warps, drains
     ones = ["V", "SFULL", "DPFULL", "DVDONE", "DQFULL", "DSEMPTY", "ACC", "NEXT", "VEMPTY"]
     for b in ones + [f"K{s}" for s in range(kst)] + [f"KEMPTY{s}" for s in range(kst)]:
@@ -501,12 +505,14 @@ def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, do_waits_dp=Tru
         sim.barrier(f"QF{s}")
         sim.barrier(f"QE{s}")
         sim.barrier(f"TF{s}")
-        sim.barrier(f"TE{s}", 1 + issuers + D + W)
+        sim.barrier(f"TE{s}", 1 + issuers + D + W + (1 if ordered else 0))
     sim.barrier("DOF")
     sim.barrier("DOE")
     for b in ["PFULL", "DSFULL", "DVEMPTY", "DKEMPTY"]:
         sim.barrier(b, W)
     sim.barrier("DQEMPTY", D)
+    sim.barrier("TURN")
+    sim.barrier("TURNE")
     ring = [None, None]
     ticket = itertools.count()
 
@@ -671,6 +677,10 @@ def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, do_waits_dp=Tru
                 yield ("wait", "DQFULL", git)
                 yield ("read", f"DP.d{q}", ("dQ", git))
                 yield ("arrive", "DQEMPTY", git)
+                if ordered and q == 0:
+                    yield ("wait", "TURN", git)
+                    yield ("read", f"turn{git & 1}", ("turn", git))
+                    yield ("arrive", "TURNE", git)
                 git += 1
 
     def compute(p):
@@ -703,7 +713,24 @@ def main_kernel(sim, tiles, warps=2, drains=2, kst=1, issuers=1, do_waits_dp=Tru
                 yield ("arrive", "DKEMPTY", kt)
                 kt += 1
 
+    def ordering():
+        git = 0
+        for t in itertools.count():
+            yield ("wait", f"TF{t & 1}", t >> 1)
+            d = ring[t & 1]
+            yield ("arrive", f"TE{t & 1}", t >> 1)
+            if d is None:
+                return
+            for _ in range(d[1]):
+                if git > 0:
+                    yield ("wait", "TURNE", git - 1)
+                yield ("write", f"turn{git & 1}", ("turn", git))
+                yield ("arrive", "TURN", git)
+                git += 1
+
     sim.add("scheduler", scheduler())
+    if ordered:
+        sim.add("ordering", ordering())
     sim.add("producer", producer())
     if issuers == 1:
         sim.add("mma", mma("all"))

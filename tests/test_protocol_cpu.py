@@ -141,3 +141,15 @@ def test_dkdv_kernel_protocol(s_behind):
             sim.run()
         except pm.ProtocolError as e:
             raise AssertionError(f"seed {seed}, steps {total}, warps {warps}: {e}") from None
+
+
+@pytest.mark.parametrize("kst", [1, 2])
+def test_main_kernel_ordered_mode_protocol(kst):
+    for seed in SEEDS:
+        tiles, warps = _tiles(seed, 0)
+        sim = pm.Sim(seed)
+        pm.main_kernel(sim, tiles, warps=warps, drains=2, kst=kst, ordered=True)
+        try:
+            sim.run()
+        except pm.ProtocolError as e:
+            raise AssertionError(f"seed {seed}, tiles {tiles}, warps {warps}: {e}") from None
