@@ -838,3 +838,131 @@ def dkdv_kernel(sim, total, warps=2, s_behind=True):
     sim.add("mma", mma())
     for p in range(W):
         sim.add(f"compute{p}", compute(p))
+
+
+# ============================================================================ wide backward
+
+def wide_bwd_kernel(sim, total, nst=2, warps=2, drains=2):
+    """The wide backward kernel on one CTA (one key tile and output slice, `total` steps of
+    64 queries), with one or two Q / dO stages.  dS^T is written into tensor memory over
+    the dP^T columns (the A operand of dK) and into shared memory (the B operand of the
+    transposed dQ product); the dQ^T columns are drained by the drain warps."""
+    W, D = warps, drains
+    for b in ["KV", "SF", "DPF", "DQF", "DSE", "ACC"]:
+        sim.barrier(b)
+    for s in range(nst):
+        for b in ["QF", "QE", "DOF", "DOE"]:
+            sim.barrier(f"{b}{s}")
+    sim.barrier("PF", W)
+    sim.barrier("DSF", W)
+    sim.barrier("DQE", D)
+
+    def producer():
+        if total == 0:
+            return
+        yield ("copy", "KV", 0, [("K", "K"), ("V", "V")])
+        for it in range(total):
+            sq = it % nst
+            if it >= nst:
+                yield ("wait", f"QE{sq}", (it - nst) // nst)
+            yield ("copy", f"QF{sq}", it // nst, [(f"Q{sq}", ("Q", it)), (f"LSE{sq}", ("lse", it))])
+            if it >= nst:
+                yield ("wait", f"DOE{sq}", (it - nst) // nst)
+            yield ("copy", f"DOF{sq}", it // nst, [(f"dO{sq}", ("dO", it))])
+
+    def do_s(i):
+        sq = i % nst
+        yield ("wait", f"QF{sq}", i // nst)
+        yield ("mma", "mma", [("K", "K"), (f"Q{sq}", ("Q", i))], [(f"S.{p}", ("S", i)) for p in range(W)])
+        yield ("commit", "mma", "SF", i)
+
+    def do_dp(i):
+        sq = i % nst
+        yield ("wait", f"DOF{sq}", i // nst)
+        yield ("mma", "mma", [("V", "V"), (f"dO{sq}", ("dO", i))], [(f"DP.{p}", ("dP", i)) for p in range(W)])
+        yield ("commit", "mma", "DPF", i)
+
+    def do_dv(i):
+        sq = i % nst
+        yield ("wait", "PF", i)
+        reads = [(f"S.{p}", ("P", i)) for p in range(W)] + [(f"dO{sq}", ("dO", i))]
+        if i > 0:
+            reads += [(f"DV.{p}", ("DV", i - 1)) for p in range(W)]
+        yield ("mma", "mma", reads, [(f"DV.{p}", ("DV", i)) for p in range(W)])
+        yield ("commit", "mma", f"DOE{sq}", i // nst)
+
+    def do_dk(i):
+        sq = i % nst
+        yield ("wait", "DSF", i)
+        reads = [(f"DP.{p}", ("dS", i)) for p in range(W)] + [(f"Q{sq}", ("Q", i))]
+        if i > 0:
+            reads += [(f"DK.{p}", ("DK", i - 1)) for p in range(W)]
+        yield ("mma", "mma", reads, [(f"DK.{p}", ("DK", i)) for p in range(W)])
+        yield ("commit", "mma", f"QE{sq}", i // nst)
+
+    def do_dq(i):
+        if i >= 1:
+            yield ("wait", "DQE", i - 1)
+        yield ("mma", "mma", [("K", "K")] + [(f"DSs.{p}", ("dS", i)) for p in range(W)],
+               [(f"DQ.{q}", ("dQ", i)) for q in range(D)])
+        yield ("commit", "mma", "DQF", i)
+        yield ("commit", "mma", "DSE", i)
+
+    def mma():
+        if total == 0:
+            return
+        yield ("wait", "KV", 0)
+        if nst == 1:
+            for it in range(total):
+                yield from do_s(it)
+                yield from do_dp(it)
+                yield from do_dv(it)
+                yield from do_dk(it)
+                yield from do_dq(it)
+        else:
+            yield from do_s(0)
+            yield from do_dp(0)
+            for it in range(total):
+                more = it + 1 < total
+                yield from do_dv(it)
+                if more:
+                    yield from do_s(it + 1)
+                yield from do_dk(it)
+                if more:
+                    yield from do_dp(it + 1)
+                yield from do_dq(it)
+        yield ("commit", "mma", "ACC", 0)
+
+    def drain(q):
+        for it in range(total):
+            yield ("wait", "DQF", it)
+            yield ("read", f"DQ.{q}", ("dQ", it))
+            yield ("arrive", "DQE", it)
+
+    def compute(p):
+        for it in range(total):
+            sq = it % nst
+            yield ("wait", "SF", it)
+            yield ("read", f"LSE{sq}", ("lse", it))
+            yield ("read", f"S.{p}", ("S", it))
+            yield ("write", f"S.{p}", ("P", it))
+            yield ("arrive", "PF", it)
+            yield ("wait", "DPF", it)
+            if it >= 1:
+                yield ("wait", "DSE", it - 1)
+            yield ("read", f"LSE{sq}", ("lse", it))
+            yield ("read", f"DP.{p}", ("dP", it))
+            yield ("write", f"DP.{p}", ("dS", it))
+            yield ("write", f"DSs.{p}", ("dS", it))
+            yield ("arrive", "DSF", it)
+        if total > 0:
+            yield ("wait", "ACC", 0)
+            yield ("read", f"DK.{p}", ("DK", total - 1))
+            yield ("read", f"DV.{p}", ("DV", total - 1))
+
+    sim.add("producer", producer())
+    sim.add("mma", mma())
+    for q in range(D):
+        sim.add(f"drain{q}", drain(q))
+    for p in range(W):
+        sim.add(f"compute{p}", compute(p))

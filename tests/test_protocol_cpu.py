@@ -153,3 +153,17 @@ def test_main_kernel_ordered_mode_protocol(kst):
             sim.run()
         except pm.ProtocolError as e:
             raise AssertionError(f"seed {seed}, tiles {tiles}, warps {warps}: {e}") from None
+
+
+@pytest.mark.parametrize("nst", [1, 2])
+def test_wide_backward_protocol(nst):
+    """The wide backward (head dims above 128) with one and two Q / dO stages."""
+    for seed in SEEDS:
+        r = random.Random(seed)
+        total, warps = r.randint(0, 9), r.choice([2, 3])
+        sim = pm.Sim(seed)
+        pm.wide_bwd_kernel(sim, total, nst=nst, warps=warps)
+        try:
+            sim.run()
+        except pm.ProtocolError as e:
+            raise AssertionError(f"seed {seed}, steps {total}, warps {warps}: {e}") from None
