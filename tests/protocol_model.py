@@ -38,7 +38,6 @@ class Sim:
         self.agents = {}   # name -> [generator, pending request, first evaluation done]
         self.pipes = {}    # issuing thread -> list of products / commits in issue order
         self.copies = []   # asynchronous copies in flight: (barrier, phase, writes)
-        self.shared = {}   # plain shared-memory variables the roles exchange
 
     def barrier(self, name, count=1):
         self.bars[name] = {"count": count, "arrived": 0, "done": 0}
@@ -324,7 +323,6 @@ def forward_kernel(sim, nvis, warps=2, kst=2, vst=2, rescale=0.3, two_issuers=Tr
         sim.barrier(f"VE{s}")
     sim.barrier("NB", W)  # the softmax warps' per-item named barrier, as a rendezvous
     resc = {(x, p): rng.random() < rescale for x in range(sum(nvis)) for p in range(W)}
-    stores = {}  # (warp, item) -> whether its tensor store has read the staged O
 
     def k_producer():
         qn = c = 0
@@ -439,7 +437,6 @@ def forward_kernel(sim, nvis, warps=2, kst=2, vst=2, rescale=0.3, two_issuers=Tr
                 qb_, ph, it_ = os_pend
                 # bulk_wait_read_all: the store has read the staged rows
                 yield ("read", f"Q{qb_}.{p}", ("Ostage", it_))
-                stores[(p, it_)] = True
                 yield ("arrive", f"OS{qb_}", ph)
                 os_pend = None
 
